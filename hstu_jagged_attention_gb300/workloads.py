@@ -1,0 +1,151 @@
+"""Seeded synthetic workloads for HSTU jagged causal attention.
+
+This module only draws random numbers: sequence lengths, and Q/K/V values
+rounded to bf16.  It holds none of the attention arithmetic, so both the
+CUDA path and the fp64 oracle can take their inputs from it without sharing
+any of the method's code.
+
+The five workloads follow the shapes the pages measure or describe:
+
+* ``tiny``    -- 4 sequences of lengths {7, 33, 64, 1}, 2 heads, d = 32.
+* ``dense``   -- the page's QKV(16, 4, 4096, 64) shape stored as a jagged
+  batch with uniform offsets (ai6s.net "HSTU fused operator" post, sections
+  2.2 and 3.2).
+* ``skewed``  -- 128 sequences, lengths i.i.d. from a truncated power law
+  p(n) ~ n^-1.5 on [16, 8192], 4 heads, d = 128 (skewed user-history lengths,
+  HSTU paper section 3.2).
+* ``long``    -- 4 sequences of 10240..20480 tokens, 4 heads, d = 64 (the
+  post's "0 < s <= 20480" range, section 3.1).
+* ``serving`` -- 512 sequences with log-normal lengths (median 512,
+  sigma 1.0) clipped to [1, 8192], 2 heads, d = 64.
+
+Seeds: lengths use ``seed = index`` (0..4); Q, K and V use
+``seed = 1000 + index`` and are drawn in that order.  Values are fp32
+standard normals times sigma, rounded to bf16 with round-to-nearest-even.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+WORKLOAD_NAMES = ("tiny", "dense", "skewed", "long", "serving")
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    batch: int
+    heads: int
+    d: int
+    sigma: float
+    lengths: np.ndarray  # int64[batch]
+    alpha: float
+    inv_n: float
+
+    @property
+    def offsets(self) -> np.ndarray:
+        off = np.zeros(self.batch + 1, dtype=np.int32)
+        np.cumsum(self.lengths, out=off[1:])
+        return off
+
+    @property
+    def total(self) -> int:
+        return int(self.lengths.sum())
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(self.lengths.max()) if self.batch else 0
+
+    def describe(self) -> dict:
+        return {
+            "workload": self.name,
+            "batch": self.batch,
+            "heads": self.heads,
+            "d": self.d,
+            "total_tokens": self.total,
+            "max_seqlen": self.max_seqlen,
+            "alpha": self.alpha,
+            "inv_n": self.inv_n,
+            "sigma": self.sigma,
+        }
+
+
+def _lengths(name: str, rng: np.random.Generator) -> np.ndarray:
+    if name == "tiny":
+        return np.array([7, 33, 64, 1], dtype=np.int64)
+    if name == "dense":
+        return np.full(16, 4096, dtype=np.int64)
+    if name == "skewed":
+        support = np.arange(16, 8193, dtype=np.int64)
+        pmf = support.astype(np.float64) ** -1.5
+        pmf /= pmf.sum()
+        return rng.choice(support, size=128, p=pmf).astype(np.int64)
+    if name == "long":
+        return rng.integers(10240, 20481, size=4).astype(np.int64)
+    if name == "serving":
+        raw = np.exp(math.log(512.0) + rng.standard_normal(512))
+        return np.clip(np.rint(raw), 1, 8192).astype(np.int64)
+    raise KeyError(f"unknown workload {name!r}; expected one of {WORKLOAD_NAMES}")
+
+
+_SHAPES = {
+    # name: (heads, d, sigma)
+    "tiny": (2, 32, 1.0),
+    "dense": (4, 64, 1.0),
+    "skewed": (4, 128, 0.5),
+    "long": (4, 64, 1.0),
+    "serving": (2, 64, 1.0),
+}
+
+
+def workload(name: str) -> Workload:
+    """The named workload's shape, lengths and scalars (no tensors drawn)."""
+    index = WORKLOAD_NAMES.index(name)
+    heads, d, sigma = _SHAPES[name]
+    lengths = _lengths(name, np.random.default_rng(index))
+    max_len = int(lengths.max())
+    alpha = 1.0 / math.sqrt(d)
+    if name == "tiny":
+        inv_n = 1.0 / 64
+    elif name == "dense":
+        inv_n = 1.0 / 4096
+    elif name == "serving":
+        inv_n = 1.0 / 8192
+    else:  # skewed, long: 1 / (largest sampled length)
+        inv_n = 1.0 / max_len
+    return Workload(name, index, len(lengths), heads, d, sigma, lengths, alpha, inv_n)
+
+
+def custom(lengths, heads: int, d: int, sigma: float = 1.0, alpha: float | None = None,
+           inv_n: float | None = None, name: str = "custom") -> Workload:
+    """A workload with caller-chosen lengths (tests: ragged tails, empties)."""
+    lengths = np.asarray(lengths, dtype=np.int64)
+    max_len = int(lengths.max()) if len(lengths) else 1
+    return Workload(name, -1, len(lengths), heads, d, sigma, lengths,
+                    1.0 / math.sqrt(d) if alpha is None else float(alpha),
+                    1.0 / max(max_len, 1) if inv_n is None else float(inv_n))
+
+
+def bf16_round(x: np.ndarray):
+    """fp32 array -> torch bf16 tensor (round to nearest even)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def draw_qkv(w: Workload, seed: int | None = None):
+    """Q, K, V as CPU torch bf16 tensors of shape (total, heads, d).
+
+    Drawn from ``default_rng(1000 + index)`` (or ``seed``) in the order Q, K, V.
+    """
+    rng = np.random.default_rng(1000 + w.index if seed is None else seed)
+    shape = (w.total, w.heads, w.d)
+    out = []
+    for _ in range(3):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        if w.sigma != 1.0:
+            x *= np.float32(w.sigma)
+        out.append(bf16_round(x))
+    return tuple(out)

@@ -1,0 +1,166 @@
+/*
+ * HSTU jagged causal attention -- fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * definition that the CUDA path is checked against.  Only the test suite,
+ * the smoke check and the benchmark's CPU-baseline leg may load it; the
+ * product path never calls it and shares no code with it.
+ *
+ * What it computes (ai6s.net "HSTU fused operator" post, section 1, the
+ * HSTU formula and its PyTorch definition; section 3.2, the block mask is
+ * a lower-triangular mask including the diagonal; section 4.2, jagged
+ * values + offsets storage; HSTU paper section 3.1, pointwise aggregated
+ * attention without softmax normalisation):
+ *
+ *   for every sequence b, head h and local row i in [0, n_b), t = off[b] + i:
+ *     out[t,h,:] = inv_n * sum_{j=0..i} silu(alpha * <q[t,h,:], k[off[b]+j,h,:]>)
+ *                                       * v[off[b]+j,h,:]
+ *   silu(x) = x / (1 + exp(-x))
+ *
+ * Inputs are fp32 arrays that hold bf16-rounded values (exact in fp32 and in
+ * fp64); every product and sum is taken in fp64 in plain loops, in the order
+ * of the formula.  Masked terms (j > i) are never formed, which equals
+ * multiplying them by zero for finite inputs.
+ *
+ * Layout: q, k, v, out are row-major (total, heads, d); offsets has batch+1
+ * non-decreasing entries starting at 0.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* silu(x) = x * sigmoid(x) = x / (1 + e^{-x}).  For x -> -inf, e^{-x}
+ * overflows to +inf and the quotient is -0, which is the limit. */
+double hstu_oracle_silu(double x) { return x / (1.0 + exp(-x)); }
+
+/* One output row: out_row[c] for c < d, fp64. */
+static void oracle_row(const float* q, const float* k, const float* v, int64_t seq_start,
+                       int64_t i, int heads, int d, int h, double alpha, double inv_n,
+                       double* acc /* d doubles, scratch */, double* out_row) {
+    const int64_t t = seq_start + i;
+    const float* qr = q + (t * heads + h) * (int64_t)d;
+    for (int c = 0; c < d; ++c) acc[c] = 0.0;
+    for (int64_t j = 0; j <= i; ++j) {
+        const int64_t s = seq_start + j;
+        const float* kr = k + (s * heads + h) * (int64_t)d;
+        const float* vr = v + (s * heads + h) * (int64_t)d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += (double)qr[c] * (double)kr[c];
+        const double p = hstu_oracle_silu(alpha * dot);
+        for (int c = 0; c < d; ++c) acc[c] += p * (double)vr[c];
+    }
+    for (int c = 0; c < d; ++c) out_row[c] = inv_n * acc[c];
+}
+
+typedef struct {
+    const float *q, *k, *v;
+    const int64_t* offsets;
+    int batch, heads, d;
+    double alpha, inv_n;
+    double* out;
+    /* row-sample mode: rows_t/rows_h/nrows set, out is (nrows, d) */
+    const int64_t* rows_t;
+    const int32_t* rows_h;
+    int64_t nrows;
+    /* shared work counter */
+    pthread_mutex_t* mu;
+    int64_t* next;
+} job_t;
+
+static int64_t take(job_t* J, int64_t chunk) {
+    pthread_mutex_lock(J->mu);
+    int64_t w = *J->next;
+    *J->next += chunk;
+    pthread_mutex_unlock(J->mu);
+    return w;
+}
+
+/* Locate the sequence that holds token t (linear scan: plain, not fast). */
+static int64_t seq_start_of(const int64_t* offsets, int batch, int64_t t) {
+    for (int b = 0; b < batch; ++b)
+        if (t >= offsets[b] && t < offsets[b + 1]) return offsets[b];
+    return -1;
+}
+
+static void* worker_full(void* arg) {
+    job_t* J = (job_t*)arg;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)J->d);
+    const int64_t units = (int64_t)J->batch * J->heads;
+    for (;;) {
+        const int64_t u = take(J, 1);
+        if (u >= units) break;
+        const int b = (int)(u / J->heads), h = (int)(u % J->heads);
+        const int64_t s0 = J->offsets[b], n = J->offsets[b + 1] - J->offsets[b];
+        for (int64_t i = 0; i < n; ++i)
+            oracle_row(J->q, J->k, J->v, s0, i, J->heads, J->d, h, J->alpha, J->inv_n, acc,
+                       J->out + ((s0 + i) * J->heads + h) * (int64_t)J->d);
+    }
+    free(acc);
+    return NULL;
+}
+
+static void* worker_rows(void* arg) {
+    job_t* J = (job_t*)arg;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)J->d);
+    for (;;) {
+        const int64_t r = take(J, 1);
+        if (r >= J->nrows) break;
+        const int64_t t = J->rows_t[r];
+        const int64_t s0 = seq_start_of(J->offsets, J->batch, t);
+        double* o = J->out + r * (int64_t)J->d;
+        if (s0 < 0) { /* token outside every sequence: not a row */
+            for (int c = 0; c < J->d; ++c) o[c] = NAN;
+            continue;
+        }
+        oracle_row(J->q, J->k, J->v, s0, t - s0, J->heads, J->d, J->rows_h[r], J->alpha,
+                   J->inv_n, acc, o);
+    }
+    free(acc);
+    return NULL;
+}
+
+static int run(job_t* J, int nthreads, void* (*fn)(void*)) {
+    pthread_mutex_t mu = PTHREAD_MUTEX_INITIALIZER;
+    int64_t next = 0;
+    J->mu = &mu;
+    J->next = &next;
+    if (nthreads < 1) nthreads = 1;
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i)
+        if (pthread_create(&th[i], NULL, fn, J) == 0) ++started;
+    if (started == 0) fn(J); /* could not start threads: run inline */
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    return 0;
+}
+
+static int check_offsets(const int64_t* offsets, int batch) {
+    if (batch < 0 || !offsets) return -1;
+    if (offsets[0] != 0) return -1;
+    for (int b = 0; b < batch; ++b)
+        if (offsets[b + 1] < offsets[b]) return -1;
+    return 0;
+}
+
+/* Every row of every sequence.  out: (total, heads, d) fp64.  Returns 0 or -1. */
+int hstu_oracle_fwd_f64(const float* q, const float* k, const float* v, const int64_t* offsets,
+                        int batch, int heads, int d, double alpha, double inv_n, double* out,
+                        int nthreads) {
+    if (check_offsets(offsets, batch) || heads < 1 || d < 1) return -1;
+    job_t J = {q, k, v, offsets, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0, NULL, NULL};
+    return run(&J, nthreads, worker_full);
+}
+
+/* Selected rows only: row r is token rows_t[r], head rows_h[r]; out: (nrows, d) fp64.
+ * A token that lies in no sequence yields a row of NaN. */
+int hstu_oracle_rows_f64(const float* q, const float* k, const float* v, const int64_t* offsets,
+                         int batch, int heads, int d, double alpha, double inv_n,
+                         const int64_t* rows_t, const int32_t* rows_h, int64_t nrows, double* out,
+                         int nthreads) {
+    if (check_offsets(offsets, batch) || heads < 1 || d < 1 || nrows < 0) return -1;
+    job_t J = {q, k, v, offsets, batch, heads, d, alpha, inv_n, out, rows_t, rows_h, nrows,
+               NULL, NULL};
+    return run(&J, nthreads, worker_rows);
+}

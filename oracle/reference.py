@@ -1,0 +1,100 @@
+"""ctypes wrapper of the fp64 C oracle (``hstu_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+The oracle evaluates, for each sequence b, head h and local row i
+(ai6s.net "HSTU fused operator" post, section 1 formula; section 3.2 tril
+block mask including the diagonal; section 4.2 jagged values + offsets):
+
+    out[t, h, :] = inv_n * sum_{j <= i} silu(alpha * q[t,h,:].k[off[b]+j,h,:]) * v[off[b]+j,h,:]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(_build.build())
+        f = ctypes.POINTER(ctypes.c_float)
+        d = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.POINTER(ctypes.c_int64)
+        i32 = ctypes.POINTER(ctypes.c_int32)
+        lib.hstu_oracle_silu.argtypes = [ctypes.c_double]
+        lib.hstu_oracle_silu.restype = ctypes.c_double
+        lib.hstu_oracle_fwd_f64.argtypes = [f, f, f, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_double, d, ctypes.c_int]
+        lib.hstu_oracle_fwd_f64.restype = ctypes.c_int
+        lib.hstu_oracle_rows_f64.argtypes = [f, f, f, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_double, ctypes.c_double, i64, i32,
+                                             ctypes.c_int64, d, ctypes.c_int]
+        lib.hstu_oracle_rows_f64.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
+
+
+def _f32(x) -> np.ndarray:
+    """Accept a torch tensor (any float dtype, incl. bf16) or numpy array -> contiguous fp32."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _ptr(a, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def silu(x: float) -> float:
+    """The oracle's own silu, exposed for pinning."""
+    return _load().hstu_oracle_silu(float(x))
+
+
+def hstu_fwd(q, k, v, offsets, alpha: float, inv_n: float, threads: int | None = None) -> np.ndarray:
+    """All rows: returns fp64 array (total, heads, d)."""
+    qf, kf, vf = _f32(q), _f32(k), _f32(v)
+    total, heads, d = qf.shape
+    off = np.ascontiguousarray(np.asarray(offsets), dtype=np.int64)
+    batch = len(off) - 1
+    if kf.shape != qf.shape or vf.shape != qf.shape or (batch >= 0 and off[-1] != total):
+        raise ValueError("shape mismatch between q/k/v/offsets")
+    out = np.zeros((total, heads, d), dtype=np.float64)
+    rc = _load().hstu_oracle_fwd_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                     _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
+                                     batch, heads, d, float(alpha), float(inv_n),
+                                     _ptr(out, ctypes.c_double), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (offsets must start at 0 and not decrease)")
+    return out
+
+
+def hstu_rows(q, k, v, offsets, alpha: float, inv_n: float, rows_t, rows_h,
+              threads: int | None = None) -> np.ndarray:
+    """Sampled rows: row r is (token rows_t[r], head rows_h[r]); returns fp64 (nrows, d)."""
+    qf, kf, vf = _f32(q), _f32(k), _f32(v)
+    total, heads, d = qf.shape
+    off = np.ascontiguousarray(np.asarray(offsets), dtype=np.int64)
+    rt = np.ascontiguousarray(rows_t, dtype=np.int64)
+    rh = np.ascontiguousarray(rows_h, dtype=np.int32)
+    if rt.shape != rh.shape:
+        raise ValueError("rows_t and rows_h differ in length")
+    out = np.zeros((len(rt), d), dtype=np.float64)
+    rc = _load().hstu_oracle_rows_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                      _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
+                                      len(off) - 1, heads, d, float(alpha), float(inv_n),
+                                      _ptr(rt, ctypes.c_int64), _ptr(rh, ctypes.c_int32), len(rt),
+                                      _ptr(out, ctypes.c_double), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out

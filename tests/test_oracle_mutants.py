@@ -1,0 +1,98 @@
+"""The oracle pins must catch plausible mistakes.
+
+Each case copies the C oracle into a temporary directory, plants one
+mistake in the copy, builds it, and checks that a pin from
+``test_oracle_pins.py`` now fails.  The committed oracle is untouched.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+from oracle import build as oracle_build
+from oracle import dense
+
+MUTANTS = {
+    "silu_sign": ("x / (1.0 + exp(-x))", "x / (1.0 + exp(x))"),
+    "drop_diagonal": ("for (int64_t j = 0; j <= i; ++j)", "for (int64_t j = 0; j < i; ++j)"),
+    "alpha_divides": ("hstu_oracle_silu(alpha * dot)", "hstu_oracle_silu(dot / alpha)"),
+    "q_dot_v": ("dot += (double)qr[c] * (double)kr[c]", "dot += (double)qr[c] * (double)vr[c]"),
+    "inv_n_missing": ("out_row[c] = inv_n * acc[c]", "out_row[c] = acc[c]"),
+    "wrong_head_stride": ("(s * heads + h) * (int64_t)d;\n        const float* vr",
+                          "(s * heads + 0) * (int64_t)d;\n        const float* vr"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    src = open(oracle_build.SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-o", str(lib), str(path),
+                    "-lm", "-lpthread"], check=True)
+    L = ctypes.CDLL(str(lib))
+    f, dptr, i64 = (ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
+                    ctypes.POINTER(ctypes.c_int64))
+    L.hstu_oracle_fwd_f64.argtypes = [f, f, f, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_double, ctypes.c_double, dptr, ctypes.c_int]
+    return L
+
+
+def _run(L, q, k, v, off, alpha, inv_n):
+    total, heads, d = q.shape
+    out = np.zeros((total, heads, d))
+    P = lambda a, t: a.ctypes.data_as(ctypes.POINTER(t))
+    L.hstu_oracle_fwd_f64(P(q, ctypes.c_float), P(k, ctypes.c_float), P(v, ctypes.c_float),
+                          P(off, ctypes.c_int64), len(off) - 1, heads, d, alpha, inv_n,
+                          P(out, ctypes.c_double), 2)
+    return out
+
+
+def _pins_pass(L) -> bool:
+    """A condensed run of the pins: brute force, large-alpha limit, row-0 closed form."""
+    rng = np.random.default_rng(0)
+    lengths = [9, 0, 21, 1]
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    T, H, d = int(off[-1]), 2, 8
+    q, k, v = (rng.standard_normal((T, H, d)).astype(np.float32) for _ in range(3))
+    ok = True
+    got = _run(L, q, k, v, off, 0.4, 0.25)
+    ref = dense.hstu_jagged_bruteforce(q, k, v, off, 0.4, 0.25)
+    ok &= bool(np.allclose(got, ref, rtol=1e-12, atol=1e-13))
+    qi, ki = (rng.integers(-3, 4, (T, H, d)).astype(np.float32) for _ in range(2))
+    lim = _run(L, qi, ki, v, off, 200.0, 1.0) / 200.0
+    for b in range(len(lengths)):
+        s0, s1 = off[b], off[b + 1]
+        for h in range(H):
+            S = qi[s0:s1, h].astype(np.float64) @ ki[s0:s1, h].astype(np.float64).T
+            ok &= bool(np.allclose(lim[s0:s1, h], np.tril(np.maximum(S, 0)) @ v[s0:s1, h], atol=1e-9))
+    for b in range(len(lengths)):
+        if lengths[b]:
+            t = off[b]
+            s = float(np.dot(q[t, 0].astype(np.float64), k[t, 0].astype(np.float64)))
+            ok &= bool(np.allclose(got[t, 0], 0.25 * 0.4 * s * expit(0.4 * s) * v[t, 0], rtol=1e-12))
+    return ok
+
+
+def test_unmutated_copy_passes(tmp_path):
+    src = open(oracle_build.SRC).read()
+    (tmp_path / "orig.c").write_text(src)
+    lib = tmp_path / "orig.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-o", str(lib),
+                    str(tmp_path / "orig.c"), "-lm", "-lpthread"], check=True)
+    L = ctypes.CDLL(str(lib))
+    f, dptr, i64 = (ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
+                    ctypes.POINTER(ctypes.c_int64))
+    L.hstu_oracle_fwd_f64.argtypes = [f, f, f, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_double, ctypes.c_double, dptr, ctypes.c_int]
+    assert _pins_pass(L)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    assert not _pins_pass(_build_mutant(tmp_path, name))
