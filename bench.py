@@ -1,0 +1,388 @@
+"""Benchmark: HSTU jagged causal attention forward on GB300.
+
+One step = one forward over the whole workload (every (sequence, head,
+query block) item; all hot-path stages run inside the one kernel).  The
+default workload is the page's dense shape QKV(16, 4, 4096, 64) stored as a
+jagged batch with uniform offsets.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--sweep]
+
+Timing: W untimed warm-up steps, then K steps; each step's kernel is
+bracketed by CUDA events on the launching stream and an L2 flush (a 256 MiB
+write) runs between steps outside the events.  The metric is causal
+TFLOP/s = 4 d heads sum_b n_b (n_b + 1) / 2 / time.  Under torchrun each
+rank runs the same workload on its own GPU (weak scaling, no data-path
+collective); rank 0 prints one JSON line with the max time over ranks.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on the host cores, each step a bounded sample of rows of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from hstu_jagged_attention_gb300 import workloads  # noqa: E402
+
+METRIC = "HSTU jagged causal attn fwd: TFLOPS & % GB300 BF16 tensor peak; ms/call"
+UNIT = "TFLOP/s"
+KERNEL_SOURCE = os.path.join(ROOT, "hstu_jagged_attention_gb300", "csrc", "hstu_fwd.cu")
+
+# DRAM traffic (read + write bytes) of one launch of the forward kernel on
+# the dense 16x4x4096x64 workload, from an ncu capture, with the sha256 of
+# the kernel source it was taken on.  The figure is reported only while the
+# source is unchanged.
+MEASURED_TRAFFIC = {"dense": None, "sha256": None}
+
+
+def causal_flops(w: workloads.Workload) -> float:
+    L = w.lengths.astype(np.float64)
+    return float(4.0 * w.d * w.heads * np.sum(L * (L + 1) / 2.0))
+
+
+def algorithmic_bytes(w: workloads.Workload) -> float:
+    # read Q, K, V once and write O once, bf16
+    return float(8.0 * w.d * w.heads * w.total)
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained": p.get("bf16_tflops_sustained"),
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons, one line every 50 ms, each stamped
+    with the host time it arrived; summarised over a chosen time window."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        import threading
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.perf_counter(), line.strip()))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self, t0: float, t1: float, t_warm: float) -> dict | None:
+        """Summary over samples in [t0, t1] (the timed region); if fewer than
+        three fall there, over [t_warm, t1] (warm-up + timed, GPU busy)."""
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        rows = [(t, r.split(",")) for t, r in self.lines if r.count(",") >= 8]
+        window = "timed region"
+        sel = [r for t, r in rows if t0 - 0.05 <= t <= t1 + 0.05]
+        if len(sel) < 3:
+            sel = [r for t, r in rows if t_warm - 0.05 <= t <= t1 + 0.05]
+            window = "warm-up + timed region"
+        if not sel:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in sel) if v is not None]
+        mx = [v for v in (num(r[2]) for r in sel) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i in range(4)
+                          if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sel), "window": window}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(flops_per_rank: float, ms_local: float, world: int, device=None):
+    """Whole-job throughput under weak scaling: every rank does flops_per_rank
+    in its own time; the job takes the slowest rank's time.
+    Returns (TFLOP/s over all ranks, max ms over ranks)."""
+    ms_max = max_over_ranks(ms_local, world, device)
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12, ms_max
+
+
+def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int | None = None):
+    """Time the oracle on a bounded, uniformly random sample of rows.
+
+    Returns (flops_of_sample / seconds, description, threads, seconds)."""
+    from oracle import reference
+    threads = threads or reference.default_threads()
+    rng = np.random.default_rng(seed)
+    off = w.offsets.astype(np.int64)
+    seq_of = np.repeat(np.arange(w.batch), w.lengths)
+
+    def rows(nr):
+        t = rng.integers(0, w.total, size=nr)
+        h = rng.integers(0, w.heads, size=nr)
+        i = t - off[seq_of[t]]
+        return t, h, float(np.sum(4.0 * w.d * (i + 1)))
+
+    # calibrate on a small sample, then size the real one to ~target_s
+    t, h, fl = rows(64)
+    t0 = time.perf_counter()
+    reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(64, min(2_000_000, 64 * target_s / dt)))
+    t, h, fl = rows(n)
+    t0 = time.perf_counter()
+    reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads)
+    dt = time.perf_counter() - t0
+    desc = (f"{n} uniformly sampled (token, head) output rows of the {w.name} workload "
+            f"({fl / 1e9:.2f} causal GFLOP), fp64 C oracle, {threads} threads")
+    return fl / dt / 1e12, desc, threads, dt
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_init()
+    if rank != 0:
+        return 0
+    q, k, v = workloads.draw_qkv(w)
+    qf, kf, vf = (t.float().numpy() for t in (q, k, v))
+    per_step_s = max(1.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
+    vals = []
+    desc, threads = "", 0
+    for s in range(args.warmup + args.steps):
+        val, desc, threads, dt = cpu_oracle_sample(w, qf, kf, vf, per_step_s, seed=s)
+        if s >= args.warmup:
+            vals.append(val)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **w.describe()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    from hstu_jagged_attention_gb300 import binding, build
+
+    world, rank, local = dist_init()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}), flush=True)
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+
+    q_h, k_h, v_h = workloads.draw_qkv(w)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    out = torch.empty_like(q)
+    plan = binding.hstu_plan_create(w.offsets, w.batch, w.heads, w.d, w.max_seqlen)
+    n_items = binding.hstu_plan_num_items(plan)
+    grid, block, smem = binding.hstu_launch_shape(plan)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+
+    sampler = ClockSampler(local)
+    t_warm = time.perf_counter()
+    for _ in range(args.warmup):
+        binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+    torch.cuda.synchronize(dev)
+    st, site = binding.hstu_last_status()
+    if st != binding.HSTU_OK:
+        raise RuntimeError(f"device wait gave up during warm-up (site {site})")
+
+    # ---- kernel-only timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(wall0, wall0 + wall, t_warm)
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(times_ms)
+    flops = causal_flops(w)
+    value, ms_max = aggregate(flops, ms, world, dev)
+    st, site = binding.hstu_last_status()
+    if st != binding.HSTU_OK:
+        raise RuntimeError(f"device wait gave up during the timed region (site {site})")
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = flops / (ms * 1e-3) / 1e12
+    traffic = None
+    if MEASURED_TRAFFIC.get(w.name) and MEASURED_TRAFFIC.get("sha256") == kernel_sha():
+        traffic = MEASURED_TRAFFIC[w.name]
+
+    # ---- end to end through the C ABI with host buffers
+    pin = [t.pin_memory() for t in (q_h, k_h, v_h)]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qe, ke, ve = (torch.empty_like(q) for _ in range(3))
+    oe = torch.empty_like(out)
+    offsets_host = w.offsets.copy()
+
+    def e2e_step():
+        qe.copy_(pin[0], non_blocking=True)
+        ke.copy_(pin[1], non_blocking=True)
+        ve.copy_(pin[2], non_blocking=True)
+        binding.hstu_attn_fwd(qe, ke, ve, offsets_host, w.batch, w.heads, w.d, w.max_seqlen,
+                              w.alpha, w.inv_n, oe, stream)
+        out_h.copy_(oe, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        flush.zero_()  # same L2 state as the kernel-only region
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    flush_ms = 0.0
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        flush.zero_()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    flush_ms = f0.elapsed_time(f1) / args.steps
+    e2e_ms = max(e0.elapsed_time(e1) / args.steps - flush_ms, 1e-6)
+    e2e_value, e2e_ms = aggregate(flops, e2e_ms, world, dev)
+    st, site = binding.hstu_last_status()
+    if st != binding.HSTU_OK:
+        raise RuntimeError(f"device wait gave up during the e2e region (site {site})")
+    elem = 2
+    h2d = 3 * w.total * w.heads * w.d * elem + offsets_host.nbytes
+    d2h = w.total * w.heads * w.d * elem
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qf, kf, vf = (t.float().numpy() for t in (q_h, k_h, v_h))
+        val, desc, threads, _ = cpu_oracle_sample(w, qf, kf, vf, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+
+    binding.hstu_plan_destroy(plan)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**w.describe(), "l2": "flushed between steps (256 MiB write)",
+                       "work_items": n_items, "grid": grid, "block": block, "smem_bytes": smem,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_bf16_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+                         "algorithmic_bytes": algorithmic_bytes(w)},
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "timed_wall_s": wall,
+            "ms_per_step_min": min(times_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=workloads.WORKLOAD_NAMES, default="dense")
+    ap.add_argument("--sweep", action="store_true", help="one line per workload (extra lines)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    names = list(workloads.WORKLOAD_NAMES) if args.sweep else [args.workload]
+    rc = 0
+    for name in names:
+        w = workloads.workload(name)
+        rc |= run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

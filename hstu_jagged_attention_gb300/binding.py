@@ -1,0 +1,227 @@
+"""Thin ctypes binding of ``libhstu.so`` (the C ABI of ``include/hstu_attn.h``).
+
+The functions keep the C names and only marshal arguments: torch tensors or
+raw integer addresses become pointers, a torch stream becomes a
+``cudaStream_t``, and a negative status becomes an ``HstuError``.  Every step
+of the attention runs in the library's CUDA kernel; there is no Python or
+CPU fallback, and a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libhstu.so")
+
+HSTU_OK = 0
+HSTU_ERR_INVALID_ARG = -1
+HSTU_ERR_UNSUPPORTED = -2
+HSTU_ERR_CUDA = -3
+HSTU_ERR_TIMEOUT = -4
+HSTU_ERR_NO_MEMORY = -5
+BLOCK_M = 128
+HSTU_DEBUG_UNSIGNALLED_WAIT = 1
+
+# name -> (restype, argtypes); the exported symbols of include/hstu_attn.h
+_VP, _I32P, _IP = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int)
+_SIGNATURES = {
+    "hstu_attn_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP, _VP]),
+    "hstu_plan_create": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(_VP)]),
+    "hstu_attn_fwd_plan": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_float, ctypes.c_float, _VP, _VP]),
+    "hstu_plan_destroy": (ctypes.c_int, [_VP]),
+    "hstu_plan_num_items": (ctypes.c_int, [_VP, _IP]),
+    "hstu_plan_worklist": (ctypes.c_int, [_VP, _I32P, ctypes.c_int, _IP]),
+    "hstu_worklist_build": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int, _IP]),
+    "hstu_launch_shape": (ctypes.c_int, [_VP, _IP, _IP, _IP]),
+    "hstu_last_status": (ctypes.c_int, [_IP, _IP]),
+    "hstu_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "hstu_set_debug_flags": (ctypes.c_int, [ctypes.c_uint32]),
+    "hstu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+class HstuError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {hstu_status_string(code)} (status {code})")
+
+
+def lib():
+    """Load libhstu.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m hstu_jagged_attention_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return sorted(_SIGNATURES)
+
+
+def _check(code: int, where: str):
+    if code != HSTU_OK:
+        raise HstuError(code, where)
+
+
+def _addr(x) -> int | None:
+    """Device/host address of a tensor or an integer address."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream or None
+        return None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _host_offsets(offsets) -> np.ndarray:
+    if hasattr(offsets, "detach"):
+        offsets = offsets.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(offsets), dtype=np.int32)
+
+
+def hstu_status_string(code: int) -> str:
+    return lib().hstu_status_string(int(code)).decode()
+
+
+def hstu_attn_fwd(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: int, alpha: float,
+                  inv_n: float, out, stream=None) -> None:
+    """Enqueue the forward on ``stream`` (default: torch's current stream).
+
+    ``offsets`` may be a CUDA int32 tensor, a CPU tensor / numpy array (host),
+    or a raw address.
+    """
+    keep = None
+    if isinstance(offsets, int):
+        off_ptr = offsets
+    elif hasattr(offsets, "is_cuda") and offsets.is_cuda:
+        if offsets.dtype.itemsize != 4 or not offsets.is_contiguous():
+            raise ValueError("device offsets must be contiguous int32")
+        off_ptr = offsets.data_ptr()
+    else:
+        keep = _host_offsets(offsets)
+        off_ptr = keep.ctypes.data
+    _check(lib().hstu_attn_fwd(_addr(q), _addr(k), _addr(v), off_ptr, int(batch), int(heads), int(d),
+                               int(max_seqlen), float(alpha), float(inv_n), _addr(out),
+                               _stream(stream)), "hstu_attn_fwd")
+
+
+class Plan:
+    """Owner of an ``hstu_plan*``; call ``hstu_plan_destroy`` or use as a context manager."""
+
+    def __init__(self, handle: int, batch: int, heads: int, d: int, max_seqlen: int, total: int):
+        self.handle = handle
+        self.batch, self.heads, self.d, self.max_seqlen, self.total = batch, heads, d, max_seqlen, total
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        hstu_plan_destroy(self)
+
+    def __del__(self):
+        try:
+            hstu_plan_destroy(self)
+        except Exception:
+            pass
+
+
+def hstu_plan_create(host_offsets, batch: int, heads: int, d: int, max_seqlen: int) -> Plan:
+    off = _host_offsets(host_offsets)
+    if len(off) < batch + 1:
+        raise ValueError("offsets needs batch + 1 entries")
+    h = _VP()
+    _check(lib().hstu_plan_create(off.ctypes.data_as(_I32P), int(batch), int(heads), int(d),
+                                  int(max_seqlen), ctypes.byref(h)), "hstu_plan_create")
+    return Plan(h.value, batch, heads, d, max_seqlen, int(off[batch]) if batch else 0)
+
+
+def hstu_attn_fwd_plan(plan: Plan, q, k, v, alpha: float, inv_n: float, out, stream=None) -> None:
+    _check(lib().hstu_attn_fwd_plan(plan.handle, _addr(q), _addr(k), _addr(v), float(alpha),
+                                    float(inv_n), _addr(out), _stream(stream)), "hstu_attn_fwd_plan")
+
+
+def hstu_plan_destroy(plan: Plan) -> None:
+    if plan.handle:
+        h, plan.handle = plan.handle, None
+        _check(lib().hstu_plan_destroy(h), "hstu_plan_destroy")
+
+
+def hstu_plan_num_items(plan: Plan) -> int:
+    n = ctypes.c_int()
+    _check(lib().hstu_plan_num_items(plan.handle, ctypes.byref(n)), "hstu_plan_num_items")
+    return n.value
+
+
+def hstu_plan_worklist(plan: Plan) -> np.ndarray:
+    n = hstu_plan_num_items(plan)
+    buf = np.zeros((max(n, 1), 4), dtype=np.int32)
+    got = ctypes.c_int()
+    _check(lib().hstu_plan_worklist(plan.handle, buf.ctypes.data_as(_I32P), max(n, 1),
+                                    ctypes.byref(got)), "hstu_plan_worklist")
+    return buf[:got.value]
+
+
+def hstu_worklist_build(host_offsets, heads: int) -> np.ndarray:
+    """Host-only work list (no CUDA call): int32 (n_items, 4)."""
+    off = _host_offsets(host_offsets)
+    batch = len(off) - 1
+    n = ctypes.c_int()
+    _check(lib().hstu_worklist_build(off.ctypes.data_as(_I32P), batch, int(heads), None, 0,
+                                     ctypes.byref(n)), "hstu_worklist_build")
+    buf = np.zeros((max(n.value, 1), 4), dtype=np.int32)
+    _check(lib().hstu_worklist_build(off.ctypes.data_as(_I32P), batch, int(heads),
+                                     buf.ctypes.data_as(_I32P), n.value, ctypes.byref(n)),
+           "hstu_worklist_build")
+    return buf[:n.value]
+
+
+def hstu_launch_shape(plan: Plan) -> tuple[int, int, int]:
+    g, b, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().hstu_launch_shape(plan.handle, ctypes.byref(g), ctypes.byref(b), ctypes.byref(s)),
+           "hstu_launch_shape")
+    return g.value, b.value, s.value
+
+
+def hstu_last_status() -> tuple[int, int]:
+    """(device status, site) -- reads and clears the device status word; synchronises."""
+    st, site = ctypes.c_int(), ctypes.c_int()
+    _check(lib().hstu_last_status(ctypes.byref(st), ctypes.byref(site)), "hstu_last_status")
+    return st.value, site.value
+
+
+def hstu_set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().hstu_set_wait_timeout_ns(int(ns)), "hstu_set_wait_timeout_ns")
+
+
+def hstu_set_debug_flags(flags: int) -> None:
+    _check(lib().hstu_set_debug_flags(int(flags)), "hstu_set_debug_flags")

@@ -1,0 +1,374 @@
+// Host side of libhstu: argument validation, the longest-first work-list
+// builder, launch plans, TMA tensor maps and the C ABI of include/hstu_attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "hstu_attn.h"
+#include "hstu_internal.h"
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;
+unsigned long long g_timeout_ns = 0;  // 0 = not yet read from the environment
+unsigned g_debug_flags = 0;
+std::mutex g_mu;
+
+unsigned long long wait_timeout_ns() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_timeout_ns == 0) {
+    const char* env = std::getenv("HSTU_WAIT_TIMEOUT_NS");
+    unsigned long long v = env ? std::strtoull(env, nullptr, 10) : 0ull;
+    g_timeout_ns = v ? v : kDefaultTimeoutNs;
+  }
+  return g_timeout_ns;
+}
+
+bool supported_d(int d) { return d == 32 || d == 64 || d == 128; }
+
+// Offsets: offsets[0] == 0, non-decreasing, every length <= max_len,
+// total < 2^31.  max_len < 0 means unbounded.
+int check_offsets(const int32_t* off, int batch, long long max_len) {
+  if (batch < 0) return HSTU_ERR_INVALID_ARG;
+  if (batch == 0) return HSTU_OK;
+  if (!off || off[0] != 0) return HSTU_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const long long len = (long long)off[b + 1] - (long long)off[b];
+    if (len < 0) return HSTU_ERR_INVALID_ARG;
+    if (max_len >= 0 && len > max_len) return HSTU_ERR_INVALID_ARG;
+  }
+  return HSTU_OK;
+}
+
+// The work list: one item per (sequence, head, 128-row query block qt),
+// costing qt+1 key blocks; ordered by cost descending, then sequence, head,
+// qt ascending.  Built level by level (qt from the largest down), which
+// yields that order without a comparison sort.
+std::vector<hstu::Item> build_items(const int32_t* off, int batch, int heads) {
+  std::vector<int> tiles(batch);
+  int max_tiles = 0;
+  size_t count = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int len = off[b + 1] - off[b];
+    tiles[b] = (len + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    max_tiles = std::max(max_tiles, tiles[b]);
+    count += (size_t)tiles[b] * (size_t)heads;
+  }
+  std::vector<hstu::Item> items;
+  items.reserve(count);
+  for (int qt = max_tiles - 1; qt >= 0; --qt)
+    for (int b = 0; b < batch; ++b)
+      if (tiles[b] > qt)
+        for (int h = 0; h < heads; ++h) items.push_back(make_int4(off[b], off[b + 1] - off[b], h, qt));
+  return items;
+}
+
+int check_buffers(const void* q, const void* k, const void* v, const void* out) {
+  const void* ptrs[4] = {q, k, v, out};
+  for (const void* p : ptrs)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// (d, heads, total) bf16 view with box (min(d,64), 1, 128) and the kernel's swizzle.
+int make_map(CUtensorMap* m, const void* ptr, long long total, int heads, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return HSTU_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)total};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2u, (cuuint64_t)heads * (cuuint64_t)d * 2u};
+  const cuuint32_t box[3] = {(cuuint32_t)std::min(d, 64), 1u, (cuuint32_t)HSTU_BLOCK_M};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapSwizzle sw = hstu::fwd_swizzle_bytes(d) == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                                   : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+int device_check(int* sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HSTU_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  if (major != 10 || minor != 3) return HSTU_ERR_UNSUPPORTED;
+  return HSTU_OK;
+}
+
+int launch(const hstu::Item* d_items, int n_items, long long total, int heads, int d,
+           const void* q, const void* k, const void* v, float alpha, float inv_n, void* out,
+           cudaStream_t stream) {
+  if (n_items == 0) return HSTU_OK;
+  int sms = 0;
+  int rc = device_check(&sms);
+  if (rc != HSTU_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_map(&tq, q, total, heads, d)) != HSTU_OK) return rc;
+  if ((rc = make_map(&tk, k, total, heads, d)) != HSTU_OK) return rc;
+  if ((rc = make_map(&tv, v, total, heads, d)) != HSTU_OK) return rc;
+  hstu::FwdArgs a;
+  a.items = d_items;
+  a.n_items = n_items;
+  a.out = out;
+  a.heads = heads;
+  a.half_alpha = 0.5f * alpha;
+  a.inv_n = inv_n;
+  a.timeout_ns = wait_timeout_ns();
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
+  }
+  const int grid = std::min(n_items, sms);
+  const cudaError_t e = hstu::launch_fwd(d, tq, tk, tv, a, grid, stream);
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+    return HSTU_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+}  // namespace
+
+struct hstu_plan {
+  int batch = 0, heads = 0, d = 0, max_seqlen = 0;
+  long long total = 0;
+  std::vector<hstu::Item> items;
+  hstu::Item* d_items = nullptr;
+  int device = -1;
+};
+
+extern "C" {
+
+const char* hstu_status_string(int status) {
+  switch (status) {
+    case HSTU_OK: return "ok";
+    case HSTU_ERR_INVALID_ARG: return "invalid argument";
+    case HSTU_ERR_UNSUPPORTED: return "unsupported head dimension or device (needs d in {32,64,128} on sm_103)";
+    case HSTU_ERR_CUDA: return "CUDA runtime or driver error";
+    case HSTU_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case HSTU_ERR_NO_MEMORY: return "out of memory";
+    default: return "unknown status";
+  }
+}
+
+int hstu_worklist_build(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
+                        int capacity, int* n_items) {
+  if (!n_items || heads < 1 || capacity < 0) return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(host_offsets, batch, -1);
+  if (rc != HSTU_OK) return rc;
+  std::vector<hstu::Item> items;
+  try {
+    items = build_items(host_offsets, batch, heads);
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  *n_items = (int)items.size();
+  if (host_dst) {
+    const size_t n = std::min(items.size(), (size_t)capacity);
+    std::memcpy(host_dst, items.data(), n * sizeof(hstu::Item));
+  }
+  return HSTU_OK;
+}
+
+int hstu_plan_create(const int32_t* host_offsets, int batch, int heads, int d, int max_seqlen,
+                     hstu_plan** plan) {
+  if (!plan) return HSTU_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (heads < 1 || max_seqlen < 0) return HSTU_ERR_INVALID_ARG;
+  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
+  int rc = check_offsets(host_offsets, batch, max_seqlen);
+  if (rc != HSTU_OK) return rc;
+  hstu_plan* p = new (std::nothrow) hstu_plan;
+  if (!p) return HSTU_ERR_NO_MEMORY;
+  p->batch = batch;
+  p->heads = heads;
+  p->d = d;
+  p->max_seqlen = max_seqlen;
+  p->total = batch ? host_offsets[batch] : 0;
+  try {
+    p->items = build_items(host_offsets, batch, heads);
+  } catch (const std::bad_alloc&) {
+    delete p;
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (p->items.size() > (size_t)INT32_MAX) {
+    delete p;
+    return HSTU_ERR_INVALID_ARG;
+  }
+  if (!p->items.empty()) {
+    const size_t bytes = p->items.size() * sizeof(hstu::Item);
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+      delete p;
+      return HSTU_ERR_CUDA;
+    }
+    const cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p->d_items), bytes);
+    if (e != cudaSuccess) {
+      delete p;
+      return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+    }
+    if (cudaMemcpy(p->d_items, p->items.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaFree(p->d_items);
+      delete p;
+      return HSTU_ERR_CUDA;
+    }
+  }
+  *plan = p;
+  return HSTU_OK;
+}
+
+int hstu_plan_destroy(hstu_plan* plan) {
+  if (!plan) return HSTU_OK;
+  int rc = HSTU_OK;
+  if (plan->d_items && cudaFree(plan->d_items) != cudaSuccess) rc = HSTU_ERR_CUDA;
+  delete plan;
+  return rc;
+}
+
+int hstu_plan_num_items(const hstu_plan* plan, int* n_items) {
+  if (!plan || !n_items) return HSTU_ERR_INVALID_ARG;
+  *n_items = (int)plan->items.size();
+  return HSTU_OK;
+}
+
+int hstu_plan_worklist(const hstu_plan* plan, int32_t* host_dst, int capacity, int* n_items) {
+  if (!plan || !n_items) return HSTU_ERR_INVALID_ARG;
+  *n_items = (int)plan->items.size();
+  if (!host_dst) return HSTU_OK;
+  if (capacity < (int)plan->items.size()) return HSTU_ERR_INVALID_ARG;
+  std::memcpy(host_dst, plan->items.data(), plan->items.size() * sizeof(hstu::Item));
+  return HSTU_OK;
+}
+
+int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_bytes) {
+  if (!plan || !grid || !block || !smem_bytes) return HSTU_ERR_INVALID_ARG;
+  int sms = 0;
+  const int rc = device_check(&sms);
+  if (rc != HSTU_OK) return rc;
+  *grid = std::min((int)plan->items.size(), sms);
+  *block = hstu::kFwdThreads;
+  *smem_bytes = hstu::fwd_smem_bytes(plan->d);
+  return HSTU_OK;
+}
+
+int hstu_attn_fwd_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                       float alpha, float inv_n, void* out, hstu_stream_t stream) {
+  if (!plan) return HSTU_ERR_INVALID_ARG;
+  if (plan->items.empty()) return HSTU_OK;
+  int rc = check_buffers(q, k, v, out);
+  if (rc != HSTU_OK) return rc;
+  return launch(plan->d_items, (int)plan->items.size(), plan->total, plan->heads, plan->d, q, k, v,
+                alpha, inv_n, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int hstu_attn_fwd(const void* q, const void* k, const void* v, const int32_t* offsets, int batch,
+                  int heads, int d, int max_seqlen, float alpha, float inv_n, void* out,
+                  hstu_stream_t stream) {
+  if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
+  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
+  if (batch == 0) return HSTU_OK;
+  if (!offsets) return HSTU_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // Offsets may live on the host or on the device.
+  std::vector<int32_t> host_off;
+  const int32_t* off = offsets;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, offsets) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (attr.type == cudaMemoryTypeDevice) {
+    try {
+      host_off.resize((size_t)batch + 1);
+    } catch (const std::bad_alloc&) {
+      return HSTU_ERR_NO_MEMORY;
+    }
+    if (cudaMemcpyAsync(host_off.data(), offsets, host_off.size() * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+    off = host_off.data();
+  }
+  int rc = check_offsets(off, batch, max_seqlen);
+  if (rc != HSTU_OK) return rc;
+  const long long total = off[batch];
+  if (total == 0) return HSTU_OK;
+  if ((rc = check_buffers(q, k, v, out)) != HSTU_OK) return rc;
+
+  std::vector<hstu::Item> items;
+  try {
+    items = build_items(off, batch, heads);
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (items.empty()) return HSTU_OK;
+  if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  const size_t bytes = items.size() * sizeof(hstu::Item);
+  hstu::Item* d_items = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_items), bytes, s);
+  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+  // Pageable source: the call returns once the bytes are staged, so the
+  // host vector may go out of scope afterwards.
+  e = cudaMemcpyAsync(d_items, items.data(), bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(d_items, s);
+    return HSTU_ERR_CUDA;
+  }
+  rc = launch(d_items, (int)items.size(), total, heads, d, q, k, v, alpha, inv_n, out, s);
+  if (cudaFreeAsync(d_items, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
+  return rc;
+}
+
+int hstu_last_status(int* device_status, int* site) {
+  if (!device_status) return HSTU_ERR_INVALID_ARG;
+  unsigned st = 0, where = 0;
+  if (hstu::read_and_clear_device_status(&st, &where) != cudaSuccess) return HSTU_ERR_CUDA;
+  *device_status = (st & 1u) ? HSTU_ERR_TIMEOUT : HSTU_OK;
+  if (site) *site = (int)where;
+  return HSTU_OK;
+}
+
+int hstu_set_wait_timeout_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timeout_ns = ns ? ns : 0;
+  if (ns == 0) {
+    const char* env = std::getenv("HSTU_WAIT_TIMEOUT_NS");
+    unsigned long long v = env ? std::strtoull(env, nullptr, 10) : 0ull;
+    g_timeout_ns = v ? v : kDefaultTimeoutNs;
+  }
+  return HSTU_OK;
+}
+
+int hstu_set_debug_flags(uint32_t flags) {
+  if (flags & ~(uint32_t)HSTU_DEBUG_UNSIGNALLED_WAIT) return HSTU_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_debug_flags = flags;
+  return HSTU_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Internal interface between the host library (hstu_api.cpp) and the
+// sm_103a kernel translation unit (hstu_fwd.cu).  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hstu {
+
+// One work item: 128 query rows of one (sequence, head).
+//   x = first token of the sequence, y = sequence length, z = head,
+//   w = query block index qt (rows x + 128*qt ...).  Key blocks 0..qt.
+using Item = int4;
+
+struct FwdArgs {
+  const Item* items;   // device, n_items entries, longest first
+  int n_items;
+  void* out;           // bf16 (total, heads, d)
+  int heads;
+  float half_alpha;    // alpha / 2 (silu(a s) = h + h tanh(h), h = a s / 2)
+  float inv_n;
+  unsigned long long timeout_ns;
+  unsigned debug_flags;  // kDebug* bits; 0 in normal use
+};
+
+// Test hook: the MMA warp first waits on a barrier nothing signals.
+constexpr unsigned kDebugUnsignalledWait = 1u;
+
+// Shared-memory bytes and grid the d-specialised kernel needs.
+int fwd_smem_bytes(int d);
+constexpr int kFwdThreads = 512;
+
+// Launch the persistent kernel for head dimension d on `grid` CTAs.
+// The three tensor maps describe q, k, v as (d, heads, total) bf16 with box
+// (min(d,64), 1, 128) and the swizzle the kernel expects (fwd_swizzle_bytes).
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, int grid, cudaStream_t stream);
+
+// Swizzle span in bytes of one shared-memory row for head dimension d (128 or 64).
+int fwd_swizzle_bytes(int d);
+
+// Device status word (bit 0: a bounded wait gave up) and the code of the
+// first wait that gave up; read and cleared together.
+cudaError_t read_and_clear_device_status(unsigned* status, unsigned* site);
+
+}  // namespace hstu

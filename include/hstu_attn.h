@@ -1,0 +1,204 @@
+/*
+ * hstu_attn.h -- C ABI of the GB300 (sm_103a) HSTU jagged causal attention
+ * forward library (libhstu.so).
+ *
+ * The operation (ai6s.net "HSTU fused operator" post: section 1, the HSTU
+ * formula and its PyTorch definition; section 3.2, the in-kernel block mask,
+ * lower-triangular including the diagonal, blocks above the diagonal
+ * skipped; section 4.2, jagged values + offsets; HSTU paper section 3.1,
+ * pointwise aggregated attention without softmax normalisation):
+ *
+ *   for every sequence b in [0, batch), head h in [0, heads) and token t with
+ *   offsets[b] <= t < offsets[b+1]:
+ *
+ *     out[t,h,:] = inv_n * sum_{j = offsets[b]..t} silu(alpha * <q[t,h,:], k[j,h,:]>) * v[j,h,:]
+ *
+ *   with silu(x) = x * sigmoid(x).  No (s x s) score or mask buffer is ever
+ *   materialised.  A dense (batch, s, heads, d) token-major tensor is the
+ *   case offsets[b] = b * s; a head-major (batch, heads, s, d) tensor must
+ *   be permuted to token-major by the caller first.
+ *
+ * Layout.  q, k, v and out are contiguous row-major bf16 arrays of shape
+ * (total, heads, d), total = offsets[batch]; the row stride is heads*d
+ * elements.  Base addresses must be 16-byte aligned.  offsets is int32 with
+ * batch+1 entries, offsets[0] == 0, non-decreasing; empty sequences are
+ * allowed and produce no rows.  d must be 32, 64 or 128.
+ *
+ * Precision.  bf16 inputs; Q.K^T and P.V accumulate in fp32 on the tensor
+ * cores; silu in fp32; P is passed to the P.V product as the exact split
+ * P = P_hi + P_lo of two bf16 terms; the output is rounded to bf16
+ * (round to nearest even).
+ *
+ * Ownership and synchronisation.  The caller owns every buffer.  Calls are
+ * asynchronous on the given stream (a cudaStream_t; NULL = legacy default
+ * stream) and return once the work is enqueued.  Outputs are complete when
+ * the stream reaches that point.  Nothing here synchronises the device
+ * except where a function says so.
+ *
+ * Errors.  Every function returns HSTU_OK (0) or a negative hstu_status.
+ * Argument checks happen before anything is enqueued; on an argument error
+ * nothing is written.  Device-side waits inside the kernel are bounded: a
+ * wait that runs out sets a device status word that hstu_last_status()
+ * reports as HSTU_ERR_TIMEOUT, and the kernel returns instead of hanging.
+ * No C++ exception crosses this interface.
+ */
+#ifndef HSTU_ATTN_H_
+#define HSTU_ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+typedef enum hstu_status {
+  HSTU_OK = 0,
+  HSTU_ERR_INVALID_ARG = -1, /* bad pointer, size, offsets or alignment */
+  HSTU_ERR_UNSUPPORTED = -2, /* d not in {32, 64, 128}, or the device is not sm_103 */
+  HSTU_ERR_CUDA = -3,        /* a CUDA runtime or driver call failed */
+  HSTU_ERR_TIMEOUT = -4,     /* a bounded device-side wait ran out (see hstu_last_status) */
+  HSTU_ERR_NO_MEMORY = -5    /* host or device allocation failed */
+} hstu_status;
+
+/* Same type as cudaStream_t, declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st* hstu_stream_t;
+
+/* Opaque, reusable launch plan for one offsets array (see hstu_plan_create). */
+typedef struct hstu_plan hstu_plan;
+
+/* Rows of queries per work item and keys per K/V block (both 128). */
+#define HSTU_BLOCK_M 128
+#define HSTU_BLOCK_N 128
+
+/*
+ * hstu_attn_fwd -- the forward operation above, in one call.
+ *
+ *   q, k, v      device pointers, bf16 (total, heads, d), read only.
+ *   offsets      int32[batch+1]; a host pointer or a device pointer (told
+ *                apart with cudaPointerGetAttributes).  A device pointer is
+ *                copied to the host first, which synchronises `stream`.
+ *   batch        number of sequences (>= 0; 0 is a no-op).
+ *   heads        number of heads (>= 1).
+ *   d            head dimension: 32, 64 or 128.
+ *   max_seqlen   upper bound on every sequence length; used for validation
+ *                only (it is not the 1/n normaliser).
+ *   alpha        the score scale: silu(alpha * q.k).
+ *   inv_n        the output scale 1/n.
+ *   out          device pointer, bf16 (total, heads, d), written.  Every
+ *                row of every sequence is written; no other byte is.
+ *   stream       CUDA stream the work is enqueued on.
+ *
+ * Builds the work list on the host (as hstu_plan_create), copies it to a
+ * stream-ordered device allocation that is released on the same stream
+ * after the kernel, and launches.  Errors: HSTU_ERR_INVALID_ARG (offsets
+ * not starting at 0, decreasing, a length above max_seqlen, null or
+ * misaligned buffers), HSTU_ERR_UNSUPPORTED, HSTU_ERR_CUDA,
+ * HSTU_ERR_NO_MEMORY.
+ */
+int hstu_attn_fwd(const void* q, const void* k, const void* v, const int32_t* offsets, int batch,
+                  int heads, int d, int max_seqlen, float alpha, float inv_n, void* out,
+                  hstu_stream_t stream);
+
+/*
+ * hstu_plan_create -- validate host offsets and build the device work list once.
+ *
+ * The work list holds one item per (sequence, head, 128-row query block);
+ * query block qt needs key blocks 0..qt (the blocks above the diagonal are
+ * skipped, ai6s.net post section 3.2), and items are ordered longest first
+ * (qt descending, then sequence, head, qt ascending) for the persistent
+ * kernel's scheduler.  The plan owns its device buffer (allocated with
+ * cudaMalloc on the current device) and is immutable after creation, so
+ * one plan may be used by several streams at once.
+ *
+ *   host_offsets  int32[batch+1], host memory, read during the call only.
+ *   *plan         receives the new plan; set to NULL on error.
+ *
+ * Errors: as hstu_attn_fwd (argument checks), HSTU_ERR_NO_MEMORY.
+ */
+int hstu_plan_create(const int32_t* host_offsets, int batch, int heads, int d, int max_seqlen,
+                     hstu_plan** plan);
+
+/*
+ * hstu_attn_fwd_plan -- the forward operation for a plan's offsets and shape.
+ * Arguments as hstu_attn_fwd.  Enqueues exactly one kernel (none when the
+ * plan has no work items) and allocates nothing.
+ */
+int hstu_attn_fwd_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                       float alpha, float inv_n, void* out, hstu_stream_t stream);
+
+/* Release a plan (device memory freed with cudaFree).  NULL is accepted. */
+int hstu_plan_destroy(hstu_plan* plan);
+
+/* Number of work items in a plan. */
+int hstu_plan_num_items(const hstu_plan* plan, int* n_items);
+
+/*
+ * hstu_plan_worklist -- copy a plan's host-side work list out.
+ *
+ *   host_dst   int32[4 * capacity] or NULL; item i is
+ *              (first token of its sequence, sequence length, head, qt).
+ *   capacity   entries host_dst can hold.
+ *   *n_items   receives the item count (also when host_dst is NULL).
+ * Errors: HSTU_ERR_INVALID_ARG if capacity is too small for a non-NULL host_dst.
+ */
+int hstu_plan_worklist(const hstu_plan* plan, int32_t* host_dst, int capacity, int* n_items);
+
+/*
+ * hstu_worklist_build -- the same work list, computed on the host only (no
+ * CUDA call): validates offsets as hstu_plan_create does (with max_seqlen
+ * taken as unbounded) and writes up to `capacity` items into host_dst.
+ * *n_items receives the full count; host_dst may be NULL to query it.
+ */
+int hstu_worklist_build(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
+                        int capacity, int* n_items);
+
+/*
+ * hstu_launch_shape -- the grid the next launch for `plan` would use on the
+ * current device: *grid persistent CTAs of *block threads with *smem_bytes
+ * of dynamic shared memory.  Queries device attributes; launches nothing.
+ */
+int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_bytes);
+
+/*
+ * hstu_last_status -- read and clear the device-side status word of the
+ * current device.  Synchronises the device.  *device_status receives
+ * HSTU_OK, or HSTU_ERR_TIMEOUT if a kernel since the last call gave up on a
+ * bounded wait; *site (may be NULL) receives an internal code of the first
+ * wait that gave up (0 if none).  Kernels running concurrently share the
+ * word.
+ */
+int hstu_last_status(int* device_status, int* site);
+
+/*
+ * hstu_set_wait_timeout_ns -- limit, in nanoseconds of %globaltimer, for
+ * any single device-side wait in kernels launched after this call
+ * (process-wide; default 4e9, or the HSTU_WAIT_TIMEOUT_NS environment
+ * variable).  0 restores the default.  A tiny limit makes the kernel give up
+ * at its first wait that is not already satisfied; tests use this to check
+ * that the give-up path returns instead of hanging.
+ */
+int hstu_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * hstu_set_debug_flags -- test hooks for kernels launched after this call
+ * (process-wide; 0 = none, the default).
+ *   HSTU_DEBUG_UNSIGNALLED_WAIT  the kernel first waits on a barrier that
+ *       nothing signals, so its bounded wait runs out after the limit of
+ *       hstu_set_wait_timeout_ns; the kernel then drains its own copies,
+ *       frees TMEM, returns, and hstu_last_status reports HSTU_ERR_TIMEOUT.
+ *       The output is not written.  Used to test the give-up path without
+ *       hanging or faulting the GPU.
+ * Errors: HSTU_ERR_INVALID_ARG for unknown bits.
+ */
+#define HSTU_DEBUG_UNSIGNALLED_WAIT 1u
+int hstu_set_debug_flags(uint32_t flags);
+
+/* Static description of a status code. */
+const char* hstu_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSTU_ATTN_H_ */

@@ -1,0 +1,125 @@
+"""The C-ABI library: load, exported symbols, host work list, validation.
+
+These run without a GPU: no call here launches a kernel.  The work list is
+compared bit for bit with the oracle's plain-Python enumeration.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from hstu_jagged_attention_gb300 import binding, build, workloads
+from oracle import worklist as oracle_worklist
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "hstu_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hstu_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert _declared_functions() == binding.exported_symbols()
+
+
+def test_library_exports_every_declared_symbol():
+    L = binding.lib()
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    out = os.popen(f"nm -D --defined-only {binding.LIB_PATH}").read()
+    exported = set(re.findall(r" T (hstu_[a-z_0-9]+)", out))
+    assert set(_declared_functions()) <= exported
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5):
+        assert binding.hstu_status_string(code)
+    assert binding.hstu_status_string(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("name", workloads.WORKLOAD_NAMES)
+def test_worklist_bit_exact_vs_oracle(name):
+    w = workloads.workload(name)
+    got = binding.hstu_worklist_build(w.offsets, w.heads)
+    ref = oracle_worklist.items(w.offsets, w.heads)
+    assert got.dtype == np.int32 and got.shape == ref.shape
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_worklist_bit_exact_random(seed):
+    rng = np.random.default_rng(seed)
+    nb = int(rng.integers(0, 40))
+    lengths = rng.integers(0, 1200, size=nb) * (rng.random(nb) > 0.2)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    heads = int(rng.integers(1, 6))
+    got = binding.hstu_worklist_build(off, heads)
+    ref = oracle_worklist.items(off, heads)
+    assert np.array_equal(got.reshape(-1, 4), ref.reshape(-1, 4))
+
+
+def test_worklist_hand_cases_through_library():
+    from tests.test_oracle_pins import _read_worklist_cases
+    for offsets, heads, expect in _read_worklist_cases():
+        got = binding.hstu_worklist_build(np.array(offsets, np.int32), heads)
+        assert got.tolist() == expect
+
+
+@pytest.mark.parametrize("offsets", [[1, 5], [0, 5, 3], [0, -1]])
+def test_worklist_rejects_bad_offsets(offsets):
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_worklist_build(np.array(offsets, np.int32), 2)
+    assert e.value.code == binding.HSTU_ERR_INVALID_ARG
+
+
+def test_worklist_rejects_bad_heads():
+    with pytest.raises(binding.HstuError):
+        binding.hstu_worklist_build(np.array([0, 4], np.int32), 0)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(offsets=[0, 5, 3], d=64, max_seqlen=10), binding.HSTU_ERR_INVALID_ARG),   # decreasing
+    (dict(offsets=[2, 5], d=64, max_seqlen=10), binding.HSTU_ERR_INVALID_ARG),      # off[0] != 0
+    (dict(offsets=[0, 50], d=64, max_seqlen=10), binding.HSTU_ERR_INVALID_ARG),     # > max_seqlen
+    (dict(offsets=[0, 5], d=96, max_seqlen=10), binding.HSTU_ERR_UNSUPPORTED),      # d
+    (dict(offsets=[0, 5], d=64, max_seqlen=-1), binding.HSTU_ERR_INVALID_ARG),
+])
+def test_plan_create_validation(args, code):
+    off = np.array(args["offsets"], np.int32)
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_plan_create(off, len(off) - 1, 2, args["d"], args["max_seqlen"])
+    assert e.value.code == code
+
+
+def test_fwd_validation_before_any_cuda_call():
+    # Errors found on the arguments return before anything is enqueued.
+    off = np.array([0, 4], np.int32)
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_attn_fwd(16, 16, 16, off, 1, 2, 48, 4, 1.0, 1.0, 16, stream=0)
+    assert e.value.code == binding.HSTU_ERR_UNSUPPORTED
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_attn_fwd(16, 16, 16, off, 1, 0, 64, 4, 1.0, 1.0, 16, stream=0)
+    assert e.value.code == binding.HSTU_ERR_INVALID_ARG
+    # batch == 0 is a no-op that succeeds without touching any pointer
+    binding.hstu_attn_fwd(0, 0, 0, np.zeros(1, np.int32), 0, 2, 64, 0, 1.0, 1.0, 0, stream=0)
+
+
+def test_empty_plan_needs_no_device():
+    # all sequences empty: no work items, so no device allocation happens
+    p = binding.hstu_plan_create(np.zeros(4, np.int32), 3, 2, 64, 0)
+    assert binding.hstu_plan_num_items(p) == 0
+    assert binding.hstu_plan_worklist(p).shape == (0, 4)
+    binding.hstu_attn_fwd_plan(p, 0, 0, 0, 1.0, 1.0, 0, stream=0)  # no-op
+    binding.hstu_plan_destroy(p)
+
+
+def test_build_flags_target_sm103a():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
