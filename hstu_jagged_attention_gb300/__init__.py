@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     HstuError,
     Plan,
     hstu_attn_fwd,
+    hstu_attn_fwd_noalloc,
     hstu_attn_fwd_plan,
     hstu_last_status,
     hstu_launch_shape,

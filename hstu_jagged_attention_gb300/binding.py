@@ -22,6 +22,8 @@ HSTU_ERR_UNSUPPORTED = -2
 HSTU_ERR_CUDA = -3
 HSTU_ERR_TIMEOUT = -4
 HSTU_ERR_NO_MEMORY = -5
+HSTU_ERR_CAPACITY = -6
+HSTU_NOALLOC_MAX_ITEMS = 65536
 BLOCK_M = 128
 HSTU_DEBUG_UNSIGNALLED_WAIT = 1
 
@@ -30,6 +32,9 @@ _VP, _I32P, _IP = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTE
 _SIGNATURES = {
     "hstu_attn_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP, _VP]),
+    "hstu_attn_fwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                             ctypes.c_float, _VP, _VP]),
     "hstu_plan_create": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(_VP)]),
     "hstu_attn_fwd_plan": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_float, ctypes.c_float, _VP, _VP]),
@@ -133,6 +138,28 @@ def hstu_attn_fwd(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: 
     _check(lib().hstu_attn_fwd(_addr(q), _addr(k), _addr(v), off_ptr, int(batch), int(heads), int(d),
                                int(max_seqlen), float(alpha), float(inv_n), _addr(out),
                                _stream(stream)), "hstu_attn_fwd")
+
+
+def hstu_attn_fwd_noalloc(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: int,
+                          alpha: float, inv_n: float, out, stream=None) -> None:
+    """As hstu_attn_fwd, for callers that cannot let the library allocate.
+
+    The work list goes into a fixed device array inside the library instead
+    of a per-call allocation; ``offsets`` must be host memory (a CPU tensor,
+    a numpy array or a host address).  Calls in flight on the GPU at the same
+    time share that array and must not overlap.
+    """
+    keep = None
+    if isinstance(offsets, int):
+        off_ptr = offsets
+    else:
+        if hasattr(offsets, "is_cuda") and offsets.is_cuda:
+            raise ValueError("hstu_attn_fwd_noalloc takes host offsets only")
+        keep = _host_offsets(offsets)
+        off_ptr = keep.ctypes.data
+    _check(lib().hstu_attn_fwd_noalloc(_addr(q), _addr(k), _addr(v), off_ptr, int(batch), int(heads),
+                                       int(d), int(max_seqlen), float(alpha), float(inv_n),
+                                       _addr(out), _stream(stream)), "hstu_attn_fwd_noalloc")
 
 
 class Plan:

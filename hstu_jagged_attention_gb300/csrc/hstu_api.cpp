@@ -156,6 +156,21 @@ int launch(const hstu::Item* d_items, int n_items, long long total, int heads, i
 
 }  // namespace
 
+// Entry points into the helpers above for the other host translation units.
+namespace hstu {
+int host_check_offsets(const int32_t* off, int batch, long long max_len) {
+  return check_offsets(off, batch, max_len);
+}
+int host_check_buffers(const void* q, const void* k, const void* v, const void* out) {
+  return check_buffers(q, k, v, out);
+}
+int host_launch(const Item* d_items, int n_items, long long total, int heads, int d, const void* q,
+                const void* k, const void* v, float alpha, float inv_n, void* out,
+                cudaStream_t stream) {
+  return launch(d_items, n_items, total, heads, d, q, k, v, alpha, inv_n, out, stream);
+}
+}  // namespace hstu
+
 struct hstu_plan {
   int batch = 0, heads = 0, d = 0, max_seqlen = 0;
   long long total = 0;
@@ -174,6 +189,8 @@ const char* hstu_status_string(int status) {
     case HSTU_ERR_CUDA: return "CUDA runtime or driver error";
     case HSTU_ERR_TIMEOUT: return "a bounded device-side wait ran out";
     case HSTU_ERR_NO_MEMORY: return "out of memory";
+    case HSTU_ERR_CAPACITY:
+      return "work list larger than the fixed capacity of hstu_attn_fwd_noalloc (HSTU_NOALLOC_MAX_ITEMS)";
     default: return "unknown status";
   }
 }

@@ -44,4 +44,12 @@ int fwd_swizzle_bytes(int d);
 // first wait that gave up; read and cleared together.
 cudaError_t read_and_clear_device_status(unsigned* status, unsigned* site);
 
+// Host helpers defined in hstu_api.cpp (argument checks and the launch),
+// shared with hstu_noalloc.cu.
+int host_check_offsets(const int32_t* off, int batch, long long max_len);
+int host_check_buffers(const void* q, const void* k, const void* v, const void* out);
+int host_launch(const Item* d_items, int n_items, long long total, int heads, int d, const void* q,
+                const void* k, const void* v, float alpha, float inv_n, void* out,
+                cudaStream_t stream);
+
 }  // namespace hstu

@@ -58,7 +58,8 @@ typedef enum hstu_status {
   HSTU_ERR_UNSUPPORTED = -2, /* d not in {32, 64, 128}, or the device is not sm_103 */
   HSTU_ERR_CUDA = -3,        /* a CUDA runtime or driver call failed */
   HSTU_ERR_TIMEOUT = -4,     /* a bounded device-side wait ran out (see hstu_last_status) */
-  HSTU_ERR_NO_MEMORY = -5    /* host or device allocation failed */
+  HSTU_ERR_NO_MEMORY = -5,   /* host or device allocation failed */
+  HSTU_ERR_CAPACITY = -6     /* work list exceeds HSTU_NOALLOC_MAX_ITEMS (hstu_attn_fwd_noalloc) */
 } hstu_status;
 
 /* Same type as cudaStream_t, declared here so this header needs no CUDA headers. */
@@ -99,6 +100,44 @@ typedef struct hstu_plan hstu_plan;
 int hstu_attn_fwd(const void* q, const void* k, const void* v, const int32_t* offsets, int batch,
                   int heads, int d, int max_seqlen, float alpha, float inv_n, void* out,
                   hstu_stream_t stream);
+
+/*
+ * hstu_attn_fwd_noalloc -- hstu_attn_fwd for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that own every byte of device memory themselves -- a serving process with
+ * a fixed memory budget, or a framework whose allocator must not be
+ * bypassed -- and so cannot let the library call cudaMalloc or
+ * cudaMallocAsync, which may also synchronise or fail under memory
+ * pressure in the middle of a request.  It computes exactly what
+ * hstu_attn_fwd computes and calls no allocating routine, on the host or
+ * the device.
+ *
+ * Instead of a per-call device allocation, the work list goes into one
+ * fixed array of HSTU_NOALLOC_MAX_ITEMS items (16 bytes each, 1 MiB) that
+ * lives in the library's device memory on every GPU that loads it, until
+ * the process exits.  Consequences:
+ *   - A call whose work list would exceed HSTU_NOALLOC_MAX_ITEMS (one item
+ *     per 128 query rows of each sequence and head) is rejected with
+ *     HSTU_ERR_CAPACITY before anything is enqueued.
+ *   - All calls on a device share the array.  Calls enqueued on one stream
+ *     run one after the other and are safe; calls whose work overlaps on
+ *     the GPU (other streams, other threads) overwrite each other's work
+ *     list and give wrong results.  Each call writes every entry it reads,
+ *     so nothing needs clearing between calls.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, with that device current);
+ *     make that first call before any stream capture.
+ *
+ *   offsets    host pointer only, int32[batch+1] (a device pointer is
+ *              rejected with HSTU_ERR_INVALID_ARG, since copying it back
+ *              would need host staging).
+ * Other arguments, layout and errors as hstu_attn_fwd.
+ */
+#define HSTU_NOALLOC_MAX_ITEMS 65536
+int hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v, const int32_t* offsets,
+                          int batch, int heads, int d, int max_seqlen, float alpha, float inv_n,
+                          void* out, hstu_stream_t stream);
 
 /*
  * hstu_plan_create -- validate host offsets and build the device work list once.
