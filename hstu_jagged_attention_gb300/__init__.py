@@ -21,5 +21,6 @@ from .binding import (  # noqa: F401
     hstu_set_debug_flags,
     hstu_set_wait_timeout_ns,
     hstu_status_string,
+    hstu_trace_read,
     hstu_worklist_build,
 )

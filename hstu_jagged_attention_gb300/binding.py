@@ -26,6 +26,10 @@ HSTU_ERR_CAPACITY = -6
 HSTU_NOALLOC_MAX_ITEMS = 65536
 BLOCK_M = 128
 HSTU_DEBUG_UNSIGNALLED_WAIT = 1
+HSTU_DEBUG_TRACE = 2
+TRACE_EVENTS = {1: "qk_issue", 2: "pv_issue", 3: "silu_start", 4: "silu_end", 5: "epi_start",
+                6: "epi_end", 7: "load_k", 8: "load_v", 9: "load_q", 10: "mma_k_ready",
+                11: "mma_qk_done", 12: "mma_p_ready", 13: "mma_pv_done"}
 
 # name -> (restype, argtypes); the exported symbols of include/hstu_attn.h
 _VP, _I32P, _IP = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int)
@@ -46,6 +50,7 @@ _SIGNATURES = {
     "hstu_last_status": (ctypes.c_int, [_IP, _IP]),
     "hstu_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "hstu_set_debug_flags": (ctypes.c_int, [ctypes.c_uint32]),
+    "hstu_trace_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int, _IP]),
     "hstu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -252,3 +257,20 @@ def hstu_set_wait_timeout_ns(ns: int) -> None:
 
 def hstu_set_debug_flags(flags: int) -> None:
     _check(lib().hstu_set_debug_flags(int(flags)), "hstu_set_debug_flags")
+
+
+def hstu_trace_read(capacity: int = 32768) -> np.ndarray:
+    """Pipeline trace of CTA 0 (see include/hstu_attn.h): structured array
+    with fields clock, event, warp, index; read and cleared."""
+    buf = np.zeros(2 * capacity, dtype=np.uint64)
+    n = ctypes.c_int()
+    _check(lib().hstu_trace_read(buf.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), capacity,
+                                 ctypes.byref(n)), "hstu_trace_read")
+    raw = buf[: 2 * n.value].reshape(-1, 2)
+    out = np.zeros(n.value, dtype=[("clock", np.int64), ("event", np.int32), ("warp", np.int32),
+                                   ("index", np.int64)])
+    out["clock"] = raw[:, 0].astype(np.int64)
+    out["event"] = (raw[:, 1] >> np.uint64(48)).astype(np.int32)
+    out["warp"] = ((raw[:, 1] >> np.uint64(40)) & np.uint64(0xFF)).astype(np.int32)
+    out["index"] = (raw[:, 1] & np.uint64((1 << 40) - 1)).astype(np.int64)
+    return out

@@ -47,26 +47,9 @@ int check_offsets(const int32_t* off, int batch, long long max_len) {
   return HSTU_OK;
 }
 
-// The work list: one item per (sequence, head, 128-row query block qt),
-// costing qt+1 key blocks; ordered by cost descending, then sequence, head,
-// qt ascending.  Built level by level (qt from the largest down), which
-// yields that order without a comparison sort.
 std::vector<hstu::Item> build_items(const int32_t* off, int batch, int heads) {
-  std::vector<int> tiles(batch);
-  int max_tiles = 0;
-  size_t count = 0;
-  for (int b = 0; b < batch; ++b) {
-    const int len = off[b + 1] - off[b];
-    tiles[b] = (len + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
-    max_tiles = std::max(max_tiles, tiles[b]);
-    count += (size_t)tiles[b] * (size_t)heads;
-  }
-  std::vector<hstu::Item> items;
-  items.reserve(count);
-  for (int qt = max_tiles - 1; qt >= 0; --qt)
-    for (int b = 0; b < batch; ++b)
-      if (tiles[b] > qt)
-        for (int h = 0; h < heads; ++h) items.push_back(make_int4(off[b], off[b + 1] - off[b], h, qt));
+  std::vector<hstu::Item> items((size_t)hstu::count_items(off, batch, heads));
+  hstu::fill_items(off, batch, heads, items.data());
   return items;
 }
 
@@ -158,6 +141,32 @@ int launch(const hstu::Item* d_items, int n_items, long long total, int heads, i
 
 // Entry points into the helpers above for the other host translation units.
 namespace hstu {
+// The work list: one item per (sequence, head, 128-row query block qt); the
+// block needs key blocks 0..qt and costs qt+1.  Ordered by cost descending,
+// then sequence, head, qt ascending: generated level by level (qt from the
+// largest down), which is that order without a comparison sort.
+long long count_items(const int32_t* off, int batch, int heads) {
+  long long n = 0;
+  for (int b = 0; b < batch; ++b)
+    n += (long long)((off[b + 1] - off[b] + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M) * heads;
+  return n;
+}
+
+void fill_items(const int32_t* off, int batch, int heads, Item* dst) {
+  int max_tiles = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int tiles = (off[b + 1] - off[b] + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    if (tiles > max_tiles) max_tiles = tiles;
+  }
+  long long i = 0;
+  for (int qt = max_tiles - 1; qt >= 0; --qt)
+    for (int b = 0; b < batch; ++b) {
+      const int n = off[b + 1] - off[b];
+      if ((n + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M > qt)
+        for (int h = 0; h < heads; ++h) dst[i++] = make_int4(off[b], n, h, qt);
+    }
+}
+
 int host_check_offsets(const int32_t* off, int batch, long long max_len) {
   return check_offsets(off, batch, max_len);
 }
@@ -382,9 +391,19 @@ int hstu_set_wait_timeout_ns(uint64_t ns) {
 }
 
 int hstu_set_debug_flags(uint32_t flags) {
-  if (flags & ~(uint32_t)HSTU_DEBUG_UNSIGNALLED_WAIT) return HSTU_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)(HSTU_DEBUG_UNSIGNALLED_WAIT | HSTU_DEBUG_TRACE)) return HSTU_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_debug_flags = flags;
+  return HSTU_OK;
+}
+
+int hstu_trace_read(uint64_t* dst, int capacity, int* n_events) {
+  if (!n_events || capacity < 0) return HSTU_ERR_INVALID_ARG;
+  int n = 0;
+  if (hstu::read_and_clear_trace(reinterpret_cast<unsigned long long*>(dst), dst ? capacity : 0,
+                                 &n) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  *n_events = n;
   return HSTU_OK;
 }
 

@@ -8,29 +8,42 @@
 // section 4.2 jagged values + offsets.  HSTU paper section 3.2: the
 // attention becomes grouped GEMMs of different sizes over ragged sequences.)
 //
-// Design (one persistent CTA per SM, 16 warps, warp-specialised):
-//   warp 4        TMA producer: Q block of the work item, then K and V blocks
-//                 kt = 0..qt into shared-memory rings (128B-swizzled tiles).
-//   warp 5        MMA issuer (one thread): S = Q K^T into a TMEM buffer
-//                 (tcgen05.mma kind::f16, fp32 accumulate), then
-//                 O += P_hi V + P_lo V with P read from TMEM.  Owns TMEM.
-//   warps 8-15    two "SiLU" warpgroups; warpgroup e handles the blocks whose
-//                 running index is e mod 2, i.e. S buffer e.  Thread r owns
-//                 score row r: tcgen05.ld S, p = h + h tanh(h) with
-//                 h = alpha s / 2 (= alpha s sigmoid(alpha s)), tril select on
-//                 the diagonal block, split p = bf16(p) + bf16(p - bf16(p)),
-//                 tcgen05.st both halves over the S columns just read.
-//   warps 0-3     epilogue: reads the finished O buffer (double-buffered in
-//                 TMEM), scales by inv_n, rounds to bf16 and stores the valid
-//                 rows with 16-byte stores.
-// The three roles overlap the way the post's three-stage pipeline does
-// (section 5.2): QK of block t+1 runs on the tensor cores while the SiLU
-// warps work on block t and PV of block t-1 drains.
+// Design (one persistent CTA per SM, 16 warps, warp-specialised).  A work
+// item is one 128-row query block of one (sequence, head); it walks the key
+// blocks 0..qt.
+//   warp 4        TMA producer (one thread): each item's Q block, then its K
+//                 blocks, into shared-memory rings (128B-swizzled tiles).
+//   warp 6        TMA producer (one thread): V blocks.  (One thread's bulk
+//                 copies are processed one box at a time, so the streams get
+//                 separate issuers.)
+//   warp 5        QK issuer (one thread, owns TMEM): S_j = Q K^T
+//                 (tcgen05.mma kind::f16, fp32 accumulate) into TMEM S
+//                 buffer j = step mod P, up to P steps ahead.
+//   warp 7        PV issuer (one thread): O += P_hi V + P_lo V with P read
+//                 from TMEM, as soon as the SiLU warps have written P.
+//   warps 8-15    two "SiLU" warpgroups taking alternate steps.  Thread r
+//                 owns score row r: tcgen05.ld S (the next 32 columns load
+//                 while the current ones are computed), p = h + h tanh(h)
+//                 with h = alpha s / 2 (= alpha s sigmoid(alpha s)), tril
+//                 select on the diagonal block, split
+//                 p = bf16(p) + bf16(p - bf16(p)), tcgen05.st both halves over
+//                 the S columns just read.
+//   warps 0-3     epilogue: reads a finished O buffer, scales by inv_n, rounds
+//                 to bf16 and stores the valid rows with 16-byte stores.
+// The roles overlap the way the post's three-stage pipeline does (section
+// 5.2): QK of later blocks, SiLU of the current one and PV of earlier ones
+// run at the same time.  The two MMA issuers are separate threads so that
+// neither waits behind the other; S-free barriers (committed by the PV
+// issuer when its products complete) let the QK issuer reuse an S buffer.
 //
-// TMEM columns (512 allocated): S0 [0,128), S1 [128,256), O0 [256,256+d),
-// O1 [256+d, 256+2d).  P of a block overwrites its own S buffer: for the
-// 32-key chunk c, P_hi keys pairs go to columns 32c+[0,16) and P_lo to
-// 32c+[16,32) (two bf16 per 32-bit column).
+// TMEM columns (512 allocated): P S buffers of 128 columns (P = 3 for
+// d <= 64, 2 for d = 128), then two O buffers of d columns.  P of a block
+// overwrites its own S buffer: for the 32-key chunk c, P_hi key pairs go to
+// columns 32c+[0,16) and P_lo to 32c+[16,32) (two bf16 per 32-bit column).
+//
+// The diagonal key block of a sequence's last query block, when the sequence
+// ends inside it, computes only keys < n rounded up to 16: its QK uses
+// N = that width and its PV stops at the last 16-key step holding a key < n.
 //
 // Every mbarrier wait is bounded by a %globaltimer limit.  A wait that runs
 // out records a status word, raises a CTA-wide abort flag that every other
@@ -40,6 +53,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "hstu_internal.h"
 
 namespace hstu {
@@ -47,59 +62,29 @@ namespace hstu {
 __device__ unsigned int g_dev_status;
 __device__ unsigned int g_dev_site;
 
+// Trace buffer for kDebugTrace: per warp of CTA 0, kTracePerWarp events of
+// two 64-bit words; g_trace_n[w] counts warp w's events.
+constexpr int kTraceWarps = 16;
+constexpr int kTracePerWarp = 2048;
+__device__ unsigned long long g_trace[kTraceWarps * kTracePerWarp * 2];
+__device__ unsigned int g_trace_n[kTraceWarps];
+
 namespace {
 
 constexpr int kBM = 128;  // query rows per item == TMEM lanes
 constexpr int kBN = 128;  // keys per K/V block
 constexpr int kEpiWarp0 = 0;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kTmaWarpK = 4;   // Q and K blocks
+constexpr int kMmaWarpQK = 5;  // QK products; owns TMEM
+constexpr int kTmaWarpV = 6;   // V blocks
+constexpr int kMmaWarpPV = 7;  // PV products
 constexpr int kEwWarp0 = 8;
 constexpr uint32_t kTmemCols = 512;
 
 // wait-site codes reported through g_dev_site
 enum : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteOEmpty,
-  kSiteVFull, kSiteSFull, kSiteOFull, kSiteUnsignalled
-};
-
-template <int D>
-struct Cfg {
-  static constexpr int CHUNK = D < 64 ? D : 64;  // elements per swizzled row
-  static constexpr int NCHUNK = D / CHUNK;
-  static constexpr int ROWB = CHUNK * 2;          // bytes per swizzled row: 128 or 64
-  static constexpr int ATOMB = 8 * ROWB;          // 8-row swizzle atom
-  static constexpr int CHUNKB = kBM * ROWB;       // 128 rows of one chunk
-  static constexpr int TILEB = kBM * D * 2;       // one 128 x D bf16 block
-  static constexpr int QS = 2;
-  static constexpr int KS = D == 128 ? 2 : 4;
-  static constexpr int VS = D == 128 ? 3 : 4;
-  static constexpr uint64_t LAYOUT = ROWB == 128 ? 2 : 4;  // descriptor layout: 128B / 64B swizzle
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + QS * TILEB;
-  static constexpr int V_OFF = K_OFF + KS * TILEB;
-  static constexpr int BAR_OFF = V_OFF + VS * TILEB;
-  static constexpr int B_QFULL = 0;
-  static constexpr int B_QEMPTY = B_QFULL + QS;
-  static constexpr int B_KFULL = B_QEMPTY + QS;
-  static constexpr int B_KEMPTY = B_KFULL + KS;
-  static constexpr int B_VFULL = B_KEMPTY + KS;
-  static constexpr int B_VEMPTY = B_VFULL + VS;
-  static constexpr int B_SFULL = B_VEMPTY + VS;
-  static constexpr int B_PFULL = B_SFULL + 2;
-  static constexpr int B_OFULL = B_PFULL + 2;
-  static constexpr int B_OEMPTY = B_OFULL + 2;
-  static constexpr int B_DRAIN = B_OEMPTY + 2;
-  static constexpr int NBARS = B_DRAIN + 1;
-  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
-  static constexpr int USED = MISC_OFF + 16;
-  static constexpr int SMEM = ((USED + 1023) / 1024) * 1024 + 1024;  // + realignment slack
-  // Ask for more than half an SM's shared memory so that exactly one CTA
-  // (and one 512-column TMEM allocation) lives on each SM.
-  static constexpr int SMEM_LAUNCH = SMEM < 120 * 1024 ? 120 * 1024 : SMEM;
-  static constexpr uint32_t O_COL = 256;
-  static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(256 + 2 * D <= (int)kTmemCols, "TMEM budget");
+  kSiteVFull, kSiteSFull, kSiteOFull, kSiteUnsignalled, kSiteSFree
 };
 
 // Instruction descriptor, tcgen05.mma kind::f16: D fp32, A and B bf16,
@@ -166,20 +151,25 @@ __device__ __noinline__ void signal_timeout(const WaitCtx& w, int site) {
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (;;) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*w.abort_flag) return false;
-    if (globaltimer() - t0 > w.limit_ns) {
-      signal_timeout(w, site);
-      return false;
+    if ((it & 3u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer() - t0 > w.limit_ns) {
+        signal_timeout(w, site);
+        return false;
+      }
     }
   }
 }
 
-// Whole-warp bounded wait with a warp-uniform result.
+// Whole-warp bounded wait with a warp-uniform result: lane 0 polls, the
+// other lanes wait at the shuffle.  The caller's tcgen05.fence::
+// after_thread_sync then orders every lane's TMEM accesses after the wait.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
-  const bool ok = wait_one(bar, parity, w, site);
-  return __all_sync(0xffffffffu, ok);
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_one(bar, parity, w, site);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // Wait used only while draining after an abort: ignores the abort flag.
@@ -215,24 +205,31 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
 }
 
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
+// tcgen05.mma kind::f16, M = 128, with enable-input-d fixed at compile time
+// (ACC = 0 overwrites the accumulator, 1 accumulates).  _ss: A and B from
+// shared-memory descriptors; _ts: A from TMEM (the P operand), B from shared.
+template <int ACC>
+__device__ __forceinline__ void mma_ss_c(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
+  if (ACC)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(a),
+                 "l"(b), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem), "l"(a),
+                 "l"(b), "r"(idesc)
+                 : "memory");
 }
 
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
+template <int ACC>
+__device__ __forceinline__ void mma_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
+  if (ACC)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b), "r"(idesc)
+                 : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -255,6 +252,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+
+// Same load without the wait: the registers are not valid until
+// tmem_wait_ld(r) below, which ties them to the wait so that no use of them
+// can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -284,6 +310,46 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Trace event codes.
+enum : unsigned {
+  kEvQkIssue = 1,  // MMA warp: QK of block index issued
+  kEvPvIssue,      // MMA warp: PV of block index issued (after its waits)
+  kEvSiluStart,    // SiLU warp: S of block index ready
+  kEvSiluEnd,      // SiLU warp: P of block index written
+  kEvEpiStart,     // epilogue warp: O of item ready
+  kEvEpiEnd,       // epilogue warp: rows of item stored
+  kEvLoadK,        // producer: K block load issued
+  kEvLoadV,        // producer: V block load issued
+  kEvLoadQ,        // producer: Q block load issued
+  kEvMmaKReady,    // MMA warp: K block index present
+  kEvMmaQkDone,    // MMA warp: QK instructions and commits of block index issued
+  kEvMmaPReady,    // MMA warp: P of block index present
+  kEvMmaPvDone,    // MMA warp: PV instructions and commits of block index issued
+};
+
+// Per-warp trace slot counters live in shared memory (set by the kernel).
+__device__ __forceinline__ uint32_t* trace_counters();
+
+// One trace event from lane 0 of the calling warp, CTA 0 only: a plain
+// store into this warp's region, so the warp does not wait on it.
+__device__ __forceinline__ void trace(const FwdArgs& a, unsigned ev, unsigned idx) {
+  if (!(a.debug_flags & kDebugTrace) || blockIdx.x != 0 || (threadIdx.x & 31) != 0) return;
+  const unsigned warp = threadIdx.x >> 5;
+  uint32_t* cnt = trace_counters() + warp;
+  const unsigned slot = *cnt;
+  if (slot < (unsigned)kTracePerWarp) {
+    *cnt = slot + 1;
+    unsigned long long* dst = g_trace + 2 * ((size_t)warp * kTracePerWarp + slot);
+    dst[0] = clock64();
+    dst[1] = ((unsigned long long)ev << 48) | ((unsigned long long)warp << 40) | idx;
+  }
+}
+
+__device__ __forceinline__ uint32_t* trace_counters() {
+  __shared__ uint32_t counters[kTraceWarps];
+  return counters;
+}
+
 __device__ __forceinline__ int item_index(int it, int cta, int grid) {
   // serpentine over the longest-first list: even rounds left to right, odd
   // rounds right to left, so that CTAs even out the cost of their items.
@@ -293,242 +359,430 @@ __device__ __forceinline__ int item_index(int it, int cta, int grid) {
 
 // ------------------------------------------------------------------ roles
 template <int D>
-__device__ void role_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                              const FwdArgs& a, uint32_t base, const WaitCtx& w, int lane) {
+struct Cfg {
+  static constexpr int CHUNK = D < 64 ? D : 64;  // elements per swizzled row
+  static constexpr int NCHUNK = D / CHUNK;
+  static constexpr int ROWB = CHUNK * 2;          // bytes per swizzled row: 128 or 64
+  static constexpr int ATOMB = 8 * ROWB;          // 8-row swizzle atom
+  static constexpr int CHUNKB = kBM * ROWB;       // 128 rows of one chunk
+  static constexpr int TILEB = kBM * D * 2;       // one 128 x D bf16 block
+  // The K ring, the V ring and the S buffers in TMEM share the period P:
+  // each MMA thread's loop, unrolled by P, sees every slot as a
+  // compile-time constant (addresses are a loop-invariant base plus
+  // constants).
+  static constexpr int P = D == 128 ? 2 : 3;
+  static constexpr int QS = 2;                    // Q slots
+  static constexpr int OB = 2;                    // O buffers in TMEM
+  static constexpr uint64_t LAYOUT = ROWB == 128 ? 2 : 4;  // descriptor layout: 128B / 64B swizzle
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + QS * TILEB;
+  static constexpr int V_OFF = K_OFF + P * TILEB;
+  static constexpr int BAR_OFF = V_OFF + P * TILEB;
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_QEMPTY = B_QFULL + QS;
+  static constexpr int B_KFULL = B_QEMPTY + QS;
+  static constexpr int B_KEMPTY = B_KFULL + P;
+  static constexpr int B_VFULL = B_KEMPTY + P;
+  static constexpr int B_VEMPTY = B_VFULL + P;
+  static constexpr int B_SFULL = B_VEMPTY + P;   // S of block written (QK done)
+  static constexpr int B_PFULL = B_SFULL + P;    // P of block written (SiLU done)
+  static constexpr int B_SFREE = B_PFULL + P;    // PV of block done: S buffer reusable
+  static constexpr int B_OFULL = B_SFREE + P;
+  static constexpr int B_OEMPTY = B_OFULL + OB;
+  static constexpr int B_DRAIN = B_OEMPTY + OB;  // [2]: QK and PV threads' drains
+  static constexpr int NBARS = B_DRAIN + 2;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
+  static constexpr int USED = MISC_OFF + 16;
+  static constexpr int SMEM = ((USED + 1023) / 1024) * 1024 + 1024;  // + realignment slack
+  // Ask for more than half an SM's shared memory so that exactly one CTA
+  // (and one 512-column TMEM allocation) lives on each SM.
+  static constexpr int SMEM_LAUNCH = SMEM < 120 * 1024 ? 120 * 1024 : SMEM;
+  // TMEM columns: S buffer j at 128 j; O buffer ob at 128 P + ob d.
+  static constexpr uint32_t O_COL = 128u * P;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(128 * P + OB * D <= (int)kTmemCols, "TMEM budget");
+};
+
+// A work item decoded: query block qt of one (sequence, head).
+struct Block {
+  int s0, n, h, qt;
+  __device__ __forceinline__ int rows() const {  // valid query rows (1..128)
+    const int r = n - kBM * qt;
+    return r < kBM ? r : kBM;
+  }
+  // Keys of key block kt that a valid row can see: 128, except for the
+  // diagonal block of the sequence's last query block when the sequence ends
+  // inside it (rounded up to the 16-key MMA step).
+  __device__ __forceinline__ int cols(int kt) const {
+    if (kt != qt) return kBN;
+    const int r = n - kBN * kt;
+    return r >= kBN ? kBN : ((r + 15) & ~15);
+  }
+};
+
+__device__ __forceinline__ bool load_block(const FwdArgs& a, int it, Block& b) {
+  const int idx = item_index(it, blockIdx.x, gridDim.x);
+  if (idx >= a.n_items) return false;
+  const Item x = __ldg(&a.items[idx]);
+  b.s0 = x.x;
+  b.n = x.y;
+  b.h = x.z;
+  b.qt = x.w;
+  return true;
+}
+
+// A cursor over the CTA's key-block steps: item `it` (block b) at key block
+// kt; tc counts the steps.
+struct Cursor {
+  int it, kt;
+  uint32_t tc;
+  Block b;
+  bool valid;
+  __device__ __forceinline__ void start(const FwdArgs& a) {
+    it = 0;
+    kt = 0;
+    tc = 0;
+    valid = load_block(a, 0, b);
+  }
+  __device__ __forceinline__ void advance(const FwdArgs& a) {
+    ++tc;
+    if (++kt > b.qt) {
+      kt = 0;
+      ++it;
+      valid = load_block(a, it, b);
+    }
+  }
+};
+
+// ------------------------------------------------------------------ roles
+// TMA producers.  A single thread's bulk-tensor copies are processed one box
+// at a time (about 620 cycles per 16 KB box measured on GB300), so the K
+// (with Q) and V streams have separate issuing threads in separate warps.
+template <int D, bool KQ>
+__device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, const FwdArgs& a,
+                              uint32_t base, const WaitCtx& w) {
   using C = Cfg<D>;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-  uint32_t qc = 0, kc = 0, vc = 0;
+  constexpr int FULL = KQ ? C::B_KFULL : C::B_VFULL;
+  constexpr int EMPTY = KQ ? C::B_KEMPTY : C::B_VEMPTY;
+  constexpr int OFF = KQ ? C::K_OFF : C::V_OFF;
+  uint32_t c = 0, qc = 0;
   bool ok = true;
-  for (int it = 0; ok; ++it) {
-    const int idx = item_index(it, blockIdx.x, gridDim.x);
-    if (idx >= a.n_items) break;
-    const Item item = __ldg(&a.items[idx]);
-    const int s0 = item.x, h = item.z, qt = item.w;
-    const int qs = (int)(qc % C::QS);
-    if (!(ok = wait_warp(bar(C::B_QEMPTY + qs), ((qc / C::QS) & 1u) ^ 1u, w, kSiteQEmpty))) break;
-    if (lane == 0) {
+  Block b;
+  for (int it = 0; ok && load_block(a, it, b); ++it) {
+    if (KQ) {
+      const int qs = (int)(qc % C::QS);
+      if (!(ok = wait_one(bar(C::B_QEMPTY + qs), ((qc / C::QS) & 1u) ^ 1u, w, kSiteQEmpty))) break;
+      trace(a, kEvLoadQ, qc);
       mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILEB);
 #pragma unroll
       for (int ch = 0; ch < C::NCHUNK; ++ch)
-        tma_load_3d(base + C::Q_OFF + qs * C::TILEB + ch * C::CHUNKB, tq, bar(C::B_QFULL + qs),
-                    ch * C::CHUNK, h, s0 + kBM * qt);
+        tma_load_3d(base + C::Q_OFF + qs * C::TILEB + ch * C::CHUNKB, tm_q, bar(C::B_QFULL + qs),
+                    ch * C::CHUNK, b.h, b.s0 + kBM * b.qt);
+      ++qc;
     }
-    __syncwarp();
-    ++qc;
-    for (int kt = 0; kt <= qt; ++kt) {
-      const int ks = (int)(kc % C::KS);
-      if (!(ok = wait_warp(bar(C::B_KEMPTY + ks), ((kc / C::KS) & 1u) ^ 1u, w, kSiteKEmpty))) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::TILEB);
+    for (int kt = 0; kt <= b.qt; ++kt) {
+      const int slot = (int)(c % C::P);
+      if (!(ok = wait_one(bar(EMPTY + slot), ((c / C::P) & 1u) ^ 1u, w, KQ ? kSiteKEmpty : kSiteVEmpty)))
+        break;
+      trace(a, KQ ? kEvLoadK : kEvLoadV, c);
+      mbar_arrive_expect_tx(bar(FULL + slot), C::TILEB);
 #pragma unroll
-        for (int ch = 0; ch < C::NCHUNK; ++ch)
-          tma_load_3d(base + C::K_OFF + ks * C::TILEB + ch * C::CHUNKB, tk, bar(C::B_KFULL + ks),
-                      ch * C::CHUNK, h, s0 + kBN * kt);
-      }
-      __syncwarp();
-      ++kc;
-      const int vs = (int)(vc % C::VS);
-      if (!(ok = wait_warp(bar(C::B_VEMPTY + vs), ((vc / C::VS) & 1u) ^ 1u, w, kSiteVEmpty))) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::TILEB);
-#pragma unroll
-        for (int ch = 0; ch < C::NCHUNK; ++ch)
-          tma_load_3d(base + C::V_OFF + vs * C::TILEB + ch * C::CHUNKB, tv, bar(C::B_VFULL + vs),
-                      ch * C::CHUNK, h, s0 + kBN * kt);
-      }
-      __syncwarp();
-      ++vc;
+      for (int ch = 0; ch < C::NCHUNK; ++ch)
+        tma_load_3d(base + OFF + slot * C::TILEB + ch * C::CHUNKB, tm_a, bar(FULL + slot),
+                    ch * C::CHUNK, b.h, b.s0 + kBN * kt);
+      ++c;
     }
   }
-  if (!ok && lane == 0) {
-    // Drain: wait for the last phase armed on every full barrier, so no
-    // copy is still landing in shared memory when the CTA exits.
-    auto drain = [&](int first, int slots, uint32_t count) {
+  if (!ok) {
+    // Drain: wait for the last phase armed on every full barrier of this
+    // thread's streams, so that no copy is still landing when the CTA exits.
+    auto drain = [&](int full, int slots, uint32_t count) {
       for (int s = 0; s < slots; ++s) {
         if (count > (uint32_t)s) {
           const uint32_t uses = (count - 1u - (uint32_t)s) / (uint32_t)slots + 1u;
-          wait_drain(bar(first + s), (uses - 1u) & 1u);
+          wait_drain(bar(full + s), (uses - 1u) & 1u);
         }
       }
     };
-    drain(C::B_QFULL, C::QS, qc);
-    drain(C::B_KFULL, C::KS, kc);
-    drain(C::B_VFULL, C::VS, vc);
+    drain(FULL, C::P, c);
+    if (KQ) drain(C::B_QFULL, C::QS, qc);
   }
 }
 
+// QK issuer (one thread): S_j = Q K^T for every key-block step, up to P
+// steps ahead of the PV issuer.  Before overwriting S buffer j it waits for
+// the PV products that last read it to complete (S-free, committed by the
+// PV issuer).
 template <int D>
-__device__ void role_mma(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w, int lane) {
+__device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
   using C = Cfg<D>;
+  constexpr int P = C::P;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   constexpr uint32_t IDESC_QK = make_idesc(kBM, kBN, 0);
-  constexpr uint32_t IDESC_PV = make_idesc(kBM, D, 1);
-  uint32_t qc = 0, kc = 0, vc = 0, tc = 0;
+  constexpr int QK_STEPS = D / 16;
+  constexpr int STEPS_PER_CHUNK = C::CHUNK / 16;
+  const uint64_t q_desc0 = smem_desc(base + C::Q_OFF, 16, C::ATOMB, C::LAYOUT);
+  const uint64_t k_desc0 = smem_desc(base + C::K_OFF, 16, C::ATOMB, C::LAYOUT);
   bool ok = true;
   // Test hook: wait on a barrier that nothing arrives on, so that the
   // bounded wait runs out and the whole CTA takes its give-up path.
-  if (a.debug_flags & kDebugUnsignalledWait)
-    ok = wait_warp(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
+  if (a.debug_flags & kDebugUnsignalledWait) ok = wait_one(bar(C::B_DRAIN), 1u ^ 1u, w, kSiteUnsignalled);
+  Cursor cur;
+  cur.start(a);
 
-  for (int it = 0; ok; ++it) {
-    const int idx = item_index(it, blockIdx.x, gridDim.x);
-    if (idx >= a.n_items) break;
-    const Item item = __ldg(&a.items[idx]);
-    const int n = item.y, qt = item.w;
-    const int qs = (int)(qc % C::QS);
-    const int ob = it & 1;
-    const uint32_t o_tmem = tmem + C::O_COL + (uint32_t)(ob * D);
-    if (!(ok = wait_warp(bar(C::B_QFULL + qs), (qc / C::QS) & 1u, w, kSiteQFull))) break;
-    const uint32_t q_addr = base + C::Q_OFF + qs * C::TILEB;
-
-    // PV of one block: waits for its P, for the O buffer (first block), for V.
-    auto issue_pv = [&](uint32_t ptc, int pkt, uint32_t pvc) -> bool {
-      const int pb = (int)(ptc & 1u);
-      if (!wait_warp(bar(C::B_PFULL + pb), (ptc >> 1) & 1u, w, kSitePFull)) return false;
-      if (pkt == 0 &&
-          !wait_warp(bar(C::B_OEMPTY + ob), ((uint32_t)(it >> 1) & 1u) ^ 1u, w, kSiteOEmpty))
-        return false;
-      const int vs = (int)(pvc % C::VS);
-      if (!wait_warp(bar(C::B_VFULL + vs), (pvc / C::VS) & 1u, w, kSiteVFull)) return false;
-      const uint32_t v_addr = base + C::V_OFF + vs * C::TILEB;
-      const int r_end = n - kBM * qt;
-      if (pkt == qt && r_end < kBN) {
-        // Keys past the end of the sequence: zero their V rows so that the
-        // zero P entries never meet non-finite values of the next sequence.
-        const int n16 = (kBN - r_end) * C::ROWB / 16;
+  auto step = [&](auto jc) -> bool {
+    constexpr int J = decltype(jc)::value;
+    const int qs = cur.it % C::QS;
+    const uint32_t use = cur.tc / P;
+    if (cur.kt == 0 &&
+        !wait_one(bar(C::B_QFULL + qs), (uint32_t)(cur.it / C::QS) & 1u, w, kSiteQFull))
+      return false;
+    if (!wait_one(bar(C::B_KFULL + J), use & 1u, w, kSiteKFull)) return false;
+    trace(a, kEvMmaKReady, cur.tc);
+    if (!wait_one(bar(C::B_SFREE + J), (use & 1u) ^ 1u, w, kSiteSFree)) return false;
+    tc_fence_after();
+    trace(a, kEvQkIssue, cur.tc);
+    const int cols = cur.b.cols(cur.kt);
+    const uint32_t s_tmem = tmem + (uint32_t)(J * 128);
+    auto body = [&](auto qsc, uint32_t idesc) {
+      constexpr int QSL = decltype(qsc)::value;
 #pragma unroll
-        for (int ch = 0; ch < C::NCHUNK; ++ch) {
-          const uint32_t z0 = v_addr + ch * C::CHUNKB + r_end * C::ROWB;
-          for (int i = lane; i < n16; i += 32)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(z0 + 16 * i), "r"(0)
-                         : "memory");
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
+      for (int kk = 0; kk < QK_STEPS; ++kk) {
+        const uint32_t off = (kk / STEPS_PER_CHUNK) * C::CHUNKB + (kk % STEPS_PER_CHUNK) * 32;
+        const uint64_t qd = q_desc0 + (uint64_t)((QSL * C::TILEB + off) >> 4);
+        const uint64_t kd = k_desc0 + (uint64_t)((J * C::TILEB + off) >> 4);
+        if (kk == 0)
+          mma_ss_c<0>(s_tmem, qd, kd, idesc);
+        else
+          mma_ss_c<1>(s_tmem, qd, kd, idesc);
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t p_tmem = tmem + (uint32_t)(pb * 128);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bdesc =
-              smem_desc(v_addr + kk * 2 * C::ATOMB, C::CHUNKB, C::ATOMB, C::LAYOUT);
-          const uint32_t col = 32u * (kk >> 1) + 8u * (kk & 1);
-          mma_ts(o_tmem, p_tmem + col, bdesc, IDESC_PV, (pkt > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bdesc =
-              smem_desc(v_addr + kk * 2 * C::ATOMB, C::CHUNKB, C::ATOMB, C::LAYOUT);
-          const uint32_t col = 32u * (kk >> 1) + 16u + 8u * (kk & 1);
-          mma_ts(o_tmem, p_tmem + col, bdesc, IDESC_PV, 1u);
-        }
-        mma_commit(bar(C::B_VEMPTY + vs));
-      }
-      __syncwarp();
-      return true;
     };
-
-    uint32_t prev_tc = 0, prev_vc = 0;
-    int prev_kt = -1;
-    for (int kt = 0; kt <= qt; ++kt) {
-      const int ks = (int)(kc % C::KS);
-      const int b = (int)(tc & 1u);
-      if (!(ok = wait_warp(bar(C::B_KFULL + ks), (kc / C::KS) & 1u, w, kSiteKFull))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t k_addr = base + C::K_OFF + ks * C::TILEB;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / (C::CHUNK / 16)) * C::CHUNKB + (kk % (C::CHUNK / 16)) * 32;
-          const uint64_t adesc = smem_desc(q_addr + off, 16, C::ATOMB, C::LAYOUT);
-          const uint64_t bdesc = smem_desc(k_addr + off, 16, C::ATOMB, C::LAYOUT);
-          mma_ss(tmem + (uint32_t)(b * 128), adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::B_SFULL + b));
-        mma_commit(bar(C::B_KEMPTY + ks));
-        if (kt == qt) mma_commit(bar(C::B_QEMPTY + qs));
-      }
-      __syncwarp();
-      ++kc;
-      if (prev_kt >= 0 && !(ok = issue_pv(prev_tc, prev_kt, prev_vc))) break;
-      prev_tc = tc;
-      prev_kt = kt;
-      prev_vc = vc;
-      ++tc;
-      ++vc;
-    }
-    if (!ok) break;
-    ++qc;
-    if (!(ok = issue_pv(prev_tc, prev_kt, prev_vc))) break;
-    if (lane == 0) mma_commit(bar(C::B_OFULL + ob));
-    __syncwarp();
+    const uint32_t idesc = cols == kBN ? IDESC_QK : make_idesc(kBM, cols, 0);
+    if (qs == 0)
+      body(std::integral_constant<int, 0>{}, idesc);
+    else
+      body(std::integral_constant<int, 1 % C::QS>{}, idesc);
+    mma_commit(bar(C::B_SFULL + J));
+    mma_commit(bar(C::B_KEMPTY + J));
+    if (cur.kt == cur.b.qt) mma_commit(bar(C::B_QEMPTY + qs));
+    trace(a, kEvMmaQkDone, cur.tc);
+    cur.advance(a);
+    return true;
+  };
+  while (ok && cur.valid) {
+    if (!(ok = step(std::integral_constant<int, 0>{})) || !cur.valid) break;
+    if (!(ok = step(std::integral_constant<int, 1 % P>{})) || !cur.valid) break;
+    if (P > 2 && (!(ok = step(std::integral_constant<int, 2 % P>{})) || !cur.valid)) break;
   }
   if (!ok) {
     // Drain: a commit arrives once every MMA issued before it has finished.
-    if (lane == 0) mma_commit(bar(C::B_DRAIN));
-    __syncwarp();
-    if (lane == 0) wait_drain(bar(C::B_DRAIN), 0);
-    __syncwarp();
+    mma_commit(bar(C::B_DRAIN));
+    wait_drain(bar(C::B_DRAIN), 0);
   }
 }
 
+// PV issuer (one thread): O += P_hi V + P_lo V for every key-block step, as
+// soon as the SiLU warps have written P.  Commits V-empty and S-free (the
+// S buffer may be overwritten) when the products complete, and O-full after
+// an item's last block.
+template <int D>
+__device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
+  using C = Cfg<D>;
+  constexpr int P = C::P;
+  const uint32_t bars = base + C::BAR_OFF;
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+  constexpr uint32_t IDESC_PV = make_idesc(kBM, D, 1);
+  const uint64_t v_desc0 = smem_desc(base + C::V_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
+  bool ok = true;
+  Cursor cur;
+  cur.start(a);
+
+  auto step = [&](auto jc) -> bool {
+    constexpr int J = decltype(jc)::value;
+    const uint32_t use = cur.tc / P;
+    const int ob = cur.it % C::OB;
+    if (!wait_one(bar(C::B_PFULL + J), use & 1u, w, kSitePFull)) return false;
+    trace(a, kEvMmaPReady, cur.tc);
+    if (cur.kt == 0 &&
+        !wait_one(bar(C::B_OEMPTY + ob), ((uint32_t)(cur.it / C::OB) & 1u) ^ 1u, w, kSiteOEmpty))
+      return false;
+    if (!wait_one(bar(C::B_VFULL + J), use & 1u, w, kSiteVFull)) return false;
+    const int cols = cur.b.cols(cur.kt);
+    const int r_end = cur.b.n - kBN * cur.kt;
+    if (cur.kt == cur.b.qt && r_end < cols) {
+      // Keys in [n, cols) lie past the end of the sequence: zero their V
+      // rows so that the zero P entries never meet non-finite values of the
+      // next sequence.
+      const uint32_t v_addr = base + C::V_OFF + J * C::TILEB;
+#pragma unroll
+      for (int ch = 0; ch < C::NCHUNK; ++ch) {
+        const uint32_t z0 = v_addr + ch * C::CHUNKB + r_end * C::ROWB;
+        const uint32_t z1 = v_addr + ch * C::CHUNKB + cols * C::ROWB;
+        for (uint32_t z = z0; z < z1; z += 16)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(z), "r"(0) : "memory");
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    tc_fence_after();
+    trace(a, kEvPvIssue, cur.tc);
+    const uint32_t p_tmem = tmem + (uint32_t)(J * 128);
+    const uint64_t vd0 = v_desc0 + (uint64_t)((J * C::TILEB) >> 4);
+    const int ksteps = cols / 16;
+    const bool first = cur.kt == 0;
+    auto body = [&](auto obc) {
+      constexpr int OBL = decltype(obc)::value;
+      const uint32_t o_tmem = tmem + C::O_COL + (uint32_t)(OBL * D);
+      if (ksteps == kBN / 16 && !first) {
+        // full block continuing an accumulation: branch-free, constant operands
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_c<1>(o_tmem, p_tmem + 32u * (kk >> 1) + 8u * (kk & 1),
+                      vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4), IDESC_PV);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_c<1>(o_tmem, p_tmem + 32u * (kk >> 1) + 16u + 8u * (kk & 1),
+                      vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4), IDESC_PV);
+      } else {
+        for (int kk = 0; kk < ksteps; ++kk) {
+          const uint64_t bd = vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4);
+          const uint32_t a_hi = p_tmem + 32u * (kk >> 1) + 8u * (kk & 1);
+          if (kk == 0 && first)
+            mma_ts_c<0>(o_tmem, a_hi, bd, IDESC_PV);
+          else
+            mma_ts_c<1>(o_tmem, a_hi, bd, IDESC_PV);
+        }
+        for (int kk = 0; kk < ksteps; ++kk)
+          mma_ts_c<1>(o_tmem, p_tmem + 32u * (kk >> 1) + 16u + 8u * (kk & 1),
+                      vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4), IDESC_PV);
+      }
+    };
+    if (ob == 0)
+      body(std::integral_constant<int, 0>{});
+    else
+      body(std::integral_constant<int, 1 % C::OB>{});
+    mma_commit(bar(C::B_VEMPTY + J));
+    mma_commit(bar(C::B_SFREE + J));
+    if (cur.kt == cur.b.qt) mma_commit(bar(C::B_OFULL + ob));
+    trace(a, kEvMmaPvDone, cur.tc);
+    cur.advance(a);
+    return true;
+  };
+  while (ok && cur.valid) {
+    if (!(ok = step(std::integral_constant<int, 0>{})) || !cur.valid) break;
+    if (!(ok = step(std::integral_constant<int, 1 % P>{})) || !cur.valid) break;
+    if (P > 2 && (!(ok = step(std::integral_constant<int, 2 % P>{})) || !cur.valid)) break;
+  }
+  if (!ok) {
+    mma_commit(bar(C::B_DRAIN + 1));
+    wait_drain(bar(C::B_DRAIN + 1), 0);
+  }
+}
+
+// silu of 32 scores of one row (two per step, packed fp32x2 arithmetic),
+// split into bf16 hi and lo halves.  MASK: zero the keys j > lim.
+template <bool MASK>
+__device__ __forceinline__ void silu_split32(const uint32_t (&s)[32], float2 ha2, int lim,
+                                             uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const float2 h = __fmul2_rn(make_float2(__uint_as_float(s[2 * m]), __uint_as_float(s[2 * m + 1])),
+                                ha2);
+    float2 p = __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+    if (MASK) {
+      p.x = (2 * m > lim) ? 0.0f : p.x;
+      p.y = (2 * m + 1 > lim) ? 0.0f : p.y;
+    }
+    const uint32_t ph = pack_bf16x2(p.x, p.y);
+    const float2 r = __fadd2_rn(
+        p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
+    hi[m] = ph;
+    lo[m] = pack_bf16x2(r.x, r.y);
+  }
+}
+
+// SiLU warpgroups (warps 8-11 and 12-15): warpgroup e takes the steps with
+// tc % 2 == e.  Thread r owns score row r of the block.
 template <int D>
 __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w, int warp,
                           int lane) {
   using C = Cfg<D>;
+  constexpr int P = C::P;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-  const int e = (warp - kEwWarp0) >> 2;  // which S buffer this warpgroup owns
+  const int e = (warp - kEwWarp0) >> 2;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
-  const uint32_t t_s = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(e * 128);
-  const float ha = a.half_alpha;
-  uint32_t tc = 0, mine = 0;
-  for (int it = 0;; ++it) {
-    const int idx = item_index(it, blockIdx.x, gridDim.x);
-    if (idx >= a.n_items) break;
-    const int qt = __ldg(&a.items[idx].w);
-    for (int kt = 0; kt <= qt; ++kt, ++tc) {
-      if ((int)(tc & 1u) != e) continue;
-      if (!wait_warp(bar(C::B_SFULL + e), mine & 1u, w, kSiteSFull)) return;
-      tc_fence_after();
-      const bool diag = kt == qt;
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  const float2 ha2 = make_float2(a.half_alpha, a.half_alpha);
+  Cursor cur;
+  cur.start(a);
+  while (cur.valid) {
+    if ((int)(cur.tc & 1u) != e) {
+      cur.advance(a);
+      continue;
+    }
+    const int j = (int)(cur.tc % P);
+    if (!wait_warp(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull)) return;
+    tc_fence_after();
+    trace(a, kEvSiluStart, cur.tc);
+    const uint32_t t_s = lane_base + (uint32_t)(j * 128);
+    const bool diag = cur.kt == cur.b.qt;
+    const int cols = cur.b.cols(cur.kt);
+    // Rows past the sequence end are never stored: a warp whose 32 rows all
+    // lie there skips its work.
+    if (quarter * 32 < cur.b.rows()) {
+      if (!diag) {
+        uint32_t s0[32], s1[32];
+        tmem_ld32_async(t_s, s0);
+        tmem_wait_ld(s0);
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t s[32];
-        tmem_ld32(t_s + 32u * c, s);
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float h0 = __uint_as_float(s[2 * m]) * ha;
-          const float h1 = __uint_as_float(s[2 * m + 1]) * ha;
-          float p0 = fmaf(h0, tanh_approx(h0), h0);
-          float p1 = fmaf(h1, tanh_approx(h1), h1);
-          if (diag) {
-            const int j = 32 * c + 2 * m;
-            p0 = (j > row) ? 0.0f : p0;
-            p1 = (j + 1 > row) ? 0.0f : p1;
-          }
-          const uint32_t ph = pack_bf16x2(p0, p1);
-          const float r0 = p0 - __uint_as_float(ph << 16);
-          const float r1 = p1 - __uint_as_float(ph & 0xFFFF0000u);
-          hi[m] = ph;
-          lo[m] = pack_bf16x2(r0, r1);
+        for (int c = 0; c < kBN / 32; c += 2) {
+          uint32_t hi[16], lo[16];
+          tmem_ld32_async(t_s + 32u * (c + 1), s1);
+          silu_split32<false>(s0, ha2, 0, hi, lo);
+          tmem_st16(t_s + 32u * c, hi);
+          tmem_st16(t_s + 32u * c + 16u, lo);
+          tmem_wait_ld(s1);
+          if (c + 2 < kBN / 32) tmem_ld32_async(t_s + 32u * (c + 2), s0);
+          silu_split32<false>(s1, ha2, 0, hi, lo);
+          tmem_st16(t_s + 32u * (c + 1), hi);
+          tmem_st16(t_s + 32u * (c + 1) + 16u, lo);
+          if (c + 2 < kBN / 32) tmem_wait_ld(s0);
         }
-        tmem_st16(t_s + 32u * c, hi);
-        tmem_st16(t_s + 32u * c + 16u, lo);
+      } else {
+        // diagonal block: keep keys j <= row; chunks c > quarter lie wholly
+        // above the diagonal for this warp (zeros); columns >= cols are not
+        // read by the PV products.
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32 && 32 * c < cols; ++c) {
+          uint32_t hi[16], lo[16];
+          if (c > quarter) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
+          } else {
+            uint32_t sv[32];
+            tmem_ld32(t_s + 32u * c, sv);
+            silu_split32<true>(sv, ha2, row - 32 * c, hi, lo);
+          }
+          tmem_st16(t_s + 32u * c, hi);
+          tmem_st16(t_s + 32u * c + 16u, lo);
+        }
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_PFULL + e));
-      ++mine;
     }
+    tc_fence_before();
+    __syncwarp();
+    trace(a, kEvSiluEnd, cur.tc);
+    if (lane == 0) mbar_arrive(bar(C::B_PFULL + j));
+    cur.advance(a);
   }
 }
 
+// Epilogue warpgroup (warps 0-3): O -> x inv_n -> bf16 -> 16-byte stores of
+// the valid rows.
 template <int D>
 __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w,
                               int warp, int lane) {
@@ -540,14 +794,12 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
   const float inv_n = a.inv_n;
   uint16_t* out = static_cast<uint16_t*>(a.out);
-  for (int it = 0;; ++it) {
-    const int idx = item_index(it, blockIdx.x, gridDim.x);
-    if (idx >= a.n_items) break;
-    const Item item = __ldg(&a.items[idx]);
-    const int s0 = item.x, n = item.y, h = item.z, qt = item.w;
-    const int ob = it & 1;
-    if (!wait_warp(bar(C::B_OFULL + ob), (uint32_t)(it >> 1) & 1u, w, kSiteOFull)) return;
+  Block b;
+  for (int it = 0; load_block(a, it, b); ++it) {
+    const int ob = it % C::OB;
+    if (!wait_warp(bar(C::B_OFULL + ob), (uint32_t)(it / C::OB) & 1u, w, kSiteOFull)) return;
     tc_fence_after();
+    trace(a, kEvEpiStart, (unsigned)it);
     uint32_t packed[D / 2];
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -559,15 +811,16 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
                                          __uint_as_float(o[2 * m + 1]) * inv_n);
     }
     tc_fence_before();
-    mbar_arrive(bar(C::B_OEMPTY + ob));
-    const int r_valid = n - kBM * qt;
-    if (row < r_valid) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + ob));
+    if (row < b.rows()) {
       uint4* dst = reinterpret_cast<uint4*>(
-          out + ((size_t)(s0 + kBM * qt + row) * (size_t)a.heads + (size_t)h) * D);
+          out + ((size_t)(b.s0 + kBM * b.qt + row) * (size_t)a.heads + (size_t)b.h) * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c)
         dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
     }
+    trace(a, kEvEpiEnd, (unsigned)it);
   }
 }
 
@@ -587,20 +840,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBARS; ++i) {
-      const bool many = (i == C::B_PFULL || i == C::B_PFULL + 1 || i == C::B_OEMPTY ||
-                         i == C::B_OEMPTY + 1);
-      mbar_init(bars + 8u * i, many ? 128u : 1u);
+      // P-full and O-empty: one arrival per warp of the arriving warpgroup
+      const bool many = (i >= C::B_PFULL && i < C::B_PFULL + C::P) ||
+                        (i >= C::B_OEMPTY && i < C::B_OEMPTY + C::OB);
+      mbar_init(bars + 8u * i, many ? 4u : 1u);
     }
     *abort_flag = 0;
+    for (int i = 0; i < kTraceWarps; ++i) trace_counters()[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == kTmaWarp && lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+  if (lane == 0 && (warp == kTmaWarpK || warp == kTmaWarpV)) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == kTmaWarpK ? &tm_k : &tm_v))
+                 : "memory");
+    if (warp == kTmaWarpK)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarpQK) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -613,10 +869,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx w{a.timeout_ns, abort_flag};
 
-  if (warp == kTmaWarp) {
-    role_producer<D>(&tm_q, &tm_k, &tm_v, a, base, w, lane);
-  } else if (warp == kMmaWarp) {
-    role_mma<D>(a, base, tmem, w, lane);
+  if (warp == kTmaWarpK) {
+    if (lane == 0) role_producer<D, true>(&tm_k, &tm_q, a, base, w);
+    __syncwarp();
+  } else if (warp == kTmaWarpV) {
+    if (lane == 0) role_producer<D, false>(&tm_v, &tm_q, a, base, w);
+    __syncwarp();
+  } else if (warp == kMmaWarpQK) {
+    if (lane == 0) role_mma_qk<D>(a, base, tmem, w);
+    __syncwarp();
+  } else if (warp == kMmaWarpPV) {
+    if (lane == 0) role_mma_pv<D>(a, base, tmem, w);
+    __syncwarp();
   } else if (warp >= kEwWarp0) {
     role_silu<D>(a, base, tmem, w, warp, lane);
   } else if (warp < kEpiWarp0 + 4) {
@@ -625,7 +889,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if ((a.debug_flags & kDebugTrace) && blockIdx.x == 0 && threadIdx.x < kTraceWarps)
+    g_trace_n[threadIdx.x] = trace_counters()[threadIdx.x];
+  if (warp == kMmaWarpQK) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -637,13 +903,9 @@ template <int D>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdArgs& a, int grid, cudaStream_t stream) {
   using C = Cfg<D>;
-  static bool configured = false;  // per process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_LAUNCH);
+  if (e != cudaSuccess) return e;
   hstu_fwd_kernel<D><<<grid, kFwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
@@ -669,6 +931,27 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
     case 128: return launch_d<128>(tq, tk, tv, a, grid, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t read_and_clear_trace(unsigned long long* dst, int capacity, int* n) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  unsigned cnt[kTraceWarps];
+  if ((e = cudaMemcpyFromSymbol(cnt, g_trace_n, sizeof(cnt))) != cudaSuccess) return e;
+  static unsigned long long buf[kTraceWarps * kTracePerWarp * 2];
+  if ((e = cudaMemcpyFromSymbol(buf, g_trace, sizeof(buf))) != cudaSuccess) return e;
+  int k = 0;
+  for (int wp = 0; wp < kTraceWarps; ++wp)
+    for (unsigned i = 0; i < cnt[wp] && i < (unsigned)kTracePerWarp; ++i) {
+      if (k < capacity && dst) {
+        dst[2 * k] = buf[2 * ((size_t)wp * kTracePerWarp + i)];
+        dst[2 * k + 1] = buf[2 * ((size_t)wp * kTracePerWarp + i) + 1];
+      }
+      ++k;
+    }
+  *n = k < capacity ? k : capacity;
+  const unsigned zero[kTraceWarps] = {};
+  return cudaMemcpyToSymbol(g_trace_n, zero, sizeof(zero));
 }
 
 cudaError_t read_and_clear_device_status(unsigned* status, unsigned* site) {

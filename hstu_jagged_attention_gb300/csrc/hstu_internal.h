@@ -13,6 +13,11 @@ namespace hstu {
 //   w = query block index qt (rows x + 128*qt ...).  Key blocks 0..qt.
 using Item = int4;
 
+// Work list (host): number of items, and the items in scheduling order
+// (qt descending, then sequence, head, qt ascending).
+long long count_items(const int32_t* off, int batch, int heads);
+void fill_items(const int32_t* off, int batch, int heads, Item* dst);
+
 struct FwdArgs {
   const Item* items;   // device, n_items entries, longest first
   int n_items;
@@ -26,6 +31,12 @@ struct FwdArgs {
 
 // Test hook: the MMA warp first waits on a barrier nothing signals.
 constexpr unsigned kDebugUnsignalledWait = 1u;
+// Tracing: CTA 0 records a clock64 stamp per pipeline event (see
+// read_and_clear_trace).
+constexpr unsigned kDebugTrace = 2u;
+
+// Trace records: {clock64, (event << 48) | (warp << 40) | index}.
+cudaError_t read_and_clear_trace(unsigned long long* dst, int capacity, int* n);
 
 // Shared-memory bytes and grid the d-specialised kernel needs.
 int fwd_smem_bytes(int d);

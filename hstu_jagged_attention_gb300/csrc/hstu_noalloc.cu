@@ -43,25 +43,6 @@ int items_address(hstu::Item** out) {
   return HSTU_OK;
 }
 
-// Longest-first items into g_host_items (the same order as the plan's list).
-// Returns the count, or -1 if it would exceed kMaxItems.
-long long fill_items(const int32_t* off, int batch, int heads) {
-  int max_tiles = 0;
-  long long count = 0;
-  for (int b = 0; b < batch; ++b) {
-    const int tiles = (off[b + 1] - off[b] + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
-    if (tiles > max_tiles) max_tiles = tiles;
-    count += (long long)tiles * heads;
-  }
-  if (count > kMaxItems) return -1;
-  long long i = 0;
-  for (int qt = max_tiles - 1; qt >= 0; --qt)
-    for (int b = 0; b < batch; ++b)
-      if ((off[b + 1] - off[b] + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M > qt)
-        for (int h = 0; h < heads; ++h) g_host_items[i++] = make_int4(off[b], off[b + 1] - off[b], h, qt);
-  return count;
-}
-
 }  // namespace
 
 extern "C" int hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v,
@@ -84,9 +65,10 @@ extern "C" int hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v
   std::lock_guard<std::mutex> lk(g_mu);
   hstu::Item* d_items = nullptr;
   if ((rc = items_address(&d_items)) != HSTU_OK) return rc;
-  const long long n = fill_items(offsets, batch, heads);
-  if (n < 0) return HSTU_ERR_CAPACITY;
+  const long long n = hstu::count_items(offsets, batch, heads);
+  if (n > kMaxItems) return HSTU_ERR_CAPACITY;
   if (n == 0) return HSTU_OK;
+  hstu::fill_items(offsets, batch, heads, g_host_items);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(d_items, g_host_items, (size_t)n * sizeof(hstu::Item), cudaMemcpyHostToDevice,
                       s) != cudaSuccess)

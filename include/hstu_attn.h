@@ -231,7 +231,26 @@ int hstu_set_wait_timeout_ns(uint64_t ns);
  * Errors: HSTU_ERR_INVALID_ARG for unknown bits.
  */
 #define HSTU_DEBUG_UNSIGNALLED_WAIT 1u
+#define HSTU_DEBUG_TRACE 2u
 int hstu_set_debug_flags(uint32_t flags);
+
+/*
+ * hstu_trace_read -- the pipeline trace of the last kernels launched with
+ * HSTU_DEBUG_TRACE set (read and cleared; synchronises the device).
+ *
+ * With the flag set, the first CTA of each launch records one event per
+ * pipeline step from lane 0 of the warp taking it: TMA loads issued (Q, K,
+ * V), QK and PV products issued, SiLU start/end of each block, epilogue
+ * start/end of each item.  Event i occupies dst[2i] = clock64 of the SM and
+ * dst[2i+1] = (event code << 48) | (warp << 40) | index, index being the
+ * running block, ring or item counter of that role.  Event codes: 1 QK
+ * issue starts, 2 PV issue starts, 3 SiLU start, 4 SiLU end, 5 epilogue
+ * start, 6 epilogue end, 7 K load, 8 V load, 9 Q load, 10 K block present
+ * at the MMA warp, 11 QK issued, 12 P present at the MMA warp, 13 PV
+ * issued.  Up to 2048 events per warp are kept, grouped by warp;
+ * `capacity` counts events (dst holds 2*capacity words).
+ */
+int hstu_trace_read(uint64_t* dst, int capacity, int* n_events);
 
 /* Static description of a status code. */
 const char* hstu_status_string(int status);
