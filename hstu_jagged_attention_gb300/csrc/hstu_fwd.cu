@@ -10,36 +10,36 @@
 //
 // Design (one persistent CTA per SM, 16 warps, warp-specialised).  A work
 // item is one 128-row query block of one (sequence, head); it walks the key
-// blocks 0..qt.
-//   warp 4        TMA producer (one thread): each item's Q block, then its K
-//                 blocks, into shared-memory rings (128B-swizzled tiles).
-//   warp 6        TMA producer (one thread): V blocks.  (One thread's bulk
-//                 copies are processed one box at a time, so the streams get
-//                 separate issuers.)
-//   warp 5        QK issuer (one thread, owns TMEM): S_j = Q K^T
-//                 (tcgen05.mma kind::f16, fp32 accumulate) into TMEM S
-//                 buffer j = step mod P, up to P steps ahead.
+// blocks 0..qt.  Step t is the t-th key block the CTA processes.
+//   warp 4        K producer (one thread): each item's Q block, then its K
+//                 blocks, by bulk-tensor copies into 128B-swizzled
+//                 shared-memory rings.
+//   warp 6        V producer (one thread): V blocks into their own ring.
+//   warp 5        QK issuer (one thread, owns TMEM): S = Q K^T
+//                 (tcgen05.mma kind::f16, fp32 accumulate) of step t into
+//                 TMEM S buffer t mod 3, up to three steps ahead of PV.
+//   warps 8-15    two "SiLU" warpgroups; warpgroup e takes key columns
+//                 [64e, 64e+64) of every block, so both finish a block
+//                 together.  Thread r owns score row r: tcgen05.ld S,
+//                 p = h + h tanh(h) with h = alpha s / 2
+//                 (= alpha s sigmoid(alpha s)), tril select on the diagonal
+//                 block, split p = bf16(p) + bf16(p - bf16(p)), tcgen05.st
+//                 both halves over the S columns just read.
 //   warp 7        PV issuer (one thread): O += P_hi V + P_lo V with P read
-//                 from TMEM, as soon as the SiLU warps have written P.
-//   warps 8-15    two "SiLU" warpgroups taking alternate steps.  Thread r
-//                 owns score row r: tcgen05.ld S (the next 32 columns load
-//                 while the current ones are computed), p = h + h tanh(h)
-//                 with h = alpha s / 2 (= alpha s sigmoid(alpha s)), tril
-//                 select on the diagonal block, split
-//                 p = bf16(p) + bf16(p - bf16(p)), tcgen05.st both halves over
-//                 the S columns just read.
-//   warps 0-3     epilogue: reads a finished O buffer, scales by inv_n, rounds
-//                 to bf16 and stores the valid rows with 16-byte stores.
+//                 from TMEM, each key half as soon as its warpgroup has
+//                 written it.
+//   warps 0-3     epilogue: reads a finished item's O, scales by inv_n,
+//                 rounds to bf16 and stores the valid rows with 16-byte
+//                 stores.
 // The roles overlap the way the post's three-stage pipeline does (section
-// 5.2): QK of later blocks, SiLU of the current one and PV of earlier ones
-// run at the same time.  The two MMA issuers are separate threads so that
-// neither waits behind the other; S-free barriers (committed by the PV
-// issuer when its products complete) let the QK issuer reuse an S buffer.
+// 5.2): QK of later blocks, SiLU of the current one and PV of an earlier
+// one run at the same time.
 //
-// TMEM columns (512 allocated): P S buffers of 128 columns (P = 3 for
-// d <= 64, 2 for d = 128), then two O buffers of d columns.  P of a block
-// overwrites its own S buffer: for the 32-key chunk c, P_hi key pairs go to
-// columns 32c+[0,16) and P_lo to 32c+[16,32) (two bf16 per 32-bit column).
+// TMEM columns (512 allocated): three S buffers of 128 columns, then the O
+// accumulator (d columns), double-buffered where TMEM has room (d <= 64).
+// P of a block overwrites its own S buffer: for the 32-key chunk c, P_hi
+// key pairs go to columns 32c+[0,16) and P_lo to 32c+[16,32) (two bf16 per
+// 32-bit column).
 //
 // The diagonal key block of a sequence's last query block, when the sequence
 // ends inside it, computes only keys < n rounded up to 16: its QK uses
@@ -74,10 +74,10 @@ namespace {
 constexpr int kBM = 128;  // query rows per item == TMEM lanes
 constexpr int kBN = 128;  // keys per K/V block
 constexpr int kEpiWarp0 = 0;
-constexpr int kTmaWarpK = 4;   // Q and K blocks
+constexpr int kTmaWarpK = 4;  // Q and K blocks
 constexpr int kMmaWarpQK = 5;  // QK products; owns TMEM
-constexpr int kTmaWarpV = 6;   // V blocks
 constexpr int kMmaWarpPV = 7;  // PV products
+constexpr int kTmaWarpV = 6;  // V blocks
 constexpr int kEwWarp0 = 8;
 constexpr uint32_t kTmemCols = 512;
 
@@ -123,6 +123,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of a phase: the result is consumed later, so its latency
+// overlaps whatever the thread issues in between.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -203,6 +217,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
                                               uint64_t layout) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+}
+
+// The value of x, materialised in a register at this point and hidden from
+// the optimiser.  A burst of tcgen05.mma issues at about half the rate when
+// its operands are computed between the instructions (measured on GB300:
+// ~104 against ~50 cycles per M=128 N=64 product), so every operand of a
+// burst is pinned before its first product.
+__device__ __forceinline__ uint64_t pin64(uint64_t x) {
+  asm volatile("mov.b64 %0, %0;" : "+l"(x));
+  return x;
+}
+__device__ __forceinline__ uint32_t pin32(uint32_t x) {
+  asm volatile("mov.b32 %0, %0;" : "+r"(x));
+  return x;
 }
 
 // tcgen05.mma kind::f16, M = 128, with enable-input-d fixed at compile time
@@ -293,6 +321,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -366,30 +401,30 @@ struct Cfg {
   static constexpr int ATOMB = 8 * ROWB;          // 8-row swizzle atom
   static constexpr int CHUNKB = kBM * ROWB;       // 128 rows of one chunk
   static constexpr int TILEB = kBM * D * 2;       // one 128 x D bf16 block
-  // The K ring, the V ring and the S buffers in TMEM share the period P:
-  // each MMA thread's loop, unrolled by P, sees every slot as a
-  // compile-time constant (addresses are a loop-invariant base plus
-  // constants).
-  static constexpr int P = D == 128 ? 2 : 3;
-  static constexpr int QS = 2;                    // Q slots
-  static constexpr int OB = 2;                    // O buffers in TMEM
+  // S buffers in TMEM, K-ring and V-ring slots all have the period P, so
+  // that "QK of step t done" frees K slot t mod P and "PV of step t done"
+  // frees V slot t mod P: the MMA issuer's loop, unrolled by P, sees every
+  // buffer and slot as a compile-time constant.
+  static constexpr int P = 3;
+  static constexpr int QS = D == 128 ? 1 : 2;  // Q slots (d = 128: shared memory is full)
+  // O accumulators (d columns each): double-buffered when TMEM has room.
+  static constexpr int OB = 128 * P + 2 * D <= (int)kTmemCols ? 2 : 1;
   static constexpr uint64_t LAYOUT = ROWB == 128 ? 2 : 4;  // descriptor layout: 128B / 64B swizzle
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + QS * TILEB;
   static constexpr int V_OFF = K_OFF + P * TILEB;
   static constexpr int BAR_OFF = V_OFF + P * TILEB;
   static constexpr int B_QFULL = 0;
-  static constexpr int B_QEMPTY = B_QFULL + QS;
-  static constexpr int B_KFULL = B_QEMPTY + QS;
-  static constexpr int B_KEMPTY = B_KFULL + P;
-  static constexpr int B_VFULL = B_KEMPTY + P;
-  static constexpr int B_VEMPTY = B_VFULL + P;
-  static constexpr int B_SFULL = B_VEMPTY + P;   // S of block written (QK done)
-  static constexpr int B_PFULL = B_SFULL + P;    // P of block written (SiLU done)
-  static constexpr int B_SFREE = B_PFULL + P;    // PV of block done: S buffer reusable
-  static constexpr int B_OFULL = B_SFREE + P;
+  static constexpr int B_QEMPTY = B_QFULL + QS;    // an item's last QK done: Q slot free
+  // QK-ready j, phase k: K of step t = P k + j landed and PV(t - P), which
+  // read P from S buffer j, done (for k = 0 an arrival at set-up stands in).
+  static constexpr int B_QKREADY = B_QEMPTY + QS;
+  static constexpr int B_VFULL = B_QKREADY + P;
+  static constexpr int B_SFULL = B_VFULL + P;      // QK done: S written, K slot free
+  static constexpr int B_PFULL = B_SFULL + P;      // [2][P]: warpgroup e wrote P of key half e
+  static constexpr int B_OFULL = B_PFULL + 2 * P;  // an item's last PV done
   static constexpr int B_OEMPTY = B_OFULL + OB;
-  static constexpr int B_DRAIN = B_OEMPTY + OB;  // [2]: QK and PV threads' drains
+  static constexpr int B_DRAIN = B_OEMPTY + OB;  // [2]: the two MMA issuers' drains
   static constexpr int NBARS = B_DRAIN + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
   static constexpr int USED = MISC_OFF + 16;
@@ -401,6 +436,14 @@ struct Cfg {
   static constexpr uint32_t O_COL = 128u * P;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(128 * P + OB * D <= (int)kTmemCols, "TMEM budget");
+  // Arrivals that complete a phase of barrier i: one per warp of a
+  // warpgroup (P-full, O-empty), the K copy's and the PV commit's
+  // (QK-ready), else one.
+  __host__ __device__ static constexpr uint32_t arrivals(int i) {
+    return ((i >= B_PFULL && i < B_PFULL + 2 * P) || (i >= B_OEMPTY && i < B_OEMPTY + OB)) ? 4u
+           : (i >= B_QKREADY && i < B_QKREADY + P)                                       ? 2u
+                                                                                           : 1u;
+  }
 };
 
 // A work item decoded: query block qt of one (sequence, head).
@@ -432,41 +475,78 @@ __device__ __forceinline__ bool load_block(const FwdArgs& a, int it, Block& b) {
 }
 
 // A cursor over the CTA's key-block steps: item `it` (block b) at key block
-// kt; tc counts the steps.
+// kt; tc counts the steps.  The next item's block is fetched one item ahead
+// so that crossing into it does not wait on a global load.
 struct Cursor {
   int it, kt;
   uint32_t tc;
-  Block b;
-  bool valid;
+  Block b, nb;
+  bool valid, nvalid;
   __device__ __forceinline__ void start(const FwdArgs& a) {
     it = 0;
     kt = 0;
     tc = 0;
     valid = load_block(a, 0, b);
+    nvalid = valid && load_block(a, 1, nb);
   }
   __device__ __forceinline__ void advance(const FwdArgs& a) {
     ++tc;
     if (++kt > b.qt) {
       kt = 0;
       ++it;
-      valid = load_block(a, it, b);
+      valid = nvalid;
+      b = nb;
+      nvalid = valid && load_block(a, it + 1, nb);
     }
   }
 };
 
 // ------------------------------------------------------------------ roles
-// TMA producers.  A single thread's bulk-tensor copies are processed one box
-// at a time (about 620 cycles per 16 KB box measured on GB300), so the K
-// (with Q) and V streams have separate issuing threads in separate warps.
+// Runs f(integral_constant<int, I>) for I = 0, 1, ..., U-1, 0, 1, ... until
+// it returns false: the step function of a role sees the step's position in
+// the unroll period as a compile-time constant.
+template <int I, int U, class F>
+__device__ __forceinline__ bool unrolled_steps(F& f) {
+  if constexpr (I == U) {
+    return true;
+  } else {
+    if (!f(std::integral_constant<int, I>{})) return false;
+    return unrolled_steps<I + 1, U>(f);
+  }
+}
+template <int U, class F>
+__device__ __forceinline__ void run_unrolled(F& f) {
+  while (unrolled_steps<0, U>(f)) {
+  }
+}
+
+// Waits after an abort for the last phase armed on each of `slots` full
+// barriers that `count` copies were issued on, so that no copy is still
+// landing when the CTA exits.
+__device__ __forceinline__ void drain_copies(uint32_t full0, int slots, uint32_t count) {
+  for (int s = 0; s < slots; ++s) {
+    if (count > (uint32_t)s) {
+      const uint32_t uses = (count - 1u - (uint32_t)s) / (uint32_t)slots + 1u;
+      wait_drain(full0 + 8u * (uint32_t)s, (uses - 1u) & 1u);
+    }
+  }
+}
+
+// TMA producers (one thread each).  A single thread's bulk-tensor copies
+// are processed one box at a time, so the K stream (with each item's Q
+// block) and the V stream have separate issuing threads in separate warps.
+// K slot t mod P is free once QK(t-P) has completed (S-full); the K copy
+// lands on QK-ready.  V slot t mod P is free once PV(t-P) has completed,
+// which QK-ready of step t includes.  A Q slot is free once the item's last
+// QK has completed (Q-empty).
 template <int D, bool KQ>
 __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, const FwdArgs& a,
                               uint32_t base, const WaitCtx& w) {
   using C = Cfg<D>;
+  constexpr int FULL = KQ ? C::B_QKREADY : C::B_VFULL;
+  constexpr int OFF = KQ ? C::K_OFF : C::V_OFF;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-  constexpr int FULL = KQ ? C::B_KFULL : C::B_VFULL;
-  constexpr int EMPTY = KQ ? C::B_KEMPTY : C::B_VEMPTY;
-  constexpr int OFF = KQ ? C::K_OFF : C::V_OFF;
   uint32_t c = 0, qc = 0;
   bool ok = true;
   Block b;
@@ -484,8 +564,15 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
     }
     for (int kt = 0; kt <= b.qt; ++kt) {
       const int slot = (int)(c % C::P);
-      if (!(ok = wait_one(bar(EMPTY + slot), ((c / C::P) & 1u) ^ 1u, w, KQ ? kSiteKEmpty : kSiteVEmpty)))
-        break;
+      // A parity wait is exact only while the barrier is at most one phase
+      // short of the awaited one.  K(c) waits for phase c/P - 1 of S-full
+      // (its first use passes at once).  V(c) waits for phase c/P of
+      // QK-ready, the first uses included: phase 0 (K landed) must be seen
+      // complete before phase 1 is awaited, or a barrier still in phase 0
+      // would pass the wait for phase 1.
+      ok = KQ ? wait_one(bar(C::B_SFULL + slot), ((c / C::P) & 1u) ^ 1u, w, kSiteKEmpty)
+              : wait_one(bar(C::B_QKREADY + slot), (c / C::P) & 1u, w, kSiteVEmpty);
+      if (!ok) break;
       trace(a, KQ ? kEvLoadK : kEvLoadV, c);
       mbar_arrive_expect_tx(bar(FULL + slot), C::TILEB);
 #pragma unroll
@@ -496,25 +583,22 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
     }
   }
   if (!ok) {
-    // Drain: wait for the last phase armed on every full barrier of this
-    // thread's streams, so that no copy is still landing when the CTA exits.
-    auto drain = [&](int full, int slots, uint32_t count) {
-      for (int s = 0; s < slots; ++s) {
-        if (count > (uint32_t)s) {
-          const uint32_t uses = (count - 1u - (uint32_t)s) / (uint32_t)slots + 1u;
-          wait_drain(bar(full + s), (uses - 1u) & 1u);
-        }
-      }
-    };
-    drain(FULL, C::P, c);
-    if (KQ) drain(C::B_QFULL, C::QS, qc);
+    drain_copies(bar(FULL), C::P, c);
+    if (KQ) drain_copies(bar(C::B_QFULL), C::QS, qc);
   }
 }
 
-// QK issuer (one thread): S_j = Q K^T for every key-block step, up to P
-// steps ahead of the PV issuer.  Before overwriting S buffer j it waits for
-// the PV products that last read it to complete (S-free, committed by the
-// PV issuer).
+// MMA issuers.  A thread's tcgen05.mma returns only when the tensor pipe
+// takes it, so a thread that issues products cannot meanwhile wait on
+// barriers or compute addresses; the QK and PV products therefore come from
+// two threads, each with little work between its products, and every
+// product's operands are pinned in registers before a burst starts.
+//
+// QK issuer (one thread, owns TMEM): S_j = Q K^T of step t into S buffer
+// j = t mod P (P = 3), once K(t) has landed and PV(t-P), which read P from
+// that buffer, has completed (QK-ready); the products of different
+// accumulators are not ordered with respect to each other, so this wait is
+// needed.  It runs up to P steps ahead of the PV issuer.
 template <int D>
 __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
   using C = Cfg<D>;
@@ -529,54 +613,43 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
   bool ok = true;
   // Test hook: wait on a barrier that nothing arrives on, so that the
   // bounded wait runs out and the whole CTA takes its give-up path.
-  if (a.debug_flags & kDebugUnsignalledWait) ok = wait_one(bar(C::B_DRAIN), 1u ^ 1u, w, kSiteUnsignalled);
-  Cursor cur;
-  cur.start(a);
-
+  if (a.debug_flags & kDebugUnsignalledWait) ok = wait_one(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
+  Cursor qc;
+  qc.start(a);
+  uint32_t ph = 0;  // (qc.tc / P) & 1
   auto step = [&](auto jc) -> bool {
     constexpr int J = decltype(jc)::value;
-    const int qs = cur.it % C::QS;
-    const uint32_t use = cur.tc / P;
-    if (cur.kt == 0 &&
-        !wait_one(bar(C::B_QFULL + qs), (uint32_t)(cur.it / C::QS) & 1u, w, kSiteQFull))
+    if (!ok || !qc.valid) return false;
+    const int qs = C::QS == 1 ? 0 : (qc.it & 1);
+    if (qc.kt == 0 &&
+        !(ok = wait_one(bar(C::B_QFULL + qs), (uint32_t)(qc.it / C::QS) & 1u, w, kSiteQFull)))
       return false;
-    if (!wait_one(bar(C::B_KFULL + J), use & 1u, w, kSiteKFull)) return false;
-    trace(a, kEvMmaKReady, cur.tc);
-    if (!wait_one(bar(C::B_SFREE + J), (use & 1u) ^ 1u, w, kSiteSFree)) return false;
+    if (!(ok = wait_one(bar(C::B_QKREADY + J), ph, w, kSiteKFull))) return false;
     tc_fence_after();
-    trace(a, kEvQkIssue, cur.tc);
-    const int cols = cur.b.cols(cur.kt);
-    const uint32_t s_tmem = tmem + (uint32_t)(J * 128);
-    auto body = [&](auto qsc, uint32_t idesc) {
-      constexpr int QSL = decltype(qsc)::value;
+    trace(a, kEvQkIssue, qc.tc);
+    const int cols = qc.b.cols(qc.kt);
+    const uint32_t s_tmem = pin32(tmem + (uint32_t)(J * 128));
+    const uint32_t idesc = pin32(cols == kBN ? IDESC_QK : make_idesc(kBM, cols, 0));
+    // 16-wide K steps: within a swizzled 64-column chunk the start address
+    // advances 32 bytes per step, across chunks by a whole chunk
+    const uint64_t qd0 = q_desc0 + (uint64_t)((qs * C::TILEB) >> 4);
+    uint64_t qd[QK_STEPS], kd[QK_STEPS];
 #pragma unroll
-      for (int kk = 0; kk < QK_STEPS; ++kk) {
-        const uint32_t off = (kk / STEPS_PER_CHUNK) * C::CHUNKB + (kk % STEPS_PER_CHUNK) * 32;
-        const uint64_t qd = q_desc0 + (uint64_t)((QSL * C::TILEB + off) >> 4);
-        const uint64_t kd = k_desc0 + (uint64_t)((J * C::TILEB + off) >> 4);
-        if (kk == 0)
-          mma_ss_c<0>(s_tmem, qd, kd, idesc);
-        else
-          mma_ss_c<1>(s_tmem, qd, kd, idesc);
-      }
-    };
-    const uint32_t idesc = cols == kBN ? IDESC_QK : make_idesc(kBM, cols, 0);
-    if (qs == 0)
-      body(std::integral_constant<int, 0>{}, idesc);
-    else
-      body(std::integral_constant<int, 1 % C::QS>{}, idesc);
+    for (int kk = 0; kk < QK_STEPS; ++kk) {
+      const uint32_t off = (kk / STEPS_PER_CHUNK) * C::CHUNKB + (kk % STEPS_PER_CHUNK) * 32;
+      qd[kk] = pin64(qd0 + (uint64_t)(off >> 4));
+      kd[kk] = pin64(k_desc0 + (uint64_t)((J * C::TILEB + off) >> 4));
+    }
+    mma_ss_c<0>(s_tmem, qd[0], kd[0], idesc);
+#pragma unroll
+    for (int kk = 1; kk < QK_STEPS; ++kk) mma_ss_c<1>(s_tmem, qd[kk], kd[kk], idesc);
     mma_commit(bar(C::B_SFULL + J));
-    mma_commit(bar(C::B_KEMPTY + J));
-    if (cur.kt == cur.b.qt) mma_commit(bar(C::B_QEMPTY + qs));
-    trace(a, kEvMmaQkDone, cur.tc);
-    cur.advance(a);
+    if (qc.kt == qc.b.qt) mma_commit(bar(C::B_QEMPTY + qs));
+    qc.advance(a);
+    if (J == P - 1) ph ^= 1u;
     return true;
   };
-  while (ok && cur.valid) {
-    if (!(ok = step(std::integral_constant<int, 0>{})) || !cur.valid) break;
-    if (!(ok = step(std::integral_constant<int, 1 % P>{})) || !cur.valid) break;
-    if (P > 2 && (!(ok = step(std::integral_constant<int, 2 % P>{})) || !cur.valid)) break;
-  }
+  run_unrolled<P>(step);
   if (!ok) {
     // Drain: a commit arrives once every MMA issued before it has finished.
     mma_commit(bar(C::B_DRAIN));
@@ -584,10 +657,14 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
   }
 }
 
-// PV issuer (one thread): O += P_hi V + P_lo V for every key-block step, as
-// soon as the SiLU warps have written P.  Commits V-empty and S-free (the
-// S buffer may be overwritten) when the products complete, and O-full after
-// an item's last block.
+// PV issuer (one thread).  Step s issues O += P_hi V + P_lo V over keys
+// 0-63 once SiLU warpgroup 0 has written them (P-full 0) and V(s) has
+// landed, then over keys 64-127 once warpgroup 1 has (P-full 1), into O
+// buffer ob = item mod OB, and commits QK-ready (S buffer and V slot free).
+// The barriers of the next group are tested (without blocking) before the
+// current group's products are issued, so that the test's latency overlaps
+// them.  16-key step k: P_hi in columns 32 (k/2) + 8 (k%2) + [0, 8), P_lo 16
+// columns further; V rows 16 k.. (two 8-row atoms per step).
 template <int D>
 __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
   using C = Cfg<D>;
@@ -597,114 +674,137 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
   constexpr uint32_t IDESC_PV = make_idesc(kBM, D, 1);
   const uint64_t v_desc0 = smem_desc(base + C::V_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
   bool ok = true;
-  Cursor cur;
-  cur.start(a);
+  Cursor pc;
+  pc.start(a);
+  uint32_t ph = 0;  // (pc.tc / P) & 1
 
-  auto step = [&](auto jc) -> bool {
+  auto issue_pv = [&](auto jc, auto hc, int ob) {
     constexpr int J = decltype(jc)::value;
-    const uint32_t use = cur.tc / P;
-    const int ob = cur.it % C::OB;
-    if (!wait_one(bar(C::B_PFULL + J), use & 1u, w, kSitePFull)) return false;
-    trace(a, kEvMmaPReady, cur.tc);
-    if (cur.kt == 0 &&
-        !wait_one(bar(C::B_OEMPTY + ob), ((uint32_t)(cur.it / C::OB) & 1u) ^ 1u, w, kSiteOEmpty))
+    constexpr int H = decltype(hc)::value;
+    const uint32_t o_tmem = pin32(tmem + C::O_COL + (uint32_t)(ob * D));
+    uint32_t pa[8];
+    uint64_t vb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int kk = 4 * H + i;
+      pa[2 * i] = pin32(tmem + (uint32_t)(J * 128 + 32 * (kk >> 1) + 8 * (kk & 1)));
+      pa[2 * i + 1] = pin32(tmem + (uint32_t)(J * 128 + 32 * (kk >> 1) + 8 * (kk & 1) + 16));
+      vb[i] = pin64(v_desc0 + (uint64_t)((J * C::TILEB + kk * 2 * C::ATOMB) >> 4));
+    }
+    if (pc.kt != pc.b.qt && (H == 1 || pc.kt != 0)) {
+      // full half continuing an accumulation
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mma_ts_c<1>(o_tmem, pa[2 * i], vb[i], IDESC_PV);
+        mma_ts_c<1>(o_tmem, pa[2 * i + 1], vb[i], IDESC_PV);
+      }
+    } else {
+      // an item's first block (the first product overwrites O) or its last
+      // (only the 16-key steps that hold keys < n)
+      const int cols = pc.b.cols(pc.kt);
+      const int n_steps = (cols - 64 * H) / 16;  // <= 0: none in this half
+      const bool first = H == 0 && pc.kt == 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i < n_steps) {
+          if (i == 0 && first)
+            mma_ts_c<0>(o_tmem, pa[0], vb[0], IDESC_PV);
+          else
+            mma_ts_c<1>(o_tmem, pa[2 * i], vb[i], IDESC_PV);
+          mma_ts_c<1>(o_tmem, pa[2 * i + 1], vb[i], IDESC_PV);
+        }
+      }
+    }
+  };
+
+  bool pa_ready = false, v_ready = false;  // tests made for the coming PV_0
+  auto step = [&](auto ic) -> bool {
+    constexpr int J = decltype(ic)::value;
+    constexpr int JN = (J + 1) % P;  // next step's buffer
+    if (!ok || !pc.valid) return false;
+    const int ob = C::OB == 1 ? 0 : (pc.it & 1);
+    const bool last = pc.kt == pc.b.qt;
+    if (!pa_ready && !(ok = wait_one(bar(C::B_PFULL + J), ph, w, kSitePFull))) return false;
+    if (pc.kt == 0 &&
+        !(ok = wait_one(bar(C::B_OEMPTY + ob), ((uint32_t)(pc.it / C::OB) & 1u) ^ 1u, w, kSiteOEmpty)))
       return false;
-    if (!wait_one(bar(C::B_VFULL + J), use & 1u, w, kSiteVFull)) return false;
-    const int cols = cur.b.cols(cur.kt);
-    const int r_end = cur.b.n - kBN * cur.kt;
-    if (cur.kt == cur.b.qt && r_end < cols) {
+    if (!v_ready && !(ok = wait_one(bar(C::B_VFULL + J), ph, w, kSiteVFull))) return false;
+    if (last) {
       // Keys in [n, cols) lie past the end of the sequence: zero their V
       // rows so that the zero P entries never meet non-finite values of the
       // next sequence.
-      const uint32_t v_addr = base + C::V_OFF + J * C::TILEB;
+      const int cols = pc.b.cols(pc.kt);
+      const int r_end = pc.b.n - kBN * pc.kt;
+      if (r_end < cols) {
+        const uint32_t v_addr = base + C::V_OFF + J * C::TILEB;
 #pragma unroll
-      for (int ch = 0; ch < C::NCHUNK; ++ch) {
-        const uint32_t z0 = v_addr + ch * C::CHUNKB + r_end * C::ROWB;
-        const uint32_t z1 = v_addr + ch * C::CHUNKB + cols * C::ROWB;
-        for (uint32_t z = z0; z < z1; z += 16)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(z), "r"(0) : "memory");
+        for (int ch = 0; ch < C::NCHUNK; ++ch) {
+          const uint32_t z0 = v_addr + ch * C::CHUNKB + r_end * C::ROWB;
+          const uint32_t z1 = v_addr + ch * C::CHUNKB + cols * C::ROWB;
+          for (uint32_t z = z0; z < z1; z += 16)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(z), "r"(0) : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     tc_fence_after();
-    trace(a, kEvPvIssue, cur.tc);
-    const uint32_t p_tmem = tmem + (uint32_t)(J * 128);
-    const uint64_t vd0 = v_desc0 + (uint64_t)((J * C::TILEB) >> 4);
-    const int ksteps = cols / 16;
-    const bool first = cur.kt == 0;
-    auto body = [&](auto obc) {
-      constexpr int OBL = decltype(obc)::value;
-      const uint32_t o_tmem = tmem + C::O_COL + (uint32_t)(OBL * D);
-      if (ksteps == kBN / 16 && !first) {
-        // full block continuing an accumulation: branch-free, constant operands
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_c<1>(o_tmem, p_tmem + 32u * (kk >> 1) + 8u * (kk & 1),
-                      vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4), IDESC_PV);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_c<1>(o_tmem, p_tmem + 32u * (kk >> 1) + 16u + 8u * (kk & 1),
-                      vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4), IDESC_PV);
-      } else {
-        for (int kk = 0; kk < ksteps; ++kk) {
-          const uint64_t bd = vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4);
-          const uint32_t a_hi = p_tmem + 32u * (kk >> 1) + 8u * (kk & 1);
-          if (kk == 0 && first)
-            mma_ts_c<0>(o_tmem, a_hi, bd, IDESC_PV);
-          else
-            mma_ts_c<1>(o_tmem, a_hi, bd, IDESC_PV);
-        }
-        for (int kk = 0; kk < ksteps; ++kk)
-          mma_ts_c<1>(o_tmem, p_tmem + 32u * (kk >> 1) + 16u + 8u * (kk & 1),
-                      vd0 + (uint64_t)((kk * 2 * C::ATOMB) >> 4), IDESC_PV);
-      }
-    };
-    if (ob == 0)
-      body(std::integral_constant<int, 0>{});
-    else
-      body(std::integral_constant<int, 1 % C::OB>{});
-    mma_commit(bar(C::B_VEMPTY + J));
-    mma_commit(bar(C::B_SFREE + J));
-    if (cur.kt == cur.b.qt) mma_commit(bar(C::B_OFULL + ob));
-    trace(a, kEvMmaPvDone, cur.tc);
-    cur.advance(a);
+    trace(a, kEvPvIssue, pc.tc);
+    const bool pb_ready = mbar_test(bar(C::B_PFULL + P + J), ph);
+    issue_pv(std::integral_constant<int, J>{}, std::integral_constant<int, 0>{}, ob);
+    if (!pb_ready && !(ok = wait_one(bar(C::B_PFULL + P + J), ph, w, kSitePFull))) return false;
+    tc_fence_after();
+    const uint32_t npar = J + 1 == P ? ph ^ 1u : ph;
+    pa_ready = mbar_test(bar(C::B_PFULL + JN), npar);
+    v_ready = mbar_test(bar(C::B_VFULL + JN), npar);
+    issue_pv(std::integral_constant<int, J>{}, std::integral_constant<int, 1>{}, ob);
+    mma_commit(bar(C::B_QKREADY + J));  // PV(s) done: S buffer J and V slot J free
+    if (last) mma_commit(bar(C::B_OFULL + ob));
+    pc.advance(a);
+    if (J == P - 1) ph ^= 1u;
     return true;
   };
-  while (ok && cur.valid) {
-    if (!(ok = step(std::integral_constant<int, 0>{})) || !cur.valid) break;
-    if (!(ok = step(std::integral_constant<int, 1 % P>{})) || !cur.valid) break;
-    if (P > 2 && (!(ok = step(std::integral_constant<int, 2 % P>{})) || !cur.valid)) break;
-  }
+  run_unrolled<P>(step);
   if (!ok) {
     mma_commit(bar(C::B_DRAIN + 1));
     wait_drain(bar(C::B_DRAIN + 1), 0);
   }
 }
 
-// silu of 32 scores of one row (two per step, packed fp32x2 arithmetic),
-// split into bf16 hi and lo halves.  MASK: zero the keys j > lim.
+// silu of the 32 scores s of one row, written over their own TMEM columns
+// at t: keys 16h..16h+15 go to P_hi columns t + 8h + [0, 8) and P_lo columns
+// t + 16 + 8h + [0, 8).  Processed in 16-key halves to keep register
+// pressure down.
 template <bool MASK>
-__device__ __forceinline__ void silu_split32(const uint32_t (&s)[32], float2 ha2, int lim,
-                                             uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+__device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, uint32_t t) {
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const float2 h = __fmul2_rn(make_float2(__uint_as_float(s[2 * m]), __uint_as_float(s[2 * m + 1])),
-                                ha2);
-    float2 p = __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
-    if (MASK) {
-      p.x = (2 * m > lim) ? 0.0f : p.x;
-      p.y = (2 * m + 1 > lim) ? 0.0f : p.y;
+  for (int h = 0; h < 2; ++h) {
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int k = 16 * h + 2 * m;
+      const float2 x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
+      float2 p = __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
+      if (MASK) {
+        p.x = (k > lim) ? 0.0f : p.x;
+        p.y = (k + 1 > lim) ? 0.0f : p.y;
+      }
+      const uint32_t ph = pack_bf16x2(p.x, p.y);
+      const float2 r = __fadd2_rn(
+          p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
+      hi[m] = ph;
+      lo[m] = pack_bf16x2(r.x, r.y);
     }
-    const uint32_t ph = pack_bf16x2(p.x, p.y);
-    const float2 r = __fadd2_rn(
-        p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
-    hi[m] = ph;
-    lo[m] = pack_bf16x2(r.x, r.y);
+    tmem_st8(t + 8u * h, hi);
+    tmem_st8(t + 16u + 8u * h, lo);
   }
 }
 
-// SiLU warpgroups (warps 8-11 and 12-15): warpgroup e takes the steps with
-// tc % 2 == e.  Thread r owns score row r of the block.
+// SiLU warpgroups (warps 8-11 and 12-15): warpgroup e takes key columns
+// [64 e, 64 e + 64) of every block, so both work on the same block at once
+// and the PV products of a half start as soon as that half is written.
+// Thread r owns score row r.  The first 32 columns of the next block are
+// loaded while the current block's last columns are computed, when that
+// block's scores are already there.
 template <int D>
 __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w, int warp,
                           int lane) {
@@ -715,60 +815,63 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
   const int e = (warp - kEwWarp0) >> 2;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
-  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(64 * e);
   const float2 ha2 = make_float2(a.half_alpha, a.half_alpha);
+  // a block whose 32 rows of this warp all lie past the sequence end is
+  // skipped (those rows are never stored); the diagonal block is masked
+  auto plain = [&](int kt, const Block& b) { return kt != b.qt && quarter * 32 < b.rows(); };
   Cursor cur;
   cur.start(a);
+  uint32_t s0[32], s1[32];
+  bool have = false;  // s0 is loading the first 32 columns of cur's half
   while (cur.valid) {
-    if ((int)(cur.tc & 1u) != e) {
-      cur.advance(a);
-      continue;
-    }
     const int j = (int)(cur.tc % P);
-    if (!wait_warp(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull)) return;
-    tc_fence_after();
+    if (!have) {
+      if (!wait_warp(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull)) return;
+      tc_fence_after();
+    }
     trace(a, kEvSiluStart, cur.tc);
     const uint32_t t_s = lane_base + (uint32_t)(j * 128);
-    const bool diag = cur.kt == cur.b.qt;
-    const int cols = cur.b.cols(cur.kt);
-    // Rows past the sequence end are never stored: a warp whose 32 rows all
-    // lie there skips its work.
-    if (quarter * 32 < cur.b.rows()) {
-      if (!diag) {
-        uint32_t s0[32], s1[32];
-        tmem_ld32_async(t_s, s0);
-        tmem_wait_ld(s0);
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; c += 2) {
-          uint32_t hi[16], lo[16];
-          tmem_ld32_async(t_s + 32u * (c + 1), s1);
-          silu_split32<false>(s0, ha2, 0, hi, lo);
-          tmem_st16(t_s + 32u * c, hi);
-          tmem_st16(t_s + 32u * c + 16u, lo);
-          tmem_wait_ld(s1);
-          if (c + 2 < kBN / 32) tmem_ld32_async(t_s + 32u * (c + 2), s0);
-          silu_split32<false>(s1, ha2, 0, hi, lo);
-          tmem_st16(t_s + 32u * (c + 1), hi);
-          tmem_st16(t_s + 32u * (c + 1) + 16u, lo);
-          if (c + 2 < kBN / 32) tmem_wait_ld(s0);
+    bool next_have = false;
+    if (plain(cur.kt, cur.b)) {
+      if (!have) tmem_ld32_async(t_s, s0);
+      tmem_wait_ld(s0);
+      tmem_ld32_async(t_s + 32u, s1);
+      silu_store32<false>(s0, ha2, 0, t_s);
+      tmem_wait_ld(s1);
+      // the next step: key block kt+1 of this item, or block 0 of the next
+      const bool same = cur.kt < cur.b.qt;
+      if (same ? plain(cur.kt + 1, cur.b) : (cur.nvalid && plain(0, cur.nb))) {
+        // prefetch only if the next block's scores are already there
+        const uint32_t tn = cur.tc + 1u;
+        const int jn = (int)(tn % P);
+        bool ready = false;
+        if (lane == 0) ready = mbar_try_wait(bar(C::B_SFULL + jn), (tn / P) & 1u);
+        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
+          tc_fence_after();
+          tmem_ld32_async(lane_base + (uint32_t)(jn * 128), s0);
+          next_have = true;
         }
-      } else {
-        // diagonal block: keep keys j <= row; chunks c > quarter lie wholly
-        // above the diagonal for this warp (zeros); columns >= cols are not
-        // read by the PV products.
+      }
+      silu_store32<false>(s1, ha2, 0, t_s + 32u);
+      tmem_wait_st();
+    } else if (quarter * 32 < cur.b.rows()) {
+      // diagonal block: keep keys j <= row; chunks g > quarter lie wholly
+      // above the diagonal for this warp (zeros); columns >= cols are not
+      // read by the PV products.
+      const int cols = cur.b.cols(cur.kt);
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32 && 32 * c < cols; ++c) {
-          uint32_t hi[16], lo[16];
-          if (c > quarter) {
+      for (int c = 0; c < 2 && 32 * (2 * e + c) < cols; ++c) {
+        const int g = 2 * e + c;  // chunk of the block
+        if (g > quarter) {
+          uint32_t z[16];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) hi[m] = lo[m] = 0u;
-          } else {
-            uint32_t sv[32];
-            tmem_ld32(t_s + 32u * c, sv);
-            silu_split32<true>(sv, ha2, row - 32 * c, hi, lo);
-          }
-          tmem_st16(t_s + 32u * c, hi);
-          tmem_st16(t_s + 32u * c + 16u, lo);
+          for (int m = 0; m < 16; ++m) z[m] = 0u;
+          tmem_st16(t_s + 32u * c, z);
+          tmem_st16(t_s + 32u * c + 16u, z);
+        } else {
+          tmem_ld32(t_s + 32u * c, s1);
+          silu_store32<true>(s1, ha2, row - 32 * g, t_s + 32u * c);
         }
       }
       tmem_wait_st();
@@ -776,13 +879,14 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
     tc_fence_before();
     __syncwarp();
     trace(a, kEvSiluEnd, cur.tc);
-    if (lane == 0) mbar_arrive(bar(C::B_PFULL + j));
+    if (lane == 0) mbar_arrive(bar(C::B_PFULL + e * P + j));
     cur.advance(a);
+    have = next_have;
   }
 }
 
-// Epilogue warpgroup (warps 0-3): O -> x inv_n -> bf16 -> 16-byte stores of
-// the valid rows.
+// Epilogue warpgroup (warps 0-3): O -> x inv_n -> bf16 -> out.  Thread r
+// owns output row r of the item; rows past the sequence end are not stored.
 template <int D>
 __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w,
                               int warp, int lane) {
@@ -800,26 +904,28 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
     if (!wait_warp(bar(C::B_OFULL + ob), (uint32_t)(it / C::OB) & 1u, w, kSiteOFull)) return;
     tc_fence_after();
     trace(a, kEvEpiStart, (unsigned)it);
-    uint32_t packed[D / 2];
+    const uint32_t o_t = tmem + lane_off + C::O_COL + (uint32_t)(ob * D);
+    uint4* dst = reinterpret_cast<uint4*>(
+        out + ((size_t)(b.s0 + kBM * b.qt + row) * (size_t)a.heads + (size_t)b.h) * D);
+    const bool live = row < b.rows();
+    // Each 32-column chunk is scaled, packed and stored as it is read.
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
-      tmem_ld32(tmem + lane_off + C::O_COL + (uint32_t)(ob * D + 32 * c), o);
+      tmem_ld32(o_t + 32u * c, o);
+      uint32_t packed[16];
 #pragma unroll
       for (int m = 0; m < 16; ++m)
-        packed[16 * c + m] = pack_bf16x2(__uint_as_float(o[2 * m]) * inv_n,
-                                         __uint_as_float(o[2 * m + 1]) * inv_n);
+        packed[m] = pack_bf16x2(__uint_as_float(o[2 * m]) * inv_n, __uint_as_float(o[2 * m + 1]) * inv_n);
+      if (live) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          dst[4 * c + u] = make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+      }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + ob));
-    if (row < b.rows()) {
-      uint4* dst = reinterpret_cast<uint4*>(
-          out + ((size_t)(b.s0 + kBM * b.qt + row) * (size_t)a.heads + (size_t)b.h) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c)
-        dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-    }
     trace(a, kEvEpiEnd, (unsigned)it);
   }
 }
@@ -839,12 +945,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t bars = base + C::BAR_OFF;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBARS; ++i) {
-      // P-full and O-empty: one arrival per warp of the arriving warpgroup
-      const bool many = (i >= C::B_PFULL && i < C::B_PFULL + C::P) ||
-                        (i >= C::B_OEMPTY && i < C::B_OEMPTY + C::OB);
-      mbar_init(bars + 8u * i, many ? 4u : 1u);
-    }
+    for (int i = 0; i < C::NBARS; ++i) mbar_init(bars + 8u * i, C::arrivals(i));
+    // QK-ready phase 0 has no PV before it: arrive for it now
+    for (int j = 0; j < C::P; ++j) mbar_arrive(bars + 8u * (C::B_QKREADY + j));
     *abort_flag = 0;
     for (int i = 0; i < kTraceWarps; ++i) trace_counters()[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -881,7 +984,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == kMmaWarpPV) {
     if (lane == 0) role_mma_pv<D>(a, base, tmem, w);
     __syncwarp();
-  } else if (warp >= kEwWarp0) {
+  } else if (warp >= kEwWarp0 && warp < kEwWarp0 + 8) {
     role_silu<D>(a, base, tmem, w, warp, lane);
   } else if (warp < kEpiWarp0 + 4) {
     role_epilogue<D>(a, base, tmem, w, warp, lane);
