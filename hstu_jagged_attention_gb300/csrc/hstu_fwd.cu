@@ -436,13 +436,14 @@ struct Cfg {
   static constexpr uint32_t O_COL = 128u * P;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(128 * P + OB * D <= (int)kTmemCols, "TMEM budget");
-  // Arrivals that complete a phase of barrier i: one per warp of a
-  // warpgroup (P-full, O-empty), the K copy's and the PV commit's
-  // (QK-ready), else one.
+  // Arrivals that complete a phase of barrier i: every thread of a SiLU
+  // warpgroup (P-full), one per epilogue warp (O-empty), the K copy's and
+  // the PV commit's (QK-ready), else one.
   __host__ __device__ static constexpr uint32_t arrivals(int i) {
-    return ((i >= B_PFULL && i < B_PFULL + 2 * P) || (i >= B_OEMPTY && i < B_OEMPTY + OB)) ? 4u
-           : (i >= B_QKREADY && i < B_QKREADY + P)                                       ? 2u
-                                                                                           : 1u;
+    return (i >= B_PFULL && i < B_PFULL + 2 * P)   ? 128u
+           : (i >= B_OEMPTY && i < B_OEMPTY + OB)   ? 4u
+           : (i >= B_QKREADY && i < B_QKREADY + P) ? 2u
+                                                   : 1u;
   }
 };
 
@@ -802,9 +803,11 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
 // SiLU warpgroups (warps 8-11 and 12-15): warpgroup e takes key columns
 // [64 e, 64 e + 64) of every block, so both work on the same block at once
 // and the PV products of a half start as soon as that half is written.
-// Thread r owns score row r.  The first 32 columns of the next block are
-// loaded while the current block's last columns are computed, when that
-// block's scores are already there.
+// Thread r owns score row r.  Every lane tests and waits on the barriers
+// itself (a vote keeps the warp's view uniform) and arrives on P-full
+// itself, so no lane-0 relay or warp barrier sits on the path.  The first
+// 32 columns of the next block are loaded while the current block's last
+// columns are computed, when that block's scores are already there.
 template <int D>
 __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w, int warp,
                           int lane) {
@@ -827,7 +830,8 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
   while (cur.valid) {
     const int j = (int)(cur.tc % P);
     if (!have) {
-      if (!wait_warp(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull)) return;
+      const bool ok = wait_one(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull);
+      if (!__all_sync(0xffffffffu, ok)) return;
       tc_fence_after();
     }
     trace(a, kEvSiluStart, cur.tc);
@@ -837,23 +841,27 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
       if (!have) tmem_ld32_async(t_s, s0);
       tmem_wait_ld(s0);
       tmem_ld32_async(t_s + 32u, s1);
+      // the next step: key block kt+1 of this item, or block 0 of the next;
+      // its barrier is tested now and the result read after this chunk
+      const bool same = cur.kt < cur.b.qt;
+      const bool next_plain = same ? plain(cur.kt + 1, cur.b) : (cur.nvalid && plain(0, cur.nb));
+      const uint32_t tn = cur.tc + 1u;
+      const int jn = (int)(tn % P);
+      const bool early = next_plain && mbar_test(bar(C::B_SFULL + jn), (tn / P) & 1u);
       silu_store32<false>(s0, ha2, 0, t_s);
       tmem_wait_ld(s1);
-      // the next step: key block kt+1 of this item, or block 0 of the next
-      const bool same = cur.kt < cur.b.qt;
-      if (same ? plain(cur.kt + 1, cur.b) : (cur.nvalid && plain(0, cur.nb))) {
-        // prefetch only if the next block's scores are already there
-        const uint32_t tn = cur.tc + 1u;
-        const int jn = (int)(tn % P);
-        bool ready = false;
-        if (lane == 0) ready = mbar_try_wait(bar(C::B_SFULL + jn), (tn / P) & 1u);
-        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
-          tc_fence_after();
-          tmem_ld32_async(lane_base + (uint32_t)(jn * 128), s0);
-          next_have = true;
-        }
+      if (__all_sync(0xffffffffu, early)) {
+        tc_fence_after();
+        tmem_ld32_async(lane_base + (uint32_t)(jn * 128), s0);
+        next_have = true;
       }
       silu_store32<false>(s1, ha2, 0, t_s + 32u);
+      if (!next_have && next_plain &&
+          __all_sync(0xffffffffu, mbar_test(bar(C::B_SFULL + jn), (tn / P) & 1u))) {
+        tc_fence_after();
+        tmem_ld32_async(lane_base + (uint32_t)(jn * 128), s0);
+        next_have = true;
+      }
       tmem_wait_st();
     } else if (quarter * 32 < cur.b.rows()) {
       // diagonal block: keep keys j <= row; chunks g > quarter lie wholly
@@ -877,9 +885,8 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
       tmem_wait_st();
     }
     tc_fence_before();
-    __syncwarp();
     trace(a, kEvSiluEnd, cur.tc);
-    if (lane == 0) mbar_arrive(bar(C::B_PFULL + e * P + j));
+    mbar_arrive(bar(C::B_PFULL + e * P + j));
     cur.advance(a);
     have = next_have;
   }
