@@ -18,16 +18,15 @@
 //   warp 5        QK issuer (one thread, owns TMEM): S = Q K^T
 //                 (tcgen05.mma kind::f16, fp32 accumulate) of step t into
 //                 TMEM S buffer t mod 3, up to three steps ahead of PV.
-//   warps 8-15    two "SiLU" warpgroups; warpgroup e takes key columns
-//                 [64e, 64e+64) of every block, so both finish a block
-//                 together.  Thread r owns score row r: tcgen05.ld S,
+//   warps 8-15    two "SiLU" warpgroups taking alternate steps.  Thread r
+//                 owns score row r: tcgen05.ld S (the next 32 columns load
+//                 while the current ones are computed),
 //                 p = h + h tanh(h) with h = alpha s / 2
 //                 (= alpha s sigmoid(alpha s)), tril select on the diagonal
 //                 block, split p = bf16(p) + bf16(p - bf16(p)), tcgen05.st
 //                 both halves over the S columns just read.
 //   warp 7        PV issuer (one thread): O += P_hi V + P_lo V with P read
-//                 from TMEM, each key half as soon as its warpgroup has
-//                 written it.
+//                 from TMEM, as soon as the SiLU warpgroup has written P.
 //   warps 0-3     epilogue: reads a finished item's O, scales by inv_n,
 //                 rounds to bf16 and stores the valid rows with 16-byte
 //                 stores.
@@ -421,8 +420,8 @@ struct Cfg {
   static constexpr int B_QKREADY = B_QEMPTY + QS;
   static constexpr int B_VFULL = B_QKREADY + P;
   static constexpr int B_SFULL = B_VFULL + P;      // QK done: S written, K slot free
-  static constexpr int B_PFULL = B_SFULL + P;      // [2][P]: warpgroup e wrote P of key half e
-  static constexpr int B_OFULL = B_PFULL + 2 * P;  // an item's last PV done
+  static constexpr int B_PFULL = B_SFULL + P;      // SiLU done: P written
+  static constexpr int B_OFULL = B_PFULL + P;      // an item's last PV done
   static constexpr int B_OEMPTY = B_OFULL + OB;
   static constexpr int B_DRAIN = B_OEMPTY + OB;  // [2]: the two MMA issuers' drains
   static constexpr int NBARS = B_DRAIN + 2;
@@ -436,11 +435,11 @@ struct Cfg {
   static constexpr uint32_t O_COL = 128u * P;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(128 * P + OB * D <= (int)kTmemCols, "TMEM budget");
-  // Arrivals that complete a phase of barrier i: every thread of a SiLU
+  // Arrivals that complete a phase of barrier i: every thread of the SiLU
   // warpgroup (P-full), one per epilogue warp (O-empty), the K copy's and
   // the PV commit's (QK-ready), else one.
   __host__ __device__ static constexpr uint32_t arrivals(int i) {
-    return (i >= B_PFULL && i < B_PFULL + 2 * P)   ? 128u
+    return (i >= B_PFULL && i < B_PFULL + P)       ? 128u
            : (i >= B_OEMPTY && i < B_OEMPTY + OB)   ? 4u
            : (i >= B_QKREADY && i < B_QKREADY + P) ? 2u
                                                    : 1u;
@@ -658,12 +657,11 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
   }
 }
 
-// PV issuer (one thread).  Step s issues O += P_hi V + P_lo V over keys
-// 0-63 once SiLU warpgroup 0 has written them (P-full 0) and V(s) has
-// landed, then over keys 64-127 once warpgroup 1 has (P-full 1), into O
-// buffer ob = item mod OB, and commits QK-ready (S buffer and V slot free).
-// The barriers of the next group are tested (without blocking) before the
-// current group's products are issued, so that the test's latency overlaps
+// PV issuer (one thread).  Step s issues O += P_hi V + P_lo V once the SiLU
+// warpgroup has written P (P-full) and V(s) has landed, into O buffer
+// ob = item mod OB, and commits QK-ready (S buffer and V slot free).  The
+// barriers of the next step are tested (without blocking) before the
+// current step's products are issued, so that the tests' latency overlaps
 // them.  16-key step k: P_hi in columns 32 (k/2) + 8 (k%2) + [0, 8), P_lo 16
 // columns further; V rows 16 k.. (two 8-row atoms per step).
 template <int D>
@@ -750,13 +748,10 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
     }
     tc_fence_after();
     trace(a, kEvPvIssue, pc.tc);
-    const bool pb_ready = mbar_test(bar(C::B_PFULL + P + J), ph);
-    issue_pv(std::integral_constant<int, J>{}, std::integral_constant<int, 0>{}, ob);
-    if (!pb_ready && !(ok = wait_one(bar(C::B_PFULL + P + J), ph, w, kSitePFull))) return false;
-    tc_fence_after();
     const uint32_t npar = J + 1 == P ? ph ^ 1u : ph;
     pa_ready = mbar_test(bar(C::B_PFULL + JN), npar);
     v_ready = mbar_test(bar(C::B_VFULL + JN), npar);
+    issue_pv(std::integral_constant<int, J>{}, std::integral_constant<int, 0>{}, ob);
     issue_pv(std::integral_constant<int, J>{}, std::integral_constant<int, 1>{}, ob);
     mma_commit(bar(C::B_QKREADY + J));  // PV(s) done: S buffer J and V slot J free
     if (last) mma_commit(bar(C::B_OFULL + ob));
@@ -800,14 +795,12 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
   }
 }
 
-// SiLU warpgroups (warps 8-11 and 12-15): warpgroup e takes key columns
-// [64 e, 64 e + 64) of every block, so both work on the same block at once
-// and the PV products of a half start as soon as that half is written.
-// Thread r owns score row r.  Every lane tests and waits on the barriers
-// itself (a vote keeps the warp's view uniform) and arrives on P-full
-// itself, so no lane-0 relay or warp barrier sits on the path.  The first
-// 32 columns of the next block are loaded while the current block's last
-// columns are computed, when that block's scores are already there.
+// SiLU warpgroups (warps 8-11 and 12-15): warpgroup e takes the steps with
+// tc % 2 == e, all 128 key columns of the block (whole blocks amortise the
+// per-step waits and arrivals twice as well as half blocks do).  Thread r
+// owns score row r.  Every lane waits on S-full and arrives on P-full
+// itself (a vote keeps the warp's view uniform), so no lane-0 relay or warp
+// barrier sits on the path.
 template <int D>
 __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w, int warp,
                           int lane) {
@@ -818,60 +811,42 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
   const int e = (warp - kEwWarp0) >> 2;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
-  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(64 * e);
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
   const float2 ha2 = make_float2(a.half_alpha, a.half_alpha);
-  // a block whose 32 rows of this warp all lie past the sequence end is
-  // skipped (those rows are never stored); the diagonal block is masked
-  auto plain = [&](int kt, const Block& b) { return kt != b.qt && quarter * 32 < b.rows(); };
   Cursor cur;
   cur.start(a);
   uint32_t s0[32], s1[32];
-  bool have = false;  // s0 is loading the first 32 columns of cur's half
   while (cur.valid) {
+    if ((int)(cur.tc & 1u) != e) {
+      cur.advance(a);
+      continue;
+    }
     const int j = (int)(cur.tc % P);
-    if (!have) {
+    {
       const bool ok = wait_one(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) return;
-      tc_fence_after();
     }
+    tc_fence_after();
     trace(a, kEvSiluStart, cur.tc);
     const uint32_t t_s = lane_base + (uint32_t)(j * 128);
-    bool next_have = false;
-    if (plain(cur.kt, cur.b)) {
-      if (!have) tmem_ld32_async(t_s, s0);
+    if (cur.kt != cur.b.qt && quarter * 32 < cur.b.rows()) {
+      tmem_ld32_async(t_s, s0);
       tmem_wait_ld(s0);
-      tmem_ld32_async(t_s + 32u, s1);
-      // the next step: key block kt+1 of this item, or block 0 of the next;
-      // its barrier is tested now and the result read after this chunk
-      const bool same = cur.kt < cur.b.qt;
-      const bool next_plain = same ? plain(cur.kt + 1, cur.b) : (cur.nvalid && plain(0, cur.nb));
-      const uint32_t tn = cur.tc + 1u;
-      const int jn = (int)(tn % P);
-      const bool early = next_plain && mbar_test(bar(C::B_SFULL + jn), (tn / P) & 1u);
-      silu_store32<false>(s0, ha2, 0, t_s);
-      tmem_wait_ld(s1);
-      if (__all_sync(0xffffffffu, early)) {
-        tc_fence_after();
-        tmem_ld32_async(lane_base + (uint32_t)(jn * 128), s0);
-        next_have = true;
-      }
-      silu_store32<false>(s1, ha2, 0, t_s + 32u);
-      if (!next_have && next_plain &&
-          __all_sync(0xffffffffu, mbar_test(bar(C::B_SFULL + jn), (tn / P) & 1u))) {
-        tc_fence_after();
-        tmem_ld32_async(lane_base + (uint32_t)(jn * 128), s0);
-        next_have = true;
+#pragma unroll 1
+      for (int c = 0; c < 4; c += 2) {
+        tmem_ld32_async(t_s + 32u * (c + 1), s1);
+        silu_store32<false>(s0, ha2, 0, t_s + 32u * c);
+        tmem_wait_ld(s1);
+        if (c + 2 < 4) tmem_ld32_async(t_s + 32u * (c + 2), s0);
+        silu_store32<false>(s1, ha2, 0, t_s + 32u * (c + 1));
+        if (c + 2 < 4) tmem_wait_ld(s0);
       }
       tmem_wait_st();
     } else if (quarter * 32 < cur.b.rows()) {
-      // diagonal block: keep keys j <= row; chunks g > quarter lie wholly
-      // above the diagonal for this warp (zeros); columns >= cols are not
-      // read by the PV products.
       const int cols = cur.b.cols(cur.kt);
 #pragma unroll 1
-      for (int c = 0; c < 2 && 32 * (2 * e + c) < cols; ++c) {
-        const int g = 2 * e + c;  // chunk of the block
-        if (g > quarter) {
+      for (int c = 0; c < 4 && 32 * c < cols; ++c) {
+        if (c > quarter) {
           uint32_t z[16];
 #pragma unroll
           for (int m = 0; m < 16; ++m) z[m] = 0u;
@@ -879,16 +854,15 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
           tmem_st16(t_s + 32u * c + 16u, z);
         } else {
           tmem_ld32(t_s + 32u * c, s1);
-          silu_store32<true>(s1, ha2, row - 32 * g, t_s + 32u * c);
+          silu_store32<true>(s1, ha2, row - 32 * c, t_s + 32u * c);
         }
       }
       tmem_wait_st();
     }
     tc_fence_before();
     trace(a, kEvSiluEnd, cur.tc);
-    mbar_arrive(bar(C::B_PFULL + e * P + j));
+    mbar_arrive(bar(C::B_PFULL + j));
     cur.advance(a);
-    have = next_have;
   }
 }
 
