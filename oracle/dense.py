@@ -71,3 +71,32 @@ def hstu_jagged_bruteforce(q, k, v, offsets, alpha: float, inv_n: float) -> np.n
     b, heads, s, _ = Q.shape
     y = hstu_dense(Q, K, V, causal_mask(b, heads, s), alpha, 1.0 / inv_n)
     return padded_to_jagged(y, offsets)
+
+
+def candidate_mask(lengths, num_targets, heads: int, s: int) -> np.ndarray:
+    """The M-FALCON mask (HSTU paper Appendix H, Algorithm 1 steps 4-5) per
+    sequence: the tril matrix, then position (i, j) cleared wherever both i
+    and j are candidate positions (>= hist = n - num_targets) and i != j."""
+    b = len(lengths)
+    m = np.zeros((b, heads, s, s), dtype=np.float64)
+    for i in range(b):
+        hist = int(lengths[i]) - int(num_targets[i])
+        L = np.tril(np.ones((s, s), dtype=np.float64))      # step 4
+        for r in range(hist, s):                             # step 5
+            for c in range(hist, s):
+                if r != c:
+                    L[r, c] = 0.0
+        m[i] = L
+    return m
+
+
+def hstu_jagged_bruteforce_targets(q, k, v, offsets, num_targets, alpha: float,
+                                   inv_n: float) -> np.ndarray:
+    """As hstu_jagged_bruteforce, with the M-FALCON mask.  Tiny inputs only."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    q64, k64, v64 = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+    Q, K, V = (jagged_to_padded(t, offsets) for t in (q64, k64, v64))
+    b, heads, s, _ = Q.shape
+    mask = candidate_mask(np.diff(offsets), num_targets, heads, s)
+    y = hstu_dense(Q, K, V, mask, alpha, 1.0 / inv_n)
+    return padded_to_jagged(y, offsets)

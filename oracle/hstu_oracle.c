@@ -24,6 +24,16 @@
  *
  * Layout: q, k, v, out are row-major (total, heads, d); offsets has batch+1
  * non-decreasing entries starting at 0.
+ *
+ * Candidate (M-FALCON) variant (HSTU paper section 3.4 and Appendix H,
+ * Algorithm 1 steps 4-5): the last num_targets[b] tokens of sequence b are
+ * ranking candidates.  With hist = n_b - num_targets[b], the causal mask is
+ * further restricted at positions i, j >= hist with i != j, so a candidate
+ * sees every history token and itself but no other candidate:
+ *
+ *     term j of row i is kept  iff  j <= i  and  (j < hist or j == i).
+ *
+ * With no candidates (hist = n_b) this is the causal formula above.
  */
 #include <math.h>
 #include <pthread.h>
@@ -34,14 +44,16 @@
  * overflows to +inf and the quotient is -0, which is the limit. */
 double hstu_oracle_silu(double x) { return x / (1.0 + exp(-x)); }
 
-/* One output row: out_row[c] for c < d, fp64. */
+/* One output row: out_row[c] for c < d, fp64.  hist: the number of history
+ * tokens of the sequence (its length when it has no candidates). */
 static void oracle_row(const float* q, const float* k, const float* v, int64_t seq_start,
-                       int64_t i, int heads, int d, int h, double alpha, double inv_n,
-                       double* acc /* d doubles, scratch */, double* out_row) {
+                       int64_t i, int64_t hist, int heads, int d, int h, double alpha,
+                       double inv_n, double* acc /* d doubles, scratch */, double* out_row) {
     const int64_t t = seq_start + i;
     const float* qr = q + (t * heads + h) * (int64_t)d;
     for (int c = 0; c < d; ++c) acc[c] = 0.0;
     for (int64_t j = 0; j <= i; ++j) {
+        if (j >= hist && j != i) continue; /* another candidate: masked */
         const int64_t s = seq_start + j;
         const float* kr = k + (s * heads + h) * (int64_t)d;
         const float* vr = v + (s * heads + h) * (int64_t)d;
@@ -56,6 +68,7 @@ static void oracle_row(const float* q, const float* k, const float* v, int64_t s
 typedef struct {
     const float *q, *k, *v;
     const int64_t* offsets;
+    const int64_t* num_targets; /* candidates per sequence, or NULL: none */
     int batch, heads, d;
     double alpha, inv_n;
     double* out;
@@ -77,10 +90,15 @@ static int64_t take(job_t* J, int64_t chunk) {
 }
 
 /* Locate the sequence that holds token t (linear scan: plain, not fast). */
-static int64_t seq_start_of(const int64_t* offsets, int batch, int64_t t) {
+static int seq_of(const int64_t* offsets, int batch, int64_t t) {
     for (int b = 0; b < batch; ++b)
-        if (t >= offsets[b] && t < offsets[b + 1]) return offsets[b];
+        if (t >= offsets[b] && t < offsets[b + 1]) return b;
     return -1;
+}
+
+static int64_t hist_of(const job_t* J, int b) {
+    const int64_t n = J->offsets[b + 1] - J->offsets[b];
+    return J->num_targets ? n - J->num_targets[b] : n;
 }
 
 static void* worker_full(void* arg) {
@@ -92,8 +110,9 @@ static void* worker_full(void* arg) {
         if (u >= units) break;
         const int b = (int)(u / J->heads), h = (int)(u % J->heads);
         const int64_t s0 = J->offsets[b], n = J->offsets[b + 1] - J->offsets[b];
+        const int64_t hist = hist_of(J, b);
         for (int64_t i = 0; i < n; ++i)
-            oracle_row(J->q, J->k, J->v, s0, i, J->heads, J->d, h, J->alpha, J->inv_n, acc,
+            oracle_row(J->q, J->k, J->v, s0, i, hist, J->heads, J->d, h, J->alpha, J->inv_n, acc,
                        J->out + ((s0 + i) * J->heads + h) * (int64_t)J->d);
     }
     free(acc);
@@ -107,14 +126,15 @@ static void* worker_rows(void* arg) {
         const int64_t r = take(J, 1);
         if (r >= J->nrows) break;
         const int64_t t = J->rows_t[r];
-        const int64_t s0 = seq_start_of(J->offsets, J->batch, t);
+        const int b = seq_of(J->offsets, J->batch, t);
         double* o = J->out + r * (int64_t)J->d;
-        if (s0 < 0) { /* token outside every sequence: not a row */
+        if (b < 0) { /* token outside every sequence: not a row */
             for (int c = 0; c < J->d; ++c) o[c] = NAN;
             continue;
         }
-        oracle_row(J->q, J->k, J->v, s0, t - s0, J->heads, J->d, J->rows_h[r], J->alpha,
-                   J->inv_n, acc, o);
+        const int64_t s0 = J->offsets[b];
+        oracle_row(J->q, J->k, J->v, s0, t - s0, hist_of(J, b), J->heads, J->d, J->rows_h[r],
+                   J->alpha, J->inv_n, acc, o);
     }
     free(acc);
     return NULL;
@@ -144,12 +164,20 @@ static int check_offsets(const int64_t* offsets, int batch) {
     return 0;
 }
 
+/* 0 <= num_targets[b] <= n_b for every sequence (NULL: no candidates). */
+static int check_targets(const int64_t* offsets, const int64_t* num_targets, int batch) {
+    if (!num_targets) return 0;
+    for (int b = 0; b < batch; ++b)
+        if (num_targets[b] < 0 || num_targets[b] > offsets[b + 1] - offsets[b]) return -1;
+    return 0;
+}
+
 /* Every row of every sequence.  out: (total, heads, d) fp64.  Returns 0 or -1. */
 int hstu_oracle_fwd_f64(const float* q, const float* k, const float* v, const int64_t* offsets,
                         int batch, int heads, int d, double alpha, double inv_n, double* out,
                         int nthreads) {
     if (check_offsets(offsets, batch) || heads < 1 || d < 1) return -1;
-    job_t J = {q, k, v, offsets, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0, NULL, NULL};
+    job_t J = {q, k, v, offsets, NULL, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0, NULL, NULL};
     return run(&J, nthreads, worker_full);
 }
 
@@ -160,7 +188,35 @@ int hstu_oracle_rows_f64(const float* q, const float* k, const float* v, const i
                          const int64_t* rows_t, const int32_t* rows_h, int64_t nrows, double* out,
                          int nthreads) {
     if (check_offsets(offsets, batch) || heads < 1 || d < 1 || nrows < 0) return -1;
-    job_t J = {q, k, v, offsets, batch, heads, d, alpha, inv_n, out, rows_t, rows_h, nrows,
+    job_t J = {q, k, v, offsets, NULL, batch, heads, d, alpha, inv_n, out, rows_t, rows_h, nrows,
                NULL, NULL};
+    return run(&J, nthreads, worker_rows);
+}
+
+/* Candidate variant of hstu_oracle_fwd_f64: the last num_targets[b] tokens of
+ * sequence b are candidates (see the header). */
+int hstu_oracle_fwd_targets_f64(const float* q, const float* k, const float* v,
+                                const int64_t* offsets, const int64_t* num_targets, int batch,
+                                int heads, int d, double alpha, double inv_n, double* out,
+                                int nthreads) {
+    if (check_offsets(offsets, batch) || check_targets(offsets, num_targets, batch) ||
+        heads < 1 || d < 1)
+        return -1;
+    job_t J = {q, k, v, offsets, num_targets, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0,
+               NULL, NULL};
+    return run(&J, nthreads, worker_full);
+}
+
+/* Candidate variant of hstu_oracle_rows_f64. */
+int hstu_oracle_rows_targets_f64(const float* q, const float* k, const float* v,
+                                 const int64_t* offsets, const int64_t* num_targets, int batch,
+                                 int heads, int d, double alpha, double inv_n,
+                                 const int64_t* rows_t, const int32_t* rows_h, int64_t nrows,
+                                 double* out, int nthreads) {
+    if (check_offsets(offsets, batch) || check_targets(offsets, num_targets, batch) ||
+        heads < 1 || d < 1 || nrows < 0)
+        return -1;
+    job_t J = {q, k, v, offsets, num_targets, batch, heads, d, alpha, inv_n, out, rows_t, rows_h,
+               nrows, NULL, NULL};
     return run(&J, nthreads, worker_rows);
 }

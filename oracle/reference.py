@@ -7,6 +7,11 @@ The oracle evaluates, for each sequence b, head h and local row i
 block mask including the diagonal; section 4.2 jagged values + offsets):
 
     out[t, h, :] = inv_n * sum_{j <= i} silu(alpha * q[t,h,:].k[off[b]+j,h,:]) * v[off[b]+j,h,:]
+
+With ``num_targets`` (HSTU paper section 3.4 and Appendix H, Algorithm 1:
+the M-FALCON mask), the last num_targets[b] tokens of sequence b are
+candidates: term j of row i is kept iff j <= i and (j < hist or j == i),
+hist = n_b - num_targets[b].
 """
 from __future__ import annotations
 
@@ -37,6 +42,14 @@ def _load():
                                              ctypes.c_double, ctypes.c_double, i64, i32,
                                              ctypes.c_int64, d, ctypes.c_int]
         lib.hstu_oracle_rows_f64.restype = ctypes.c_int
+        lib.hstu_oracle_fwd_targets_f64.argtypes = [f, f, f, i64, i64, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                                    d, ctypes.c_int]
+        lib.hstu_oracle_fwd_targets_f64.restype = ctypes.c_int
+        lib.hstu_oracle_rows_targets_f64.argtypes = [f, f, f, i64, i64, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                                     i64, i32, ctypes.c_int64, d, ctypes.c_int]
+        lib.hstu_oracle_rows_targets_f64.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -61,7 +74,8 @@ def silu(x: float) -> float:
     return _load().hstu_oracle_silu(float(x))
 
 
-def hstu_fwd(q, k, v, offsets, alpha: float, inv_n: float, threads: int | None = None) -> np.ndarray:
+def hstu_fwd(q, k, v, offsets, alpha: float, inv_n: float, threads: int | None = None,
+             num_targets=None) -> np.ndarray:
     """All rows: returns fp64 array (total, heads, d)."""
     qf, kf, vf = _f32(q), _f32(k), _f32(v)
     total, heads, d = qf.shape
@@ -70,17 +84,29 @@ def hstu_fwd(q, k, v, offsets, alpha: float, inv_n: float, threads: int | None =
     if kf.shape != qf.shape or vf.shape != qf.shape or (batch >= 0 and off[-1] != total):
         raise ValueError("shape mismatch between q/k/v/offsets")
     out = np.zeros((total, heads, d), dtype=np.float64)
-    rc = _load().hstu_oracle_fwd_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
-                                     _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
-                                     batch, heads, d, float(alpha), float(inv_n),
-                                     _ptr(out, ctypes.c_double), threads or default_threads())
+    if num_targets is None:
+        rc = _load().hstu_oracle_fwd_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                         _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
+                                         batch, heads, d, float(alpha), float(inv_n),
+                                         _ptr(out, ctypes.c_double), threads or default_threads())
+    else:
+        nt = np.ascontiguousarray(np.asarray(num_targets), dtype=np.int64)
+        if nt.shape != (batch,):
+            raise ValueError("num_targets needs one entry per sequence")
+        rc = _load().hstu_oracle_fwd_targets_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                                 _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
+                                                 _ptr(nt, ctypes.c_int64), batch, heads, d,
+                                                 float(alpha), float(inv_n),
+                                                 _ptr(out, ctypes.c_double),
+                                                 threads or default_threads())
     if rc != 0:
-        raise ValueError("oracle rejected its arguments (offsets must start at 0 and not decrease)")
+        raise ValueError("oracle rejected its arguments (offsets must start at 0 and not decrease; "
+                         "0 <= num_targets <= length)")
     return out
 
 
 def hstu_rows(q, k, v, offsets, alpha: float, inv_n: float, rows_t, rows_h,
-              threads: int | None = None) -> np.ndarray:
+              threads: int | None = None, num_targets=None) -> np.ndarray:
     """Sampled rows: row r is (token rows_t[r], head rows_h[r]); returns fp64 (nrows, d)."""
     qf, kf, vf = _f32(q), _f32(k), _f32(v)
     total, heads, d = qf.shape
@@ -90,11 +116,22 @@ def hstu_rows(q, k, v, offsets, alpha: float, inv_n: float, rows_t, rows_h,
     if rt.shape != rh.shape:
         raise ValueError("rows_t and rows_h differ in length")
     out = np.zeros((len(rt), d), dtype=np.float64)
-    rc = _load().hstu_oracle_rows_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
-                                      _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
-                                      len(off) - 1, heads, d, float(alpha), float(inv_n),
-                                      _ptr(rt, ctypes.c_int64), _ptr(rh, ctypes.c_int32), len(rt),
-                                      _ptr(out, ctypes.c_double), threads or default_threads())
+    if num_targets is None:
+        rc = _load().hstu_oracle_rows_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                          _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
+                                          len(off) - 1, heads, d, float(alpha), float(inv_n),
+                                          _ptr(rt, ctypes.c_int64), _ptr(rh, ctypes.c_int32), len(rt),
+                                          _ptr(out, ctypes.c_double), threads or default_threads())
+    else:
+        nt = np.ascontiguousarray(np.asarray(num_targets), dtype=np.int64)
+        if nt.shape != (len(off) - 1,):
+            raise ValueError("num_targets needs one entry per sequence")
+        rc = _load().hstu_oracle_rows_targets_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                                  _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
+                                                  _ptr(nt, ctypes.c_int64), len(off) - 1, heads, d,
+                                                  float(alpha), float(inv_n), _ptr(rt, ctypes.c_int64),
+                                                  _ptr(rh, ctypes.c_int32), len(rt),
+                                                  _ptr(out, ctypes.c_double), threads or default_threads())
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out

@@ -12,6 +12,15 @@ ascending.  Empty sequences contribute no items (section 4.2, jagged storage).
 
 Each item is four int32: (first token of the sequence, sequence length,
 head, qt).
+
+With candidates (HSTU paper section 3.4 and Appendix H, Algorithm 1: the
+M-FALCON mask), the last num_targets[b] tokens of sequence b see the
+history and themselves only.  With hist = n - num_targets[b] and
+KH = ceil(hist / 128) the key blocks that hold history keys, query block qt
+needs key blocks 0 .. min(qt, KH) - 1 and its diagonal block qt: a block
+strictly between them holds only keys of other candidates, which no row of
+the query block sees.  Such an item costs min(qt, KH) + 1 key blocks, and
+items_targets also returns each item's hist.
 """
 from __future__ import annotations
 
@@ -32,3 +41,23 @@ def items(offsets, heads: int, block_m: int = BLOCK_M) -> np.ndarray:
     rows.sort()
     out = np.array([(s0, n, h, qt) for (_, b, h, qt, s0, n) in rows], dtype=np.int32)
     return out.reshape(-1, 4)
+
+
+def items_targets(offsets, num_targets, heads: int, block_m: int = BLOCK_M):
+    """(items (n, 4) int32, hist (n,) int32), ordered by cost descending,
+    then b, h, qt ascending."""
+    offsets = [int(x) for x in offsets]
+    rows = []
+    for b in range(len(offsets) - 1):
+        n = offsets[b + 1] - offsets[b]
+        hist = n - int(num_targets[b])
+        kh = (hist + block_m - 1) // block_m
+        tiles = (n + block_m - 1) // block_m
+        for h in range(heads):
+            for qt in range(tiles):
+                cost = min(qt, kh) + 1
+                rows.append((-cost, b, h, qt, offsets[b], n, hist))
+    rows.sort()
+    it = np.array([(s0, n, h, qt) for (_, b, h, qt, s0, n, _hist) in rows], dtype=np.int32)
+    hs = np.array([hist for (*_, hist) in rows], dtype=np.int32)
+    return it.reshape(-1, 4), hs

@@ -96,3 +96,69 @@ def test_unmutated_copy_passes(tmp_path):
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(tmp_path, name):
     assert not _pins_pass(_build_mutant(tmp_path, name))
+
+
+# ------------------------------------------------ the candidate (M-FALCON) mask
+TARGET_MUTANTS = {
+    "drop_self_term": ("if (j >= hist && j != i) continue;", "if (j >= hist) continue;"),
+    "history_off_by_one": ("if (j >= hist && j != i) continue;", "if (j > hist && j != i) continue;"),
+    "candidates_see_each_other": ("if (j >= hist && j != i) continue;", "if (j > i) continue;"),
+}
+
+
+def _targets_pins_pass(L) -> bool:
+    """Separate causal passes (the committed causal oracle) and the closed form
+    of a candidates-only sequence, as in test_oracle_targets.py."""
+    from oracle import reference
+    f, dptr, i64 = (ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
+                    ctypes.POINTER(ctypes.c_int64))
+    L.hstu_oracle_fwd_targets_f64.argtypes = [f, f, f, i64, i64, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_double, ctypes.c_double, dptr,
+                                              ctypes.c_int]
+    P = lambda a, t: a.ctypes.data_as(ctypes.POINTER(t))
+
+    def run(q, k, v, off, nt, alpha, inv_n):
+        total, heads, d = q.shape
+        out = np.zeros((total, heads, d))
+        off = np.asarray(off, dtype=np.int64)
+        nt = np.asarray(nt, dtype=np.int64)
+        L.hstu_oracle_fwd_targets_f64(P(q, ctypes.c_float), P(k, ctypes.c_float),
+                                      P(v, ctypes.c_float), P(off, ctypes.c_int64),
+                                      P(nt, ctypes.c_int64), len(off) - 1, heads, d, alpha, inv_n,
+                                      P(out, ctypes.c_double), 2)
+        return out
+
+    rng = np.random.default_rng(5)
+    hist, bm, H, d = 11, 5, 2, 8
+    q, k, v = (rng.standard_normal((hist + bm, H, d)).astype(np.float32) for _ in range(3))
+    got = run(q, k, v, [0, hist + bm], [bm], 0.6, 0.1)
+    ok = True
+    for c in range(bm):
+        idx = list(range(hist)) + [hist + c]
+        sub = reference.hstu_fwd(q[idx], k[idx], v[idx], [0, hist + 1], 0.6, 0.1)
+        ok &= bool(np.allclose(got[hist + c], sub[hist], rtol=1e-12, atol=1e-14))
+    only = run(q, k, v, [0, hist + bm], [hist + bm], 0.6, 0.1)
+    s = 0.6 * np.einsum("thc,thc->th", q.astype(np.float64), k.astype(np.float64))
+    ok &= bool(np.allclose(only, 0.1 * (s * expit(s))[..., None] * v, rtol=1e-12, atol=1e-14))
+    return ok
+
+
+def _build(tmp_path, name, src):
+    path = tmp_path / f"{name}.c"
+    path.write_text(src)
+    lib = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-o", str(lib), str(path),
+                    "-lm", "-lpthread"], check=True)
+    return ctypes.CDLL(str(lib))
+
+
+def test_unmutated_copy_passes_the_candidate_pins(tmp_path):
+    assert _targets_pins_pass(_build(tmp_path, "orig_t", open(oracle_build.SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(TARGET_MUTANTS))
+def test_candidate_mutant_is_caught(tmp_path, name):
+    src = open(oracle_build.SRC).read()
+    old, new = TARGET_MUTANTS[name]
+    assert src.count(old) == 1
+    assert not _targets_pins_pass(_build(tmp_path, name, src.replace(old, new)))
