@@ -52,6 +52,14 @@ _SIGNATURES = {
     "hstu_set_debug_flags": (ctypes.c_int, [ctypes.c_uint32]),
     "hstu_trace_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int, _IP]),
     "hstu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "hstu_attn_fwd_targets": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32P, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                             ctypes.c_float, _VP, _VP]),
+    "hstu_plan_create_targets": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.POINTER(_VP)]),
+    "hstu_plan_item_hist": (ctypes.c_int, [_VP, _I32P, ctypes.c_int, _IP]),
+    "hstu_worklist_build_targets": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int, _I32P,
+                                                   _I32P, ctypes.c_int, _IP]),
 }
 
 _lib = None
@@ -145,6 +153,35 @@ def hstu_attn_fwd(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: 
                                _stream(stream)), "hstu_attn_fwd")
 
 
+def _host_targets(num_targets, batch: int) -> np.ndarray:
+    nt = _host_offsets(num_targets)
+    if nt.shape != (batch,):
+        raise ValueError("num_targets needs one entry per sequence")
+    return nt
+
+
+def hstu_attn_fwd_targets(q, k, v, offsets, num_targets, batch: int, heads: int, d: int,
+                          max_seqlen: int, alpha: float, inv_n: float, out, stream=None) -> None:
+    """hstu_attn_fwd with the M-FALCON candidate mask: the last num_targets[b]
+    tokens of sequence b see the history and themselves only.  ``num_targets``
+    is host memory (CPU tensor or numpy array), one entry per sequence."""
+    keep = None
+    if isinstance(offsets, int):
+        off_ptr = offsets
+    elif hasattr(offsets, "is_cuda") and offsets.is_cuda:
+        if offsets.dtype.itemsize != 4 or not offsets.is_contiguous():
+            raise ValueError("device offsets must be contiguous int32")
+        off_ptr = offsets.data_ptr()
+    else:
+        keep = _host_offsets(offsets)
+        off_ptr = keep.ctypes.data
+    nt = _host_targets(num_targets, int(batch))
+    _check(lib().hstu_attn_fwd_targets(_addr(q), _addr(k), _addr(v), off_ptr,
+                                       nt.ctypes.data_as(_I32P), int(batch), int(heads), int(d),
+                                       int(max_seqlen), float(alpha), float(inv_n), _addr(out),
+                                       _stream(stream)), "hstu_attn_fwd_targets")
+
+
 def hstu_attn_fwd_noalloc(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: int,
                           alpha: float, inv_n: float, out, stream=None) -> None:
     """As hstu_attn_fwd, for callers that cannot let the library allocate.
@@ -195,6 +232,47 @@ def hstu_plan_create(host_offsets, batch: int, heads: int, d: int, max_seqlen: i
     _check(lib().hstu_plan_create(off.ctypes.data_as(_I32P), int(batch), int(heads), int(d),
                                   int(max_seqlen), ctypes.byref(h)), "hstu_plan_create")
     return Plan(h.value, batch, heads, d, max_seqlen, int(off[batch]) if batch else 0)
+
+
+def hstu_plan_create_targets(host_offsets, num_targets, batch: int, heads: int, d: int,
+                             max_seqlen: int) -> Plan:
+    """A plan with the M-FALCON candidate mask (see hstu_attn_fwd_targets)."""
+    off = _host_offsets(host_offsets)
+    if len(off) < batch + 1:
+        raise ValueError("offsets needs batch + 1 entries")
+    nt = _host_targets(num_targets, int(batch))
+    h = _VP()
+    _check(lib().hstu_plan_create_targets(off.ctypes.data_as(_I32P), nt.ctypes.data_as(_I32P),
+                                          int(batch), int(heads), int(d), int(max_seqlen),
+                                          ctypes.byref(h)), "hstu_plan_create_targets")
+    return Plan(h.value, batch, heads, d, max_seqlen, int(off[batch]) if batch else 0)
+
+
+def hstu_plan_item_hist(plan: Plan) -> np.ndarray:
+    n = hstu_plan_num_items(plan)
+    buf = np.zeros(max(n, 1), dtype=np.int32)
+    got = ctypes.c_int()
+    _check(lib().hstu_plan_item_hist(plan.handle, buf.ctypes.data_as(_I32P), max(n, 1),
+                                     ctypes.byref(got)), "hstu_plan_item_hist")
+    return buf[:got.value]
+
+
+def hstu_worklist_build_targets(host_offsets, num_targets, heads: int):
+    """Host-only candidate work list: (items int32 (n, 4), hist int32 (n,))."""
+    off = _host_offsets(host_offsets)
+    batch = len(off) - 1
+    nt = _host_targets(num_targets, batch)
+    n = ctypes.c_int()
+    _check(lib().hstu_worklist_build_targets(off.ctypes.data_as(_I32P), nt.ctypes.data_as(_I32P),
+                                             batch, int(heads), None, None, 0, ctypes.byref(n)),
+           "hstu_worklist_build_targets")
+    items = np.zeros((max(n.value, 1), 4), dtype=np.int32)
+    hist = np.zeros(max(n.value, 1), dtype=np.int32)
+    _check(lib().hstu_worklist_build_targets(off.ctypes.data_as(_I32P), nt.ctypes.data_as(_I32P),
+                                             batch, int(heads), items.ctypes.data_as(_I32P),
+                                             hist.ctypes.data_as(_I32P), n.value, ctypes.byref(n)),
+           "hstu_worklist_build_targets")
+    return items[:n.value], hist[:n.value]
 
 
 def hstu_attn_fwd_plan(plan: Plan, q, k, v, alpha: float, inv_n: float, out, stream=None) -> None:

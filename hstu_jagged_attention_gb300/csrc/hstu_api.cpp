@@ -47,6 +47,31 @@ int check_offsets(const int32_t* off, int batch, long long max_len) {
   return HSTU_OK;
 }
 
+// 0 <= num_targets[b] <= n_b for every sequence.
+int check_targets(const int32_t* off, const int32_t* nt, int batch) {
+  for (int b = 0; b < batch; ++b)
+    if (nt[b] < 0 || nt[b] > off[b + 1] - off[b]) return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
+
+// Work list and (with candidates) the per-item history lengths.
+int build_worklist(const int32_t* off, const int32_t* nt, int batch, int heads,
+                   std::vector<hstu::Item>& items, std::vector<int32_t>& hist) {
+  try {
+    items.resize((size_t)hstu::count_items(off, batch, heads));
+    if (nt) {
+      hist.resize(items.size());
+      hstu::fill_items_targets(off, nt, batch, heads, items.data(), hist.data());
+    } else {
+      hstu::fill_items(off, batch, heads, items.data());
+    }
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
+
 std::vector<hstu::Item> build_items(const int32_t* off, int batch, int heads) {
   std::vector<hstu::Item> items((size_t)hstu::count_items(off, batch, heads));
   hstu::fill_items(off, batch, heads, items.data());
@@ -107,9 +132,9 @@ int device_check(int* sm_count) {
   return HSTU_OK;
 }
 
-int launch(const hstu::Item* d_items, int n_items, long long total, int heads, int d,
-           const void* q, const void* k, const void* v, float alpha, float inv_n, void* out,
-           cudaStream_t stream) {
+int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long long total,
+           int heads, int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
+           void* out, cudaStream_t stream) {
   if (n_items == 0) return HSTU_OK;
   int sms = 0;
   int rc = device_check(&sms);
@@ -120,6 +145,7 @@ int launch(const hstu::Item* d_items, int n_items, long long total, int heads, i
   if ((rc = make_map(&tv, v, total, heads, d)) != HSTU_OK) return rc;
   hstu::FwdArgs a;
   a.items = d_items;
+  a.item_hist = d_hist;
   a.n_items = n_items;
   a.out = out;
   a.heads = heads;
@@ -136,6 +162,14 @@ int launch(const hstu::Item* d_items, int n_items, long long total, int heads, i
     return HSTU_ERR_UNSUPPORTED;
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
+
+// (The plan type is defined below; make_plan and oneshot are declared here
+// and defined after it.)
+int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d, int max_seqlen,
+              hstu_plan** plan);
+int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
+            const int32_t* num_targets, int batch, int heads, int d, int max_seqlen, float alpha,
+            float inv_n, void* out, cudaStream_t s);
 
 }  // namespace
 
@@ -167,16 +201,42 @@ void fill_items(const int32_t* off, int batch, int heads, Item* dst) {
     }
 }
 
+void fill_items_targets(const int32_t* off, const int32_t* num_targets, int batch, int heads,
+                        Item* dst, int32_t* hist_dst) {
+  // (cost, b, h, qt) generated in b, h, qt order; a stable sort by cost
+  // descending then gives cost descending, then b, h, qt ascending
+  struct Entry {
+    int cost, hist;
+    Item item;
+  };
+  std::vector<Entry> e;
+  e.reserve((size_t)count_items(off, batch, heads));
+  for (int b = 0; b < batch; ++b) {
+    const int n = off[b + 1] - off[b];
+    const int hist = n - num_targets[b];
+    const int kh = (hist + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    const int tiles = (n + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    for (int h = 0; h < heads; ++h)
+      for (int qt = 0; qt < tiles; ++qt)
+        e.push_back(Entry{(qt < kh ? qt : kh) + 1, hist, make_int4(off[b], n, h, qt)});
+  }
+  std::stable_sort(e.begin(), e.end(), [](const Entry& x, const Entry& y) { return x.cost > y.cost; });
+  for (size_t i = 0; i < e.size(); ++i) {
+    dst[i] = e[i].item;
+    hist_dst[i] = e[i].hist;
+  }
+}
+
 int host_check_offsets(const int32_t* off, int batch, long long max_len) {
   return check_offsets(off, batch, max_len);
 }
 int host_check_buffers(const void* q, const void* k, const void* v, const void* out) {
   return check_buffers(q, k, v, out);
 }
-int host_launch(const Item* d_items, int n_items, long long total, int heads, int d, const void* q,
-                const void* k, const void* v, float alpha, float inv_n, void* out,
-                cudaStream_t stream) {
-  return launch(d_items, n_items, total, heads, d, q, k, v, alpha, inv_n, out, stream);
+int host_launch(const Item* d_items, const int32_t* d_hist, int n_items, long long total, int heads,
+                int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
+                void* out, cudaStream_t stream) {
+  return launch(d_items, d_hist, n_items, total, heads, d, q, k, v, alpha, inv_n, out, stream);
 }
 }  // namespace hstu
 
@@ -184,9 +244,118 @@ struct hstu_plan {
   int batch = 0, heads = 0, d = 0, max_seqlen = 0;
   long long total = 0;
   std::vector<hstu::Item> items;
-  hstu::Item* d_items = nullptr;
+  std::vector<int32_t> hist;        // history length per item; empty: no candidates
+  hstu::Item* d_items = nullptr;    // device copy of items, then hist (one allocation)
+  int32_t* d_hist = nullptr;
   int device = -1;
 };
+
+namespace {
+
+int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d, int max_seqlen,
+              hstu_plan** plan) {
+  if (!plan) return HSTU_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (heads < 1 || max_seqlen < 0) return HSTU_ERR_INVALID_ARG;
+  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
+  int rc = check_offsets(off, batch, max_seqlen);
+  if (rc != HSTU_OK) return rc;
+  if (nt && (rc = check_targets(off, nt, batch)) != HSTU_OK) return rc;
+  hstu_plan* p = new (std::nothrow) hstu_plan;
+  if (!p) return HSTU_ERR_NO_MEMORY;
+  p->batch = batch;
+  p->heads = heads;
+  p->d = d;
+  p->max_seqlen = max_seqlen;
+  p->total = batch ? off[batch] : 0;
+  if ((rc = build_worklist(off, nt, batch, heads, p->items, p->hist)) != HSTU_OK) {
+    delete p;
+    return rc;
+  }
+  if (!p->items.empty()) {
+    // one allocation: the items, then (with candidates) the history lengths
+    const size_t ibytes = p->items.size() * sizeof(hstu::Item);
+    const size_t hbytes = p->hist.size() * sizeof(int32_t);
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+      delete p;
+      return HSTU_ERR_CUDA;
+    }
+    const cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p->d_items), ibytes + hbytes);
+    if (e != cudaSuccess) {
+      delete p;
+      return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+    }
+    if (hbytes) p->d_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(p->d_items) + ibytes);
+    if (cudaMemcpy(p->d_items, p->items.data(), ibytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+        (hbytes &&
+         cudaMemcpy(p->d_hist, p->hist.data(), hbytes, cudaMemcpyHostToDevice) != cudaSuccess)) {
+      cudaFree(p->d_items);
+      delete p;
+      return HSTU_ERR_CUDA;
+    }
+  }
+  *plan = p;
+  return HSTU_OK;
+}
+
+int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
+            const int32_t* num_targets, int batch, int heads, int d, int max_seqlen, float alpha,
+            float inv_n, void* out, cudaStream_t s) {
+  if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
+  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
+  if (batch == 0) return HSTU_OK;
+  if (!offsets) return HSTU_ERR_INVALID_ARG;
+
+  // Offsets may live on the host or on the device.
+  std::vector<int32_t> host_off;
+  const int32_t* off = offsets;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, offsets) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (attr.type == cudaMemoryTypeDevice) {
+    try {
+      host_off.resize((size_t)batch + 1);
+    } catch (const std::bad_alloc&) {
+      return HSTU_ERR_NO_MEMORY;
+    }
+    if (cudaMemcpyAsync(host_off.data(), offsets, host_off.size() * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+    off = host_off.data();
+  }
+  int rc = check_offsets(off, batch, max_seqlen);
+  if (rc != HSTU_OK) return rc;
+  if (num_targets && (rc = check_targets(off, num_targets, batch)) != HSTU_OK) return rc;
+  const long long total = off[batch];
+  if (total == 0) return HSTU_OK;
+  if ((rc = check_buffers(q, k, v, out)) != HSTU_OK) return rc;
+
+  std::vector<hstu::Item> items;
+  std::vector<int32_t> hist;
+  if ((rc = build_worklist(off, num_targets, batch, heads, items, hist)) != HSTU_OK) return rc;
+  if (items.empty()) return HSTU_OK;
+  const size_t ibytes = items.size() * sizeof(hstu::Item);
+  const size_t hbytes = hist.size() * sizeof(int32_t);
+  hstu::Item* d_items = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_items), ibytes + hbytes, s);
+  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+  int32_t* d_hist =
+      hbytes ? reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_items) + ibytes) : nullptr;
+  // Pageable sources: each call returns once the bytes are staged, so the
+  // host vectors may go out of scope afterwards.
+  e = cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && hbytes)
+    e = cudaMemcpyAsync(d_hist, hist.data(), hbytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(d_items, s);
+    return HSTU_ERR_CUDA;
+  }
+  rc = launch(d_items, d_hist, (int)items.size(), total, heads, d, q, k, v, alpha, inv_n, out, s);
+  if (cudaFreeAsync(d_items, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
+  return rc;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -226,48 +395,13 @@ int hstu_worklist_build(const int32_t* host_offsets, int batch, int heads, int32
 
 int hstu_plan_create(const int32_t* host_offsets, int batch, int heads, int d, int max_seqlen,
                      hstu_plan** plan) {
-  if (!plan) return HSTU_ERR_INVALID_ARG;
-  *plan = nullptr;
-  if (heads < 1 || max_seqlen < 0) return HSTU_ERR_INVALID_ARG;
-  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
-  int rc = check_offsets(host_offsets, batch, max_seqlen);
-  if (rc != HSTU_OK) return rc;
-  hstu_plan* p = new (std::nothrow) hstu_plan;
-  if (!p) return HSTU_ERR_NO_MEMORY;
-  p->batch = batch;
-  p->heads = heads;
-  p->d = d;
-  p->max_seqlen = max_seqlen;
-  p->total = batch ? host_offsets[batch] : 0;
-  try {
-    p->items = build_items(host_offsets, batch, heads);
-  } catch (const std::bad_alloc&) {
-    delete p;
-    return HSTU_ERR_NO_MEMORY;
-  }
-  if (p->items.size() > (size_t)INT32_MAX) {
-    delete p;
-    return HSTU_ERR_INVALID_ARG;
-  }
-  if (!p->items.empty()) {
-    const size_t bytes = p->items.size() * sizeof(hstu::Item);
-    if (cudaGetDevice(&p->device) != cudaSuccess) {
-      delete p;
-      return HSTU_ERR_CUDA;
-    }
-    const cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p->d_items), bytes);
-    if (e != cudaSuccess) {
-      delete p;
-      return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
-    }
-    if (cudaMemcpy(p->d_items, p->items.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess) {
-      cudaFree(p->d_items);
-      delete p;
-      return HSTU_ERR_CUDA;
-    }
-  }
-  *plan = p;
-  return HSTU_OK;
+  return make_plan(host_offsets, nullptr, batch, heads, d, max_seqlen, plan);
+}
+
+int hstu_plan_create_targets(const int32_t* host_offsets, const int32_t* host_num_targets, int batch,
+                             int heads, int d, int max_seqlen, hstu_plan** plan) {
+  if (!host_num_targets && batch > 0) return HSTU_ERR_INVALID_ARG;
+  return make_plan(host_offsets, host_num_targets, batch, heads, d, max_seqlen, plan);
 }
 
 int hstu_plan_destroy(hstu_plan* plan) {
@@ -293,6 +427,35 @@ int hstu_plan_worklist(const hstu_plan* plan, int32_t* host_dst, int capacity, i
   return HSTU_OK;
 }
 
+int hstu_plan_item_hist(const hstu_plan* plan, int32_t* host_dst, int capacity, int* n_items) {
+  if (!plan || !n_items) return HSTU_ERR_INVALID_ARG;
+  *n_items = (int)plan->items.size();
+  if (!host_dst) return HSTU_OK;
+  if (capacity < (int)plan->items.size()) return HSTU_ERR_INVALID_ARG;
+  for (size_t i = 0; i < plan->items.size(); ++i)
+    host_dst[i] = plan->hist.empty() ? plan->items[i].y : plan->hist[i];
+  return HSTU_OK;
+}
+
+int hstu_worklist_build_targets(const int32_t* host_offsets, const int32_t* host_num_targets,
+                                int batch, int heads, int32_t* host_items, int32_t* host_hist,
+                                int capacity, int* n_items) {
+  if (!n_items || heads < 1 || capacity < 0 || (!host_num_targets && batch > 0))
+    return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(host_offsets, batch, -1);
+  if (rc != HSTU_OK) return rc;
+  if ((rc = check_targets(host_offsets, host_num_targets, batch)) != HSTU_OK) return rc;
+  std::vector<hstu::Item> items;
+  std::vector<int32_t> hist;
+  if ((rc = build_worklist(host_offsets, host_num_targets, batch, heads, items, hist)) != HSTU_OK)
+    return rc;
+  *n_items = (int)items.size();
+  const size_t n = std::min(items.size(), (size_t)capacity);
+  if (host_items) std::memcpy(host_items, items.data(), n * sizeof(hstu::Item));
+  if (host_hist) std::memcpy(host_hist, hist.data(), n * sizeof(int32_t));
+  return HSTU_OK;
+}
+
 int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_bytes) {
   if (!plan || !grid || !block || !smem_bytes) return HSTU_ERR_INVALID_ARG;
   int sms = 0;
@@ -310,64 +473,25 @@ int hstu_attn_fwd_plan(const hstu_plan* plan, const void* q, const void* k, cons
   if (plan->items.empty()) return HSTU_OK;
   int rc = check_buffers(q, k, v, out);
   if (rc != HSTU_OK) return rc;
-  return launch(plan->d_items, (int)plan->items.size(), plan->total, plan->heads, plan->d, q, k, v,
+  return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
+                plan->d, q, k, v,
                 alpha, inv_n, out, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_attn_fwd(const void* q, const void* k, const void* v, const int32_t* offsets, int batch,
                   int heads, int d, int max_seqlen, float alpha, float inv_n, void* out,
                   hstu_stream_t stream) {
-  if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
-  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
-  if (batch == 0) return HSTU_OK;
-  if (!offsets) return HSTU_ERR_INVALID_ARG;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return oneshot(q, k, v, offsets, nullptr, batch, heads, d, max_seqlen, alpha, inv_n, out,
+                 reinterpret_cast<cudaStream_t>(stream));
+}
 
-  // Offsets may live on the host or on the device.
-  std::vector<int32_t> host_off;
-  const int32_t* off = offsets;
-  cudaPointerAttributes attr;
-  if (cudaPointerGetAttributes(&attr, offsets) != cudaSuccess) return HSTU_ERR_CUDA;
-  if (attr.type == cudaMemoryTypeDevice) {
-    try {
-      host_off.resize((size_t)batch + 1);
-    } catch (const std::bad_alloc&) {
-      return HSTU_ERR_NO_MEMORY;
-    }
-    if (cudaMemcpyAsync(host_off.data(), offsets, host_off.size() * sizeof(int32_t),
-                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-      return HSTU_ERR_CUDA;
-    off = host_off.data();
-  }
-  int rc = check_offsets(off, batch, max_seqlen);
-  if (rc != HSTU_OK) return rc;
-  const long long total = off[batch];
-  if (total == 0) return HSTU_OK;
-  if ((rc = check_buffers(q, k, v, out)) != HSTU_OK) return rc;
-
-  std::vector<hstu::Item> items;
-  try {
-    items = build_items(off, batch, heads);
-  } catch (const std::bad_alloc&) {
-    return HSTU_ERR_NO_MEMORY;
-  }
-  if (items.empty()) return HSTU_OK;
-  if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
-  const size_t bytes = items.size() * sizeof(hstu::Item);
-  hstu::Item* d_items = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_items), bytes, s);
-  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
-  // Pageable source: the call returns once the bytes are staged, so the
-  // host vector may go out of scope afterwards.
-  e = cudaMemcpyAsync(d_items, items.data(), bytes, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) {
-    cudaFreeAsync(d_items, s);
-    return HSTU_ERR_CUDA;
-  }
-  rc = launch(d_items, (int)items.size(), total, heads, d, q, k, v, alpha, inv_n, out, s);
-  if (cudaFreeAsync(d_items, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
-  return rc;
+int hstu_attn_fwd_targets(const void* q, const void* k, const void* v, const int32_t* offsets,
+                          const int32_t* host_num_targets, int batch, int heads, int d,
+                          int max_seqlen, float alpha, float inv_n, void* out,
+                          hstu_stream_t stream) {
+  if (!host_num_targets && batch > 0) return HSTU_ERR_INVALID_ARG;
+  return oneshot(q, k, v, offsets, host_num_targets, batch, heads, d, max_seqlen, alpha, inv_n, out,
+                 reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_last_status(int* device_status, int* site) {

@@ -449,6 +449,7 @@ struct Cfg {
 // A work item decoded: query block qt of one (sequence, head).
 struct Block {
   int s0, n, h, qt;
+  int hist;  // history tokens of the sequence (n when it has no candidates)
   __device__ __forceinline__ int rows() const {  // valid query rows (1..128)
     const int r = n - kBM * qt;
     return r < kBM ? r : kBM;
@@ -461,6 +462,20 @@ struct Block {
     const int r = n - kBN * kt;
     return r >= kBN ? kBN : ((r + 15) & ~15);
   }
+  // Key blocks the item walks (HSTU paper Appendix H, the M-FALCON mask):
+  // the blocks that hold history keys, 0 .. min(qt, KH) - 1 with
+  // KH = ceil(hist / 128), then the diagonal block qt.  A block between them
+  // holds only keys of other candidates.  Without candidates (hist = n,
+  // KH > qt) this is 0 .. qt.
+  __device__ __forceinline__ int nk() const {
+    const int kh = (hist + kBN - 1) / kBN;
+    return (qt < kh ? qt : kh) + 1;
+  }
+  __device__ __forceinline__ int key_block(int ki) const { return ki == nk() - 1 ? qt : ki; }
+  // No key of block kt is masked: an off-diagonal block of history keys only.
+  __device__ __forceinline__ bool unmasked(int kt) const {
+    return kt != qt && kBN * kt + kBN <= hist;
+  }
 };
 
 __device__ __forceinline__ bool load_block(const FwdArgs& a, int it, Block& b) {
@@ -471,27 +486,33 @@ __device__ __forceinline__ bool load_block(const FwdArgs& a, int it, Block& b) {
   b.n = x.y;
   b.h = x.z;
   b.qt = x.w;
+  b.hist = a.item_hist ? __ldg(&a.item_hist[idx]) : x.y;
   return true;
 }
 
-// A cursor over the CTA's key-block steps: item `it` (block b) at key block
-// kt; tc counts the steps.  The next item's block is fetched one item ahead
+// A cursor over the CTA's key-block steps: item `it` (block b) at its
+// ki-th key block kt; tc counts the steps.  The next item's block is fetched one item ahead
 // so that crossing into it does not wait on a global load.
 struct Cursor {
-  int it, kt;
+  int it, kt, ki;  // ki: index of the step among the item's key blocks; kt = b.key_block(ki)
   uint32_t tc;
   Block b, nb;
   bool valid, nvalid;
   __device__ __forceinline__ void start(const FwdArgs& a) {
     it = 0;
     kt = 0;
+    ki = 0;
     tc = 0;
     valid = load_block(a, 0, b);
     nvalid = valid && load_block(a, 1, nb);
   }
   __device__ __forceinline__ void advance(const FwdArgs& a) {
     ++tc;
-    if (++kt > b.qt) {
+    const int nk = b.nk();
+    if (++ki < nk) {
+      kt = ki == nk - 1 ? b.qt : ki;
+    } else {
+      ki = 0;
       kt = 0;
       ++it;
       valid = nvalid;
@@ -562,7 +583,9 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
                     ch * C::CHUNK, b.h, b.s0 + kBM * b.qt);
       ++qc;
     }
-    for (int kt = 0; kt <= b.qt; ++kt) {
+    const int nk = b.nk();
+    for (int ki = 0; ki < nk; ++ki) {
+      const int kt = b.key_block(ki);
       const int slot = (int)(c % C::P);
       // A parity wait is exact only while the barrier is at most one phase
       // short of the awaited one.  K(c) waits for phase c/P - 1 of S-full
@@ -771,7 +794,8 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
 // t + 16 + 8h + [0, 8).  Processed in 16-key halves to keep register
 // pressure down.
 template <bool MASK>
-__device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, uint32_t t) {
+__device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, int lim_hist,
+                                             uint32_t t) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t hi[8], lo[8];
@@ -781,8 +805,10 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
       const float2 x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
       float2 p = __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
       if (MASK) {
-        p.x = (k > lim) ? 0.0f : p.x;
-        p.y = (k + 1 > lim) ? 0.0f : p.y;
+        // keep key k iff k <= lim (causal) and (k < lim_hist or k == lim):
+        // a key past the history is seen by its own row only
+        p.x = (k > lim || (k >= lim_hist && k != lim)) ? 0.0f : p.x;
+        p.y = (k + 1 > lim || (k + 1 >= lim_hist && k + 1 != lim)) ? 0.0f : p.y;
       }
       const uint32_t ph = pack_bf16x2(p.x, p.y);
       const float2 r = __fadd2_rn(
@@ -829,24 +855,33 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
     tc_fence_after();
     trace(a, kEvSiluStart, cur.tc);
     const uint32_t t_s = lane_base + (uint32_t)(j * 128);
-    if (cur.kt != cur.b.qt && quarter * 32 < cur.b.rows()) {
+    if (cur.b.unmasked(cur.kt) && quarter * 32 < cur.b.rows()) {
       tmem_ld32_async(t_s, s0);
       tmem_wait_ld(s0);
 #pragma unroll 1
       for (int c = 0; c < 4; c += 2) {
         tmem_ld32_async(t_s + 32u * (c + 1), s1);
-        silu_store32<false>(s0, ha2, 0, t_s + 32u * c);
+        silu_store32<false>(s0, ha2, 0, 0, t_s + 32u * c);
         tmem_wait_ld(s1);
         if (c + 2 < 4) tmem_ld32_async(t_s + 32u * (c + 2), s0);
-        silu_store32<false>(s1, ha2, 0, t_s + 32u * (c + 1));
+        silu_store32<false>(s1, ha2, 0, 0, t_s + 32u * (c + 1));
         if (c + 2 < 4) tmem_wait_ld(s0);
       }
       tmem_wait_st();
     } else if (quarter * 32 < cur.b.rows()) {
+      // masked block: the diagonal one (keep keys j <= row), or one that
+      // reaches past the history (keys of candidates are seen by their own
+      // row only).  On the diagonal block, chunks c > quarter lie wholly
+      // above the diagonal for this warp (zeros); columns >= cols are not
+      // read by the PV products.
       const int cols = cur.b.cols(cur.kt);
+      const bool diag = cur.kt == cur.b.qt;
+      // row and history end relative to the block's first key
+      const int lim0 = kBM * cur.b.qt + row - kBN * cur.kt;
+      const int hist0 = cur.b.hist - kBN * cur.kt;
 #pragma unroll 1
       for (int c = 0; c < 4 && 32 * c < cols; ++c) {
-        if (c > quarter) {
+        if (diag && c > quarter) {
           uint32_t z[16];
 #pragma unroll
           for (int m = 0; m < 16; ++m) z[m] = 0u;
@@ -854,7 +889,7 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
           tmem_st16(t_s + 32u * c + 16u, z);
         } else {
           tmem_ld32(t_s + 32u * c, s1);
-          silu_store32<true>(s1, ha2, row - 32 * c, t_s + 32u * c);
+          silu_store32<true>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c, t_s + 32u * c);
         }
       }
       tmem_wait_st();

@@ -17,9 +17,16 @@ using Item = int4;
 // (qt descending, then sequence, head, qt ascending).
 long long count_items(const int32_t* off, int batch, int heads);
 void fill_items(const int32_t* off, int batch, int heads, Item* dst);
+// With candidates (the last num_targets[b] tokens of sequence b see the
+// history and themselves only): the same items, each costing
+// min(qt, ceil(hist/128)) + 1 key blocks, ordered by cost descending, then
+// sequence, head, qt ascending; hist_dst[i] is item i's history length.
+void fill_items_targets(const int32_t* off, const int32_t* num_targets, int batch, int heads,
+                        Item* dst, int32_t* hist_dst);
 
 struct FwdArgs {
   const Item* items;   // device, n_items entries, longest first
+  const int32_t* item_hist;  // device, history length per item; null: no candidates
   int n_items;
   void* out;           // bf16 (total, heads, d)
   int heads;
@@ -59,8 +66,8 @@ cudaError_t read_and_clear_device_status(unsigned* status, unsigned* site);
 // shared with hstu_noalloc.cu.
 int host_check_offsets(const int32_t* off, int batch, long long max_len);
 int host_check_buffers(const void* q, const void* k, const void* v, const void* out);
-int host_launch(const Item* d_items, int n_items, long long total, int heads, int d, const void* q,
-                const void* k, const void* v, float alpha, float inv_n, void* out,
-                cudaStream_t stream);
+int host_launch(const Item* d_items, const int32_t* d_hist, int n_items, long long total, int heads,
+                int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
+                void* out, cudaStream_t stream);
 
 }  // namespace hstu

@@ -22,6 +22,12 @@ The five workloads follow the shapes the pages measure or describe:
 Seeds: lengths use ``seed = index`` (0..4); Q, K and V use
 ``seed = 1000 + index`` and are drawn in that order.  Values are fp32
 standard normals times sigma, rounded to bf16 with round-to-nearest-even.
+
+One more workload exercises the candidate (M-FALCON) mask of the HSTU paper
+(section 3.4, Appendix H): ``candidates`` -- 32 sequences, each a user
+history of 2048..8192 tokens followed by b_m = 1024 ranking candidates
+(the appendix takes b_m of the order of n), 4 heads, d = 64.  Its lengths
+use seed 5 and Q, K, V seed 1005.
 """
 from __future__ import annotations
 
@@ -149,3 +155,17 @@ def draw_qkv(w: Workload, seed: int | None = None):
             x *= np.float32(w.sigma)
         out.append(bf16_round(x))
     return tuple(out)
+
+
+CANDIDATES_INDEX = 5
+CANDIDATES_BM = 1024
+
+
+def candidate_workload() -> tuple[Workload, np.ndarray]:
+    """The ``candidates`` workload and its int32 num_targets (see the module doc)."""
+    rng = np.random.default_rng(CANDIDATES_INDEX)
+    hist = rng.integers(2048, 8193, size=32).astype(np.int64)
+    lengths = hist + CANDIDATES_BM
+    w = Workload("candidates", CANDIDATES_INDEX, len(lengths), 4, 64, 1.0, lengths,
+                 1.0 / math.sqrt(64), 1.0 / int(lengths.max()))
+    return w, np.full(len(lengths), CANDIDATES_BM, dtype=np.int32)

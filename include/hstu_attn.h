@@ -193,6 +193,46 @@ int hstu_worklist_build(const int32_t* host_offsets, int batch, int heads, int32
                         int capacity, int* n_items);
 
 /*
+ * Candidates (M-FALCON): HSTU paper section 3.4 and Appendix H, Algorithm 1.
+ *
+ * For ranking, the last num_targets[b] tokens of sequence b are candidates
+ * that must not see one another: with hist = n_b - num_targets[b] (the
+ * history) the causal sum above is further restricted, for token t = the
+ * i-th of its sequence, to
+ *
+ *     keys j (sequence-local) with  j <= i  and  (j < hist  or  j == i),
+ *
+ * so each candidate's output equals that of a separate causal pass over the
+ * history followed by that candidate alone.  Query block qt then needs only
+ * the key blocks that hold history keys, 0 .. min(qt, ceil(hist/128)) - 1,
+ * and its diagonal block qt; its work item costs min(qt, ceil(hist/128)) + 1
+ * key blocks.  num_targets[b] = 0 everywhere is the causal operation.
+ *
+ *   host_num_targets  int32[batch], host memory, 0 <= num_targets[b] <= n_b;
+ *                     read during the call only.
+ *
+ * hstu_attn_fwd_targets    as hstu_attn_fwd, with the candidate mask.
+ * hstu_plan_create_targets as hstu_plan_create; hstu_attn_fwd_plan then
+ *                          applies the mask.  Items are ordered by cost
+ *                          descending, then sequence, head, qt ascending.
+ * hstu_plan_item_hist      copies each item's history length (the sequence
+ *                          length for a plan without candidates).
+ * hstu_worklist_build_targets  the host-only work list: items as
+ *                          hstu_worklist_build, and each item's history length.
+ * Errors: as the causal counterparts; HSTU_ERR_INVALID_ARG also for a NULL
+ * host_num_targets with batch > 0 or a count outside [0, n_b].
+ */
+int hstu_attn_fwd_targets(const void* q, const void* k, const void* v, const int32_t* offsets,
+                          const int32_t* host_num_targets, int batch, int heads, int d,
+                          int max_seqlen, float alpha, float inv_n, void* out, hstu_stream_t stream);
+int hstu_plan_create_targets(const int32_t* host_offsets, const int32_t* host_num_targets, int batch,
+                             int heads, int d, int max_seqlen, hstu_plan** plan);
+int hstu_plan_item_hist(const hstu_plan* plan, int32_t* host_dst, int capacity, int* n_items);
+int hstu_worklist_build_targets(const int32_t* host_offsets, const int32_t* host_num_targets,
+                                int batch, int heads, int32_t* host_items, int32_t* host_hist,
+                                int capacity, int* n_items);
+
+/*
  * hstu_launch_shape -- the grid the next launch for `plan` would use on the
  * current device: *grid persistent CTAs of *block threads with *smem_bytes
  * of dynamic shared memory.  Queries device attributes; launches nothing.

@@ -123,3 +123,36 @@ def test_empty_plan_needs_no_device():
 
 def test_build_flags_target_sm103a():
     assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+# ------------------------------------------------ candidates (M-FALCON mask)
+@pytest.mark.parametrize("seed", range(12))
+def test_candidate_worklist_bit_exact_random(seed):
+    rng = np.random.default_rng(300 + seed)
+    nb = int(rng.integers(0, 30))
+    lengths = rng.integers(0, 900, size=nb)
+    nt = [int(rng.integers(0, n + 1)) if rng.random() < 0.8 else 0 for n in lengths]
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    heads = int(rng.integers(1, 5))
+    items, hist = binding.hstu_worklist_build_targets(off, nt, heads)
+    ref_items, ref_hist = oracle_worklist.items_targets(off, nt, heads)
+    assert np.array_equal(items, ref_items.reshape(-1, 4))
+    assert np.array_equal(hist, ref_hist)
+
+
+def test_candidate_worklist_without_candidates_is_the_causal_one():
+    w = workloads.workload("serving")
+    items, hist = binding.hstu_worklist_build_targets(w.offsets, np.zeros(w.batch, np.int32), w.heads)
+    assert np.array_equal(items, binding.hstu_worklist_build(w.offsets, w.heads))
+    assert np.array_equal(hist, items[:, 1])
+
+
+@pytest.mark.parametrize("nt", [[-1, 0], [0, 4], [6, 0]])
+def test_candidate_counts_are_validated(nt):
+    off = np.array([0, 5, 8], np.int32)   # lengths 5 and 3
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_worklist_build_targets(off, nt, 1)
+    assert e.value.code == binding.HSTU_ERR_INVALID_ARG
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_plan_create_targets(off, nt, 2, 1, 64, 8)
+    assert e.value.code == binding.HSTU_ERR_INVALID_ARG
