@@ -49,9 +49,25 @@ KERNEL_SOURCE = os.path.join(ROOT, "hstu_jagged_attention_gb300", "csrc", "hstu_
 MEASURED_TRAFFIC = {"dense": 165491456.0, "sha256": "7f54c974fa66484b1de7ed999dd2c7ee3bbcc40a9988093a636196bef2cc3d48"}
 
 
-def causal_flops(w: workloads.Workload) -> float:
+def causal_flops(w: workloads.Workload, num_targets=None) -> float:
+    """4 d FLOPs per kept (query, key) pair, every head.  With candidates
+    (M-FALCON mask) a sequence keeps hist (hist + 1) / 2 history pairs and,
+    per candidate, hist + 1 pairs (the history and itself)."""
     L = w.lengths.astype(np.float64)
-    return float(4.0 * w.d * w.heads * np.sum(L * (L + 1) / 2.0))
+    if num_targets is None:
+        pairs = np.sum(L * (L + 1) / 2.0)
+    else:
+        bm = np.asarray(num_targets, dtype=np.float64)
+        hist = L - bm
+        pairs = np.sum(hist * (hist + 1) / 2.0 + bm * (hist + 1))
+    return float(4.0 * w.d * w.heads * pairs)
+
+
+def workload_by_name(name: str):
+    """(workload, num_targets or None)."""
+    if name == "candidates":
+        return workloads.candidate_workload()
+    return workloads.workload(name), None
 
 
 def algorithmic_bytes(w: workloads.Workload) -> float:
@@ -163,7 +179,8 @@ def aggregate(flops_per_rank: float, ms_local: float, world: int, device=None):
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12, ms_max
 
 
-def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int | None = None):
+def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int | None = None,
+                      num_targets=None):
     """Time the oracle on a bounded, uniformly random sample of rows.
 
     Returns (flops_of_sample / seconds, description, threads, seconds)."""
@@ -172,29 +189,37 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
     rng = np.random.default_rng(seed)
     off = w.offsets.astype(np.int64)
     seq_of = np.repeat(np.arange(w.batch), w.lengths)
+    hist_of = (w.lengths - (np.asarray(num_targets, dtype=np.int64) if num_targets is not None
+                            else 0)).astype(np.int64)
 
     def rows(nr):
         t = rng.integers(0, w.total, size=nr)
         h = rng.integers(0, w.heads, size=nr)
         i = t - off[seq_of[t]]
-        return t, h, float(np.sum(4.0 * w.d * (i + 1)))
+        hist = hist_of[seq_of[t]]
+        kept = np.where(i < hist, i + 1, hist + 1)
+        return t, h, float(np.sum(4.0 * w.d * kept))
+
+    def oracle(t, h):
+        reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads,
+                            num_targets=num_targets)
 
     # calibrate on a small sample, then size the real one to ~target_s
     t, h, fl = rows(64)
     t0 = time.perf_counter()
-    reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads)
+    oracle(t, h)
     dt = max(time.perf_counter() - t0, 1e-4)
     n = int(max(64, min(2_000_000, 64 * target_s / dt)))
     t, h, fl = rows(n)
     t0 = time.perf_counter()
-    reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads)
+    oracle(t, h)
     dt = time.perf_counter() - t0
     desc = (f"{n} uniformly sampled (token, head) output rows of the {w.name} workload "
             f"({fl / 1e9:.2f} causal GFLOP), fp64 C oracle, {threads} threads")
     return fl / dt / 1e12, desc, threads, dt
 
 
-def run_reference(args, w):
+def run_reference(args, w, nt=None):
     world, rank, _ = dist_init()
     if rank != 0:
         return 0
@@ -204,7 +229,8 @@ def run_reference(args, w):
     vals = []
     desc, threads = "", 0
     for s in range(args.warmup + args.steps):
-        val, desc, threads, dt = cpu_oracle_sample(w, qf, kf, vf, per_step_s, seed=s)
+        val, desc, threads, dt = cpu_oracle_sample(w, qf, kf, vf, per_step_s, seed=s,
+                                                   num_targets=nt)
         if s >= args.warmup:
             vals.append(val)
     value = statistics.mean(vals)
@@ -212,7 +238,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, **w.describe()},
+        "config": {"workload": w.name, **w.describe(), **_targets_desc(nt)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -220,7 +246,15 @@ def run_reference(args, w):
     return 0
 
 
-def run_ours(args, w):
+def _targets_desc(nt) -> dict:
+    if nt is None:
+        return {}
+    return {"mask": "M-FALCON candidates (HSTU paper Appendix H)",
+            "num_targets_per_sequence": int(np.asarray(nt)[0]) if len(set(np.asarray(nt).tolist())) == 1
+            else "varies"}
+
+
+def run_ours(args, w, nt=None):
     import torch
     from hstu_jagged_attention_gb300 import binding, build
 
@@ -238,7 +272,10 @@ def run_ours(args, w):
     q_h, k_h, v_h = workloads.draw_qkv(w)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     out = torch.empty_like(q)
-    plan = binding.hstu_plan_create(w.offsets, w.batch, w.heads, w.d, w.max_seqlen)
+    if nt is None:
+        plan = binding.hstu_plan_create(w.offsets, w.batch, w.heads, w.d, w.max_seqlen)
+    else:
+        plan = binding.hstu_plan_create_targets(w.offsets, nt, w.batch, w.heads, w.d, w.max_seqlen)
     n_items = binding.hstu_plan_num_items(plan)
     grid, block, smem = binding.hstu_launch_shape(plan)
     stream = torch.cuda.current_stream(dev)
@@ -272,7 +309,7 @@ def run_ours(args, w):
     clocks = sampler.stop(wall0, wall0 + wall, t_warm)
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(times_ms)
-    flops = causal_flops(w)
+    flops = causal_flops(w, nt)
     value, ms_max = aggregate(flops, ms, world, dev)
     st, site = binding.hstu_last_status()
     if st != binding.HSTU_OK:
@@ -296,8 +333,12 @@ def run_ours(args, w):
         qe.copy_(pin[0], non_blocking=True)
         ke.copy_(pin[1], non_blocking=True)
         ve.copy_(pin[2], non_blocking=True)
-        binding.hstu_attn_fwd(qe, ke, ve, offsets_host, w.batch, w.heads, w.d, w.max_seqlen,
-                              w.alpha, w.inv_n, oe, stream)
+        if nt is None:
+            binding.hstu_attn_fwd(qe, ke, ve, offsets_host, w.batch, w.heads, w.d, w.max_seqlen,
+                                  w.alpha, w.inv_n, oe, stream)
+        else:
+            binding.hstu_attn_fwd_targets(qe, ke, ve, offsets_host, nt, w.batch, w.heads, w.d,
+                                          w.max_seqlen, w.alpha, w.inv_n, oe, stream)
         out_h.copy_(oe, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -332,7 +373,7 @@ def run_ours(args, w):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         qf, kf, vf = (t.float().numpy() for t in (q_h, k_h, v_h))
-        val, desc, threads, _ = cpu_oracle_sample(w, qf, kf, vf, args.cpu_seconds)
+        val, desc, threads, _ = cpu_oracle_sample(w, qf, kf, vf, args.cpu_seconds, num_targets=nt)
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
 
     binding.hstu_plan_destroy(plan)
@@ -341,7 +382,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {**w.describe(), "l2": "flushed between steps (256 MiB write)",
+            "config": {**w.describe(), **_targets_desc(nt), "l2": "flushed between steps (256 MiB write)",
                        "work_items": n_items, "grid": grid, "block": block, "smem_bytes": smem,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * achieved / peak,
@@ -369,18 +410,19 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=workloads.WORKLOAD_NAMES, default="dense")
+    ap.add_argument("--workload", choices=list(workloads.WORKLOAD_NAMES) + ["candidates"],
+                    default="dense")
     ap.add_argument("--sweep", action="store_true", help="one line per workload (extra lines)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    names = list(workloads.WORKLOAD_NAMES) if args.sweep else [args.workload]
+    names = list(workloads.WORKLOAD_NAMES) + ["candidates"] if args.sweep else [args.workload]
     rc = 0
     for name in names:
-        w = workloads.workload(name)
-        rc |= run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+        w, nt = workload_by_name(name)
+        rc |= run_reference(args, w, nt) if args.impl == "reference" else run_ours(args, w, nt)
     return rc
 
 

@@ -449,7 +449,6 @@ struct Cfg {
 // A work item decoded: query block qt of one (sequence, head).
 struct Block {
   int s0, n, h, qt;
-  int hist;  // history tokens of the sequence (n when it has no candidates)
   __device__ __forceinline__ int rows() const {  // valid query rows (1..128)
     const int r = n - kBM * qt;
     return r < kBM ? r : kBM;
@@ -462,23 +461,27 @@ struct Block {
     const int r = n - kBN * kt;
     return r >= kBN ? kBN : ((r + 15) & ~15);
   }
-  // Key blocks the item walks (HSTU paper Appendix H, the M-FALCON mask):
-  // the blocks that hold history keys, 0 .. min(qt, KH) - 1 with
-  // KH = ceil(hist / 128), then the diagonal block qt.  A block between them
-  // holds only keys of other candidates.  Without candidates (hist = n,
-  // KH > qt) this is 0 .. qt.
-  __device__ __forceinline__ int nk() const {
-    const int kh = (hist + kBN - 1) / kBN;
-    return (qt < kh ? qt : kh) + 1;
-  }
-  __device__ __forceinline__ int key_block(int ki) const { return ki == nk() - 1 ? qt : ki; }
+};
+
+// An item of the candidate mask, with its history length.
+struct BlockTgt : Block {
+  int hist;  // history tokens of the sequence
+  int nk;    // key blocks the item walks (see load_block)
+  // The ki-th key block the item walks: 0 .. nk - 2, then the diagonal qt.
+  __device__ __forceinline__ int key_block(int ki) const { return ki == nk - 1 ? qt : ki; }
   // No key of block kt is masked: an off-diagonal block of history keys only.
   __device__ __forceinline__ bool unmasked(int kt) const {
     return kt != qt && kBN * kt + kBN <= hist;
   }
 };
 
-__device__ __forceinline__ bool load_block(const FwdArgs& a, int it, Block& b) {
+template <bool TGT>
+using BlockOf = typename std::conditional<TGT, BlockTgt, Block>::type;
+
+// TGT: items carry a history length (the candidate mask); otherwise every
+// item walks key blocks 0 .. qt.
+template <bool TGT>
+__device__ __forceinline__ bool load_block(const FwdArgs& a, int it, BlockOf<TGT>& b) {
   const int idx = item_index(it, blockIdx.x, gridDim.x);
   if (idx >= a.n_items) return false;
   const Item x = __ldg(&a.items[idx]);
@@ -486,38 +489,52 @@ __device__ __forceinline__ bool load_block(const FwdArgs& a, int it, Block& b) {
   b.n = x.y;
   b.h = x.z;
   b.qt = x.w;
-  b.hist = a.item_hist ? __ldg(&a.item_hist[idx]) : x.y;
+  if constexpr (TGT) {
+    // Key blocks the item walks (HSTU paper Appendix H, the M-FALCON mask):
+    // the blocks that hold history keys, 0 .. min(qt, KH) - 1 with
+    // KH = ceil(hist / 128), then the diagonal block qt.  A block between
+    // them holds only keys of other candidates.
+    b.hist = __ldg(&a.item_hist[idx]);
+    const int kh = (b.hist + kBN - 1) / kBN;
+    b.nk = (b.qt < kh ? b.qt : kh) + 1;
+  }
   return true;
 }
 
 // A cursor over the CTA's key-block steps: item `it` (block b) at its
 // ki-th key block kt; tc counts the steps.  The next item's block is fetched one item ahead
 // so that crossing into it does not wait on a global load.
+template <bool TGT>
 struct Cursor {
   int it, kt, ki;  // ki: index of the step among the item's key blocks; kt = b.key_block(ki)
   uint32_t tc;
-  Block b, nb;
+  BlockOf<TGT> b, nb;
   bool valid, nvalid;
   __device__ __forceinline__ void start(const FwdArgs& a) {
     it = 0;
     kt = 0;
     ki = 0;
     tc = 0;
-    valid = load_block(a, 0, b);
-    nvalid = valid && load_block(a, 1, nb);
+    valid = load_block<TGT>(a, 0, b);
+    nvalid = valid && load_block<TGT>(a, 1, nb);
   }
   __device__ __forceinline__ void advance(const FwdArgs& a) {
     ++tc;
-    const int nk = b.nk();
-    if (++ki < nk) {
-      kt = ki == nk - 1 ? b.qt : ki;
+    bool next_item;
+    if constexpr (TGT) {
+      next_item = ++ki >= b.nk;
+      if (!next_item) kt = ki == b.nk - 1 ? b.qt : ki;
     } else {
+      next_item = ++kt > b.qt;
+      ki = kt;
+    }
+    if (next_item) {
       ki = 0;
       kt = 0;
       ++it;
       valid = nvalid;
       b = nb;
-      nvalid = valid && load_block(a, it + 1, nb);
+      nvalid = valid && load_block<TGT>(a, it + 1, nb);
     }
   }
 };
@@ -560,7 +577,7 @@ __device__ __forceinline__ void drain_copies(uint32_t full0, int slots, uint32_t
 // lands on QK-ready.  V slot t mod P is free once PV(t-P) has completed,
 // which QK-ready of step t includes.  A Q slot is free once the item's last
 // QK has completed (Q-empty).
-template <int D, bool KQ>
+template <int D, bool KQ, bool TGT>
 __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, const FwdArgs& a,
                               uint32_t base, const WaitCtx& w) {
   using C = Cfg<D>;
@@ -570,8 +587,8 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   uint32_t c = 0, qc = 0;
   bool ok = true;
-  Block b;
-  for (int it = 0; ok && load_block(a, it, b); ++it) {
+  BlockOf<TGT> b;
+  for (int it = 0; ok && load_block<TGT>(a, it, b); ++it) {
     if (KQ) {
       const int qs = (int)(qc % C::QS);
       if (!(ok = wait_one(bar(C::B_QEMPTY + qs), ((qc / C::QS) & 1u) ^ 1u, w, kSiteQEmpty))) break;
@@ -583,9 +600,11 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
                     ch * C::CHUNK, b.h, b.s0 + kBM * b.qt);
       ++qc;
     }
-    const int nk = b.nk();
+    int nk = b.qt + 1;
+    if constexpr (TGT) nk = b.nk;
     for (int ki = 0; ki < nk; ++ki) {
-      const int kt = b.key_block(ki);
+      int kt = ki;
+      if constexpr (TGT) kt = b.key_block(ki);
       const int slot = (int)(c % C::P);
       // A parity wait is exact only while the barrier is at most one phase
       // short of the awaited one.  K(c) waits for phase c/P - 1 of S-full
@@ -622,7 +641,7 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
 // that buffer, has completed (QK-ready); the products of different
 // accumulators are not ordered with respect to each other, so this wait is
 // needed.  It runs up to P steps ahead of the PV issuer.
-template <int D>
+template <int D, bool TGT>
 __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
   using C = Cfg<D>;
   constexpr int P = C::P;
@@ -637,7 +656,7 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
   // Test hook: wait on a barrier that nothing arrives on, so that the
   // bounded wait runs out and the whole CTA takes its give-up path.
   if (a.debug_flags & kDebugUnsignalledWait) ok = wait_one(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
-  Cursor qc;
+  Cursor<TGT> qc;
   qc.start(a);
   uint32_t ph = 0;  // (qc.tc / P) & 1
   auto step = [&](auto jc) -> bool {
@@ -687,7 +706,7 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
 // current step's products are issued, so that the tests' latency overlaps
 // them.  16-key step k: P_hi in columns 32 (k/2) + 8 (k%2) + [0, 8), P_lo 16
 // columns further; V rows 16 k.. (two 8-row atoms per step).
-template <int D>
+template <int D, bool TGT>
 __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
   using C = Cfg<D>;
   constexpr int P = C::P;
@@ -696,7 +715,7 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
   constexpr uint32_t IDESC_PV = make_idesc(kBM, D, 1);
   const uint64_t v_desc0 = smem_desc(base + C::V_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
   bool ok = true;
-  Cursor pc;
+  Cursor<TGT> pc;
   pc.start(a);
   uint32_t ph = 0;  // (pc.tc / P) & 1
 
@@ -792,8 +811,10 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
 // silu of the 32 scores s of one row, written over their own TMEM columns
 // at t: keys 16h..16h+15 go to P_hi columns t + 8h + [0, 8) and P_lo columns
 // t + 16 + 8h + [0, 8).  Processed in 16-key halves to keep register
-// pressure down.
-template <bool MASK>
+// pressure down.  MASK 0: no mask; 1: keep keys k <= lim (the diagonal
+// block); 2: also drop keys k >= lim_hist other than k == lim (the candidate
+// mask).
+template <int MASK>
 __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, int lim_hist,
                                              uint32_t t) {
 #pragma unroll
@@ -804,9 +825,12 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
       const int k = 16 * h + 2 * m;
       const float2 x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
       float2 p = __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
-      if (MASK) {
-        // keep key k iff k <= lim (causal) and (k < lim_hist or k == lim):
-        // a key past the history is seen by its own row only
+      if (MASK == 1) {  // keep key k iff k <= lim (causal)
+        p.x = (k > lim) ? 0.0f : p.x;
+        p.y = (k + 1 > lim) ? 0.0f : p.y;
+      } else if (MASK == 2) {
+        // and a key past the history (k >= lim_hist) is seen by its own row
+        // (k == lim) only
         p.x = (k > lim || (k >= lim_hist && k != lim)) ? 0.0f : p.x;
         p.y = (k + 1 > lim || (k + 1 >= lim_hist && k + 1 != lim)) ? 0.0f : p.y;
       }
@@ -827,7 +851,7 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
 // owns score row r.  Every lane waits on S-full and arrives on P-full
 // itself (a vote keeps the warp's view uniform), so no lane-0 relay or warp
 // barrier sits on the path.
-template <int D>
+template <int D, bool TGT>
 __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w, int warp,
                           int lane) {
   using C = Cfg<D>;
@@ -839,7 +863,7 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
   const float2 ha2 = make_float2(a.half_alpha, a.half_alpha);
-  Cursor cur;
+  Cursor<TGT> cur;
   cur.start(a);
   uint32_t s0[32], s1[32];
   while (cur.valid) {
@@ -855,16 +879,18 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
     tc_fence_after();
     trace(a, kEvSiluStart, cur.tc);
     const uint32_t t_s = lane_base + (uint32_t)(j * 128);
-    if (cur.b.unmasked(cur.kt) && quarter * 32 < cur.b.rows()) {
+    bool plain = cur.kt != cur.b.qt;
+    if constexpr (TGT) plain = cur.b.unmasked(cur.kt);
+    if (plain && quarter * 32 < cur.b.rows()) {
       tmem_ld32_async(t_s, s0);
       tmem_wait_ld(s0);
 #pragma unroll 1
       for (int c = 0; c < 4; c += 2) {
         tmem_ld32_async(t_s + 32u * (c + 1), s1);
-        silu_store32<false>(s0, ha2, 0, 0, t_s + 32u * c);
+        silu_store32<0>(s0, ha2, 0, 0, t_s + 32u * c);
         tmem_wait_ld(s1);
         if (c + 2 < 4) tmem_ld32_async(t_s + 32u * (c + 2), s0);
-        silu_store32<false>(s1, ha2, 0, 0, t_s + 32u * (c + 1));
+        silu_store32<0>(s1, ha2, 0, 0, t_s + 32u * (c + 1));
         if (c + 2 < 4) tmem_wait_ld(s0);
       }
       tmem_wait_st();
@@ -878,7 +904,8 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
       const bool diag = cur.kt == cur.b.qt;
       // row and history end relative to the block's first key
       const int lim0 = kBM * cur.b.qt + row - kBN * cur.kt;
-      const int hist0 = cur.b.hist - kBN * cur.kt;
+      int hist0 = 0;
+      if constexpr (TGT) hist0 = cur.b.hist - kBN * cur.kt;
 #pragma unroll 1
       for (int c = 0; c < 4 && 32 * c < cols; ++c) {
         if (diag && c > quarter) {
@@ -889,7 +916,7 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
           tmem_st16(t_s + 32u * c + 16u, z);
         } else {
           tmem_ld32(t_s + 32u * c, s1);
-          silu_store32<true>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c, t_s + 32u * c);
+          silu_store32<TGT ? 2 : 1>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c, t_s + 32u * c);
         }
       }
       tmem_wait_st();
@@ -903,7 +930,7 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
 
 // Epilogue warpgroup (warps 0-3): O -> x inv_n -> bf16 -> out.  Thread r
 // owns output row r of the item; rows past the sequence end are not stored.
-template <int D>
+template <int D, bool TGT>
 __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w,
                               int warp, int lane) {
   using C = Cfg<D>;
@@ -914,8 +941,8 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
   const float inv_n = a.inv_n;
   uint16_t* out = static_cast<uint16_t*>(a.out);
-  Block b;
-  for (int it = 0; load_block(a, it, b); ++it) {
+  BlockOf<TGT> b;
+  for (int it = 0; load_block<TGT>(a, it, b); ++it) {
     const int ob = it % C::OB;
     if (!wait_warp(bar(C::B_OFULL + ob), (uint32_t)(it / C::OB) & 1u, w, kSiteOFull)) return;
     tc_fence_after();
@@ -946,7 +973,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
   }
 }
 
-template <int D>
+template <int D, bool TGT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -989,21 +1016,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const WaitCtx w{a.timeout_ns, abort_flag};
 
   if (warp == kTmaWarpK) {
-    if (lane == 0) role_producer<D, true>(&tm_k, &tm_q, a, base, w);
+    if (lane == 0) role_producer<D, true, TGT>(&tm_k, &tm_q, a, base, w);
     __syncwarp();
   } else if (warp == kTmaWarpV) {
-    if (lane == 0) role_producer<D, false>(&tm_v, &tm_q, a, base, w);
+    if (lane == 0) role_producer<D, false, TGT>(&tm_v, &tm_q, a, base, w);
     __syncwarp();
   } else if (warp == kMmaWarpQK) {
-    if (lane == 0) role_mma_qk<D>(a, base, tmem, w);
+    if (lane == 0) role_mma_qk<D, TGT>(a, base, tmem, w);
     __syncwarp();
   } else if (warp == kMmaWarpPV) {
-    if (lane == 0) role_mma_pv<D>(a, base, tmem, w);
+    if (lane == 0) role_mma_pv<D, TGT>(a, base, tmem, w);
     __syncwarp();
   } else if (warp >= kEwWarp0 && warp < kEwWarp0 + 8) {
-    role_silu<D>(a, base, tmem, w, warp, lane);
+    role_silu<D, TGT>(a, base, tmem, w, warp, lane);
   } else if (warp < kEpiWarp0 + 4) {
-    role_epilogue<D>(a, base, tmem, w, warp, lane);
+    role_epilogue<D, TGT>(a, base, tmem, w, warp, lane);
   }
 
   tc_fence_before();
@@ -1018,15 +1045,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
+template <int D, bool TGT>
+cudaError_t launch_dt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const FwdArgs& a, int grid, cudaStream_t stream) {
+  using C = Cfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<D, TGT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
+  if (e != cudaSuccess) return e;
+  hstu_fwd_kernel<D, TGT><<<grid, kFwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+// Items with a history array (the candidate mask) run the TGT instantiation;
+// causal items the other, which has none of its bookkeeping.
 template <int D>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdArgs& a, int grid, cudaStream_t stream) {
-  using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_LAUNCH);
-  if (e != cudaSuccess) return e;
-  hstu_fwd_kernel<D><<<grid, kFwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  return a.item_hist ? launch_dt<D, true>(tq, tk, tv, a, grid, stream)
+                     : launch_dt<D, false>(tq, tk, tv, a, grid, stream);
 }
 
 }  // namespace
