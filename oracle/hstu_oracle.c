@@ -34,6 +34,9 @@
  *     term j of row i is kept  iff  j <= i  and  (j < hist or j == i).
  *
  * With no candidates (hist = n_b) this is the causal formula above.
+ *
+ * hstu_oracle_norm_gate_f64 (at the end of the file) applies the HSTU
+ * layer's output stage, Norm(A V) (.) U, to rows the functions above made.
  */
 #include <math.h>
 #include <pthread.h>
@@ -219,4 +222,44 @@ int hstu_oracle_rows_targets_f64(const float* q, const float* k, const float* v,
     job_t J = {q, k, v, offsets, num_targets, batch, heads, d, alpha, inv_n, out, rows_t, rows_h,
                nrows, NULL, NULL};
     return run(&J, nthreads, worker_rows);
+}
+
+/*
+ * The HSTU layer's output stage applied to attention rows: Norm(A V) (.) U
+ * (HSTU paper section 3, the layer's spatial aggregation followed by the
+ * pointwise transformation; section 3.1 requires a layer norm after the
+ * pointwise pooling; the feature-interaction paragraph writes the term as
+ * Norm(A(X) V(X)) (.) U(X)).  The paper's equations are lost in
+ * extraction; the plainest reading is taken:
+ *
+ *   Norm is a layer norm over one token's attention output with all heads
+ *   concatenated (width = heads * d): mean and biased variance over the
+ *   width, then (x - mean) / sqrt(var + eps) * gamma + beta, gamma and beta
+ *   of that width;
+ *   (.) U multiplies elementwise by U, which already went through the
+ *   SiLU of the paper's first sub-layer (phi_1 acts on U).
+ *
+ * x: fp64 (rows, width), the attention output; u: fp32 (rows, width)
+ * holding bf16 values; gamma, beta: fp32 (width); y: fp64 (rows, width).
+ * Mean and variance are two plain passes over the row in fp64.
+ */
+int hstu_oracle_norm_gate_f64(const double* x, const float* u, const float* gamma,
+                              const float* beta, double eps, int64_t rows, int64_t width,
+                              double* y) {
+    if (rows < 0 || width < 1 || !(eps >= 0.0)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * width;
+        double mean = 0.0;
+        for (int64_t c = 0; c < width; ++c) mean += xr[c];
+        mean /= (double)width;
+        double var = 0.0;
+        for (int64_t c = 0; c < width; ++c) var += (xr[c] - mean) * (xr[c] - mean);
+        var /= (double)width;
+        const double rstd = 1.0 / sqrt(var + eps);
+        for (int64_t c = 0; c < width; ++c) {
+            const double normed = (xr[c] - mean) * rstd * (double)gamma[c] + (double)beta[c];
+            y[r * width + c] = normed * (double)u[r * width + c];
+        }
+    }
+    return 0;
 }

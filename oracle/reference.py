@@ -12,6 +12,10 @@ With ``num_targets`` (HSTU paper section 3.4 and Appendix H, Algorithm 1:
 the M-FALCON mask), the last num_targets[b] tokens of sequence b are
 candidates: term j of row i is kept iff j <= i and (j < hist or j == i),
 hist = n_b - num_targets[b].
+
+``norm_gate`` is the layer's output stage on those rows, Norm(A V) (.) U
+(HSTU paper section 3 and section 3.1): a layer norm over each token's
+heads * d outputs with affine gamma, beta, times U elementwise.
 """
 from __future__ import annotations
 
@@ -50,6 +54,9 @@ def _load():
                                                      ctypes.c_int, ctypes.c_double, ctypes.c_double,
                                                      i64, i32, ctypes.c_int64, d, ctypes.c_int]
         lib.hstu_oracle_rows_targets_f64.restype = ctypes.c_int
+        lib.hstu_oracle_norm_gate_f64.argtypes = [d, f, f, f, ctypes.c_double, ctypes.c_int64,
+                                                  ctypes.c_int64, d]
+        lib.hstu_oracle_norm_gate_f64.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -135,3 +142,42 @@ def hstu_rows(q, k, v, offsets, alpha: float, inv_n: float, rows_t, rows_h,
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out
+
+
+def norm_gate(x, u, gamma, beta, eps: float) -> np.ndarray:
+    """Layer norm over the last two axes of x (heads * d per token), affine
+    gamma/beta of that width, times u elementwise.  x: (rows, heads, d) any
+    float type (taken as fp64); u: same shape; returns fp64."""
+    xf = np.ascontiguousarray(x, dtype=np.float64)
+    if xf.ndim != 3:
+        raise ValueError("x must be (rows, heads, d)")
+    rows, heads, d = xf.shape
+    uf = _f32(u)
+    g, b = _f32(gamma).reshape(-1), _f32(beta).reshape(-1)
+    if uf.shape != xf.shape or g.shape != (heads * d,) or b.shape != (heads * d,):
+        raise ValueError("u must match x and gamma/beta must have heads * d entries")
+    y = np.zeros_like(xf)
+    rc = _load().hstu_oracle_norm_gate_f64(_ptr(xf, ctypes.c_double), _ptr(uf, ctypes.c_float),
+                                           _ptr(g, ctypes.c_float), _ptr(b, ctypes.c_float),
+                                           float(eps), rows, heads * d, _ptr(y, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (eps must be >= 0)")
+    return y
+
+
+def hstu_fwd_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, alpha: float, inv_n: float,
+                       threads: int | None = None, num_targets=None) -> np.ndarray:
+    """Norm(A V) (.) U over all tokens: fp64 (total, heads, d)."""
+    x = hstu_fwd(q, k, v, offsets, alpha, inv_n, threads=threads, num_targets=num_targets)
+    return norm_gate(x, u, gamma, beta, eps)
+
+
+def hstu_rows_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, alpha: float, inv_n: float,
+                        rows_t, threads: int | None = None, num_targets=None) -> np.ndarray:
+    """Norm(A V) (.) U for the sampled tokens rows_t: fp64 (nrows, heads, d)."""
+    heads, d = np.shape(q)[1], np.shape(q)[2]
+    rt = np.repeat(np.asarray(rows_t, dtype=np.int64), heads)
+    rh = np.tile(np.arange(heads, dtype=np.int32), len(rows_t))
+    x = hstu_rows(q, k, v, offsets, alpha, inv_n, rt, rh, threads=threads,
+                  num_targets=num_targets).reshape(len(rows_t), heads, d)
+    return norm_gate(x, _f32(u)[np.asarray(rows_t, dtype=np.int64)], gamma, beta, eps)

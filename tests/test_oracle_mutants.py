@@ -162,3 +162,46 @@ def test_candidate_mutant_is_caught(tmp_path, name):
     old, new = TARGET_MUTANTS[name]
     assert src.count(old) == 1
     assert not _targets_pins_pass(_build(tmp_path, name, src.replace(old, new)))
+
+
+# ------------------------------------------------ the output stage Norm(A V) (.) U
+NORM_MUTANTS = {
+    "unbiased_variance": ("var /= (double)width;", "var /= (double)(width - 1);"),
+    "eps_outside_sqrt": ("1.0 / sqrt(var + eps)", "1.0 / (sqrt(var) + eps)"),
+    "mean_not_subtracted": ("(xr[c] - mean) * rstd", "xr[c] * rstd"),
+    "beta_dropped": ("* (double)gamma[c] + (double)beta[c]", "* (double)gamma[c]"),
+    "gate_by_first_column": ("(double)u[r * width + c]", "(double)u[r * width]"),
+    "gamma_per_row": ("(double)gamma[c]", "(double)gamma[r % width]"),
+}
+
+
+def _norm_pins_pass(L) -> bool:
+    """torch's layer_norm times u, as in test_oracle_norm_gate.py."""
+    import torch
+    f, dptr, i64 = ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double), ctypes.c_int64
+    L.hstu_oracle_norm_gate_f64.argtypes = [dptr, f, f, f, ctypes.c_double, i64, i64, dptr]
+    P = lambda a, t: a.ctypes.data_as(ctypes.POINTER(t))
+    rng = np.random.default_rng(12)
+    rows, width, eps = 6, 16, 1e-2
+    x = rng.standard_normal((rows, width)) * 0.3 + 0.5
+    u = rng.standard_normal((rows, width)).astype(np.float32)
+    g = (1.0 + 0.3 * rng.standard_normal(width)).astype(np.float32)
+    b = (0.3 * rng.standard_normal(width)).astype(np.float32)
+    y = np.zeros_like(x)
+    L.hstu_oracle_norm_gate_f64(P(x, ctypes.c_double), P(u, ctypes.c_float), P(g, ctypes.c_float),
+                                P(b, ctypes.c_float), eps, rows, width, P(y, ctypes.c_double))
+    want = torch.nn.functional.layer_norm(torch.tensor(x), (width,), torch.tensor(g, dtype=torch.float64),
+                                          torch.tensor(b, dtype=torch.float64), eps).numpy() * u
+    return bool(np.abs(y - want).max() <= 1e-12 * np.abs(want).max())
+
+
+def test_unmutated_copy_passes_the_norm_pins(tmp_path):
+    assert _norm_pins_pass(_build(tmp_path, "orig_n", open(oracle_build.SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(NORM_MUTANTS))
+def test_norm_mutant_is_caught(tmp_path, name):
+    src = open(oracle_build.SRC).read()
+    old, new = NORM_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    assert not _norm_pins_pass(_build(tmp_path, name, src.replace(old, new)))
