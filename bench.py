@@ -70,9 +70,9 @@ def workload_by_name(name: str):
     return workloads.workload(name), None
 
 
-def algorithmic_bytes(w: workloads.Workload) -> float:
-    # read Q, K, V once and write O once, bf16
-    return float(8.0 * w.d * w.heads * w.total)
+def algorithmic_bytes(w: workloads.Workload, norm_gate: bool = False) -> float:
+    # read Q, K, V (and U with the output stage) once and write O once, bf16
+    return float((10.0 if norm_gate else 8.0) * w.d * w.heads * w.total)
 
 
 def kernel_sha() -> str:
@@ -180,9 +180,11 @@ def aggregate(flops_per_rank: float, ms_local: float, world: int, device=None):
 
 
 def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int | None = None,
-                      num_targets=None):
+                      num_targets=None, norm_gate=None):
     """Time the oracle on a bounded, uniformly random sample of rows.
 
+    With ``norm_gate`` = (u, gamma, beta, eps) the sample is of tokens, each
+    with all its heads and the output stage.
     Returns (flops_of_sample / seconds, description, threads, seconds)."""
     from oracle import reference
     threads = threads or reference.default_threads()
@@ -192,17 +194,25 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
     hist_of = (w.lengths - (np.asarray(num_targets, dtype=np.int64) if num_targets is not None
                             else 0)).astype(np.int64)
 
+    per_row = w.heads if norm_gate is not None else 1
+
     def rows(nr):
+        nr = max(1, nr // per_row)
         t = rng.integers(0, w.total, size=nr)
         h = rng.integers(0, w.heads, size=nr)
         i = t - off[seq_of[t]]
         hist = hist_of[seq_of[t]]
         kept = np.where(i < hist, i + 1, hist + 1)
-        return t, h, float(np.sum(4.0 * w.d * kept))
+        return t, h, float(np.sum(4.0 * w.d * per_row * kept))
 
     def oracle(t, h):
-        reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads,
-                            num_targets=num_targets)
+        if norm_gate is not None:
+            u, g, b, eps = norm_gate
+            reference.hstu_rows_norm_gate(q, k, v, u, g, b, eps, w.offsets, w.alpha, w.inv_n, t,
+                                          threads=threads, num_targets=num_targets)
+        else:
+            reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads,
+                                num_targets=num_targets)
 
     # calibrate on a small sample, then size the real one to ~target_s
     t, h, fl = rows(64)
@@ -214,9 +224,28 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
     t0 = time.perf_counter()
     oracle(t, h)
     dt = time.perf_counter() - t0
-    desc = (f"{n} uniformly sampled (token, head) output rows of the {w.name} workload "
-            f"({fl / 1e9:.2f} causal GFLOP), fp64 C oracle, {threads} threads")
+    if norm_gate is not None:
+        desc = (f"{len(t)} uniformly sampled tokens (all {w.heads} heads, then the output stage) "
+                f"of the {w.name} workload ({fl / 1e9:.2f} causal GFLOP), fp64 C oracle, "
+                f"{threads} threads")
+    else:
+        desc = (f"{n} uniformly sampled (token, head) output rows of the {w.name} workload "
+                f"({fl / 1e9:.2f} causal GFLOP), fp64 C oracle, {threads} threads")
     return fl / dt / 1e12, desc, threads, dt
+
+
+def _norm_gate_desc(args) -> dict:
+    if not args.norm_gate:
+        return {}
+    return {"output_stage": "Norm(A V) * U: layer norm over heads*d, affine gamma/beta, "
+                            f"eps {workloads.NORM_EPS:g}, times U (HSTU paper section 3)"}
+
+
+def _cpu_norm_gate(args, w):
+    if not args.norm_gate:
+        return None
+    u, g, b = workloads.draw_norm_gate(w)
+    return u.float().numpy(), g, b, workloads.NORM_EPS
 
 
 def run_reference(args, w, nt=None):
@@ -225,12 +254,13 @@ def run_reference(args, w, nt=None):
         return 0
     q, k, v = workloads.draw_qkv(w)
     qf, kf, vf = (t.float().numpy() for t in (q, k, v))
+    ng = _cpu_norm_gate(args, w)
     per_step_s = max(1.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
     vals = []
     desc, threads = "", 0
     for s in range(args.warmup + args.steps):
         val, desc, threads, dt = cpu_oracle_sample(w, qf, kf, vf, per_step_s, seed=s,
-                                                   num_targets=nt)
+                                                   num_targets=nt, norm_gate=ng)
         if s >= args.warmup:
             vals.append(val)
     value = statistics.mean(vals)
@@ -238,7 +268,7 @@ def run_reference(args, w, nt=None):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, **w.describe(), **_targets_desc(nt)},
+        "config": {"workload": w.name, **w.describe(), **_targets_desc(nt), **_norm_gate_desc(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -272,10 +302,23 @@ def run_ours(args, w, nt=None):
     q_h, k_h, v_h = workloads.draw_qkv(w)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     out = torch.empty_like(q)
-    if nt is None:
-        plan = binding.hstu_plan_create(w.offsets, w.batch, w.heads, w.d, w.max_seqlen)
-    else:
-        plan = binding.hstu_plan_create_targets(w.offsets, nt, w.batch, w.heads, w.d, w.max_seqlen)
+    ng = args.norm_gate
+    if ng:
+        # gamma and beta are the layer's weights: resident on the device
+        u_h, g_h, b_h = workloads.draw_norm_gate(w)
+        u = u_h.to(dev)
+        gamma, beta = torch.from_numpy(g_h).to(dev), torch.from_numpy(b_h).to(dev)
+        eps = workloads.NORM_EPS
+    plan = binding.hstu_plan_create_ex(w.offsets, nt, w.batch, w.heads, w.d, w.max_seqlen,
+                                       binding.HSTU_PLAN_NORM_GATE if ng else 0)
+
+    def launch():
+        if ng:
+            binding.hstu_attn_fwd_norm_gate_plan(plan, q, k, v, u, gamma, beta, eps, w.alpha,
+                                                 w.inv_n, out, stream)
+        else:
+            binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+
     n_items = binding.hstu_plan_num_items(plan)
     grid, block, smem = binding.hstu_launch_shape(plan)
     stream = torch.cuda.current_stream(dev)
@@ -284,7 +327,7 @@ def run_ours(args, w, nt=None):
     sampler = ClockSampler(local)
     t_warm = time.perf_counter()
     for _ in range(args.warmup):
-        binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+        launch()
     torch.cuda.synchronize(dev)
     st, site = binding.hstu_last_status()
     if st != binding.HSTU_OK:
@@ -300,7 +343,7 @@ def run_ours(args, w, nt=None):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+        launch()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -319,13 +362,14 @@ def run_ours(args, w, nt=None):
     peak = peaks["bf16_tflops"]
     achieved = flops / (ms * 1e-3) / 1e12
     traffic = None
-    if MEASURED_TRAFFIC.get(w.name) and MEASURED_TRAFFIC.get("sha256") == kernel_sha():
-        traffic = MEASURED_TRAFFIC[w.name]
+    key = w.name + ("+norm_gate" if ng else "")
+    if MEASURED_TRAFFIC.get(key) and MEASURED_TRAFFIC.get("sha256") == kernel_sha():
+        traffic = MEASURED_TRAFFIC[key]
 
     # ---- end to end through the C ABI with host buffers
-    pin = [t.pin_memory() for t in (q_h, k_h, v_h)]
+    pin = [t.pin_memory() for t in ((q_h, k_h, v_h, u_h) if ng else (q_h, k_h, v_h))]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    qe, ke, ve = (torch.empty_like(q) for _ in range(3))
+    qe, ke, ve, ue = (torch.empty_like(q) for _ in range(4))
     oe = torch.empty_like(out)
     offsets_host = w.offsets.copy()
 
@@ -333,7 +377,12 @@ def run_ours(args, w, nt=None):
         qe.copy_(pin[0], non_blocking=True)
         ke.copy_(pin[1], non_blocking=True)
         ve.copy_(pin[2], non_blocking=True)
-        if nt is None:
+        if ng:
+            ue.copy_(pin[3], non_blocking=True)
+            binding.hstu_attn_fwd_norm_gate(qe, ke, ve, ue, gamma, beta, eps, offsets_host, nt,
+                                            w.batch, w.heads, w.d, w.max_seqlen, w.alpha, w.inv_n,
+                                            oe, stream)
+        elif nt is None:
             binding.hstu_attn_fwd(qe, ke, ve, offsets_host, w.batch, w.heads, w.d, w.max_seqlen,
                                   w.alpha, w.inv_n, oe, stream)
         else:
@@ -367,13 +416,14 @@ def run_ours(args, w, nt=None):
     if st != binding.HSTU_OK:
         raise RuntimeError(f"device wait gave up during the e2e region (site {site})")
     elem = 2
-    h2d = 3 * w.total * w.heads * w.d * elem + offsets_host.nbytes
+    h2d = (4 if ng else 3) * w.total * w.heads * w.d * elem + offsets_host.nbytes
     d2h = w.total * w.heads * w.d * elem
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         qf, kf, vf = (t.float().numpy() for t in (q_h, k_h, v_h))
-        val, desc, threads, _ = cpu_oracle_sample(w, qf, kf, vf, args.cpu_seconds, num_targets=nt)
+        val, desc, threads, _ = cpu_oracle_sample(w, qf, kf, vf, args.cpu_seconds, num_targets=nt,
+                                                  norm_gate=_cpu_norm_gate(args, w))
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
 
     binding.hstu_plan_destroy(plan)
@@ -382,18 +432,20 @@ def run_ours(args, w, nt=None):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {**w.describe(), **_targets_desc(nt), "l2": "flushed between steps (256 MiB write)",
+            "config": {**w.describe(), **_targets_desc(nt), **_norm_gate_desc(args),
+                       "l2": "flushed between steps (256 MiB write)",
                        "work_items": n_items, "grid": grid, "block": block, "smem_bytes": smem,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * achieved / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peaks['source']} bf16_tflops (burst)",
-                         "algorithmic_bytes": algorithmic_bytes(w)},
+                         "algorithmic_bytes": algorithmic_bytes(w, ng)},
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "cpu_baseline": cpu,
-            "gpu_launches": args.steps,
+            # the attention kernel per step, and the output-stage kernel after it
+            "gpu_launches": args.steps * (2 if ng else 1),
             "clocks": clocks,
             "timed_wall_s": wall,
             "ms_per_step_min": min(times_ms),
@@ -415,6 +467,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="one line per workload (extra lines)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--norm-gate", action="store_true",
+                    help="fuse the layer's output stage Norm(A V) * U into the timed call")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

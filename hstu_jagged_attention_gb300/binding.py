@@ -60,7 +60,17 @@ _SIGNATURES = {
     "hstu_plan_item_hist": (ctypes.c_int, [_VP, _I32P, ctypes.c_int, _IP]),
     "hstu_worklist_build_targets": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int, _I32P,
                                                    _I32P, ctypes.c_int, _IP]),
+    "hstu_plan_create_ex": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_uint32, ctypes.POINTER(_VP)]),
+    "hstu_attn_fwd_norm_gate_plan": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float,
+                                                    ctypes.c_float, ctypes.c_float, _VP, _VP]),
+    "hstu_attn_fwd_norm_gate": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP,
+                                               _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP,
+                                               _VP]),
 }
+
+HSTU_PLAN_NORM_GATE = 1
 
 _lib = None
 
@@ -182,6 +192,36 @@ def hstu_attn_fwd_targets(q, k, v, offsets, num_targets, batch: int, heads: int,
                                        _stream(stream)), "hstu_attn_fwd_targets")
 
 
+def _offsets_arg(offsets):
+    """(address, keep-alive) for offsets given as a CUDA tensor, host data or an address."""
+    if isinstance(offsets, int):
+        return offsets, None
+    if hasattr(offsets, "is_cuda") and offsets.is_cuda:
+        if offsets.dtype.itemsize != 4 or not offsets.is_contiguous():
+            raise ValueError("device offsets must be contiguous int32")
+        return offsets.data_ptr(), None
+    keep = _host_offsets(offsets)
+    return keep.ctypes.data, keep
+
+
+def hstu_attn_fwd_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, num_targets, batch: int,
+                            heads: int, d: int, max_seqlen: int, alpha: float, inv_n: float, y,
+                            stream=None) -> None:
+    """y = Norm(attention output) (.) u: a layer norm over each token's
+    heads * d outputs with affine gamma, beta (fp32, heads * d), times u
+    (bf16, like q).  ``num_targets`` is None (causal) or host memory with one
+    entry per sequence (the candidate mask)."""
+    off_ptr, keep = _offsets_arg(offsets)
+    nt = None if num_targets is None else _host_targets(num_targets, int(batch))
+    _check(lib().hstu_attn_fwd_norm_gate(_addr(q), _addr(k), _addr(v), _addr(u), _addr(gamma),
+                                         _addr(beta), float(eps), off_ptr,
+                                         None if nt is None else nt.ctypes.data_as(_I32P),
+                                         int(batch), int(heads), int(d), int(max_seqlen),
+                                         float(alpha), float(inv_n), _addr(y), _stream(stream)),
+           "hstu_attn_fwd_norm_gate")
+    del keep
+
+
 def hstu_attn_fwd_noalloc(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: int,
                           alpha: float, inv_n: float, out, stream=None) -> None:
     """As hstu_attn_fwd, for callers that cannot let the library allocate.
@@ -246,6 +286,30 @@ def hstu_plan_create_targets(host_offsets, num_targets, batch: int, heads: int, 
                                           int(batch), int(heads), int(d), int(max_seqlen),
                                           ctypes.byref(h)), "hstu_plan_create_targets")
     return Plan(h.value, batch, heads, d, max_seqlen, int(off[batch]) if batch else 0)
+
+
+def hstu_plan_create_ex(host_offsets, num_targets, batch: int, heads: int, d: int, max_seqlen: int,
+                        flags: int = 0) -> Plan:
+    """A plan with optional candidates (``num_targets`` None or one entry per
+    sequence) and flags (HSTU_PLAN_NORM_GATE: the output stage's scratch)."""
+    off = _host_offsets(host_offsets)
+    if len(off) < batch + 1:
+        raise ValueError("offsets needs batch + 1 entries")
+    nt = None if num_targets is None else _host_targets(num_targets, int(batch))
+    h = _VP()
+    _check(lib().hstu_plan_create_ex(off.ctypes.data_as(_I32P),
+                                     None if nt is None else nt.ctypes.data_as(_I32P), int(batch),
+                                     int(heads), int(d), int(max_seqlen), int(flags),
+                                     ctypes.byref(h)), "hstu_plan_create_ex")
+    return Plan(h.value, batch, heads, d, max_seqlen, int(off[batch]) if batch else 0)
+
+
+def hstu_attn_fwd_norm_gate_plan(plan: Plan, q, k, v, u, gamma, beta, eps: float, alpha: float,
+                                 inv_n: float, y, stream=None) -> None:
+    _check(lib().hstu_attn_fwd_norm_gate_plan(plan.handle, _addr(q), _addr(k), _addr(v), _addr(u),
+                                              _addr(gamma), _addr(beta), float(eps), float(alpha),
+                                              float(inv_n), _addr(y), _stream(stream)),
+           "hstu_attn_fwd_norm_gate_plan")
 
 
 def hstu_plan_item_hist(plan: Plan) -> np.ndarray:

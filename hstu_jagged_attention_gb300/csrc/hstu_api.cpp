@@ -132,9 +132,12 @@ int device_check(int* sm_count) {
   return HSTU_OK;
 }
 
+// CTAs of a launch: one per SM at most, and no more than there are items.
+int grid_for(int n_items, int sms) { return std::min(n_items, sms); }
+
 int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long long total,
            int heads, int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
-           void* out, cudaStream_t stream) {
+           void* out, const hstu::NormGate* ng, cudaStream_t stream) {
   if (n_items == 0) return HSTU_OK;
   int sms = 0;
   int rc = device_check(&sms);
@@ -148,6 +151,15 @@ int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long l
   a.item_hist = d_hist;
   a.n_items = n_items;
   a.out = out;
+  a.u = ng ? ng->u : nullptr;
+  a.gamma = ng ? ng->gamma : nullptr;
+  a.beta = ng ? ng->beta : nullptr;
+  a.eps = ng ? ng->eps : 0.f;
+  a.xs = ng ? ng->xs : nullptr;
+  a.stats = ng ? ng->stats : nullptr;
+  a.total = total;
+  // the output-stage kernel: one warp per token, up to 8 blocks of 8 warps per SM
+  a.norm_grid = (int)std::min<long long>((total + 7) / 8, 8LL * sms);
   a.heads = heads;
   a.half_alpha = 0.5f * alpha;
   a.inv_n = inv_n;
@@ -156,7 +168,7 @@ int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long l
     std::lock_guard<std::mutex> lk(g_mu);
     a.debug_flags = g_debug_flags;
   }
-  const int grid = std::min(n_items, sms);
+  const int grid = grid_for(n_items, sms);
   const cudaError_t e = hstu::launch_fwd(d, tq, tk, tv, a, grid, stream);
   if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
     return HSTU_ERR_UNSUPPORTED;
@@ -166,10 +178,20 @@ int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long l
 // (The plan type is defined below; make_plan and oneshot are declared here
 // and defined after it.)
 int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d, int max_seqlen,
-              hstu_plan** plan);
+              unsigned flags, hstu_plan** plan);
 int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
             const int32_t* num_targets, int batch, int heads, int d, int max_seqlen, float alpha,
-            float inv_n, void* out, cudaStream_t s);
+            float inv_n, void* out, const hstu::NormGate* ng, cudaStream_t s);
+
+// The output stage's buffers: u and y like q, gamma and beta 16-byte
+// aligned, eps finite and >= 0.
+int check_norm_gate(const void* u, const float* gamma, const float* beta, float eps) {
+  const void* ptrs[3] = {u, gamma, beta};
+  for (const void* p : ptrs)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return HSTU_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || eps > 3.0e38f) return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
 
 }  // namespace
 
@@ -235,8 +257,8 @@ int host_check_buffers(const void* q, const void* k, const void* v, const void* 
 }
 int host_launch(const Item* d_items, const int32_t* d_hist, int n_items, long long total, int heads,
                 int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
-                void* out, cudaStream_t stream) {
-  return launch(d_items, d_hist, n_items, total, heads, d, q, k, v, alpha, inv_n, out, stream);
+                void* out, const NormGate* ng, cudaStream_t stream) {
+  return launch(d_items, d_hist, n_items, total, heads, d, q, k, v, alpha, inv_n, out, ng, stream);
 }
 }  // namespace hstu
 
@@ -245,18 +267,30 @@ struct hstu_plan {
   long long total = 0;
   std::vector<hstu::Item> items;
   std::vector<int32_t> hist;        // history length per item; empty: no candidates
+  unsigned flags = 0;               // HSTU_PLAN_* bits
   hstu::Item* d_items = nullptr;    // device copy of items, then hist (one allocation)
   int32_t* d_hist = nullptr;
+  // output-stage scratch (HSTU_PLAN_NORM_GATE): xs, then stats
+  char* d_norm = nullptr;
   int device = -1;
 };
 
 namespace {
 
+hstu::NormGate norm_views(char* block, long long total, int heads, int d) {
+  hstu::NormGate ng{};
+  ng.xs = reinterpret_cast<float*>(block);
+  ng.stats = reinterpret_cast<float2*>(block + hstu::norm_xs_bytes(total, heads, d));
+  return ng;
+}
+
 int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d, int max_seqlen,
-              hstu_plan** plan) {
+              unsigned flags, hstu_plan** plan) {
   if (!plan) return HSTU_ERR_INVALID_ARG;
   *plan = nullptr;
-  if (heads < 1 || max_seqlen < 0) return HSTU_ERR_INVALID_ARG;
+  if (heads < 1 || max_seqlen < 0 || (flags & ~(unsigned)HSTU_PLAN_NORM_GATE))
+    return HSTU_ERR_INVALID_ARG;
+  const bool norm = (flags & HSTU_PLAN_NORM_GATE) != 0;
   if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
   int rc = check_offsets(off, batch, max_seqlen);
   if (rc != HSTU_OK) return rc;
@@ -267,32 +301,40 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
   p->heads = heads;
   p->d = d;
   p->max_seqlen = max_seqlen;
+  p->flags = flags;
   p->total = batch ? off[batch] : 0;
   if ((rc = build_worklist(off, nt, batch, heads, p->items, p->hist)) != HSTU_OK) {
     delete p;
     return rc;
   }
-  if (!p->items.empty()) {
-    // one allocation: the items, then (with candidates) the history lengths
-    const size_t ibytes = p->items.size() * sizeof(hstu::Item);
-    const size_t hbytes = p->hist.size() * sizeof(int32_t);
-    if (cudaGetDevice(&p->device) != cudaSuccess) {
-      delete p;
-      return HSTU_ERR_CUDA;
-    }
-    const cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p->d_items), ibytes + hbytes);
-    if (e != cudaSuccess) {
-      delete p;
-      return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
-    }
-    if (hbytes) p->d_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(p->d_items) + ibytes);
-    if (cudaMemcpy(p->d_items, p->items.data(), ibytes, cudaMemcpyHostToDevice) != cudaSuccess ||
-        (hbytes &&
-         cudaMemcpy(p->d_hist, p->hist.data(), hbytes, cudaMemcpyHostToDevice) != cudaSuccess)) {
-      cudaFree(p->d_items);
-      delete p;
-      return HSTU_ERR_CUDA;
-    }
+  if (p->items.empty()) {
+    *plan = p;
+    return HSTU_OK;
+  }
+  auto fail = [&](int code) {
+    if (p->d_items) cudaFree(p->d_items);
+    if (p->d_norm) cudaFree(p->d_norm);
+    delete p;
+    return code;
+  };
+  auto mem_code = [](cudaError_t e) {
+    return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+  };
+  if (cudaGetDevice(&p->device) != cudaSuccess) return fail(HSTU_ERR_CUDA);
+  // one allocation: the items, then (with candidates) the history lengths
+  const size_t ibytes = p->items.size() * sizeof(hstu::Item);
+  const size_t hbytes = p->hist.size() * sizeof(int32_t);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p->d_items), ibytes + hbytes);
+  if (e != cudaSuccess) return fail(mem_code(e));
+  if (hbytes) p->d_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(p->d_items) + ibytes);
+  if (cudaMemcpy(p->d_items, p->items.data(), ibytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+      (hbytes &&
+       cudaMemcpy(p->d_hist, p->hist.data(), hbytes, cudaMemcpyHostToDevice) != cudaSuccess))
+    return fail(HSTU_ERR_CUDA);
+  if (norm) {
+    if ((e = cudaMalloc(reinterpret_cast<void**>(&p->d_norm),
+                        hstu::norm_scratch_bytes(p->total, heads, d))) != cudaSuccess)
+      return fail(mem_code(e));
   }
   *plan = p;
   return HSTU_OK;
@@ -300,11 +342,13 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
 
 int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
             const int32_t* num_targets, int batch, int heads, int d, int max_seqlen, float alpha,
-            float inv_n, void* out, cudaStream_t s) {
+            float inv_n, void* out, const hstu::NormGate* ng, cudaStream_t s) {
   if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
   if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
   if (batch == 0) return HSTU_OK;
   if (!offsets) return HSTU_ERR_INVALID_ARG;
+  int rc = HSTU_OK;
+  if (ng && (rc = check_norm_gate(ng->u, ng->gamma, ng->beta, ng->eps)) != HSTU_OK) return rc;
 
   // Offsets may live on the host or on the device.
   std::vector<int32_t> host_off;
@@ -323,8 +367,7 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
       return HSTU_ERR_CUDA;
     off = host_off.data();
   }
-  int rc = check_offsets(off, batch, max_seqlen);
-  if (rc != HSTU_OK) return rc;
+  if ((rc = check_offsets(off, batch, max_seqlen)) != HSTU_OK) return rc;
   if (num_targets && (rc = check_targets(off, num_targets, batch)) != HSTU_OK) return rc;
   const long long total = off[batch];
   if (total == 0) return HSTU_OK;
@@ -334,24 +377,36 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
   std::vector<int32_t> hist;
   if ((rc = build_worklist(off, num_targets, batch, heads, items, hist)) != HSTU_OK) return rc;
   if (items.empty()) return HSTU_OK;
+  // one stream-ordered allocation: the output-stage scratch (if any), the
+  // items, then (with candidates) the history lengths
+  const size_t nbytes = ng ? hstu::norm_scratch_bytes(total, heads, d) : 0;
   const size_t ibytes = items.size() * sizeof(hstu::Item);
   const size_t hbytes = hist.size() * sizeof(int32_t);
-  hstu::Item* d_items = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_items), ibytes + hbytes, s);
+  char* block = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&block), nbytes + ibytes + hbytes, s);
   if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
-  int32_t* d_hist =
-      hbytes ? reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_items) + ibytes) : nullptr;
-  // Pageable sources: each call returns once the bytes are staged, so the
+  hstu::Item* d_items = reinterpret_cast<hstu::Item*>(block + nbytes);
+  int32_t* d_hist = hbytes ? reinterpret_cast<int32_t*>(block + nbytes + ibytes) : nullptr;
+  // Pageable sources: each copy returns once the bytes are staged, so the
   // host vectors may go out of scope afterwards.
   e = cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && hbytes)
     e = cudaMemcpyAsync(d_hist, hist.data(), hbytes, cudaMemcpyHostToDevice, s);
+  hstu::NormGate ngw;
+  if (ng && e == cudaSuccess) {
+    ngw = norm_views(block, total, heads, d);
+    ngw.u = ng->u;
+    ngw.gamma = ng->gamma;
+    ngw.beta = ng->beta;
+    ngw.eps = ng->eps;
+  }
   if (e != cudaSuccess) {
-    cudaFreeAsync(d_items, s);
+    cudaFreeAsync(block, s);
     return HSTU_ERR_CUDA;
   }
-  rc = launch(d_items, d_hist, (int)items.size(), total, heads, d, q, k, v, alpha, inv_n, out, s);
-  if (cudaFreeAsync(d_items, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
+  rc = launch(d_items, d_hist, (int)items.size(), total, heads, d, q, k, v, alpha, inv_n, out,
+              ng ? &ngw : nullptr, s);
+  if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
   return rc;
 }
 
@@ -395,19 +450,25 @@ int hstu_worklist_build(const int32_t* host_offsets, int batch, int heads, int32
 
 int hstu_plan_create(const int32_t* host_offsets, int batch, int heads, int d, int max_seqlen,
                      hstu_plan** plan) {
-  return make_plan(host_offsets, nullptr, batch, heads, d, max_seqlen, plan);
+  return make_plan(host_offsets, nullptr, batch, heads, d, max_seqlen, 0u, plan);
 }
 
 int hstu_plan_create_targets(const int32_t* host_offsets, const int32_t* host_num_targets, int batch,
                              int heads, int d, int max_seqlen, hstu_plan** plan) {
   if (!host_num_targets && batch > 0) return HSTU_ERR_INVALID_ARG;
-  return make_plan(host_offsets, host_num_targets, batch, heads, d, max_seqlen, plan);
+  return make_plan(host_offsets, host_num_targets, batch, heads, d, max_seqlen, 0u, plan);
+}
+
+int hstu_plan_create_ex(const int32_t* host_offsets, const int32_t* host_num_targets, int batch,
+                        int heads, int d, int max_seqlen, uint32_t flags, hstu_plan** plan) {
+  return make_plan(host_offsets, host_num_targets, batch, heads, d, max_seqlen, flags, plan);
 }
 
 int hstu_plan_destroy(hstu_plan* plan) {
   if (!plan) return HSTU_OK;
   int rc = HSTU_OK;
   if (plan->d_items && cudaFree(plan->d_items) != cudaSuccess) rc = HSTU_ERR_CUDA;
+  if (plan->d_norm && cudaFree(plan->d_norm) != cudaSuccess) rc = HSTU_ERR_CUDA;
   delete plan;
   return rc;
 }
@@ -461,7 +522,7 @@ int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_by
   int sms = 0;
   const int rc = device_check(&sms);
   if (rc != HSTU_OK) return rc;
-  *grid = std::min((int)plan->items.size(), sms);
+  *grid = grid_for((int)plan->items.size(), sms);
   *block = hstu::kFwdThreads;
   *smem_bytes = hstu::fwd_smem_bytes(plan->d);
   return HSTU_OK;
@@ -474,15 +535,46 @@ int hstu_attn_fwd_plan(const hstu_plan* plan, const void* q, const void* k, cons
   int rc = check_buffers(q, k, v, out);
   if (rc != HSTU_OK) return rc;
   return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
-                plan->d, q, k, v,
-                alpha, inv_n, out, reinterpret_cast<cudaStream_t>(stream));
+                plan->d, q, k, v, alpha, inv_n, out, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int hstu_attn_fwd_norm_gate_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                                 const void* u, const float* gamma, const float* beta, float eps,
+                                 float alpha, float inv_n, void* y, hstu_stream_t stream) {
+  if (!plan || !(plan->flags & HSTU_PLAN_NORM_GATE)) return HSTU_ERR_INVALID_ARG;
+  if (plan->items.empty()) return HSTU_OK;
+  int rc = check_buffers(q, k, v, y);
+  if (rc != HSTU_OK) return rc;
+  if ((rc = check_norm_gate(u, gamma, beta, eps)) != HSTU_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  hstu::NormGate ng = norm_views(plan->d_norm, plan->total, plan->heads, plan->d);
+  ng.u = u;
+  ng.gamma = gamma;
+  ng.beta = beta;
+  ng.eps = eps;
+  return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
+                plan->d, q, k, v, alpha, inv_n, y, &ng, s);
+}
+
+int hstu_attn_fwd_norm_gate(const void* q, const void* k, const void* v, const void* u,
+                            const float* gamma, const float* beta, float eps, const int32_t* offsets,
+                            const int32_t* host_num_targets, int batch, int heads, int d,
+                            int max_seqlen, float alpha, float inv_n, void* y,
+                            hstu_stream_t stream) {
+  hstu::NormGate ng{};
+  ng.u = u;
+  ng.gamma = gamma;
+  ng.beta = beta;
+  ng.eps = eps;
+  return oneshot(q, k, v, offsets, host_num_targets, batch, heads, d, max_seqlen, alpha, inv_n, y,
+                 &ng, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_attn_fwd(const void* q, const void* k, const void* v, const int32_t* offsets, int batch,
                   int heads, int d, int max_seqlen, float alpha, float inv_n, void* out,
                   hstu_stream_t stream) {
   return oneshot(q, k, v, offsets, nullptr, batch, heads, d, max_seqlen, alpha, inv_n, out,
-                 reinterpret_cast<cudaStream_t>(stream));
+                 nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_attn_fwd_targets(const void* q, const void* k, const void* v, const int32_t* offsets,
@@ -491,7 +583,7 @@ int hstu_attn_fwd_targets(const void* q, const void* k, const void* v, const int
                           hstu_stream_t stream) {
   if (!host_num_targets && batch > 0) return HSTU_ERR_INVALID_ARG;
   return oneshot(q, k, v, offsets, host_num_targets, batch, heads, d, max_seqlen, alpha, inv_n, out,
-                 reinterpret_cast<cudaStream_t>(stream));
+                 nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_last_status(int* device_status, int* site) {

@@ -83,7 +83,7 @@ constexpr uint32_t kTmemCols = 512;
 // wait-site codes reported through g_dev_site
 enum : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSitePFull, kSiteOEmpty,
-  kSiteVFull, kSiteSFull, kSiteOFull, kSiteUnsignalled, kSiteSFree
+  kSiteVFull, kSiteSFull, kSiteOFull, kSiteUnsignalled, kSiteSFree, kSiteCheckIn
 };
 
 // Instruction descriptor, tcgen05.mma kind::f16: D fp32, A and B bf16,
@@ -478,10 +478,21 @@ struct BlockTgt : Block {
 template <bool TGT>
 using BlockOf = typename std::conditional<TGT, BlockTgt, Block>::type;
 
+// Kernel variants, one instantiation each so that the plain causal kernel
+// carries none of the others' bookkeeping: the candidate mask (items carry
+// a history length) and the output stage (Norm(O) (.) U in
+// the epilogue).
+constexpr int kVarTargets = 1, kVarNorm = 2;
+template <int VAR>
+constexpr bool has_targets = (VAR & kVarTargets) != 0;
+template <int VAR>
+constexpr bool has_norm = (VAR & kVarNorm) != 0;
+
 // TGT: items carry a history length (the candidate mask); otherwise every
 // item walks key blocks 0 .. qt.
-template <bool TGT>
-__device__ __forceinline__ bool load_block(const FwdArgs& a, int it, BlockOf<TGT>& b) {
+template <int VAR>
+__device__ __forceinline__ bool load_block(const FwdArgs& a, int it, BlockOf<has_targets<VAR>>& b) {
+  constexpr bool TGT = has_targets<VAR>;
   const int idx = item_index(it, blockIdx.x, gridDim.x);
   if (idx >= a.n_items) return false;
   const Item x = __ldg(&a.items[idx]);
@@ -504,8 +515,9 @@ __device__ __forceinline__ bool load_block(const FwdArgs& a, int it, BlockOf<TGT
 // A cursor over the CTA's key-block steps: item `it` (block b) at its
 // ki-th key block kt; tc counts the steps.  The next item's block is fetched one item ahead
 // so that crossing into it does not wait on a global load.
-template <bool TGT>
+template <int VAR>
 struct Cursor {
+  static constexpr bool TGT = has_targets<VAR>;
   int it, kt, ki;  // ki: index of the step among the item's key blocks; kt = b.key_block(ki)
   uint32_t tc;
   BlockOf<TGT> b, nb;
@@ -515,8 +527,8 @@ struct Cursor {
     kt = 0;
     ki = 0;
     tc = 0;
-    valid = load_block<TGT>(a, 0, b);
-    nvalid = valid && load_block<TGT>(a, 1, nb);
+    valid = load_block<VAR>(a, 0, b);
+    nvalid = valid && load_block<VAR>(a, 1, nb);
   }
   __device__ __forceinline__ void advance(const FwdArgs& a) {
     ++tc;
@@ -534,7 +546,7 @@ struct Cursor {
       ++it;
       valid = nvalid;
       b = nb;
-      nvalid = valid && load_block<TGT>(a, it + 1, nb);
+      nvalid = valid && load_block<VAR>(a, it + 1, nb);
     }
   }
 };
@@ -577,10 +589,11 @@ __device__ __forceinline__ void drain_copies(uint32_t full0, int slots, uint32_t
 // lands on QK-ready.  V slot t mod P is free once PV(t-P) has completed,
 // which QK-ready of step t includes.  A Q slot is free once the item's last
 // QK has completed (Q-empty).
-template <int D, bool KQ, bool TGT>
+template <int D, bool KQ, int VAR>
 __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, const FwdArgs& a,
                               uint32_t base, const WaitCtx& w) {
   using C = Cfg<D>;
+  constexpr bool TGT = has_targets<VAR>;
   constexpr int FULL = KQ ? C::B_QKREADY : C::B_VFULL;
   constexpr int OFF = KQ ? C::K_OFF : C::V_OFF;
   const uint32_t bars = base + C::BAR_OFF;
@@ -588,7 +601,7 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
   uint32_t c = 0, qc = 0;
   bool ok = true;
   BlockOf<TGT> b;
-  for (int it = 0; ok && load_block<TGT>(a, it, b); ++it) {
+  for (int it = 0; ok && load_block<VAR>(a, it, b); ++it) {
     if (KQ) {
       const int qs = (int)(qc % C::QS);
       if (!(ok = wait_one(bar(C::B_QEMPTY + qs), ((qc / C::QS) & 1u) ^ 1u, w, kSiteQEmpty))) break;
@@ -641,9 +654,10 @@ __device__ void role_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_q, 
 // that buffer, has completed (QK-ready); the products of different
 // accumulators are not ordered with respect to each other, so this wait is
 // needed.  It runs up to P steps ahead of the PV issuer.
-template <int D, bool TGT>
+template <int D, int VAR>
 __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
   using C = Cfg<D>;
+  constexpr bool TGT = has_targets<VAR>;
   constexpr int P = C::P;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
@@ -656,7 +670,7 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
   // Test hook: wait on a barrier that nothing arrives on, so that the
   // bounded wait runs out and the whole CTA takes its give-up path.
   if (a.debug_flags & kDebugUnsignalledWait) ok = wait_one(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
-  Cursor<TGT> qc;
+  Cursor<VAR> qc;
   qc.start(a);
   uint32_t ph = 0;  // (qc.tc / P) & 1
   auto step = [&](auto jc) -> bool {
@@ -706,16 +720,17 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
 // current step's products are issued, so that the tests' latency overlaps
 // them.  16-key step k: P_hi in columns 32 (k/2) + 8 (k%2) + [0, 8), P_lo 16
 // columns further; V rows 16 k.. (two 8-row atoms per step).
-template <int D, bool TGT>
+template <int D, int VAR>
 __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w) {
   using C = Cfg<D>;
+  constexpr bool TGT = has_targets<VAR>;
   constexpr int P = C::P;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   constexpr uint32_t IDESC_PV = make_idesc(kBM, D, 1);
   const uint64_t v_desc0 = smem_desc(base + C::V_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
   bool ok = true;
-  Cursor<TGT> pc;
+  Cursor<VAR> pc;
   pc.start(a);
   uint32_t ph = 0;  // (pc.tc / P) & 1
 
@@ -851,10 +866,11 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
 // owns score row r.  Every lane waits on S-full and arrives on P-full
 // itself (a vote keeps the warp's view uniform), so no lane-0 relay or warp
 // barrier sits on the path.
-template <int D, bool TGT>
+template <int D, int VAR>
 __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w, int warp,
                           int lane) {
   using C = Cfg<D>;
+  constexpr bool TGT = has_targets<VAR>;
   constexpr int P = C::P;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
@@ -863,7 +879,7 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
   const float2 ha2 = make_float2(a.half_alpha, a.half_alpha);
-  Cursor<TGT> cur;
+  Cursor<VAR> cur;
   cur.start(a);
   uint32_t s0[32], s1[32];
   while (cur.valid) {
@@ -930,10 +946,78 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
 
 // Epilogue warpgroup (warps 0-3): O -> x inv_n -> bf16 -> out.  Thread r
 // owns output row r of the item; rows past the sequence end are not stored.
-template <int D, bool TGT>
+// ------------------------------------------------ output stage Norm(O) (.) U
+// HSTU paper section 3: the layer's pointwise transformation takes
+// Norm(A(X) V(X)) (.) U(X), where Norm is a layer norm (section 3.1 requires
+// it right after the pointwise pooling) over the token's outputs of all
+// heads, with affine gamma and beta, and U already went through the SiLU
+// of the first sub-layer.
+//
+// The heads of a token are separate items, on any CTAs, so the norm is
+// split in two.  Here, in the attention epilogue, each row of each head
+// leaves its fp32 values x = O inv_n in xs (total, heads * d) and their
+// mean and M2 in stats (total, heads).  A second, bandwidth-bound kernel on
+// the same stream (norm_gate_kernel below) merges the heads' moments and
+// writes y.  Nothing waits on another CTA.
+struct RowStats {
+  float n, mean, m2;
+};
+
+// Fold 32 values of a row into (n, mean, m2): Chan, Golub and LeVeque's
+// pairwise update with the chunk's own mean and M2.
+__device__ __forceinline__ void stats_add32(RowStats& st, const float (&x)[32]) {
+  float sum = 0.f;
+#pragma unroll
+  for (int m = 0; m < 32; ++m) sum += x[m];
+  const float cmean = sum * (1.f / 32.f);
+  float cm2 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 32; ++m) {
+    const float e = x[m] - cmean;
+    cm2 = fmaf(e, e, cm2);
+  }
+  const float n1 = st.n + 32.f;
+  const float delta = cmean - st.mean;
+  const float wgt = 32.f / n1;
+  st.mean = fmaf(delta, wgt, st.mean);
+  st.m2 += cm2 + delta * delta * st.n * wgt;
+  st.n = n1;
+}
+
+// One head of one item for the warp's 32 rows (lane = row): x and the
+// row's moments out, then the O buffer released.
+template <int D, int VAR>
+__device__ __forceinline__ void norm_item(const FwdArgs& a, const BlockOf<has_targets<VAR>>& b,
+                                          uint32_t o_t, uint32_t oempty, int quarter, int lane) {
+  const int live = b.rows() - 32 * quarter;  // rows of the warp's quarter that exist (may be <= 0)
+  const size_t t = (size_t)b.s0 + kBM * b.qt + 32 * quarter + lane;
+  float* xrow = a.xs + t * (size_t)(a.heads * D) + (size_t)b.h * D;
+  RowStats st{0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(o_t + 32u * c, o);
+    float x[32];
+#pragma unroll
+    for (int m = 0; m < 32; ++m) x[m] = __uint_as_float(o[m]) * a.inv_n;
+    stats_add32(st, x);
+    if (lane < live) {
+      float4* dst = reinterpret_cast<float4*>(xrow + 32 * c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(oempty);
+  if (lane < live) a.stats[t * (size_t)a.heads + b.h] = make_float2(st.mean, st.m2);
+}
+
+template <int D, int VAR>
 __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, const WaitCtx& w,
                               int warp, int lane) {
   using C = Cfg<D>;
+  constexpr bool TGT = has_targets<VAR>;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   const int quarter = warp & 3;
@@ -941,13 +1025,19 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
   const float inv_n = a.inv_n;
   uint16_t* out = static_cast<uint16_t*>(a.out);
+  constexpr bool norm = has_norm<VAR>;
   BlockOf<TGT> b;
-  for (int it = 0; load_block<TGT>(a, it, b); ++it) {
+  for (int it = 0; load_block<VAR>(a, it, b); ++it) {
     const int ob = it % C::OB;
     if (!wait_warp(bar(C::B_OFULL + ob), (uint32_t)(it / C::OB) & 1u, w, kSiteOFull)) return;
     tc_fence_after();
     trace(a, kEvEpiStart, (unsigned)it);
     const uint32_t o_t = tmem + lane_off + C::O_COL + (uint32_t)(ob * D);
+    if constexpr (norm) {
+      norm_item<D, VAR>(a, b, o_t, bar(C::B_OEMPTY + ob), quarter, lane);
+      trace(a, kEvEpiEnd, (unsigned)it);
+      continue;
+    }
     uint4* dst = reinterpret_cast<uint4*>(
         out + ((size_t)(b.s0 + kBM * b.qt + row) * (size_t)a.heads + (size_t)b.h) * D);
     const bool live = row < b.rows();
@@ -973,7 +1063,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
   }
 }
 
-template <int D, bool TGT>
+template <int D, int VAR>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -1016,21 +1106,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const WaitCtx w{a.timeout_ns, abort_flag};
 
   if (warp == kTmaWarpK) {
-    if (lane == 0) role_producer<D, true, TGT>(&tm_k, &tm_q, a, base, w);
+    if (lane == 0) role_producer<D, true, VAR>(&tm_k, &tm_q, a, base, w);
     __syncwarp();
   } else if (warp == kTmaWarpV) {
-    if (lane == 0) role_producer<D, false, TGT>(&tm_v, &tm_q, a, base, w);
+    if (lane == 0) role_producer<D, false, VAR>(&tm_v, &tm_q, a, base, w);
     __syncwarp();
   } else if (warp == kMmaWarpQK) {
-    if (lane == 0) role_mma_qk<D, TGT>(a, base, tmem, w);
+    if (lane == 0) role_mma_qk<D, VAR>(a, base, tmem, w);
     __syncwarp();
   } else if (warp == kMmaWarpPV) {
-    if (lane == 0) role_mma_pv<D, TGT>(a, base, tmem, w);
+    if (lane == 0) role_mma_pv<D, VAR>(a, base, tmem, w);
     __syncwarp();
   } else if (warp >= kEwWarp0 && warp < kEwWarp0 + 8) {
-    role_silu<D, TGT>(a, base, tmem, w, warp, lane);
+    role_silu<D, VAR>(a, base, tmem, w, warp, lane);
   } else if (warp < kEpiWarp0 + 4) {
-    role_epilogue<D, TGT>(a, base, tmem, w, warp, lane);
+    role_epilogue<D, VAR>(a, base, tmem, w, warp, lane);
   }
 
   tc_fence_before();
@@ -1045,24 +1135,107 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool TGT>
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// y = Norm(x) (.) u over all tokens, grid-stride over tiles of R
+// consecutive tokens per warp, R = 128 / n4 when a row has n4 <= 128
+// 4-column chunks (so that every lane issues kLoads loads per round), else 1.
+// The heads' moments merge with equal counts d: mean = mean of the means,
+// M2 = sum of (M2_h + d (mean_h - mean)^2); lane r < R merges token r's and
+// hands them out by shuffle.  Consecutive lanes take consecutive chunks of
+// the tile's contiguous rows, so every access coalesces.
+constexpr int kNormThreads = 256;
+constexpr int kLoads = 4;
+__global__ void __launch_bounds__(kNormThreads) norm_gate_kernel(const FwdArgs a, int d,
+                                                                 long long total) {
+  const int lane = threadIdx.x & 31;
+  const int heads = a.heads;
+  const int n4 = heads * d / 4;  // chunks of a row: a multiple of 8
+  const int rows = n4 <= 32 * kLoads ? 32 * kLoads / n4 : 1;  // tokens per tile
+  const int span = rows * n4;    // chunks of a tile
+  const long long tiles = (total + rows - 1) / rows;
+  const long long nwarps = (long long)gridDim.x * (kNormThreads / 32);
+  const float4* g4 = reinterpret_cast<const float4*>(a.gamma);
+  const float4* b4 = reinterpret_cast<const float4*>(a.beta);
+  for (long long tile = (long long)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5);
+       tile < tiles; tile += nwarps) {
+    const long long t0 = tile * rows;
+    const int live = (int)(total - t0 < rows ? total - t0 : rows);  // tokens of the tile
+    const int lim = live * n4;
+    const float4* xs = reinterpret_cast<const float4*>(a.xs) + t0 * n4;
+    const uint2* u = reinterpret_cast<const uint2*>(a.u) + t0 * n4;
+    uint2* y = reinterpret_cast<uint2*>(a.out) + t0 * n4;
+    // the moments of token t0 + lane (lanes < live)
+    float mean = 0.f, rstd = 0.f;
+    if (lane < live) {
+      const float2* st = a.stats + (t0 + lane) * heads;
+      float msum = 0.f;
+      for (int h = 0; h < heads; ++h) msum += __ldg(st + h).x;
+      mean = msum / (float)heads;
+      float m2 = 0.f;
+      for (int h = 0; h < heads; ++h) {
+        const float2 v = __ldg(st + h);
+        const float dm = v.x - mean;
+        m2 += v.y + (float)d * dm * dm;
+      }
+      rstd = rsqrtf(m2 / (float)(heads * d) + a.eps);
+    }
+    for (int e0 = 0; e0 < span; e0 += 32 * kLoads) {
+      float4 x[kLoads];
+      uint2 uu[kLoads];
+#pragma unroll
+      for (int k = 0; k < kLoads; ++k) {
+        const int e = e0 + 32 * k + lane;
+        if (e < lim) {
+          x[k] = __ldcs(xs + e);
+          uu[k] = __ldcs(u + e);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kLoads; ++k) {
+        const int e = e0 + 32 * k + lane;
+        const int r = e / n4;  // token of the tile (< rows <= 32)
+        const int c = e - r * n4;
+        const float mr = __shfl_sync(0xffffffffu, mean, r & 31);
+        const float rr = __shfl_sync(0xffffffffu, rstd, r & 31);
+        if (e < lim) {
+          const float4 g = __ldg(g4 + c), bb = __ldg(b4 + c);
+          const float y0 = fmaf((x[k].x - mr) * rr, g.x, bb.x) * bf16_lo(uu[k].x);
+          const float y1 = fmaf((x[k].y - mr) * rr, g.y, bb.y) * bf16_hi(uu[k].x);
+          const float y2 = fmaf((x[k].z - mr) * rr, g.z, bb.z) * bf16_lo(uu[k].y);
+          const float y3 = fmaf((x[k].w - mr) * rr, g.w, bb.w) * bf16_hi(uu[k].y);
+          y[e] = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+        }
+      }
+    }
+  }
+}
+
+template <int D, int VAR>
 cudaError_t launch_dt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const FwdArgs& a, int grid, cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<D, TGT>,
+  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<D, VAR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
   if (e != cudaSuccess) return e;
-  hstu_fwd_kernel<D, TGT><<<grid, kFwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, a);
+  hstu_fwd_kernel<D, VAR><<<grid, kFwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, a);
+  if ((e = cudaGetLastError()) != cudaSuccess || !has_norm<VAR>) return e;
+  norm_gate_kernel<<<a.norm_grid, kNormThreads, 0, stream>>>(a, D, a.total);
   return cudaGetLastError();
 }
 
-// Items with a history array (the candidate mask) run the TGT instantiation;
-// causal items the other, which has none of its bookkeeping.
+// The variant follows the arguments: a history array selects the candidate
+// mask, a U pointer the output stage.
 template <int D>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdArgs& a, int grid, cudaStream_t stream) {
-  return a.item_hist ? launch_dt<D, true>(tq, tk, tv, a, grid, stream)
-                     : launch_dt<D, false>(tq, tk, tv, a, grid, stream);
+  switch ((a.item_hist ? kVarTargets : 0) | (a.u ? kVarNorm : 0)) {
+    case 0: return launch_dt<D, 0>(tq, tk, tv, a, grid, stream);
+    case kVarTargets: return launch_dt<D, kVarTargets>(tq, tk, tv, a, grid, stream);
+    case kVarNorm: return launch_dt<D, kVarNorm>(tq, tk, tv, a, grid, stream);
+    default: return launch_dt<D, kVarTargets | kVarNorm>(tq, tk, tv, a, grid, stream);
+  }
 }
 
 }  // namespace

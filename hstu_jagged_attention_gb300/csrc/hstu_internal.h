@@ -23,12 +23,44 @@ void fill_items(const int32_t* off, int batch, int heads, Item* dst);
 // sequence, head, qt ascending; hist_dst[i] is item i's history length.
 void fill_items_targets(const int32_t* off, const int32_t* num_targets, int batch, int heads,
                         Item* dst, int32_t* hist_dst);
+// The output stage's arguments (null: plain attention output).
+struct NormGate {
+  const void* u;
+  const float* gamma;
+  const float* beta;
+  float eps;
+  float* xs;
+  float2* stats;
+};
+// Scratch of the output stage in one allocation: xs, then stats (each part
+// rounded up to 16 bytes, so that what follows stays aligned).
+inline size_t norm_xs_bytes(long long total, int heads, int d) {
+  return (size_t)total * (size_t)heads * (size_t)d * sizeof(float);
+}
+inline size_t norm_stats_bytes(long long total, int heads) {
+  return ((size_t)total * (size_t)heads * 2u * sizeof(float) + 15u) & ~(size_t)15u;
+}
+inline size_t norm_scratch_bytes(long long total, int heads, int d) {
+  return norm_xs_bytes(total, heads, d) + norm_stats_bytes(total, heads);
+}
 
 struct FwdArgs {
   const Item* items;   // device, n_items entries, longest first
   const int32_t* item_hist;  // device, history length per item; null: no candidates
   int n_items;
-  void* out;           // bf16 (total, heads, d)
+  void* out;           // bf16 (total, heads, d): the attention output, or y with the output stage
+  // Output stage y = Norm(out) (.) u (null u: none).  u bf16 (total, heads, d);
+  // gamma, beta fp32 (heads * d); xs fp32 (total, heads * d) and stats
+  // (total, heads): the attention kernel's rows and per-head moments, read
+  // by the output-stage kernel (norm_grid blocks) that follows it.
+  const void* u;
+  const float* gamma;
+  const float* beta;
+  float eps;
+  float* xs;
+  float2* stats;
+  long long total;
+  int norm_grid;
   int heads;
   float half_alpha;    // alpha / 2 (silu(a s) = h + h tanh(h), h = a s / 2)
   float inv_n;
@@ -49,7 +81,8 @@ cudaError_t read_and_clear_trace(unsigned long long* dst, int capacity, int* n);
 int fwd_smem_bytes(int d);
 constexpr int kFwdThreads = 512;
 
-// Launch the persistent kernel for head dimension d on `grid` CTAs.
+// Launch the persistent kernel for head dimension d on `grid` CTAs (and,
+// with the output stage, the output-stage kernel after it).
 // The three tensor maps describe q, k, v as (d, heads, total) bf16 with box
 // (min(d,64), 1, 128) and the swizzle the kernel expects (fwd_swizzle_bytes).
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -68,6 +101,6 @@ int host_check_offsets(const int32_t* off, int batch, long long max_len);
 int host_check_buffers(const void* q, const void* k, const void* v, const void* out);
 int host_launch(const Item* d_items, const int32_t* d_hist, int n_items, long long total, int heads,
                 int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
-                void* out, cudaStream_t stream);
+                void* out, const NormGate* ng, cudaStream_t stream);
 
 }  // namespace hstu

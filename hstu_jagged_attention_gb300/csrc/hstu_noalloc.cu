@@ -73,5 +73,6 @@ extern "C" int hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v
   if (cudaMemcpyAsync(d_items, g_host_items, (size_t)n * sizeof(hstu::Item), cudaMemcpyHostToDevice,
                       s) != cudaSuccess)
     return HSTU_ERR_CUDA;
-  return hstu::host_launch(d_items, nullptr, (int)n, total, heads, d, q, k, v, alpha, inv_n, out, s);
+  return hstu::host_launch(d_items, nullptr, (int)n, total, heads, d, q, k, v, alpha, inv_n, out,
+                           nullptr, s);
 }

@@ -28,6 +28,12 @@ One more workload exercises the candidate (M-FALCON) mask of the HSTU paper
 history of 2048..8192 tokens followed by b_m = 1024 ranking candidates
 (the appendix takes b_m of the order of n), 4 heads, d = 64.  Its lengths
 use seed 5 and Q, K, V seed 1005.
+
+The layer's output stage, Norm(A V) (.) U (HSTU paper section 3), takes
+three more inputs, drawn by ``draw_norm_gate`` from ``default_rng(2000 +
+index)`` in this order: U of Q's shape, fp32 standard normals rounded to
+bf16; gamma = 1 + 0.1 N(0, 1) and beta = 0.1 N(0, 1), fp32, heads * d each.
+The layer norm's eps is NORM_EPS = 1e-6.
 """
 from __future__ import annotations
 
@@ -169,3 +175,17 @@ def candidate_workload() -> tuple[Workload, np.ndarray]:
     w = Workload("candidates", CANDIDATES_INDEX, len(lengths), 4, 64, 1.0, lengths,
                  1.0 / math.sqrt(64), 1.0 / int(lengths.max()))
     return w, np.full(len(lengths), CANDIDATES_BM, dtype=np.int32)
+
+
+NORM_EPS = 1e-6
+
+
+def draw_norm_gate(w: Workload, seed: int | None = None):
+    """U (CPU torch bf16, (total, heads, d)), gamma and beta (fp32 numpy,
+    heads * d) for the output stage; ``default_rng(2000 + index)`` or ``seed``."""
+    rng = np.random.default_rng(2000 + w.index if seed is None else seed)
+    u = bf16_round(rng.standard_normal((w.total, w.heads, w.d), dtype=np.float32))
+    width = w.heads * w.d
+    gamma = (1.0 + 0.1 * rng.standard_normal(width)).astype(np.float32)
+    beta = (0.1 * rng.standard_normal(width)).astype(np.float32)
+    return u, gamma, beta

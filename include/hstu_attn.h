@@ -233,6 +233,63 @@ int hstu_worklist_build_targets(const int32_t* host_offsets, const int32_t* host
                                 int capacity, int* n_items);
 
 /*
+ * Output stage Norm(A V) (.) U: HSTU paper section 3 (the layer's pointwise
+ * transformation after the spatial aggregation), section 3.1 (a layer norm
+ * must follow the pointwise pooling) and the feature-interaction paragraph,
+ * which writes the term as Norm(A(X) V(X)) (.) U(X).  The paper's equations
+ * are lost in extraction; the operation implemented is the plain reading:
+ *
+ *     x[t, :]  = the attention output of token t, all heads concatenated
+ *                (heads * d values, fp32 inside the kernel, never rounded)
+ *     y[t, c]  = ((x[t,c] - mean_t) / sqrt(var_t + eps) * gamma[c] + beta[c]) * u[t, c]
+ *
+ * with mean_t and var_t (biased, 1/(heads*d)) over the heads * d values of
+ * token t.  U is taken as given: it already went through the SiLU of the
+ * layer's first sub-layer.  Dropout is not applied.
+ *
+ *   u      bf16 device ptr, (total, heads, d) like q; 16-byte aligned.
+ *   gamma, beta  fp32 device ptrs, heads * d entries each (index h * d + c);
+ *          16-byte aligned.
+ *   eps    finite, >= 0.
+ *   y      bf16 device ptr, (total, heads, d); caller-allocated, written for
+ *          every token (bf16, round to nearest even).  The attention output
+ *          itself is not stored.
+ *
+ * The norm spans all heads of a token, while each work item is one head,
+ * so the call enqueues two kernels on the stream.  The attention kernel's
+ * epilogue writes every row's fp32 values and, per row and head, their mean
+ * and M2 to a scratch; an output-stage kernel then merges the heads'
+ * moments, normalises, applies gamma and beta and gates by U.  Scratch:
+ * 4 * total * heads * d bytes (rows) and 8 * total * heads (moments).
+ *
+ * hstu_plan_create_ex       as hstu_plan_create_targets (host_num_targets
+ *                           may be NULL: no candidates) with flags.
+ *                           HSTU_PLAN_NORM_GATE makes the plan own the
+ *                           output stage's scratch.  Such a plan also serves
+ *                           hstu_attn_fwd_plan.
+ * hstu_attn_fwd_norm_gate_plan  y for a HSTU_PLAN_NORM_GATE plan (else
+ *                           HSTU_ERR_INVALID_ARG); asynchronous on stream.
+ *                           Launches on one stream at a time per plan: the
+ *                           scratch is shared by its launches.
+ * hstu_attn_fwd_norm_gate   the one-shot form: offsets as hstu_attn_fwd,
+ *                           host_num_targets may be NULL; the scratch is
+ *                           allocated and freed stream-ordered.
+ * Errors: as hstu_attn_fwd; HSTU_ERR_INVALID_ARG also for a NULL or
+ * misaligned u, gamma, beta, a negative or non-finite eps, or unknown flags.
+ */
+#define HSTU_PLAN_NORM_GATE 1u
+int hstu_plan_create_ex(const int32_t* host_offsets, const int32_t* host_num_targets, int batch,
+                        int heads, int d, int max_seqlen, uint32_t flags, hstu_plan** plan);
+int hstu_attn_fwd_norm_gate_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                                 const void* u, const float* gamma, const float* beta, float eps,
+                                 float alpha, float inv_n, void* y, hstu_stream_t stream);
+int hstu_attn_fwd_norm_gate(const void* q, const void* k, const void* v, const void* u,
+                            const float* gamma, const float* beta, float eps, const int32_t* offsets,
+                            const int32_t* host_num_targets, int batch, int heads, int d,
+                            int max_seqlen, float alpha, float inv_n, void* y,
+                            hstu_stream_t stream);
+
+/*
  * hstu_launch_shape -- the grid the next launch for `plan` would use on the
  * current device: *grid persistent CTAs of *block threads with *smem_bytes
  * of dynamic shared memory.  Queries device attributes; launches nothing.

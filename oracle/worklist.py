@@ -21,12 +21,6 @@ needs key blocks 0 .. min(qt, KH) - 1 and its diagonal block qt: a block
 strictly between them holds only keys of other candidates, which no row of
 the query block sees.  Such an item costs min(qt, KH) + 1 key blocks, and
 items_targets also returns each item's hist.
-
-For the layer's output stage, Norm(A V) (.) U (HSTU paper section 3), the
-norm runs over all heads of a token, so the heads of one (sequence, query
-block) form a group that one worker takes whole.  ``grouped=True`` orders
-by cost descending, then b, qt, h ascending, which puts a group's heads
-next to each other.
 """
 from __future__ import annotations
 
@@ -35,7 +29,7 @@ import numpy as np
 BLOCK_M = 128
 
 
-def items(offsets, heads: int, block_m: int = BLOCK_M, grouped: bool = False) -> np.ndarray:
+def items(offsets, heads: int, block_m: int = BLOCK_M) -> np.ndarray:
     offsets = [int(x) for x in offsets]
     rows = []
     for b in range(len(offsets) - 1):
@@ -43,16 +37,15 @@ def items(offsets, heads: int, block_m: int = BLOCK_M, grouped: bool = False) ->
         tiles = (n + block_m - 1) // block_m
         for h in range(heads):
             for qt in range(tiles):
-                key = (b, qt, h) if grouped else (b, h, qt)
-                rows.append((-(qt + 1), *key, h, qt, offsets[b], n))
+                rows.append((-(qt + 1), b, h, qt, offsets[b], n))
     rows.sort()
-    out = np.array([(s0, n, h, qt) for (*_k, h, qt, s0, n) in rows], dtype=np.int32)
+    out = np.array([(s0, n, h, qt) for (_, b, h, qt, s0, n) in rows], dtype=np.int32)
     return out.reshape(-1, 4)
 
 
-def items_targets(offsets, num_targets, heads: int, block_m: int = BLOCK_M, grouped: bool = False):
+def items_targets(offsets, num_targets, heads: int, block_m: int = BLOCK_M):
     """(items (n, 4) int32, hist (n,) int32), ordered by cost descending,
-    then b, h, qt ascending (b, qt, h when grouped)."""
+    then b, h, qt ascending."""
     offsets = [int(x) for x in offsets]
     rows = []
     for b in range(len(offsets) - 1):
@@ -63,9 +56,9 @@ def items_targets(offsets, num_targets, heads: int, block_m: int = BLOCK_M, grou
         for h in range(heads):
             for qt in range(tiles):
                 cost = min(qt, kh) + 1
-                key = (b, qt, h) if grouped else (b, h, qt)
-                rows.append((-cost, *key, h, qt, offsets[b], n, hist))
+                rows.append((-cost, b, h, qt, offsets[b], n, hist))
     rows.sort()
-    it = np.array([(s0, n, h, qt) for (*_k, h, qt, s0, n, _hist) in rows], dtype=np.int32)
+    it = np.array([(s0, n, h, qt) for (_, b, h, qt, s0, n, _hist) in rows], dtype=np.int32)
     hs = np.array([hist for (*_, hist) in rows], dtype=np.int32)
     return it.reshape(-1, 4), hs
+

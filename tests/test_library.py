@@ -156,3 +156,33 @@ def test_candidate_counts_are_validated(nt):
     with pytest.raises(binding.HstuError) as e:
         binding.hstu_plan_create_targets(off, nt, 2, 1, 64, 8)
     assert e.value.code == binding.HSTU_ERR_INVALID_ARG
+
+
+# ------------------------------------------------ output stage Norm(A V) (.) U
+def test_norm_gate_validation_before_any_cuda_call():
+    off = np.array([0, 4], np.int32)
+    bad = [dict(u=0), dict(gamma=8), dict(eps=-1.0), dict(eps=float("nan")), dict(beta=0)]
+    for kw in bad:
+        args = dict(u=16, gamma=16, beta=16, eps=1e-5, heads=2)
+        args.update(kw)
+        with pytest.raises(binding.HstuError) as e:
+            binding.hstu_attn_fwd_norm_gate(16, 16, 16, args["u"], args["gamma"], args["beta"],
+                                            args["eps"], off, None, 1, args["heads"], 64, 4, 1.0,
+                                            1.0, 16, stream=0)
+        assert e.value.code == binding.HSTU_ERR_INVALID_ARG, kw
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_plan_create_ex(off, None, 1, 2, 64, 4, flags=4)
+    assert e.value.code == binding.HSTU_ERR_INVALID_ARG
+
+
+def test_norm_gate_on_a_plan_without_the_flag_is_rejected():
+    # an empty plan needs no device; the flag check comes first
+    p = binding.hstu_plan_create(np.zeros(3, np.int32), 2, 2, 64, 0)
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_attn_fwd_norm_gate_plan(p, 0, 0, 0, 0, 0, 0, 1e-5, 1.0, 1.0, 0, stream=0)
+    assert e.value.code == binding.HSTU_ERR_INVALID_ARG
+    binding.hstu_plan_destroy(p)
+    q = binding.hstu_plan_create_ex(np.zeros(3, np.int32), None, 2, 2, 64, 0,
+                                    flags=binding.HSTU_PLAN_NORM_GATE)
+    binding.hstu_attn_fwd_norm_gate_plan(q, 0, 0, 0, 0, 0, 0, 1e-5, 1.0, 1.0, 0, stream=0)  # no-op
+    binding.hstu_plan_destroy(q)

@@ -162,23 +162,3 @@ def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         reference.norm_gate(x, u, g[:4], g, 1e-5)
 
-
-@pytest.mark.parametrize("targets", [False, True])
-def test_grouped_worklist_keeps_a_groups_heads_together(targets):
-    from oracle import worklist
-    off = [0, 300, 300, 1000, 1001, 1257]
-    nt = [250, 0, 100, 1, 0]
-    heads = 3
-    if targets:
-        it, hs = worklist.items_targets(off, nt, heads, grouped=True)
-        flat, _ = worklist.items_targets(off, nt, heads)
-    else:
-        it, flat = worklist.items(off, heads, grouped=True), worklist.items(off, heads)
-    # the same item set as the ungrouped list
-    assert sorted(map(tuple, it)) == sorted(map(tuple, flat))
-    groups = it.reshape(-1, heads, 4)
-    assert np.all(groups[:, :, 0] == groups[:, :1, 0]) and np.all(groups[:, :, 3] == groups[:, :1, 3])
-    assert np.all(groups[:, :, 2] == np.arange(heads))
-    if not targets:
-        # causal: one cost per query block, so the grouped order is the plain one
-        assert np.array_equal(it, flat)
