@@ -35,8 +35,10 @@
  *
  * With no candidates (hist = n_b) this is the causal formula above.
  *
- * hstu_oracle_norm_gate_f64 (at the end of the file) applies the HSTU
- * layer's output stage, Norm(A V) (.) U, to rows the functions above made.
+ * hstu_oracle_fwd_rab_f64 adds the relative attention bias rab_{p,t}
+ * (see rab_t) to the scores; hstu_oracle_norm_gate_f64 (at the end of the
+ * file) applies the HSTU layer's output stage, Norm(A V) (.) U, to rows the
+ * functions above made.
  */
 #include <math.h>
 #include <pthread.h>
@@ -47,11 +49,62 @@
  * overflows to +inf and the quotient is -0, which is the limit. */
 double hstu_oracle_silu(double x) { return x / (1.0 + exp(-x)); }
 
+/*
+ * Relative attention bias rab_{p,t} (HSTU paper section 3: a bias that
+ * merges relative position p and time t, added inside the attention's
+ * nonlinearity; section 3.4: M-FALCON modifies it for candidates; Appendix G
+ * fuses its construction into the attention operator).  The construction
+ * is lost in extraction; the plain reading taken, in the style of bucketed
+ * relative position biases:
+ *
+ *   bias(i, j) = pos[min(floor(log2(dp + 1)), npos - 1)]
+ *              + time[min(floor(log2(dt + 1)), ntime - 1)]
+ *   dp = p(i) - p(j),  dt = max(ts[i] - ts[j], 0)
+ *
+ * with p(i) = i for history tokens and p(i) = hist for every candidate: a
+ * candidate sits right after the history, as in its own causal pass
+ * (Appendix H), so the identity one pass == separate causal passes holds
+ * with the bias too.  The bias is added to the scaled score:
+ * silu(alpha * <q_i, k_j> + bias(i, j)).
+ */
+typedef struct {
+    const int64_t* ts;  /* timestamp per token */
+    const float* pos;   /* npos entries */
+    int npos;
+    const float* time;  /* ntime entries */
+    int ntime;
+} rab_t;
+
+/* floor(log2(x)) for x >= 1, by halving. */
+static int floor_log2_u64(uint64_t x) {
+    int r = 0;
+    while (x > 1) {
+        x >>= 1;
+        ++r;
+    }
+    return r;
+}
+
+int hstu_oracle_rab_bucket(int64_t delta, int nbuckets) {
+    if (delta < 0) delta = 0;
+    const int b = floor_log2_u64((uint64_t)delta + 1);
+    return b < nbuckets - 1 ? b : nbuckets - 1;
+}
+
+static double rab_bias(const rab_t* R, int64_t seq_start, int64_t i, int64_t j, int64_t hist) {
+    const int64_t pi = i < hist ? i : hist, pj = j < hist ? j : hist;
+    const int bp = hstu_oracle_rab_bucket(pi - pj, R->npos);
+    const int bt = hstu_oracle_rab_bucket(R->ts[seq_start + i] - R->ts[seq_start + j], R->ntime);
+    return (double)R->pos[bp] + (double)R->time[bt];
+}
+
 /* One output row: out_row[c] for c < d, fp64.  hist: the number of history
- * tokens of the sequence (its length when it has no candidates). */
-static void oracle_row(const float* q, const float* k, const float* v, int64_t seq_start,
-                       int64_t i, int64_t hist, int heads, int d, int h, double alpha,
-                       double inv_n, double* acc /* d doubles, scratch */, double* out_row) {
+ * tokens of the sequence (its length when it has no candidates).  R: the
+ * relative attention bias, or NULL. */
+static void oracle_row(const float* q, const float* k, const float* v, const rab_t* R,
+                       int64_t seq_start, int64_t i, int64_t hist, int heads, int d, int h,
+                       double alpha, double inv_n, double* acc /* d doubles, scratch */,
+                       double* out_row) {
     const int64_t t = seq_start + i;
     const float* qr = q + (t * heads + h) * (int64_t)d;
     for (int c = 0; c < d; ++c) acc[c] = 0.0;
@@ -62,7 +115,8 @@ static void oracle_row(const float* q, const float* k, const float* v, int64_t s
         const float* vr = v + (s * heads + h) * (int64_t)d;
         double dot = 0.0;
         for (int c = 0; c < d; ++c) dot += (double)qr[c] * (double)kr[c];
-        const double p = hstu_oracle_silu(alpha * dot);
+        const double bias = R ? rab_bias(R, seq_start, i, j, hist) : 0.0;
+        const double p = hstu_oracle_silu(alpha * dot + bias);
         for (int c = 0; c < d; ++c) acc[c] += p * (double)vr[c];
     }
     for (int c = 0; c < d; ++c) out_row[c] = inv_n * acc[c];
@@ -72,6 +126,7 @@ typedef struct {
     const float *q, *k, *v;
     const int64_t* offsets;
     const int64_t* num_targets; /* candidates per sequence, or NULL: none */
+    const rab_t* rab;           /* relative attention bias, or NULL: none */
     int batch, heads, d;
     double alpha, inv_n;
     double* out;
@@ -115,7 +170,7 @@ static void* worker_full(void* arg) {
         const int64_t s0 = J->offsets[b], n = J->offsets[b + 1] - J->offsets[b];
         const int64_t hist = hist_of(J, b);
         for (int64_t i = 0; i < n; ++i)
-            oracle_row(J->q, J->k, J->v, s0, i, hist, J->heads, J->d, h, J->alpha, J->inv_n, acc,
+            oracle_row(J->q, J->k, J->v, J->rab, s0, i, hist, J->heads, J->d, h, J->alpha, J->inv_n, acc,
                        J->out + ((s0 + i) * J->heads + h) * (int64_t)J->d);
     }
     free(acc);
@@ -136,7 +191,7 @@ static void* worker_rows(void* arg) {
             continue;
         }
         const int64_t s0 = J->offsets[b];
-        oracle_row(J->q, J->k, J->v, s0, t - s0, hist_of(J, b), J->heads, J->d, J->rows_h[r],
+        oracle_row(J->q, J->k, J->v, J->rab, s0, t - s0, hist_of(J, b), J->heads, J->d, J->rows_h[r],
                    J->alpha, J->inv_n, acc, o);
     }
     free(acc);
@@ -180,7 +235,8 @@ int hstu_oracle_fwd_f64(const float* q, const float* k, const float* v, const in
                         int batch, int heads, int d, double alpha, double inv_n, double* out,
                         int nthreads) {
     if (check_offsets(offsets, batch) || heads < 1 || d < 1) return -1;
-    job_t J = {q, k, v, offsets, NULL, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0, NULL, NULL};
+    job_t J = {q, k, v, offsets, NULL, NULL, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0, NULL,
+               NULL};
     return run(&J, nthreads, worker_full);
 }
 
@@ -191,7 +247,7 @@ int hstu_oracle_rows_f64(const float* q, const float* k, const float* v, const i
                          const int64_t* rows_t, const int32_t* rows_h, int64_t nrows, double* out,
                          int nthreads) {
     if (check_offsets(offsets, batch) || heads < 1 || d < 1 || nrows < 0) return -1;
-    job_t J = {q, k, v, offsets, NULL, batch, heads, d, alpha, inv_n, out, rows_t, rows_h, nrows,
+    job_t J = {q, k, v, offsets, NULL, NULL, batch, heads, d, alpha, inv_n, out, rows_t, rows_h, nrows,
                NULL, NULL};
     return run(&J, nthreads, worker_rows);
 }
@@ -205,7 +261,7 @@ int hstu_oracle_fwd_targets_f64(const float* q, const float* k, const float* v,
     if (check_offsets(offsets, batch) || check_targets(offsets, num_targets, batch) ||
         heads < 1 || d < 1)
         return -1;
-    job_t J = {q, k, v, offsets, num_targets, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0,
+    job_t J = {q, k, v, offsets, num_targets, NULL, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0,
                NULL, NULL};
     return run(&J, nthreads, worker_full);
 }
@@ -219,7 +275,38 @@ int hstu_oracle_rows_targets_f64(const float* q, const float* k, const float* v,
     if (check_offsets(offsets, batch) || check_targets(offsets, num_targets, batch) ||
         heads < 1 || d < 1 || nrows < 0)
         return -1;
-    job_t J = {q, k, v, offsets, num_targets, batch, heads, d, alpha, inv_n, out, rows_t, rows_h,
+    job_t J = {q, k, v, offsets, num_targets, NULL, batch, heads, d, alpha, inv_n, out, rows_t, rows_h,
+               nrows, NULL, NULL};
+    return run(&J, nthreads, worker_rows);
+}
+
+/* With the relative attention bias (see rab_t): ts has one timestamp per
+ * token, pos npos >= 1 and time ntime >= 1 entries.  num_targets may be
+ * NULL (no candidates).  Otherwise as hstu_oracle_fwd_targets_f64. */
+int hstu_oracle_fwd_rab_f64(const float* q, const float* k, const float* v, const int64_t* offsets,
+                            const int64_t* num_targets, const int64_t* ts, const float* pos,
+                            int npos, const float* time, int ntime, int batch, int heads, int d,
+                            double alpha, double inv_n, double* out, int nthreads) {
+    if (check_offsets(offsets, batch) || (num_targets && check_targets(offsets, num_targets, batch)) ||
+        heads < 1 || d < 1 || npos < 1 || ntime < 1)
+        return -1;
+    const rab_t R = {ts, pos, npos, time, ntime};
+    job_t J = {q, k, v, offsets, num_targets, &R, batch, heads, d, alpha, inv_n, out, NULL, NULL, 0,
+               NULL, NULL};
+    return run(&J, nthreads, worker_full);
+}
+
+/* Sampled rows with the relative attention bias. */
+int hstu_oracle_rows_rab_f64(const float* q, const float* k, const float* v,
+                             const int64_t* offsets, const int64_t* num_targets, const int64_t* ts,
+                             const float* pos, int npos, const float* time, int ntime, int batch,
+                             int heads, int d, double alpha, double inv_n, const int64_t* rows_t,
+                             const int32_t* rows_h, int64_t nrows, double* out, int nthreads) {
+    if (check_offsets(offsets, batch) || (num_targets && check_targets(offsets, num_targets, batch)) ||
+        heads < 1 || d < 1 || nrows < 0 || npos < 1 || ntime < 1)
+        return -1;
+    const rab_t R = {ts, pos, npos, time, ntime};
+    job_t J = {q, k, v, offsets, num_targets, &R, batch, heads, d, alpha, inv_n, out, rows_t, rows_h,
                nrows, NULL, NULL};
     return run(&J, nthreads, worker_rows);
 }

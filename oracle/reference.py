@@ -13,6 +13,13 @@ the M-FALCON mask), the last num_targets[b] tokens of sequence b are
 candidates: term j of row i is kept iff j <= i and (j < hist or j == i),
 hist = n_b - num_targets[b].
 
+With ``rab`` = (ts, pos, time) -- one timestamp per token and two bias
+tables -- the scores get the relative attention bias of the HSTU paper
+(section 3, rab_{p,t}; reading in hstu_oracle.c): silu(alpha q.k + pos[bp]
++ time[bt]), bp and bt the clipped floor(log2(delta + 1)) buckets of the
+relative position (candidates sit at position hist) and of the timestamp
+difference (clamped at 0).
+
 ``norm_gate`` is the layer's output stage on those rows, Norm(A V) (.) U
 (HSTU paper section 3 and section 3.1): a layer norm over each token's
 heads * d outputs with affine gamma, beta, times U elementwise.
@@ -57,6 +64,18 @@ def _load():
         lib.hstu_oracle_norm_gate_f64.argtypes = [d, f, f, f, ctypes.c_double, ctypes.c_int64,
                                                   ctypes.c_int64, d]
         lib.hstu_oracle_norm_gate_f64.restype = ctypes.c_int
+        lib.hstu_oracle_rab_bucket.argtypes = [ctypes.c_int64, ctypes.c_int]
+        lib.hstu_oracle_rab_bucket.restype = ctypes.c_int
+        lib.hstu_oracle_fwd_rab_f64.argtypes = [f, f, f, i64, i64, i64, f, ctypes.c_int, f,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_double, ctypes.c_double, d,
+                                                ctypes.c_int]
+        lib.hstu_oracle_fwd_rab_f64.restype = ctypes.c_int
+        lib.hstu_oracle_rows_rab_f64.argtypes = [f, f, f, i64, i64, i64, f, ctypes.c_int, f,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_double, ctypes.c_double, i64,
+                                                 i32, ctypes.c_int64, d, ctypes.c_int]
+        lib.hstu_oracle_rows_rab_f64.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -81,8 +100,31 @@ def silu(x: float) -> float:
     return _load().hstu_oracle_silu(float(x))
 
 
+def rab_bucket(delta: int, nbuckets: int) -> int:
+    """The oracle's bias bucket min(floor(log2(max(delta, 0) + 1)), nbuckets - 1), for pinning."""
+    return _load().hstu_oracle_rab_bucket(int(delta), int(nbuckets))
+
+
+def _rab_arrays(rab, total):
+    ts, pos, time = rab
+    ts = np.ascontiguousarray(np.asarray(ts), dtype=np.int64).reshape(-1)
+    pos, time = _f32(pos).reshape(-1), _f32(time).reshape(-1)
+    if ts.shape != (total,) or pos.size < 1 or time.size < 1:
+        raise ValueError("rab needs one timestamp per token and non-empty tables")
+    return ts, pos, time
+
+
+def _targets_ptr(num_targets, batch):
+    if num_targets is None:
+        return None, None
+    nt = np.ascontiguousarray(np.asarray(num_targets), dtype=np.int64)
+    if nt.shape != (batch,):
+        raise ValueError("num_targets needs one entry per sequence")
+    return nt, _ptr(nt, ctypes.c_int64)
+
+
 def hstu_fwd(q, k, v, offsets, alpha: float, inv_n: float, threads: int | None = None,
-             num_targets=None) -> np.ndarray:
+             num_targets=None, rab=None) -> np.ndarray:
     """All rows: returns fp64 array (total, heads, d)."""
     qf, kf, vf = _f32(q), _f32(k), _f32(v)
     total, heads, d = qf.shape
@@ -91,7 +133,16 @@ def hstu_fwd(q, k, v, offsets, alpha: float, inv_n: float, threads: int | None =
     if kf.shape != qf.shape or vf.shape != qf.shape or (batch >= 0 and off[-1] != total):
         raise ValueError("shape mismatch between q/k/v/offsets")
     out = np.zeros((total, heads, d), dtype=np.float64)
-    if num_targets is None:
+    if rab is not None:
+        ts, pos, time = _rab_arrays(rab, total)
+        nt, ntp = _targets_ptr(num_targets, batch)
+        rc = _load().hstu_oracle_fwd_rab_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                             _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64), ntp,
+                                             _ptr(ts, ctypes.c_int64), _ptr(pos, ctypes.c_float),
+                                             pos.size, _ptr(time, ctypes.c_float), time.size, batch,
+                                             heads, d, float(alpha), float(inv_n),
+                                             _ptr(out, ctypes.c_double), threads or default_threads())
+    elif num_targets is None:
         rc = _load().hstu_oracle_fwd_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
                                          _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
                                          batch, heads, d, float(alpha), float(inv_n),
@@ -113,7 +164,7 @@ def hstu_fwd(q, k, v, offsets, alpha: float, inv_n: float, threads: int | None =
 
 
 def hstu_rows(q, k, v, offsets, alpha: float, inv_n: float, rows_t, rows_h,
-              threads: int | None = None, num_targets=None) -> np.ndarray:
+              threads: int | None = None, num_targets=None, rab=None) -> np.ndarray:
     """Sampled rows: row r is (token rows_t[r], head rows_h[r]); returns fp64 (nrows, d)."""
     qf, kf, vf = _f32(q), _f32(k), _f32(v)
     total, heads, d = qf.shape
@@ -123,7 +174,19 @@ def hstu_rows(q, k, v, offsets, alpha: float, inv_n: float, rows_t, rows_h,
     if rt.shape != rh.shape:
         raise ValueError("rows_t and rows_h differ in length")
     out = np.zeros((len(rt), d), dtype=np.float64)
-    if num_targets is None:
+    if rab is not None:
+        ts, pos, time = _rab_arrays(rab, total)
+        nt, ntp = _targets_ptr(num_targets, len(off) - 1)
+        rc = _load().hstu_oracle_rows_rab_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                              _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
+                                              ntp, _ptr(ts, ctypes.c_int64),
+                                              _ptr(pos, ctypes.c_float), pos.size,
+                                              _ptr(time, ctypes.c_float), time.size, len(off) - 1,
+                                              heads, d, float(alpha), float(inv_n),
+                                              _ptr(rt, ctypes.c_int64), _ptr(rh, ctypes.c_int32),
+                                              len(rt), _ptr(out, ctypes.c_double),
+                                              threads or default_threads())
+    elif num_targets is None:
         rc = _load().hstu_oracle_rows_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
                                           _ptr(vf, ctypes.c_float), _ptr(off, ctypes.c_int64),
                                           len(off) - 1, heads, d, float(alpha), float(inv_n),
@@ -166,18 +229,18 @@ def norm_gate(x, u, gamma, beta, eps: float) -> np.ndarray:
 
 
 def hstu_fwd_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, alpha: float, inv_n: float,
-                       threads: int | None = None, num_targets=None) -> np.ndarray:
+                       threads: int | None = None, num_targets=None, rab=None) -> np.ndarray:
     """Norm(A V) (.) U over all tokens: fp64 (total, heads, d)."""
-    x = hstu_fwd(q, k, v, offsets, alpha, inv_n, threads=threads, num_targets=num_targets)
+    x = hstu_fwd(q, k, v, offsets, alpha, inv_n, threads=threads, num_targets=num_targets, rab=rab)
     return norm_gate(x, u, gamma, beta, eps)
 
 
 def hstu_rows_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, alpha: float, inv_n: float,
-                        rows_t, threads: int | None = None, num_targets=None) -> np.ndarray:
+                        rows_t, threads: int | None = None, num_targets=None, rab=None) -> np.ndarray:
     """Norm(A V) (.) U for the sampled tokens rows_t: fp64 (nrows, heads, d)."""
     heads, d = np.shape(q)[1], np.shape(q)[2]
     rt = np.repeat(np.asarray(rows_t, dtype=np.int64), heads)
     rh = np.tile(np.arange(heads, dtype=np.int32), len(rows_t))
     x = hstu_rows(q, k, v, offsets, alpha, inv_n, rt, rh, threads=threads,
-                  num_targets=num_targets).reshape(len(rows_t), heads, d)
+                  num_targets=num_targets, rab=rab).reshape(len(rows_t), heads, d)
     return norm_gate(x, _f32(u)[np.asarray(rows_t, dtype=np.int64)], gamma, beta, eps)

@@ -18,7 +18,7 @@ from oracle import dense
 MUTANTS = {
     "silu_sign": ("x / (1.0 + exp(-x))", "x / (1.0 + exp(x))"),
     "drop_diagonal": ("for (int64_t j = 0; j <= i; ++j)", "for (int64_t j = 0; j < i; ++j)"),
-    "alpha_divides": ("hstu_oracle_silu(alpha * dot)", "hstu_oracle_silu(dot / alpha)"),
+    "alpha_divides": ("hstu_oracle_silu(alpha * dot + bias)", "hstu_oracle_silu(dot / alpha + bias)"),
     "q_dot_v": ("dot += (double)qr[c] * (double)kr[c]", "dot += (double)qr[c] * (double)vr[c]"),
     "inv_n_missing": ("out_row[c] = inv_n * acc[c]", "out_row[c] = acc[c]"),
     "wrong_head_stride": ("(s * heads + h) * (int64_t)d;\n        const float* vr",
@@ -205,3 +205,65 @@ def test_norm_mutant_is_caught(tmp_path, name):
     old, new = NORM_MUTANTS[name]
     assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     assert not _norm_pins_pass(_build(tmp_path, name, src.replace(old, new)))
+
+
+# ------------------------------------------------ the relative attention bias rab_{p,t}
+RAB_MUTANTS = {
+    "bucket_of_delta_not_delta_plus_one": ("floor_log2_u64((uint64_t)delta + 1)",
+                                           "floor_log2_u64((uint64_t)delta + (delta == 0))"),
+    "time_difference_reversed": ("R->ts[seq_start + i] - R->ts[seq_start + j]",
+                                 "R->ts[seq_start + j] - R->ts[seq_start + i]"),
+    "candidates_keep_their_position": ("pi = i < hist ? i : hist", "pi = i"),
+    "bias_scaled_by_alpha": ("hstu_oracle_silu(alpha * dot + bias)",
+                             "hstu_oracle_silu(alpha * (dot + bias))"),
+    "time_table_by_position_bucket": ("(double)R->pos[bp] + (double)R->time[bt]",
+                                      "(double)R->pos[bp] + (double)R->time[bp < R->ntime ? bp : 0]"),
+}
+
+
+def _rab_pins_pass(L) -> bool:
+    """Brute force with numpy-built buckets and the candidate identity, as in
+    test_oracle_rab.py, through the planted copy."""
+    from tests.test_oracle_rab import _bruteforce, _case, _tables
+    f, dptr, i64 = (ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
+                    ctypes.POINTER(ctypes.c_int64))
+    L.hstu_oracle_fwd_rab_f64.argtypes = [f, f, f, i64, i64, i64, f, ctypes.c_int, f, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                          ctypes.c_double, dptr, ctypes.c_int]
+    P = lambda a, t: a.ctypes.data_as(ctypes.POINTER(t))
+
+    def run(q, k, v, off, nt, ts, pos, time, alpha, inv_n):
+        total, heads, d = q.shape
+        out = np.zeros((total, heads, d))
+        off = np.asarray(off, dtype=np.int64)
+        keep = None if nt is None else np.asarray(nt, dtype=np.int64)
+        ntp = None if keep is None else P(keep, ctypes.c_int64)
+        ts = np.asarray(ts, dtype=np.int64)
+        L.hstu_oracle_fwd_rab_f64(P(q, ctypes.c_float), P(k, ctypes.c_float), P(v, ctypes.c_float),
+                                  P(off, ctypes.c_int64), ntp, P(ts, ctypes.c_int64),
+                                  P(pos, ctypes.c_float), len(pos), P(time, ctypes.c_float),
+                                  len(time), len(off) - 1, heads, d, alpha, inv_n,
+                                  P(out, ctypes.c_double), 2)
+        return out
+
+    ok = True
+    rng = np.random.default_rng(21)
+    q, k, v, off, ts = _case(rng, [40, 25], 2, 8)
+    pos, time = _tables(rng, 32, 32)
+    nt = [11, 0]
+    got = run(q, k, v, off, nt, ts, pos, time, 0.4, 0.05)
+    want = _bruteforce(q, k, v, off, ts, pos, time, 0.4, 0.05, nt)
+    ok &= bool(np.abs(got - want).max() <= 1e-12 * np.abs(want).max())
+    return ok
+
+
+def test_unmutated_copy_passes_the_rab_pins(tmp_path):
+    assert _rab_pins_pass(_build(tmp_path, "orig_r", open(oracle_build.SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(RAB_MUTANTS))
+def test_rab_mutant_is_caught(tmp_path, name):
+    src = open(oracle_build.SRC).read()
+    old, new = RAB_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    assert not _rab_pins_pass(_build(tmp_path, name, src.replace(old, new)))
