@@ -182,7 +182,7 @@ def aggregate(flops_per_rank: float, ms_local: float, world: int, device=None):
 
 
 def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int | None = None,
-                      num_targets=None, norm_gate=None):
+                      num_targets=None, norm_gate=None, rab=None):
     """Time the oracle on a bounded, uniformly random sample of rows.
 
     With ``norm_gate`` = (u, gamma, beta, eps) the sample is of tokens, each
@@ -211,10 +211,10 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
         if norm_gate is not None:
             u, g, b, eps = norm_gate
             reference.hstu_rows_norm_gate(q, k, v, u, g, b, eps, w.offsets, w.alpha, w.inv_n, t,
-                                          threads=threads, num_targets=num_targets)
+                                          threads=threads, num_targets=num_targets, rab=rab)
         else:
             reference.hstu_rows(q, k, v, w.offsets, w.alpha, w.inv_n, t, h, threads=threads,
-                                num_targets=num_targets)
+                                num_targets=num_targets, rab=rab)
 
     # calibrate on a small sample, then size the real one to ~target_s
     t, h, fl = rows(64)
@@ -243,6 +243,17 @@ def _norm_gate_desc(args) -> dict:
                             f"eps {workloads.NORM_EPS:g}, times U (HSTU paper section 3)"}
 
 
+def _rab_desc(args) -> dict:
+    if not args.rab:
+        return {}
+    return {"rab": "relative attention bias rab_{p,t}: log2-bucketed position and time tables, "
+                   f"{workloads.RAB_BUCKETS} entries each (HSTU paper section 3)"}
+
+
+def _cpu_rab(args, w):
+    return workloads.draw_rab(w) if args.rab else None
+
+
 def _cpu_norm_gate(args, w):
     if not args.norm_gate:
         return None
@@ -262,7 +273,7 @@ def run_reference(args, w, nt=None):
     desc, threads = "", 0
     for s in range(args.warmup + args.steps):
         val, desc, threads, dt = cpu_oracle_sample(w, qf, kf, vf, per_step_s, seed=s,
-                                                   num_targets=nt, norm_gate=ng)
+                                                   num_targets=nt, norm_gate=ng, rab=_cpu_rab(args, w))
         if s >= args.warmup:
             vals.append(val)
     value = statistics.mean(vals)
@@ -270,7 +281,8 @@ def run_reference(args, w, nt=None):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, **w.describe(), **_targets_desc(nt), **_norm_gate_desc(args)},
+        "config": {"workload": w.name, **w.describe(), **_targets_desc(nt), **_norm_gate_desc(args),
+                   **_rab_desc(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -311,15 +323,19 @@ def run_ours(args, w, nt=None):
         u = u_h.to(dev)
         gamma, beta = torch.from_numpy(g_h).to(dev), torch.from_numpy(b_h).to(dev)
         eps = workloads.NORM_EPS
+    rab = None
+    if args.rab:
+        # the tables are weights, resident on the device; the timestamps are
+        # per-token inputs
+        ts_h, pos_h, time_h = workloads.draw_rab(w)
+        ts_pin = torch.from_numpy(ts_h).pin_memory()
+        rab = (ts_pin.to(dev), torch.from_numpy(pos_h).to(dev), torch.from_numpy(time_h).to(dev))
     plan = binding.hstu_plan_create_ex(w.offsets, nt, w.batch, w.heads, w.d, w.max_seqlen,
                                        binding.HSTU_PLAN_NORM_GATE if ng else 0)
 
     def launch():
-        if ng:
-            binding.hstu_attn_fwd_norm_gate_plan(plan, q, k, v, u, gamma, beta, eps, w.alpha,
-                                                 w.inv_n, out, stream)
-        else:
-            binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+        binding.hstu_attn_fwd_plan_ex(plan, q, k, v, w.alpha, w.inv_n, out, rab=rab,
+                                      norm_gate=(u, gamma, beta, eps) if ng else None, stream=stream)
 
     n_items = binding.hstu_plan_num_items(plan)
     grid, block, smem = binding.hstu_launch_shape(plan)
@@ -364,7 +380,7 @@ def run_ours(args, w, nt=None):
     peak = peaks["bf16_tflops"]
     achieved = flops / (ms * 1e-3) / 1e12
     traffic = None
-    key = w.name + ("+norm_gate" if ng else "")
+    key = w.name + ("+norm_gate" if ng else "") + ("+rab" if args.rab else "")
     if MEASURED_TRAFFIC.get(key) and MEASURED_TRAFFIC.get("sha256") == kernel_sha():
         traffic = MEASURED_TRAFFIC[key]
 
@@ -375,15 +391,21 @@ def run_ours(args, w, nt=None):
     oe = torch.empty_like(out)
     offsets_host = w.offsets.copy()
 
+    tse = torch.empty_like(rab[0]) if rab is not None else None
+
     def e2e_step():
         qe.copy_(pin[0], non_blocking=True)
         ke.copy_(pin[1], non_blocking=True)
         ve.copy_(pin[2], non_blocking=True)
         if ng:
             ue.copy_(pin[3], non_blocking=True)
-            binding.hstu_attn_fwd_norm_gate(qe, ke, ve, ue, gamma, beta, eps, offsets_host, nt,
-                                            w.batch, w.heads, w.d, w.max_seqlen, w.alpha, w.inv_n,
-                                            oe, stream)
+        if rab is not None:
+            tse.copy_(ts_pin, non_blocking=True)
+        if ng or rab is not None:
+            binding.hstu_attn_fwd_ex(qe, ke, ve, offsets_host, w.batch, w.heads, w.d, w.max_seqlen,
+                                     w.alpha, w.inv_n, oe, num_targets=nt,
+                                     rab=(tse, rab[1], rab[2]) if rab is not None else None,
+                                     norm_gate=(ue, gamma, beta, eps) if ng else None, stream=stream)
         elif nt is None:
             binding.hstu_attn_fwd(qe, ke, ve, offsets_host, w.batch, w.heads, w.d, w.max_seqlen,
                                   w.alpha, w.inv_n, oe, stream)
@@ -419,13 +441,16 @@ def run_ours(args, w, nt=None):
         raise RuntimeError(f"device wait gave up during the e2e region (site {site})")
     elem = 2
     h2d = (4 if ng else 3) * w.total * w.heads * w.d * elem + offsets_host.nbytes
+    if rab is not None:
+        h2d += 4 * w.total
     d2h = w.total * w.heads * w.d * elem
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         qf, kf, vf = (t.float().numpy() for t in (q_h, k_h, v_h))
         val, desc, threads, _ = cpu_oracle_sample(w, qf, kf, vf, args.cpu_seconds, num_targets=nt,
-                                                  norm_gate=_cpu_norm_gate(args, w))
+                                                  norm_gate=_cpu_norm_gate(args, w),
+                                                  rab=_cpu_rab(args, w))
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
 
     binding.hstu_plan_destroy(plan)
@@ -434,7 +459,7 @@ def run_ours(args, w, nt=None):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {**w.describe(), **_targets_desc(nt), **_norm_gate_desc(args),
+            "config": {**w.describe(), **_targets_desc(nt), **_norm_gate_desc(args), **_rab_desc(args),
                        "l2": "flushed between steps (256 MiB write)",
                        "work_items": n_items, "grid": grid, "block": block, "smem_bytes": smem,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -471,6 +496,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--norm-gate", action="store_true",
                     help="fuse the layer's output stage Norm(A V) * U into the timed call")
+    ap.add_argument("--rab", action="store_true",
+                    help="add the relative attention bias rab_{p,t} (timestamps and bucketed tables)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

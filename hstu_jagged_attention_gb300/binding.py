@@ -33,6 +33,21 @@ TRACE_EVENTS = {1: "qk_issue", 2: "pv_issue", 3: "silu_start", 4: "silu_end", 5:
 
 # name -> (restype, argtypes); the exported symbols of include/hstu_attn.h
 _VP, _I32P, _IP = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int)
+
+
+class _Rab(ctypes.Structure):
+    """struct hstu_rab"""
+    _fields_ = [("timestamps", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("num_pos", ctypes.c_int),
+                ("time", ctypes.c_void_p), ("num_time", ctypes.c_int)]
+
+
+class _NormGate(ctypes.Structure):
+    """struct hstu_norm_gate"""
+    _fields_ = [("u", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+                ("eps", ctypes.c_float)]
+
+
+_RABP, _NGP = ctypes.POINTER(_Rab), ctypes.POINTER(_NormGate)
 _SIGNATURES = {
     "hstu_attn_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP, _VP]),
@@ -64,6 +79,11 @@ _SIGNATURES = {
                                            ctypes.c_int, ctypes.c_uint32, ctypes.POINTER(_VP)]),
     "hstu_attn_fwd_norm_gate_plan": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float,
                                                     ctypes.c_float, ctypes.c_float, _VP, _VP]),
+    "hstu_attn_fwd_plan_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _RABP, _NGP, ctypes.c_float,
+                                             ctypes.c_float, _VP, _VP]),
+    "hstu_attn_fwd_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32P, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, _RABP, _NGP, ctypes.c_float,
+                                        ctypes.c_float, _VP, _VP]),
     "hstu_attn_fwd_norm_gate": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP,
                                                _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP,
@@ -202,6 +222,47 @@ def _offsets_arg(offsets):
         return offsets.data_ptr(), None
     keep = _host_offsets(offsets)
     return keep.ctypes.data, keep
+
+
+def _rab_struct(rab):
+    """rab = (timestamps int32 device tensor, pos fp32 table, time fp32 table) or None."""
+    if rab is None:
+        return None
+    ts, pos, time = rab
+    n_pos = int(pos.numel()) if hasattr(pos, "numel") else len(pos)
+    n_time = int(time.numel()) if hasattr(time, "numel") else len(time)
+    return ctypes.pointer(_Rab(_addr(ts), _addr(pos), n_pos, _addr(time), n_time))
+
+
+def _ng_struct(norm_gate):
+    """norm_gate = (u, gamma, beta, eps) or None."""
+    if norm_gate is None:
+        return None
+    u, gamma, beta, eps = norm_gate
+    return ctypes.pointer(_NormGate(_addr(u), _addr(gamma), _addr(beta), float(eps)))
+
+
+def hstu_attn_fwd_plan_ex(plan: Plan, q, k, v, alpha: float, inv_n: float, out, rab=None,
+                          norm_gate=None, stream=None) -> None:
+    """Every option on a plan: ``rab`` = (timestamps, pos, time), ``norm_gate`` =
+    (u, gamma, beta, eps) (the plan needs HSTU_PLAN_NORM_GATE)."""
+    _check(lib().hstu_attn_fwd_plan_ex(plan.handle, _addr(q), _addr(k), _addr(v), _rab_struct(rab),
+                                       _ng_struct(norm_gate), float(alpha), float(inv_n), _addr(out),
+                                       _stream(stream)), "hstu_attn_fwd_plan_ex")
+
+
+def hstu_attn_fwd_ex(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: int, alpha: float,
+                     inv_n: float, out, num_targets=None, rab=None, norm_gate=None,
+                     stream=None) -> None:
+    """Every option in one call (see hstu_attn_fwd_plan_ex; num_targets host memory or None)."""
+    off_ptr, keep = _offsets_arg(offsets)
+    nt = None if num_targets is None else _host_targets(num_targets, int(batch))
+    _check(lib().hstu_attn_fwd_ex(_addr(q), _addr(k), _addr(v), off_ptr,
+                                  None if nt is None else nt.ctypes.data_as(_I32P), int(batch),
+                                  int(heads), int(d), int(max_seqlen), _rab_struct(rab),
+                                  _ng_struct(norm_gate), float(alpha), float(inv_n), _addr(out),
+                                  _stream(stream)), "hstu_attn_fwd_ex")
+    del keep
 
 
 def hstu_attn_fwd_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, num_targets, batch: int,

@@ -137,7 +137,7 @@ int grid_for(int n_items, int sms) { return std::min(n_items, sms); }
 
 int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long long total,
            int heads, int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
-           void* out, const hstu::NormGate* ng, cudaStream_t stream) {
+           void* out, const hstu::NormGate* ng, cudaStream_t stream, const hstu_rab* rab = nullptr) {
   if (n_items == 0) return HSTU_OK;
   int sms = 0;
   int rc = device_check(&sms);
@@ -160,6 +160,11 @@ int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long l
   a.total = total;
   // the output-stage kernel: one warp per token, up to 8 blocks of 8 warps per SM
   a.norm_grid = (int)std::min<long long>((total + 7) / 8, 8LL * sms);
+  a.rab_ts = rab ? rab->timestamps : nullptr;
+  a.rab_pos = rab ? rab->pos : nullptr;
+  a.rab_time = rab ? rab->time : nullptr;
+  a.rab_npos = rab ? rab->num_pos : 0;
+  a.rab_ntime = rab ? rab->num_time : 0;
   a.heads = heads;
   a.half_alpha = 0.5f * alpha;
   a.inv_n = inv_n;
@@ -181,7 +186,19 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
               unsigned flags, hstu_plan** plan);
 int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
             const int32_t* num_targets, int batch, int heads, int d, int max_seqlen, float alpha,
-            float inv_n, void* out, const hstu::NormGate* ng, cudaStream_t s);
+            float inv_n, void* out, const hstu::NormGate* ng, cudaStream_t s,
+            const hstu_rab* rab = nullptr);
+
+// The bias: timestamps 4-byte aligned, tables 4-byte aligned with 1..32 entries.
+int check_rab(const hstu_rab* r) {
+  if (!r->timestamps || !r->pos || !r->time) return HSTU_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(r->timestamps) | reinterpret_cast<uintptr_t>(r->pos) |
+       reinterpret_cast<uintptr_t>(r->time)) & 3u)
+    return HSTU_ERR_INVALID_ARG;
+  if (r->num_pos < 1 || r->num_pos > 32 || r->num_time < 1 || r->num_time > 32)
+    return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
 
 // The output stage's buffers: u and y like q, gamma and beta 16-byte
 // aligned, eps finite and >= 0.
@@ -342,13 +359,15 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
 
 int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
             const int32_t* num_targets, int batch, int heads, int d, int max_seqlen, float alpha,
-            float inv_n, void* out, const hstu::NormGate* ng, cudaStream_t s) {
+            float inv_n, void* out, const hstu::NormGate* ng, cudaStream_t s,
+            const hstu_rab* rab) {
   if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
   if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
   if (batch == 0) return HSTU_OK;
   if (!offsets) return HSTU_ERR_INVALID_ARG;
   int rc = HSTU_OK;
   if (ng && (rc = check_norm_gate(ng->u, ng->gamma, ng->beta, ng->eps)) != HSTU_OK) return rc;
+  if (rab && (rc = check_rab(rab)) != HSTU_OK) return rc;
 
   // Offsets may live on the host or on the device.
   std::vector<int32_t> host_off;
@@ -405,7 +424,7 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
     return HSTU_ERR_CUDA;
   }
   rc = launch(d_items, d_hist, (int)items.size(), total, heads, d, q, k, v, alpha, inv_n, out,
-              ng ? &ngw : nullptr, s);
+              ng ? &ngw : nullptr, s, rab);
   if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
   return rc;
 }
@@ -554,6 +573,43 @@ int hstu_attn_fwd_norm_gate_plan(const hstu_plan* plan, const void* q, const voi
   ng.eps = eps;
   return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
                 plan->d, q, k, v, alpha, inv_n, y, &ng, s);
+}
+
+int hstu_attn_fwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                          const hstu_rab* rab, const hstu_norm_gate* ng, float alpha, float inv_n,
+                          void* out, hstu_stream_t stream) {
+  if (!plan || (ng && !(plan->flags & HSTU_PLAN_NORM_GATE))) return HSTU_ERR_INVALID_ARG;
+  if (plan->items.empty()) return HSTU_OK;
+  int rc = check_buffers(q, k, v, out);
+  if (rc != HSTU_OK) return rc;
+  if (ng && (rc = check_norm_gate(ng->u, ng->gamma, ng->beta, ng->eps)) != HSTU_OK) return rc;
+  if (rab && (rc = check_rab(rab)) != HSTU_OK) return rc;
+  hstu::NormGate ngw{};
+  if (ng) {
+    ngw = norm_views(plan->d_norm, plan->total, plan->heads, plan->d);
+    ngw.u = ng->u;
+    ngw.gamma = ng->gamma;
+    ngw.beta = ng->beta;
+    ngw.eps = ng->eps;
+  }
+  return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
+                plan->d, q, k, v, alpha, inv_n, out, ng ? &ngw : nullptr,
+                reinterpret_cast<cudaStream_t>(stream), rab);
+}
+
+int hstu_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* offsets,
+                     const int32_t* host_num_targets, int batch, int heads, int d, int max_seqlen,
+                     const hstu_rab* rab, const hstu_norm_gate* ng, float alpha, float inv_n,
+                     void* out, hstu_stream_t stream) {
+  hstu::NormGate ngw{};
+  if (ng) {
+    ngw.u = ng->u;
+    ngw.gamma = ng->gamma;
+    ngw.beta = ng->beta;
+    ngw.eps = ng->eps;
+  }
+  return oneshot(q, k, v, offsets, host_num_targets, batch, heads, d, max_seqlen, alpha, inv_n, out,
+                 ng ? &ngw : nullptr, reinterpret_cast<cudaStream_t>(stream), rab);
 }
 
 int hstu_attn_fwd_norm_gate(const void* q, const void* k, const void* v, const void* u,

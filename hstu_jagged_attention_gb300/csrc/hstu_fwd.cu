@@ -480,13 +480,16 @@ using BlockOf = typename std::conditional<TGT, BlockTgt, Block>::type;
 
 // Kernel variants, one instantiation each so that the plain causal kernel
 // carries none of the others' bookkeeping: the candidate mask (items carry
-// a history length) and the output stage (Norm(O) (.) U in
-// the epilogue).
-constexpr int kVarTargets = 1, kVarNorm = 2;
+// a history length), the output stage (Norm(O) (.) U; the epilogue writes
+// fp32 rows and moments) and the relative attention bias (in the SiLU
+// stage).
+constexpr int kVarTargets = 1, kVarNorm = 2, kVarRab = 4;
 template <int VAR>
 constexpr bool has_targets = (VAR & kVarTargets) != 0;
 template <int VAR>
 constexpr bool has_norm = (VAR & kVarNorm) != 0;
+template <int VAR>
+constexpr bool has_rab = (VAR & kVarRab) != 0;
 
 // TGT: items carry a history length (the candidate mask); otherwise every
 // item walks key blocks 0 .. qt.
@@ -829,16 +832,53 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
 // pressure down.  MASK 0: no mask; 1: keep keys k <= lim (the diagonal
 // block); 2: also drop keys k >= lim_hist other than k == lim (the candidate
 // mask).
-template <int MASK>
+// The relative attention bias rab_{p,t} (HSTU paper section 3; section 3.4
+// for candidates).  The construction is lost in extraction; the reading
+// taken is a pair of bucketed tables added to the scaled score:
+//   bias(i, j) = pos[min(floor(log2(dp + 1)), npos - 1)]
+//              + time[min(floor(log2(dt + 1)), ntime - 1)],
+//   dp = p(i) - p(j) (p(i) = i, or hist for a candidate), dt = max(ts_i - ts_j, 0).
+// floor(log2(x)) = 31 - clz(x) for 1 <= x <= 2^31, so lane l holds half the
+// entry of bucket 31 - l (clamped to the table), and a lookup is one shuffle
+// from lane clz(x): no gather, no clamp.
+struct RabRow {
+  const int32_t* ts;  // timestamps of the item's sequence
+  int last;           // its last token (sequence-local)
+  int pe_i;           // the row's position (hist for a candidate)
+  int ts_i;
+  int hist;           // candidates: the history length
+  float pos_l, time_l;  // this lane's table entries, halved
+};
+
+template <bool TGT>
+__device__ __forceinline__ float rab_half(const RabRow& r, int j) {
+  const int pe_j = TGT ? (j < r.hist ? j : r.hist) : j;
+  const int dp = r.pe_i - pe_j;
+  const int dt = r.ts_i - __ldg(r.ts + (j < r.last ? j : r.last));
+  const uint32_t xp = (uint32_t)(dp > 0 ? dp : 0) + 1u;
+  const uint32_t xt = (uint32_t)(dt > 0 ? dt : 0) + 1u;
+  return __shfl_sync(0xffffffffu, r.pos_l, __clz((int)xp)) +
+         __shfl_sync(0xffffffffu, r.time_l, __clz((int)xt));
+}
+
+// MASK 0: none; 1: keep key k iff k <= lim; 2: the candidate mask.  RAB:
+// add the relative attention bias of keys j0 .. j0 + 31 (sequence-local).
+template <int MASK, bool RAB = false, bool TGT = false>
 __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, int lim_hist,
-                                             uint32_t t) {
+                                             uint32_t t, const RabRow* rab = nullptr, int j0 = 0) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t hi[8], lo[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int k = 16 * h + 2 * m;
-      const float2 x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
+      float2 x;
+      if constexpr (RAB) {
+        const float2 bh = make_float2(rab_half<TGT>(*rab, j0 + k), rab_half<TGT>(*rab, j0 + k + 1));
+        x = __ffma2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2, bh);
+      } else {
+        x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
+      }
       float2 p = __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
       if (MASK == 1) {  // keep key k iff k <= lim (causal)
         p.x = (k > lim) ? 0.0f : p.x;
@@ -879,6 +919,13 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
   const float2 ha2 = make_float2(a.half_alpha, a.half_alpha);
+  constexpr bool RAB = has_rab<VAR>;
+  RabRow rr{};
+  if constexpr (RAB) {
+    const int bp = 31 - lane, bt = 31 - lane;
+    rr.pos_l = 0.5f * __ldg(a.rab_pos + (bp < a.rab_npos - 1 ? bp : a.rab_npos - 1));
+    rr.time_l = 0.5f * __ldg(a.rab_time + (bt < a.rab_ntime - 1 ? bt : a.rab_ntime - 1));
+  }
   Cursor<VAR> cur;
   cur.start(a);
   uint32_t s0[32], s1[32];
@@ -895,18 +942,41 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
     tc_fence_after();
     trace(a, kEvSiluStart, cur.tc);
     const uint32_t t_s = lane_base + (uint32_t)(j * 128);
+    if constexpr (RAB) {
+      // the row's position and timestamp (a row past the sequence reads its
+      // last token; its results are never stored)
+      const int i = kBM * cur.b.qt + row;
+      rr.ts = a.rab_ts + cur.b.s0;
+      rr.last = cur.b.n - 1;
+      if constexpr (TGT) {
+        rr.hist = cur.b.hist;
+        rr.pe_i = i < cur.b.hist ? i : cur.b.hist;
+      } else {
+        rr.pe_i = i;
+      }
+      rr.ts_i = __ldg(rr.ts + (i < rr.last ? i : rr.last));
+    }
+    const int kbase = kBN * cur.kt;
     bool plain = cur.kt != cur.b.qt;
     if constexpr (TGT) plain = cur.b.unmasked(cur.kt);
-    if (plain && quarter * 32 < cur.b.rows()) {
+    if (RAB && plain && quarter * 32 < cur.b.rows()) {
+      // one score buffer: the bias computation needs the registers
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(t_s + 32u * c, s1);
+        silu_store32<0, RAB, TGT>(s1, ha2, 0, 0, t_s + 32u * c, &rr, kbase + 32 * c);
+      }
+      tmem_wait_st();
+    } else if (plain && quarter * 32 < cur.b.rows()) {
       tmem_ld32_async(t_s, s0);
       tmem_wait_ld(s0);
 #pragma unroll 1
       for (int c = 0; c < 4; c += 2) {
         tmem_ld32_async(t_s + 32u * (c + 1), s1);
-        silu_store32<0>(s0, ha2, 0, 0, t_s + 32u * c);
+        silu_store32<0, RAB, TGT>(s0, ha2, 0, 0, t_s + 32u * c, &rr, kbase + 32 * c);
         tmem_wait_ld(s1);
         if (c + 2 < 4) tmem_ld32_async(t_s + 32u * (c + 2), s0);
-        silu_store32<0>(s1, ha2, 0, 0, t_s + 32u * (c + 1));
+        silu_store32<0, RAB, TGT>(s1, ha2, 0, 0, t_s + 32u * (c + 1), &rr, kbase + 32 * (c + 1));
         if (c + 2 < 4) tmem_wait_ld(s0);
       }
       tmem_wait_st();
@@ -932,7 +1002,8 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
           tmem_st16(t_s + 32u * c + 16u, z);
         } else {
           tmem_ld32(t_s + 32u * c, s1);
-          silu_store32<TGT ? 2 : 1>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c, t_s + 32u * c);
+          silu_store32<TGT ? 2 : 1, RAB, TGT>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c, t_s + 32u * c,
+                                              &rr, kbase + 32 * c);
         }
       }
       tmem_wait_st();
@@ -1226,15 +1297,19 @@ cudaError_t launch_dt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 }
 
 // The variant follows the arguments: a history array selects the candidate
-// mask, a U pointer the output stage.
+// mask, a U pointer the output stage, a timestamp array the bias.
 template <int D>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdArgs& a, int grid, cudaStream_t stream) {
-  switch ((a.item_hist ? kVarTargets : 0) | (a.u ? kVarNorm : 0)) {
+  switch ((a.item_hist ? kVarTargets : 0) | (a.u ? kVarNorm : 0) | (a.rab_ts ? kVarRab : 0)) {
     case 0: return launch_dt<D, 0>(tq, tk, tv, a, grid, stream);
-    case kVarTargets: return launch_dt<D, kVarTargets>(tq, tk, tv, a, grid, stream);
-    case kVarNorm: return launch_dt<D, kVarNorm>(tq, tk, tv, a, grid, stream);
-    default: return launch_dt<D, kVarTargets | kVarNorm>(tq, tk, tv, a, grid, stream);
+    case 1: return launch_dt<D, 1>(tq, tk, tv, a, grid, stream);
+    case 2: return launch_dt<D, 2>(tq, tk, tv, a, grid, stream);
+    case 3: return launch_dt<D, 3>(tq, tk, tv, a, grid, stream);
+    case 4: return launch_dt<D, 4>(tq, tk, tv, a, grid, stream);
+    case 5: return launch_dt<D, 5>(tq, tk, tv, a, grid, stream);
+    case 6: return launch_dt<D, 6>(tq, tk, tv, a, grid, stream);
+    default: return launch_dt<D, 7>(tq, tk, tv, a, grid, stream);
   }
 }
 

@@ -61,6 +61,12 @@ struct FwdArgs {
   float2* stats;
   long long total;
   int norm_grid;
+  // Relative attention bias (null rab_ts: none): int32 timestamp per token,
+  // fp32 tables of rab_npos and rab_ntime (1..32) entries.
+  const int32_t* rab_ts;
+  const float* rab_pos;
+  const float* rab_time;
+  int rab_npos, rab_ntime;
   int heads;
   float half_alpha;    // alpha / 2 (silu(a s) = h + h tanh(h), h = a s / 2)
   float inv_n;

@@ -34,6 +34,14 @@ three more inputs, drawn by ``draw_norm_gate`` from ``default_rng(2000 +
 index)`` in this order: U of Q's shape, fp32 standard normals rounded to
 bf16; gamma = 1 + 0.1 N(0, 1) and beta = 0.1 N(0, 1), fp32, heads * d each.
 The layer norm's eps is NORM_EPS = 1e-6.
+
+The relative attention bias (HSTU paper section 3, rab_{p,t}) takes
+timestamps and two tables, drawn by ``draw_rab`` from
+``default_rng(3000 + index)``:
+- Each sequence starts at a uniform integer time in [0, 10^9) seconds.
+- Its tokens follow in time order with log-normal gaps, exp(N(6, 2.5^2))
+  seconds (a median of about 7 minutes), summed and capped below 2^31.
+- The tables have RAB_BUCKETS = 32 entries each, 0.2 N(0, 1), fp32.
 """
 from __future__ import annotations
 
@@ -189,3 +197,26 @@ def draw_norm_gate(w: Workload, seed: int | None = None):
     gamma = (1.0 + 0.1 * rng.standard_normal(width)).astype(np.float32)
     beta = (0.1 * rng.standard_normal(width)).astype(np.float32)
     return u, gamma, beta
+
+
+RAB_BUCKETS = 32
+
+
+def draw_rab(w: Workload, seed: int | None = None, backwards: float = 0.0):
+    """Timestamps (int32 numpy, one per token) and the position and time
+    tables (fp32 numpy, RAB_BUCKETS each); ``default_rng(3000 + index)`` or
+    ``seed``.  ``backwards``: the fraction of gaps drawn negative (tests of
+    the clamp at dt = 0)."""
+    rng = np.random.default_rng(3000 + w.index if seed is None else seed)
+    ts = np.zeros(w.total, dtype=np.int64)
+    off = w.offsets.astype(np.int64)
+    for b in range(w.batch):
+        n = int(w.lengths[b])
+        start = int(rng.integers(0, 10 ** 9))
+        gaps = np.exp(rng.normal(6.0, 2.5, size=n)).astype(np.int64)
+        if backwards:
+            gaps[rng.random(n) < backwards] *= -1
+        ts[off[b]:off[b + 1]] = np.clip(start + np.cumsum(gaps), 0, 2 ** 31 - 1)
+    pos = (0.2 * rng.standard_normal(RAB_BUCKETS)).astype(np.float32)
+    time = (0.2 * rng.standard_normal(RAB_BUCKETS)).astype(np.float32)
+    return ts.astype(np.int32), pos, time

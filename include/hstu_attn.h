@@ -278,8 +278,58 @@ int hstu_worklist_build_targets(const int32_t* host_offsets, const int32_t* host
  * misaligned u, gamma, beta, a negative or non-finite eps, or unknown flags.
  */
 #define HSTU_PLAN_NORM_GATE 1u
+typedef struct hstu_norm_gate {
+  const void* u;        /* bf16 (total, heads, d), 16-byte aligned */
+  const float* gamma;   /* fp32 heads * d, 16-byte aligned */
+  const float* beta;    /* fp32 heads * d, 16-byte aligned */
+  float eps;            /* finite, >= 0 */
+} hstu_norm_gate;
 int hstu_plan_create_ex(const int32_t* host_offsets, const int32_t* host_num_targets, int batch,
                         int heads, int d, int max_seqlen, uint32_t flags, hstu_plan** plan);
+
+/*
+ * Relative attention bias rab_{p,t}: HSTU paper section 3 (a bias that
+ * merges relative position p and time t, added inside the attention's
+ * nonlinearity), section 3.4 (M-FALCON modifies it for candidates) and
+ * Appendix G (its construction fused into the attention operator).  The
+ * construction is lost in extraction; the reading implemented is a pair of
+ * bucketed tables added to the scaled score:
+ *
+ *   score(i, j) = alpha * <q_i, k_j> + pos[min(floor(log2(dp + 1)), num_pos - 1)]
+ *                                    + time[min(floor(log2(dt + 1)), num_time - 1)]
+ *   dp = p(i) - p(j),  dt = max(ts_i - ts_j, 0)
+ *
+ * with sequence-local positions p(i) = i, except that every candidate
+ * (with host_num_targets) sits at p = hist, as in its own causal pass.
+ *
+ *   timestamps  device int32, one per token, in [0, 2^31); 4-byte aligned.
+ *   pos, time   device fp32 tables of num_pos and num_time entries, 1..32
+ *               each (log2 buckets of 32-bit differences never exceed 31).
+ */
+typedef struct hstu_rab {
+  const int32_t* timestamps;
+  const float* pos;
+  int num_pos;
+  const float* time;
+  int num_time;
+} hstu_rab;
+
+/*
+ * hstu_attn_fwd_plan_ex / hstu_attn_fwd_ex -- every option in one call:
+ * rab (NULL: no bias) and ng (NULL: out is the attention output; else out
+ * is y of the output stage, and a plan needs HSTU_PLAN_NORM_GATE).  The
+ * one-shot form takes host_num_targets (NULL: none) as
+ * hstu_attn_fwd_targets.  Errors: as the specific calls, and
+ * HSTU_ERR_INVALID_ARG for NULL or misaligned rab pointers or table sizes
+ * outside 1..32.
+ */
+int hstu_attn_fwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                          const hstu_rab* rab, const hstu_norm_gate* ng, float alpha, float inv_n,
+                          void* out, hstu_stream_t stream);
+int hstu_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* offsets,
+                     const int32_t* host_num_targets, int batch, int heads, int d, int max_seqlen,
+                     const hstu_rab* rab, const hstu_norm_gate* ng, float alpha, float inv_n,
+                     void* out, hstu_stream_t stream);
 int hstu_attn_fwd_norm_gate_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
                                  const void* u, const float* gamma, const float* beta, float eps,
                                  float alpha, float inv_n, void* y, hstu_stream_t stream);

@@ -186,3 +186,28 @@ def test_norm_gate_on_a_plan_without_the_flag_is_rejected():
                                     flags=binding.HSTU_PLAN_NORM_GATE)
     binding.hstu_attn_fwd_norm_gate_plan(q, 0, 0, 0, 0, 0, 0, 1e-5, 1.0, 1.0, 0, stream=0)  # no-op
     binding.hstu_plan_destroy(q)
+
+
+# ------------------------------------------------ relative attention bias
+def test_rab_validation_before_any_cuda_call():
+    off = np.array([0, 4], np.int32)
+    good = dict(ts=16, pos=16, npos=8, time=16, ntime=8)
+    bad = [dict(ts=0), dict(pos=0), dict(time=0), dict(ts=18), dict(npos=0), dict(npos=33),
+           dict(ntime=0), dict(ntime=40)]
+    for kw in bad:
+        a = dict(good)
+        a.update(kw)
+        rab = binding._Rab(a["ts"], a["pos"], a["npos"], a["time"], a["ntime"])
+        code = binding.lib().hstu_attn_fwd_ex(16, 16, 16, off.ctypes.data, None, 1, 2, 64, 4,
+                                              binding.ctypes.pointer(rab), None, 1.0, 1.0, 16, None)
+        assert code == binding.HSTU_ERR_INVALID_ARG, kw
+
+
+def test_rab_draws_are_in_range():
+    w = workloads.workload("dense")
+    ts, pos, time = workloads.draw_rab(w)
+    assert ts.dtype == np.int32 and ts.shape == (w.total,) and ts.min() >= 0
+    assert len(pos) == len(time) == workloads.RAB_BUCKETS
+    off = w.offsets
+    for b in range(w.batch):
+        assert np.all(np.diff(ts[off[b]:off[b + 1]].astype(np.int64)) >= 0)
