@@ -850,22 +850,72 @@ struct RabRow {
   float pos_l, time_l;  // this lane's table entries, halved
 };
 
+// A chunk of 32 keys j0 .. j0 + 31 for the warp's 32 rows.  Position buckets
+// never grow with j (p is non-decreasing), and neither do time buckets
+// when the chunk's timestamps are in order.  So a part whose buckets at the
+// chunk's two ends agree on every lane of the warp is one value per row;
+// only the other parts are looked up per key.
+struct RabChunk {
+  int ts_lane;       // timestamp of key j0 + lane
+  float pos_c, time_c;  // the row's halved entries at the chunk's first key
+  bool fix_p, fix_t;    // warp-uniform: the part is constant over the chunk
+};
+
 template <bool TGT>
-__device__ __forceinline__ float rab_half(const RabRow& r, int j) {
-  const int pe_j = TGT ? (j < r.hist ? j : r.hist) : j;
-  const int dp = r.pe_i - pe_j;
-  const int dt = r.ts_i - __ldg(r.ts + (j < r.last ? j : r.last));
-  const uint32_t xp = (uint32_t)(dp > 0 ? dp : 0) + 1u;
-  const uint32_t xt = (uint32_t)(dt > 0 ? dt : 0) + 1u;
-  return __shfl_sync(0xffffffffu, r.pos_l, __clz((int)xp)) +
-         __shfl_sync(0xffffffffu, r.time_l, __clz((int)xt));
+__device__ __forceinline__ int rab_pe(const RabRow& r, int j) {
+  return TGT ? (j < r.hist ? j : r.hist) : j;
+}
+
+__device__ __forceinline__ int rab_lane(int delta) {  // source lane of delta's bucket
+  return __clz((int)((uint32_t)(delta > 0 ? delta : 0) + 1u));
+}
+
+// ts_lane: the timestamp of key j0 + lane (loaded ahead by the caller).
+template <bool TGT>
+__device__ __forceinline__ RabChunk rab_chunk(const RabRow& r, int j0, int ts_lane) {
+  RabChunk c;
+  const int lane = threadIdx.x & 31;
+  c.ts_lane = ts_lane;
+  const int nxt = __shfl_down_sync(0xffffffffu, c.ts_lane, 1);
+  const bool in_order = __all_sync(0xffffffffu, lane == 31 || c.ts_lane <= nxt);
+  const int ts_first = __shfl_sync(0xffffffffu, c.ts_lane, 0);
+  const int ts_end = __shfl_sync(0xffffffffu, c.ts_lane, 31);
+  const int lp0 = rab_lane(r.pe_i - rab_pe<TGT>(r, j0));
+  const int lp1 = rab_lane(r.pe_i - rab_pe<TGT>(r, j0 + 31));
+  const int lt0 = rab_lane(r.ts_i - ts_first);
+  const int lt1 = rab_lane(r.ts_i - ts_end);
+  c.fix_p = __all_sync(0xffffffffu, lp0 == lp1);
+  c.fix_t = in_order && __all_sync(0xffffffffu, lt0 == lt1);
+  c.pos_c = __shfl_sync(0xffffffffu, r.pos_l, lp0);
+  c.time_c = __shfl_sync(0xffffffffu, r.time_l, lt0);
+  return c;
+}
+
+// Halved bias of key j0 + k (k a compile-time constant after unrolling).
+template <bool TGT, bool FP, bool FT>
+__device__ __forceinline__ float rab_half(const RabRow& r, const RabChunk& c, int j0, int k) {
+  float bp, bt;
+  if constexpr (FP) {
+    bp = c.pos_c;
+  } else {
+    bp = __shfl_sync(0xffffffffu, r.pos_l, rab_lane(r.pe_i - rab_pe<TGT>(r, j0 + k)));
+  }
+  if constexpr (FT) {
+    bt = c.time_c;
+  } else {
+    const int ts_j = __shfl_sync(0xffffffffu, c.ts_lane, k);
+    bt = __shfl_sync(0xffffffffu, r.time_l, rab_lane(r.ts_i - ts_j));
+  }
+  return bp + bt;
 }
 
 // MASK 0: none; 1: keep key k iff k <= lim; 2: the candidate mask.  RAB:
-// add the relative attention bias of keys j0 .. j0 + 31 (sequence-local).
-template <int MASK, bool RAB = false, bool TGT = false>
-__device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, int lim_hist,
-                                             uint32_t t, const RabRow* rab = nullptr, int j0 = 0) {
+// add the relative attention bias of keys j0 .. j0 + 31 (sequence-local),
+// FP / FT: its position / time part is constant over the chunk.
+template <int MASK, bool RAB = false, bool TGT = false, bool FP = false, bool FT = false>
+__device__ __forceinline__ void silu_store32_body(const uint32_t (&s)[32], float2 ha2, int lim,
+                                                  int lim_hist, uint32_t t, const RabRow* rab,
+                                                  const RabChunk* rc, int j0) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t hi[8], lo[8];
@@ -874,7 +924,8 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
       const int k = 16 * h + 2 * m;
       float2 x;
       if constexpr (RAB) {
-        const float2 bh = make_float2(rab_half<TGT>(*rab, j0 + k), rab_half<TGT>(*rab, j0 + k + 1));
+        const float2 bh = make_float2(rab_half<TGT, FP, FT>(*rab, *rc, j0, k),
+                                      rab_half<TGT, FP, FT>(*rab, *rc, j0, k + 1));
         x = __ffma2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2, bh);
       } else {
         x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
@@ -897,6 +948,25 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
     }
     tmem_st8(t + 8u * h, hi);
     tmem_st8(t + 16u + 8u * h, lo);
+  }
+}
+
+template <int MASK, bool RAB = false, bool TGT = false>
+__device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, int lim_hist,
+                                             uint32_t t, const RabRow* rab = nullptr, int j0 = 0,
+                                             int ts_lane = 0) {
+  if constexpr (!RAB) {
+    silu_store32_body<MASK>(s, ha2, lim, lim_hist, t, nullptr, nullptr, 0);
+  } else {
+    const RabChunk rc = rab_chunk<TGT>(*rab, j0, ts_lane);
+    if (rc.fix_p && rc.fix_t)
+      silu_store32_body<MASK, true, TGT, true, true>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
+    else if (rc.fix_p)
+      silu_store32_body<MASK, true, TGT, true, false>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
+    else if (rc.fix_t)
+      silu_store32_body<MASK, true, TGT, false, true>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
+    else
+      silu_store32_body<MASK, true, TGT, false, false>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
   }
 }
 
@@ -935,16 +1005,12 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
       continue;
     }
     const int j = (int)(cur.tc % P);
-    {
-      const bool ok = wait_one(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull);
-      if (!__all_sync(0xffffffffu, ok)) return;
-    }
-    tc_fence_after();
-    trace(a, kEvSiluStart, cur.tc);
-    const uint32_t t_s = lane_base + (uint32_t)(j * 128);
+    const int kbase = kBN * cur.kt;
+    int tsk[4];  // the block's key timestamps, key kbase + 32 c + lane
     if constexpr (RAB) {
       // the row's position and timestamp (a row past the sequence reads its
-      // last token; its results are never stored)
+      // last token; its results are never stored), loaded with the keys'
+      // timestamps before the wait so that their latency hides behind it
       const int i = kBM * cur.b.qt + row;
       rr.ts = a.rab_ts + cur.b.s0;
       rr.last = cur.b.n - 1;
@@ -955,8 +1021,19 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
         rr.pe_i = i;
       }
       rr.ts_i = __ldg(rr.ts + (i < rr.last ? i : rr.last));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int jk = kbase + 32 * c + lane;
+        tsk[c] = __ldg(rr.ts + (jk < rr.last ? jk : rr.last));
+      }
     }
-    const int kbase = kBN * cur.kt;
+    {
+      const bool ok = wait_one(bar(C::B_SFULL + j), (cur.tc / P) & 1u, w, kSiteSFull);
+      if (!__all_sync(0xffffffffu, ok)) return;
+    }
+    tc_fence_after();
+    trace(a, kEvSiluStart, cur.tc);
+    const uint32_t t_s = lane_base + (uint32_t)(j * 128);
     bool plain = cur.kt != cur.b.qt;
     if constexpr (TGT) plain = cur.b.unmasked(cur.kt);
     if (RAB && plain && quarter * 32 < cur.b.rows()) {
@@ -964,19 +1041,20 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(t_s + 32u * c, s1);
-        silu_store32<0, RAB, TGT>(s1, ha2, 0, 0, t_s + 32u * c, &rr, kbase + 32 * c);
+        const int tsl = c == 0 ? tsk[0] : c == 1 ? tsk[1] : c == 2 ? tsk[2] : tsk[3];
+        silu_store32<0, RAB, TGT>(s1, ha2, 0, 0, t_s + 32u * c, &rr, kbase + 32 * c, tsl);
       }
       tmem_wait_st();
-    } else if (plain && quarter * 32 < cur.b.rows()) {
+    } else if (plain && quarter * 32 < cur.b.rows()) {  // (without the bias)
       tmem_ld32_async(t_s, s0);
       tmem_wait_ld(s0);
 #pragma unroll 1
       for (int c = 0; c < 4; c += 2) {
         tmem_ld32_async(t_s + 32u * (c + 1), s1);
-        silu_store32<0, RAB, TGT>(s0, ha2, 0, 0, t_s + 32u * c, &rr, kbase + 32 * c);
+        silu_store32<0>(s0, ha2, 0, 0, t_s + 32u * c);
         tmem_wait_ld(s1);
         if (c + 2 < 4) tmem_ld32_async(t_s + 32u * (c + 2), s0);
-        silu_store32<0, RAB, TGT>(s1, ha2, 0, 0, t_s + 32u * (c + 1), &rr, kbase + 32 * (c + 1));
+        silu_store32<0>(s1, ha2, 0, 0, t_s + 32u * (c + 1));
         if (c + 2 < 4) tmem_wait_ld(s0);
       }
       tmem_wait_st();
@@ -1002,8 +1080,9 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
           tmem_st16(t_s + 32u * c + 16u, z);
         } else {
           tmem_ld32(t_s + 32u * c, s1);
+          const int tsl = c == 0 ? tsk[0] : c == 1 ? tsk[1] : c == 2 ? tsk[2] : tsk[3];
           silu_store32<TGT ? 2 : 1, RAB, TGT>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c, t_s + 32u * c,
-                                              &rr, kbase + 32 * c);
+                                              &rr, kbase + 32 * c, tsl);
         }
       }
       tmem_wait_st();
