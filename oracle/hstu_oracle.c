@@ -98,6 +98,10 @@ static double rab_bias(const rab_t* R, int64_t seq_start, int64_t i, int64_t j, 
     return (double)R->pos[bp] + (double)R->time[bt];
 }
 
+/* Term j of row i is kept (sequence-local indices): the causal mask, and a
+ * candidate (i >= hist) sees no other candidate. */
+static int kept(int64_t i, int64_t j, int64_t hist) { return j <= i && (j < hist || j == i); }
+
 /* One output row: out_row[c] for c < d, fp64.  hist: the number of history
  * tokens of the sequence (its length when it has no candidates).  R: the
  * relative attention bias, or NULL. */
@@ -109,7 +113,7 @@ static void oracle_row(const float* q, const float* k, const float* v, const rab
     const float* qr = q + (t * heads + h) * (int64_t)d;
     for (int c = 0; c < d; ++c) acc[c] = 0.0;
     for (int64_t j = 0; j <= i; ++j) {
-        if (j >= hist && j != i) continue; /* another candidate: masked */
+        if (!kept(i, j, hist)) continue;
         const int64_t s = seq_start + j;
         const float* kr = k + (s * heads + h) * (int64_t)d;
         const float* vr = v + (s * heads + h) * (int64_t)d;
@@ -309,6 +313,107 @@ int hstu_oracle_rows_rab_f64(const float* q, const float* k, const float* v,
     job_t J = {q, k, v, offsets, num_targets, &R, batch, heads, d, alpha, inv_n, out, rows_t, rows_h,
                nrows, NULL, NULL};
     return run(&J, nthreads, worker_rows);
+}
+
+/*
+ * Backward pass (HSTU paper Appendix G: the backward recomputes the
+ * attention; its gradients are those of the forward definition above).
+ * With s_ij = alpha <q_i, k_j> (+ bias), P_ij = inv_n silu(s_ij) on kept
+ * pairs and out_i = sum_j P_ij v_j, the chain rule gives, for dO = d out:
+ *
+ *   dv_j  = sum_i P_ij do_i
+ *   dp_ij = <do_i, v_j>
+ *   ds_ij = inv_n silu'(s_ij) dp_ij,   silu'(x) = sig(x) (1 + x (1 - sig(x)))
+ *   dq_i  = alpha sum_j ds_ij k_j
+ *   dk_j  = alpha sum_i ds_ij q_i
+ *
+ * summed over kept pairs only (the same mask as the forward, candidates
+ * included).  All in fp64 from the bf16-valued fp32 inputs.
+ */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+static void* worker_bwd(void* arg);
+
+typedef struct {
+    job_t base;          /* q, k, v, offsets, num_targets, rab, batch, heads, d, alpha, inv_n */
+    const float* dout;   /* (total, heads, d) */
+    double *dq, *dk, *dv;
+} bwd_job_t;
+
+static void bwd_seq_head(const bwd_job_t* B, int b, int h) {
+    const job_t* J = &B->base;
+    const int64_t s0 = J->offsets[b], n = J->offsets[b + 1] - s0;
+    const int64_t hist = hist_of(J, b);
+    const int d = J->d, heads = J->heads;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t ti = s0 + i;
+        const float* qi = J->q + (ti * heads + h) * (int64_t)d;
+        const float* doi = B->dout + (ti * heads + h) * (int64_t)d;
+        double* dqi = B->dq + (ti * heads + h) * (int64_t)d;
+        for (int64_t j = 0; j < n; ++j) {
+            if (!kept(i, j, hist)) continue;
+            const int64_t tj = s0 + j;
+            const float* kj = J->k + (tj * heads + h) * (int64_t)d;
+            const float* vj = J->v + (tj * heads + h) * (int64_t)d;
+            double* dkj = B->dk + (tj * heads + h) * (int64_t)d;
+            double* dvj = B->dv + (tj * heads + h) * (int64_t)d;
+            double dot = 0.0, dp = 0.0;
+            for (int c = 0; c < d; ++c) {
+                dot += (double)qi[c] * (double)kj[c];
+                dp += (double)doi[c] * (double)vj[c];
+            }
+            const double bias = J->rab ? rab_bias(J->rab, s0, i, j, hist) : 0.0;
+            const double x = J->alpha * dot + bias;
+            const double sg = sigmoid(x);
+            const double p = J->inv_n * x * sg;
+            const double ds = J->inv_n * sg * (1.0 + x * (1.0 - sg)) * dp;
+            for (int c = 0; c < d; ++c) {
+                dvj[c] += p * (double)doi[c];
+                dqi[c] += J->alpha * ds * (double)kj[c];
+                dkj[c] += J->alpha * ds * (double)qi[c];
+            }
+        }
+    }
+}
+
+/* Sequences are independent and a (sequence, head) pair writes only its own
+ * rows, so the workers take whole pairs. */
+static void* worker_bwd(void* arg) {
+    bwd_job_t* B = (bwd_job_t*)arg;
+    job_t* J = &B->base;
+    const int64_t units = (int64_t)J->batch * J->heads;
+    for (;;) {
+        const int64_t u = take(J, 1);
+        if (u >= units) break;
+        bwd_seq_head(B, (int)(u / J->heads), (int)(u % J->heads));
+    }
+    return NULL;
+}
+
+/* dq, dk, dv: fp64 (total, heads, d), written (zeroed here first).
+ * num_targets and the rab arguments as hstu_oracle_fwd_rab_f64 (ts NULL:
+ * no bias). */
+int hstu_oracle_bwd_f64(const float* q, const float* k, const float* v, const float* dout,
+                        const int64_t* offsets, const int64_t* num_targets, const int64_t* ts,
+                        const float* pos, int npos, const float* time, int ntime, int batch,
+                        int heads, int d, double alpha, double inv_n, double* dq, double* dk,
+                        double* dv, int nthreads) {
+    if (check_offsets(offsets, batch) || (num_targets && check_targets(offsets, num_targets, batch)) ||
+        heads < 1 || d < 1 || (ts && (npos < 1 || ntime < 1)))
+        return -1;
+    const int64_t total = batch ? offsets[batch] : 0;
+    for (int64_t e = 0; e < total * heads * (int64_t)d; ++e) dq[e] = dk[e] = dv[e] = 0.0;
+    const rab_t R = {ts, pos, npos, time, ntime};
+    bwd_job_t B;
+    job_t J = {q, k, v, offsets, num_targets, ts ? &R : NULL, batch, heads, d, alpha, inv_n, NULL,
+               NULL, NULL, 0, NULL, NULL};
+    B.base = J;
+    B.dout = dout;
+    B.dq = dq;
+    B.dk = dk;
+    B.dv = dv;
+    /* run() hands each worker the job pointer; the job is the first member */
+    return run(&B.base, nthreads, worker_bwd);
 }
 
 /*

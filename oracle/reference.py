@@ -76,6 +76,10 @@ def _load():
                                                  ctypes.c_int, ctypes.c_double, ctypes.c_double, i64,
                                                  i32, ctypes.c_int64, d, ctypes.c_int]
         lib.hstu_oracle_rows_rab_f64.restype = ctypes.c_int
+        lib.hstu_oracle_bwd_f64.argtypes = [f, f, f, f, i64, i64, i64, f, ctypes.c_int, f,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_double, d, d, d, ctypes.c_int]
+        lib.hstu_oracle_bwd_f64.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -244,3 +248,34 @@ def hstu_rows_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, alpha: flo
     x = hstu_rows(q, k, v, offsets, alpha, inv_n, rt, rh, threads=threads,
                   num_targets=num_targets, rab=rab).reshape(len(rows_t), heads, d)
     return norm_gate(x, _f32(u)[np.asarray(rows_t, dtype=np.int64)], gamma, beta, eps)
+
+
+def hstu_bwd(q, k, v, dout, offsets, alpha: float, inv_n: float, threads: int | None = None,
+             num_targets=None, rab=None):
+    """Gradients of sum(out * dout) with respect to q, k, v: fp64 arrays
+    (total, heads, d) each (HSTU paper Appendix G: the backward of the
+    forward definition; the chain rule is written out in hstu_oracle.c)."""
+    qf, kf, vf, df = _f32(q), _f32(k), _f32(v), _f32(dout)
+    total, heads, d = qf.shape
+    off = np.ascontiguousarray(np.asarray(offsets), dtype=np.int64)
+    batch = len(off) - 1
+    if (kf.shape != qf.shape or vf.shape != qf.shape or df.shape != qf.shape
+            or (batch >= 0 and off[-1] != total)):
+        raise ValueError("shape mismatch between q/k/v/dout/offsets")
+    nt, ntp = _targets_ptr(num_targets, batch)
+    tsp = posp = timep = None
+    npos = ntime = 0
+    if rab is not None:
+        ts, pos, time = _rab_arrays(rab, total)
+        tsp, posp, timep = _ptr(ts, ctypes.c_int64), _ptr(pos, ctypes.c_float), _ptr(time, ctypes.c_float)
+        npos, ntime = pos.size, time.size
+    dq, dk, dv = (np.zeros((total, heads, d), dtype=np.float64) for _ in range(3))
+    rc = _load().hstu_oracle_bwd_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                     _ptr(vf, ctypes.c_float), _ptr(df, ctypes.c_float),
+                                     _ptr(off, ctypes.c_int64), ntp, tsp, posp, npos, timep, ntime,
+                                     batch, heads, d, float(alpha), float(inv_n),
+                                     _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                     _ptr(dv, ctypes.c_double), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return dq, dk, dv

@@ -1,0 +1,129 @@
+"""Pins of the oracle's backward pass.
+
+HSTU paper Appendix G: the backward recomputes the attention and
+accumulates the gradients of the forward definition.  The oracle writes the
+chain rule out (hstu_oracle.c).  Pins, each independent of that code:
+* central finite differences of the (pinned) forward oracle;
+* torch autograd of a dense fp64 formulation (the post's PyTorch
+  definition: score matmul, scale, SiLU, tril mask, 1/n, matmul with V);
+* linearity: the gradients are linear in dout;
+* a one-token sequence's closed form.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import reference
+
+
+def _case(rng, lengths, heads, d, scale=1.0):
+    total = int(np.sum(lengths))
+    mk = lambda: (scale * rng.standard_normal((total, heads, d))).astype(np.float32)
+    off = np.zeros(len(lengths) + 1, dtype=np.int64)
+    np.cumsum(lengths, out=off[1:])
+    return mk(), mk(), mk(), mk(), off
+
+
+def _loss(q, k, v, dout, off, alpha, inv_n, nt=None, rab=None):
+    out = reference.hstu_fwd(q, k, v, off, alpha, inv_n, num_targets=nt, rab=rab)
+    return float(np.sum(out * dout.astype(np.float64)))
+
+
+@pytest.mark.parametrize("targets", [False, True])
+def test_finite_differences(targets):
+    rng = np.random.default_rng(5 + targets)
+    q, k, v, do, off = _case(rng, [6, 0, 9], 2, 4)
+    nt = [2, 0, 4] if targets else None
+    alpha, inv_n = 0.6, 0.2
+    dq, dk, dv = reference.hstu_bwd(q, k, v, do, off, alpha, inv_n, num_targets=nt)
+    eps = 1e-3
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0, 0), (3, 1, 2), (5, 0, 3), (6, 1, 1), (14, 0, 0), (10, 1, 3)]:
+            xp, xm = x.copy(), x.copy()
+            # fp32 inputs: step by a representable amount and use it exactly
+            xp[idx] = np.float32(x[idx] + eps)
+            xm[idx] = np.float32(x[idx] - eps)
+            h = float(xp[idx]) - float(xm[idx])
+            args = {"q": q, "k": k, "v": v}
+            lp = _loss(*(xp if n == name else args[n] for n in "qkv"), do, off, alpha, inv_n, nt)
+            lm = _loss(*(xm if n == name else args[n] for n in "qkv"), do, off, alpha, inv_n, nt)
+            fd = (lp - lm) / h
+            assert abs(fd - g[idx]) <= 1e-5 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
+def _dense_torch(q, k, v, do, off, alpha, inv_n):
+    """torch autograd of the dense definition, per sequence, fp64."""
+    Q, K, V = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    loss = 0.0
+    for b in range(len(off) - 1):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        if s1 == s0:
+            continue
+        qb, kb, vb = (x[s0:s1].transpose(0, 1) for x in (Q, K, V))   # (heads, n, d)
+        s = alpha * qb @ kb.transpose(1, 2)
+        mask = torch.tril(torch.ones(s1 - s0, s1 - s0, dtype=torch.float64))
+        p = torch.nn.functional.silu(s) * mask * inv_n
+        out = (p @ vb).transpose(0, 1)
+        loss = loss + (out * torch.tensor(do[s0:s1], dtype=torch.float64)).sum()
+    loss.backward()
+    return Q.grad.numpy(), K.grad.numpy(), V.grad.numpy()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_matches_torch_autograd_of_the_dense_definition(seed):
+    rng = np.random.default_rng(20 + seed)
+    lengths = rng.integers(0, 40, size=4)
+    q, k, v, do, off = _case(rng, lengths, 2, 8)
+    got = reference.hstu_bwd(q, k, v, do, off, 0.4, 0.05)
+    want = _dense_torch(q, k, v, do, off, 0.4, 0.05)
+    for g, w_ in zip(got, want):
+        assert np.abs(g - w_).max() <= 1e-12 * max(1.0, np.abs(w_).max())
+
+
+def test_linear_in_dout():
+    rng = np.random.default_rng(9)
+    q, k, v, _, off = _case(rng, [12, 5], 2, 8)
+    # small integers: do + do2 is exact in fp32
+    do = rng.integers(-4, 5, size=q.shape).astype(np.float32)
+    do2 = rng.integers(-4, 5, size=q.shape).astype(np.float32)
+    a = reference.hstu_bwd(q, k, v, do, off, 0.5, 0.1)
+    b = reference.hstu_bwd(q, k, v, do2, off, 0.5, 0.1)
+    c = reference.hstu_bwd(q, k, v, do + do2, off, 0.5, 0.1)
+    for x, y, z in zip(a, b, c):
+        assert np.abs(x + y - z).max() <= 1e-12 * max(1.0, np.abs(z).max())
+
+
+def test_one_token_closed_form():
+    rng = np.random.default_rng(10)
+    q, k, v, do, off = _case(rng, [1], 1, 4)
+    alpha, inv_n = 0.8, 0.5
+    dq, dk, dv = reference.hstu_bwd(q, k, v, do, off, alpha, inv_n)
+    q0, k0, v0, d0 = (x[0, 0].astype(np.float64) for x in (q, k, v, do))
+    x = alpha * q0 @ k0
+    sg = 1.0 / (1.0 + np.exp(-x))
+    ds = inv_n * sg * (1 + x * (1 - sg)) * (d0 @ v0)
+    np.testing.assert_allclose(dv[0, 0], inv_n * x * sg * d0, rtol=1e-13)
+    np.testing.assert_allclose(dq[0, 0], alpha * ds * k0, rtol=1e-12)
+    np.testing.assert_allclose(dk[0, 0], alpha * ds * q0, rtol=1e-12)
+
+
+def test_bias_gradients_by_finite_differences():
+    # with the relative attention bias the q/k/v gradients still follow the chain rule
+    rng = np.random.default_rng(11)
+    q, k, v, do, off = _case(rng, [10, 7], 2, 4)
+    ts = np.cumsum(rng.integers(0, 5000, size=17)).astype(np.int64)
+    pos = (0.3 * rng.standard_normal(8)).astype(np.float32)
+    time = (0.3 * rng.standard_normal(16)).astype(np.float32)
+    rab = (ts, pos, time)
+    dq, dk, dv = reference.hstu_bwd(q, k, v, do, off, 0.6, 0.2, num_targets=[3, 2], rab=rab)
+    eps = 1e-3
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0, 1), (9, 1, 2), (12, 0, 3), (16, 1, 0)]:
+            xp, xm = x.copy(), x.copy()
+            xp[idx] = np.float32(x[idx] + eps)
+            xm[idx] = np.float32(x[idx] - eps)
+            h = float(xp[idx]) - float(xm[idx])
+            args = {"q": q, "k": k, "v": v}
+            lp = _loss(*(xp if n == name else args[n] for n in "qkv"), do, off, 0.6, 0.2, [3, 2], rab)
+            lm = _loss(*(xm if n == name else args[n] for n in "qkv"), do, off, 0.6, 0.2, [3, 2], rab)
+            assert abs((lp - lm) / h - g[idx]) <= 1e-5 * max(1.0, abs(g[idx])), (name, idx)

@@ -17,7 +17,7 @@ from oracle import dense
 
 MUTANTS = {
     "silu_sign": ("x / (1.0 + exp(-x))", "x / (1.0 + exp(x))"),
-    "drop_diagonal": ("for (int64_t j = 0; j <= i; ++j)", "for (int64_t j = 0; j < i; ++j)"),
+    "drop_diagonal": ("return j <= i && (j < hist || j == i);", "return j < i && (j < hist || j == i);"),
     "alpha_divides": ("hstu_oracle_silu(alpha * dot + bias)", "hstu_oracle_silu(dot / alpha + bias)"),
     "q_dot_v": ("dot += (double)qr[c] * (double)kr[c]", "dot += (double)qr[c] * (double)vr[c]"),
     "inv_n_missing": ("out_row[c] = inv_n * acc[c]", "out_row[c] = acc[c]"),
@@ -100,9 +100,10 @@ def test_mutant_is_caught(tmp_path, name):
 
 # ------------------------------------------------ the candidate (M-FALCON) mask
 TARGET_MUTANTS = {
-    "drop_self_term": ("if (j >= hist && j != i) continue;", "if (j >= hist) continue;"),
-    "history_off_by_one": ("if (j >= hist && j != i) continue;", "if (j > hist && j != i) continue;"),
-    "candidates_see_each_other": ("if (j >= hist && j != i) continue;", "if (j > i) continue;"),
+    "drop_self_term": ("return j <= i && (j < hist || j == i);", "return j <= i && (j < hist);"),
+    "history_off_by_one": ("return j <= i && (j < hist || j == i);",
+                           "return j <= i && (j <= hist || j == i);"),
+    "candidates_see_each_other": ("return j <= i && (j < hist || j == i);", "return j <= i;"),
 }
 
 
@@ -267,3 +268,46 @@ def test_rab_mutant_is_caught(tmp_path, name):
     old, new = RAB_MUTANTS[name]
     assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     assert not _rab_pins_pass(_build(tmp_path, name, src.replace(old, new)))
+
+
+# ------------------------------------------------ the backward pass
+BWD_MUTANTS = {
+    "silu_derivative_first_term_only": ("sg * (1.0 + x * (1.0 - sg)) * dp", "sg * dp"),
+    "dv_without_inv_n": ("const double p = J->inv_n * x * sg;", "const double p = x * sg;"),
+    "dk_from_k": ("dkj[c] += J->alpha * ds * (double)qi[c];", "dkj[c] += J->alpha * ds * (double)kj[c];"),
+    "dq_without_alpha": ("dqi[c] += J->alpha * ds * (double)kj[c];", "dqi[c] += ds * (double)kj[c];"),
+    "dp_from_q": ("dp += (double)doi[c] * (double)vj[c];", "dp += (double)doi[c] * (double)qi[c];"),
+}
+
+
+def _bwd_pins_pass(L) -> bool:
+    """torch autograd of the dense definition, as in test_oracle_bwd.py."""
+    from tests.test_oracle_bwd import _case, _dense_torch
+    f, dptr, i64 = (ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
+                    ctypes.POINTER(ctypes.c_int64))
+    L.hstu_oracle_bwd_f64.argtypes = [f, f, f, f, i64, i64, i64, f, ctypes.c_int, f, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                      ctypes.c_double, dptr, dptr, dptr, ctypes.c_int]
+    P = lambda a, t: a.ctypes.data_as(ctypes.POINTER(t))
+    rng = np.random.default_rng(31)
+    q, k, v, do, off = _case(rng, [13, 20], 2, 8)
+    off = off.astype(np.int64)
+    grads = [np.zeros(q.shape) for _ in range(3)]
+    L.hstu_oracle_bwd_f64(P(q, ctypes.c_float), P(k, ctypes.c_float), P(v, ctypes.c_float),
+                          P(do, ctypes.c_float), P(off, ctypes.c_int64), None, None, None, 0, None, 0,
+                          len(off) - 1, q.shape[1], q.shape[2], 0.4, 0.05,
+                          *(P(g, ctypes.c_double) for g in grads), 2)
+    want = _dense_torch(q, k, v, do, off, 0.4, 0.05)
+    return all(np.abs(g - w_).max() <= 1e-12 * max(1.0, np.abs(w_).max()) for g, w_ in zip(grads, want))
+
+
+def test_unmutated_copy_passes_the_bwd_pins(tmp_path):
+    assert _bwd_pins_pass(_build(tmp_path, "orig_b", open(oracle_build.SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_bwd_mutant_is_caught(tmp_path, name):
+    src = open(oracle_build.SRC).read()
+    old, new = BWD_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    assert not _bwd_pins_pass(_build(tmp_path, name, src.replace(old, new)))
