@@ -84,6 +84,10 @@ _SIGNATURES = {
     "hstu_attn_fwd_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32P, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, _RABP, _NGP, ctypes.c_float,
                                         ctypes.c_float, _VP, _VP]),
+    "hstu_attn_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP, _VP, _VP, _VP]),
+    "hstu_worklist_build_bwd": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int,
+                                               _IP]),
     "hstu_attn_fwd_norm_gate": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP,
                                                _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP,
@@ -263,6 +267,30 @@ def hstu_attn_fwd_ex(q, k, v, offsets, batch: int, heads: int, d: int, max_seqle
                                   _ng_struct(norm_gate), float(alpha), float(inv_n), _addr(out),
                                   _stream(stream)), "hstu_attn_fwd_ex")
     del keep
+
+
+def hstu_attn_bwd(q, k, v, dout, offsets, batch: int, heads: int, d: int, max_seqlen: int,
+                  alpha: float, inv_n: float, dq, dk, dv, stream=None) -> None:
+    """Gradients of the forward for ``dout``: dq, dk, dv (bf16, like q) are written."""
+    off_ptr, keep = _offsets_arg(offsets)
+    _check(lib().hstu_attn_bwd(_addr(q), _addr(k), _addr(v), _addr(dout), off_ptr, int(batch),
+                               int(heads), int(d), int(max_seqlen), float(alpha), float(inv_n),
+                               _addr(dq), _addr(dk), _addr(dv), _stream(stream)), "hstu_attn_bwd")
+    del keep
+
+
+def hstu_worklist_build_bwd(host_offsets, heads: int) -> np.ndarray:
+    """Host-only work list of the backward: int32 (n, 4) items (first token, length, head, kt)."""
+    off = _host_offsets(host_offsets)
+    batch = len(off) - 1
+    n = ctypes.c_int()
+    _check(lib().hstu_worklist_build_bwd(off.ctypes.data_as(_I32P), batch, int(heads), None, 0,
+                                         ctypes.byref(n)), "hstu_worklist_build_bwd")
+    buf = np.zeros((max(n.value, 1), 4), dtype=np.int32)
+    _check(lib().hstu_worklist_build_bwd(off.ctypes.data_as(_I32P), batch, int(heads),
+                                         buf.ctypes.data_as(_I32P), n.value, ctypes.byref(n)),
+           "hstu_worklist_build_bwd")
+    return buf[:n.value]
 
 
 def hstu_attn_fwd_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, num_targets, batch: int,

@@ -266,6 +266,25 @@ void fill_items_targets(const int32_t* off, const int32_t* num_targets, int batc
   }
 }
 
+void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst) {
+  // (cost, b, h, kt) generated in b, h, kt order; a stable sort by cost
+  // descending then gives cost descending, then b, h, kt ascending
+  struct Entry {
+    int cost;
+    Item item;
+  };
+  std::vector<Entry> e;
+  e.reserve((size_t)count_items(off, batch, heads));
+  for (int b = 0; b < batch; ++b) {
+    const int n = off[b + 1] - off[b];
+    const int nq = (n + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    for (int h = 0; h < heads; ++h)
+      for (int kt = 0; kt < nq; ++kt) e.push_back(Entry{nq - kt, make_int4(off[b], n, h, kt)});
+  }
+  std::stable_sort(e.begin(), e.end(), [](const Entry& x, const Entry& y) { return x.cost > y.cost; });
+  for (size_t i = 0; i < e.size(); ++i) dst[i] = e[i].item;
+}
+
 int host_check_offsets(const int32_t* off, int batch, long long max_len) {
   return check_offsets(off, batch, max_len);
 }
@@ -427,6 +446,38 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
               ng ? &ngw : nullptr, s, rab);
   if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
   return rc;
+}
+
+int launch_backward(const hstu::Item* d_items, int n_items, long long total, int heads, int d,
+                    const void* q, const void* k, const void* v, const void* dout, float alpha,
+                    float inv_n, float* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream) {
+  int sms = 0;
+  int rc = device_check(&sms);
+  if (rc != HSTU_OK) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = make_map(&tq, q, total, heads, d)) != HSTU_OK) return rc;
+  if ((rc = make_map(&tk, k, total, heads, d)) != HSTU_OK) return rc;
+  if ((rc = make_map(&tv, v, total, heads, d)) != HSTU_OK) return rc;
+  if ((rc = make_map(&tdo, dout, total, heads, d)) != HSTU_OK) return rc;
+  hstu::BwdArgs a;
+  a.items = d_items;
+  a.n_items = n_items;
+  a.heads = heads;
+  a.alpha = alpha;
+  a.inv_n = inv_n;
+  a.dq_acc = dq_acc;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.total = total;
+  a.timeout_ns = wait_timeout_ns();
+  // the accumulator starts at zero on the stream, before the kernel
+  if (cudaMemsetAsync(dq_acc, 0, (size_t)total * heads * d * sizeof(float), stream) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  const cudaError_t e = hstu::launch_bwd(d, tq, tk, tv, tdo, a, grid_for(n_items, sms), stream);
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+    return HSTU_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 
 }  // namespace
@@ -640,6 +691,81 @@ int hstu_attn_fwd_targets(const void* q, const void* k, const void* v, const int
   if (!host_num_targets && batch > 0) return HSTU_ERR_INVALID_ARG;
   return oneshot(q, k, v, offsets, host_num_targets, batch, heads, d, max_seqlen, alpha, inv_n, out,
                  nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
+                            int capacity, int* n_items) {
+  if (!n_items || heads < 1 || capacity < 0) return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(host_offsets, batch, -1);
+  if (rc != HSTU_OK) return rc;
+  std::vector<hstu::Item> items;
+  try {
+    items.resize((size_t)hstu::count_items(host_offsets, batch, heads));
+    hstu::fill_items_bwd(host_offsets, batch, heads, items.data());
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  *n_items = (int)items.size();
+  if (host_dst)
+    std::memcpy(host_dst, items.data(), std::min(items.size(), (size_t)capacity) * sizeof(hstu::Item));
+  return HSTU_OK;
+}
+
+int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
+                  const int32_t* offsets, int batch, int heads, int d, int max_seqlen, float alpha,
+                  float inv_n, void* dq, void* dk, void* dv, hstu_stream_t stream) {
+  if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
+  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
+  if (batch == 0) return HSTU_OK;
+  if (!offsets) return HSTU_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<int32_t> host_off;
+  const int32_t* off = offsets;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, offsets) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (attr.type == cudaMemoryTypeDevice) {
+    try {
+      host_off.resize((size_t)batch + 1);
+    } catch (const std::bad_alloc&) {
+      return HSTU_ERR_NO_MEMORY;
+    }
+    if (cudaMemcpyAsync(host_off.data(), offsets, host_off.size() * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+    off = host_off.data();
+  }
+  int rc = check_offsets(off, batch, max_seqlen);
+  if (rc != HSTU_OK) return rc;
+  const long long total = off[batch];
+  if (total == 0) return HSTU_OK;
+  if ((rc = check_buffers(q, k, v, dout)) != HSTU_OK || (rc = check_buffers(dq, dk, dv, dv)) != HSTU_OK)
+    return rc;
+  std::vector<hstu::Item> items;
+  try {
+    items.resize((size_t)hstu::count_items(off, batch, heads));
+    hstu::fill_items_bwd(off, batch, heads, items.data());
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (items.empty()) return HSTU_OK;
+  if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  // one stream-ordered allocation: the fp32 dQ accumulator, then the items
+  const size_t abytes = (size_t)total * heads * d * sizeof(float);
+  const size_t ibytes = items.size() * sizeof(hstu::Item);
+  char* block = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&block), abytes + ibytes, s);
+  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+  hstu::Item* d_items = reinterpret_cast<hstu::Item*>(block + abytes);
+  if (cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaFreeAsync(block, s);
+    return HSTU_ERR_CUDA;
+  }
+  rc = launch_backward(d_items, (int)items.size(), total, heads, d, q, k, v, dout, alpha, inv_n,
+                       reinterpret_cast<float*>(block), dq, dk, dv, s);
+  if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
+  return rc;
 }
 
 int hstu_last_status(int* device_status, int* site) {

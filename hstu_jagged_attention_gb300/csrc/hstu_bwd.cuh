@@ -1,0 +1,391 @@
+// Backward pass of the HSTU jagged attention (HSTU paper Appendix G: the
+// backward recomputes the attention; its gradients follow the forward
+// definition).  With s_ij = alpha q_i.k_j, P_ij = inv_n silu(s_ij) on kept
+// pairs (causal, same sequence) and out_i = sum_j P_ij v_j:
+//
+//   dV = P^T dO,   dP = dO V^T,   dS = inv_n silu'(s) (.) dP (kept pairs),
+//   dQ = alpha dS K,   dK = alpha dS^T Q,   silu'(x) = sig(x) (1 + x (1 - sig(x))).
+//
+// Included into hstu_fwd.cu's anonymous namespace: it shares that file's
+// PTX helpers, bounded waits and device status word.
+//
+// Work item: one 128-key block kt of one (sequence, head); the CTA walks the
+// query blocks qt = kt .. last that see it.  K and V load once per item,
+// Q and dO once per query block.  One thread issues the copies and the
+// products; the 128 threads (thread r owns TMEM lane r) turn S and dP into
+// P and dS.  Per query block:
+//   1. S = Q K^T and dP = dO V^T into TMEM (fp32).
+//   2. P = inv_n silu(alpha S), split into bf16 hi + lo, written to two
+//      128B-swizzled shared tiles (rows = queries, 64-key chunks).
+//   3. dV += P_hi^T dO + P_lo^T dO: the tile read as an MN-major A operand
+//      (M = keys), dO as an MN-major B operand, accumulated in TMEM.
+//   4. dS, split the same way into the same tiles (P's products are done).
+//   5. dK += dS^T Q (as step 3) and dQ_part = dS K (the tile read as a
+//      K-major A operand, K as an MN-major B), dQ_part over S in TMEM.
+//   6. dQ_part * alpha is added into an fp32 accumulator in global memory
+//      (vector atomics): query block qt gets one part per key block.
+// At the item's end dV and alpha dK leave TMEM as bf16.  The P and dS
+// splits keep the products' error at the bf16 output rounding, as in the
+// forward.  Phases run one after another (synchronous waits).
+
+template <int D>
+struct BCfg {
+  static constexpr int CHUNK = D < 64 ? D : 64;  // elements per swizzled row of a d-wide tile
+  static constexpr int NCHUNK = D / CHUNK;
+  static constexpr int ROWB = CHUNK * 2;
+  static constexpr int ATOMB = 8 * ROWB;
+  static constexpr int CHUNKB = kBM * ROWB;
+  static constexpr int TILEB = kBM * D * 2;
+  static constexpr uint64_t LAYOUT = ROWB == 128 ? 2 : 4;  // 128B / 64B swizzle
+  // P / dS tiles: 128 rows x 128 keys bf16 as two 64-key chunks, 128B swizzle
+  static constexpr int PCHUNKB = kBM * 128;
+  static constexpr int PTILEB = 2 * PCHUNKB;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + TILEB;
+  static constexpr int Q_OFF = V_OFF + TILEB;
+  static constexpr int DO_OFF = Q_OFF + TILEB;
+  static constexpr int HI_OFF = DO_OFF + TILEB;
+  static constexpr int LO_OFF = HI_OFF + PTILEB;
+  static constexpr int BAR_OFF = LO_OFF + PTILEB;
+  static constexpr int B_KV = 0, B_QD = 1, B_MMA = 2, B_DRAIN = 3, NBARS = 4;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
+  static constexpr int USED = MISC_OFF + 16;
+  static constexpr int SMEM = ((USED + 1023) / 1024) * 1024 + 1024;  // + realignment slack
+  // more than half an SM's shared memory: one CTA (and one TMEM allocation) per SM
+  static constexpr int SMEM_LAUNCH = SMEM < 120 * 1024 ? 120 * 1024 : SMEM;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  // TMEM columns: S (then dQ_part) at 0, dP at 128, dV at 256, dK at 256 + D
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+  static_assert(256 + 2 * D <= (int)kTmemCols, "TMEM budget");
+};
+
+constexpr int kBwdThreads = 128;
+
+// Instruction descriptor with both operand majors: A MN-major at bit 15.
+__host__ __device__ constexpr uint32_t make_idesc_ab(int M, int N, int a_mn_major, int b_mn_major) {
+  return make_idesc(M, N, b_mn_major) | ((uint32_t)a_mn_major << 15);
+}
+
+// Byte offset of element (row r, key c) in a 128 x 128 bf16 tile stored as
+// two 64-key chunks with the 128-byte swizzle: within a chunk row r is 128
+// bytes at r * 128, and its 16-byte granule g sits at granule g ^ (r % 8).
+__device__ __forceinline__ uint32_t ptile_off(int r, int c) {
+  return (uint32_t)((c >> 6) * (kBM * 128) + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
+                    ((c & 7) << 1));
+}
+
+struct BwdBlock {
+  int s0, n, h, kt;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    hstu_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs a) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bars = base + C::BAR_OFF;
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+
+  if (tid == 0) {
+    for (int i = 0; i < C::NBARS; ++i) mbar_init(bar(i), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_do)) : "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_tm = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+  const WaitCtx w{a.timeout_ns, abort_flag};
+
+  constexpr uint32_t IDESC_S = make_idesc(kBM, kBN, 0);
+  constexpr uint32_t IDESC_T = make_idesc_ab(kBM, D, 1, 1);   // dV, dK: A and B MN-major
+  constexpr uint32_t IDESC_DQ = make_idesc_ab(kBM, D, 0, 1);  // dQ: A K-major, B MN-major
+  constexpr int DSTEPS = D / 16, SPC = C::CHUNK / 16;
+  const uint64_t q_kmaj = smem_desc(base + C::Q_OFF, 16, C::ATOMB, C::LAYOUT);
+  const uint64_t k_kmaj = smem_desc(base + C::K_OFF, 16, C::ATOMB, C::LAYOUT);
+  const uint64_t v_kmaj = smem_desc(base + C::V_OFF, 16, C::ATOMB, C::LAYOUT);
+  const uint64_t do_kmaj = smem_desc(base + C::DO_OFF, 16, C::ATOMB, C::LAYOUT);
+  const uint64_t q_mn = smem_desc(base + C::Q_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
+  const uint64_t k_mn = smem_desc(base + C::K_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
+  const uint64_t do_mn = smem_desc(base + C::DO_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
+  const uint64_t hi_mn = smem_desc(base + C::HI_OFF, C::PCHUNKB, 1024, 2);
+  const uint64_t lo_mn = smem_desc(base + C::LO_OFF, C::PCHUNKB, 1024, 2);
+  const uint64_t hi_kmaj = smem_desc(base + C::HI_OFF, 16, 1024, 2);
+  const uint64_t lo_kmaj = smem_desc(base + C::LO_OFF, 16, 1024, 2);
+
+  uint32_t ph_kv = 0, ph_qd = 0, ph_mma = 0;
+  bool ok = true;
+  // every thread waits (bounded); the CTA continues only if all succeeded
+  auto wait_all = [&](int b, uint32_t& ph, int site) -> bool {
+    const bool mine = wait_one(bar(b), ph, w, site);
+    ph ^= 1u;
+    return !__syncthreads_or(mine ? 0 : 1);
+  };
+  auto load_tile = [&](const CUtensorMap* map, int off, int b, int h, int row0) {
+#pragma unroll
+    for (int ch = 0; ch < C::NCHUNK; ++ch)
+      tma_load_3d(base + off + ch * C::CHUNKB, map, bar(b), ch * C::CHUNK, h, row0);
+  };
+  // S or dP = X Y^T over d: both K-major
+  auto mma_xyt = [&](uint32_t d_col, uint64_t xd, uint64_t yd) {
+#pragma unroll
+    for (int kk = 0; kk < DSTEPS; ++kk) {
+      const uint32_t off = (kk / SPC) * C::CHUNKB + (kk % SPC) * 32;
+      if (kk == 0)
+        mma_ss_c<0>(tmem + d_col, xd + (off >> 4), yd + (off >> 4), IDESC_S);
+      else
+        mma_ss_c<1>(tmem + d_col, xd + (off >> 4), yd + (off >> 4), IDESC_S);
+    }
+  };
+  // T += tile^T B over the 128 query rows: tile MN-major (M = keys), B MN-major
+  auto mma_tt = [&](uint32_t d_col, uint64_t tile_mn, uint64_t bd, bool first) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t ad = tile_mn + (uint64_t)((kk * 2048) >> 4);
+      const uint64_t b2 = bd + (uint64_t)((kk * 2 * C::ATOMB) >> 4);
+      if (first && kk == 0)
+        mma_ss_c<0>(tmem + d_col, ad, b2, IDESC_T);
+      else
+        mma_ss_c<1>(tmem + d_col, ad, b2, IDESC_T);
+    }
+  };
+  // dQ_part (+)= tile K over the 128 keys: tile K-major, K MN-major
+  auto mma_dq = [&](uint64_t tile_k, bool first) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t ad = tile_k + (uint64_t)(((kk >> 2) * C::PCHUNKB + (kk & 3) * 32) >> 4);
+      const uint64_t b2 = k_mn + (uint64_t)((kk * 2 * C::ATOMB) >> 4);
+      if (first && kk == 0)
+        mma_ss_c<0>(tmem + C::S_COL, ad, b2, IDESC_DQ);
+      else
+        mma_ss_c<1>(tmem + C::S_COL, ad, b2, IDESC_DQ);
+    }
+  };
+  // Element (row r = tid, key c) of the current block pair is kept.
+  const float alpha = a.alpha, inv_n = a.inv_n;
+  uint8_t* hi_tile = smem + C::HI_OFF;
+  uint8_t* lo_tile = smem + C::LO_OFF;
+  // write 8 keys (c8 .. c8 + 7) of row tid, split into hi and lo
+  auto put8 = [&](int c8, const float (&v)[8]) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t ph = pack_bf16x2(v[2 * m], v[2 * m + 1]);
+      const float r0 = v[2 * m] - __uint_as_float(ph << 16);
+      const float r1 = v[2 * m + 1] - __uint_as_float(ph & 0xFFFF0000u);
+      hw[m] = ph;
+      lw[m] = pack_bf16x2(r0, r1);
+    }
+    const uint32_t o = ptile_off(tid, c8);
+    *reinterpret_cast<uint4*>(hi_tile + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo_tile + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  };
+
+  for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+    const Item it = __ldg(&a.items[idx]);
+    const BwdBlock b{it.x, it.y, it.z, it.w};
+    const int nq = (b.n + kBM - 1) / kBM;
+    const int key_rows = b.n - kBN * b.kt;  // keys of the block that exist (>= 1)
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILEB);
+      load_tile(&tm_k, C::K_OFF, C::B_KV, b.h, b.s0 + kBN * b.kt);
+      load_tile(&tm_v, C::V_OFF, C::B_KV, b.h, b.s0 + kBN * b.kt);
+    }
+    if (!(ok = wait_all(C::B_KV, ph_kv, kSiteKFull))) break;
+    for (int qt = b.kt; qt < nq; ++qt) {
+      const bool first = qt == b.kt;
+      if (tid == 0) {
+        mbar_arrive_expect_tx(bar(C::B_QD), 2 * C::TILEB);
+        load_tile(&tm_q, C::Q_OFF, C::B_QD, b.h, b.s0 + kBM * qt);
+        load_tile(&tm_do, C::DO_OFF, C::B_QD, b.h, b.s0 + kBM * qt);
+      }
+      if (!(ok = wait_all(C::B_QD, ph_qd, kSiteQFull))) break;
+      if (tid == 0) {
+        tc_fence_after();
+        mma_xyt(C::S_COL, q_kmaj, k_kmaj);
+        mma_xyt(C::DP_COL, do_kmaj, v_kmaj);
+        mma_commit(bar(C::B_MMA));
+      }
+      if (!(ok = wait_all(C::B_MMA, ph_mma, kSiteSFull))) break;
+      tc_fence_after();
+      // row tid of query block qt sees key c of block kt iff both exist and
+      // the key is not after the row
+      const int row_i = kBM * qt + tid;               // sequence-local query
+      const int lim = row_i - kBN * b.kt;             // keys c <= lim are not after the row
+      const int cmax = key_rows < lim + 1 ? key_rows : lim + 1;  // kept keys: c < cmax
+      const bool row_ok = row_i < b.n;
+      // 2. P
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int col = 32 * c + 8 * g + e;
+            const float x = alpha * __uint_as_float(sr[8 * g + e]);
+            const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+            v[e] = (row_ok && col < cmax) ? inv_n * x * sg : 0.0f;
+          }
+          put8(32 * c + 8 * g, v);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncthreads();
+      // 3. dV += P^T dO
+      if (tid == 0) {
+        tc_fence_after();
+        mma_tt(C::DV_COL, hi_mn, do_mn, first);
+        mma_tt(C::DV_COL, lo_mn, do_mn, false);
+        mma_commit(bar(C::B_MMA));
+      }
+      if (!(ok = wait_all(C::B_MMA, ph_mma, kSiteOFull))) break;
+      tc_fence_after();
+      // 4. dS
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], pr[32];
+        tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
+        tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int col = 32 * c + 8 * g + e;
+            const float x = alpha * __uint_as_float(sr[8 * g + e]);
+            const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+            const float ds = inv_n * sg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[8 * g + e]);
+            v[e] = (row_ok && col < cmax) ? ds : 0.0f;
+          }
+          put8(32 * c + 8 * g, v);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncthreads();
+      // 5. dK += dS^T Q, dQ_part = dS K (over S: every thread has read it)
+      if (tid == 0) {
+        tc_fence_after();
+        mma_tt(C::DK_COL, hi_mn, q_mn, first);
+        mma_tt(C::DK_COL, lo_mn, q_mn, false);
+        mma_dq(hi_kmaj, true);
+        mma_dq(lo_kmaj, false);
+        mma_commit(bar(C::B_MMA));
+      }
+      if (!(ok = wait_all(C::B_MMA, ph_mma, kSiteVFull))) break;
+      tc_fence_after();
+      // 6. dQ += alpha dQ_part, for the rows that exist
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(lane_tm + C::S_COL + 32u * c, r);
+        if (row_ok) {
+          float4* dst = reinterpret_cast<float4*>(
+              a.dq_acc + ((size_t)(b.s0 + row_i) * a.heads + b.h) * D + 32 * c);
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            atomicAdd(dst + m, make_float4(alpha * __uint_as_float(r[4 * m]),
+                                           alpha * __uint_as_float(r[4 * m + 1]),
+                                           alpha * __uint_as_float(r[4 * m + 2]),
+                                           alpha * __uint_as_float(r[4 * m + 3])));
+        }
+      }
+      tc_fence_before();
+      __syncthreads();  // S, dP, the tiles and Q / dO are free for the next block
+    }
+    if (!ok) break;
+    // dV and alpha dK of the item's keys (key row tid)
+    tc_fence_after();
+    {
+      const bool key_ok = tid < key_rows;
+      const size_t trow = ((size_t)(b.s0 + kBN * b.kt + tid) * a.heads + b.h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32(lane_tm + C::DV_COL + 32u * c, rv);
+        tmem_ld32(lane_tm + C::DK_COL + 32u * c, rk);
+        if (key_ok) {
+          uint4* dv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dv) + trow + 32 * c);
+          uint4* dk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dk) + trow + 32 * c);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t pv[4], pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int q = 8 * m + 2 * e;
+              pv[e] = pack_bf16x2(__uint_as_float(rv[q]), __uint_as_float(rv[q + 1]));
+              pk[e] = pack_bf16x2(alpha * __uint_as_float(rk[q]), alpha * __uint_as_float(rk[q + 1]));
+            }
+            dv[m] = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+            dk[m] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // dV and dK read before the next item overwrites them
+  }
+  if (!ok && tid == 0) {
+    // drain: a commit arrives once every product issued before it is done
+    mma_commit(bar(C::B_DRAIN));
+    wait_drain(bar(C::B_DRAIN), 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// dQ = bf16(acc): the accumulated fp32 gradient, rounded once.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* acc, uint16_t* dq, long long n8) {
+  for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n8; i += (long long)gridDim.x * 256) {
+    const float4 x0 = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 x1 = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w),
+                                                 pack_bf16x2(x1.x, x1.y), pack_bf16x2(x1.z, x1.w));
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+  using C = BCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(hstu_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_LAUNCH);
+  if (e != cudaSuccess) return e;
+  hstu_bwd_kernel<D><<<grid, kBwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, tdo, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const long long n8 = a.total * a.heads * D / 8;
+  const int cgrid = (int)std::min<long long>((n8 + 255) / 256, 4LL * 1024);
+  dq_convert_kernel<<<cgrid, 256, 0, stream>>>(a.dq_acc, static_cast<uint16_t*>(a.dq), n8);
+  return cudaGetLastError();
+}

@@ -52,6 +52,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "hstu_internal.h"
@@ -1392,6 +1393,8 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   }
 }
 
+#include "hstu_bwd.cuh"
+
 }  // namespace
 
 int fwd_smem_bytes(int d) {
@@ -1404,6 +1407,16 @@ int fwd_smem_bytes(int d) {
 }
 
 int fwd_swizzle_bytes(int d) { return d >= 64 ? 128 : 64; }
+
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+  switch (d) {
+    case 32: return launch_bwd_d<32>(tq, tk, tv, tdo, a, grid, stream);
+    case 64: return launch_bwd_d<64>(tq, tk, tv, tdo, a, grid, stream);
+    case 128: return launch_bwd_d<128>(tq, tk, tv, tdo, a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, int grid, cudaStream_t stream) {

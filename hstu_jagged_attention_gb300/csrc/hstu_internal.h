@@ -74,6 +74,30 @@ struct FwdArgs {
   unsigned debug_flags;  // kDebug* bits; 0 in normal use
 };
 
+// Backward pass: items (first token, length, head, key block kt), each
+// walking the query blocks kt .. last; dq_acc: fp32 (total, heads, d),
+// zeroed before the launch; dq, dk, dv: bf16 (total, heads, d).
+struct BwdArgs {
+  const Item* items;
+  int n_items;
+  int heads;
+  float alpha, inv_n;
+  float* dq_acc;
+  void* dq;
+  void* dk;
+  void* dv;
+  long long total;
+  unsigned long long timeout_ns;
+};
+// Work list of the backward: one item per (sequence, head, key block kt),
+// costing nq - kt query blocks; ordered by cost descending, then sequence,
+// head, kt ascending.
+void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst);
+// The backward kernel for head dimension d on `grid` CTAs, then the dQ
+// conversion; tdo describes dout like q.
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+
 // Test hook: the MMA warp first waits on a barrier nothing signals.
 constexpr unsigned kDebugUnsignalledWait = 1u;
 // Tracing: CTA 0 records a clock64 stamp per pipeline event (see

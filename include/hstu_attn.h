@@ -340,6 +340,36 @@ int hstu_attn_fwd_norm_gate(const void* q, const void* k, const void* v, const v
                             hstu_stream_t stream);
 
 /*
+ * Backward pass -- HSTU paper Appendix G: the backward recomputes the
+ * attention (no (s x s) buffer is kept from the forward) and its gradients
+ * are those of the forward definition.  For dout = d out:
+ *
+ *   dv[j] = sum_i P_ij dout[i],   P_ij = inv_n silu(alpha q_i.k_j)   (kept pairs)
+ *   ds_ij = inv_n silu'(alpha q_i.k_j) <dout[i], v[j]>
+ *   dq[i] = alpha sum_j ds_ij k[j],   dk[j] = alpha sum_i ds_ij q[i]
+ *
+ * over the causal pairs of each sequence, silu'(x) = sig(x) (1 + x (1 - sig(x))).
+ *
+ * hstu_attn_bwd  q, k, v, dout: bf16 device (total, heads, d); dq, dk, dv:
+ *                bf16 device (total, heads, d), written for every token.
+ *                offsets, batch, heads, d, max_seqlen, alpha, inv_n as
+ *                hstu_attn_fwd.  Enqueues, on `stream`: a zeroing of an
+ *                fp32 dQ accumulator (4 * total * heads * d bytes, allocated
+ *                and freed stream-ordered with the work list), the backward
+ *                kernel and the dQ conversion.  One work item per (sequence,
+ *                head, 128-key block kt) walks the query blocks kt .. last.
+ * hstu_worklist_build_bwd  the host-only work list: items (first token,
+ *                length, head, kt), costing nq - kt query blocks, ordered by
+ *                cost descending, then sequence, head, kt ascending.
+ * Errors: as hstu_attn_fwd (all seven buffers non-null and 16-byte aligned).
+ */
+int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
+                  const int32_t* offsets, int batch, int heads, int d, int max_seqlen, float alpha,
+                  float inv_n, void* dq, void* dk, void* dv, hstu_stream_t stream);
+int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
+                            int capacity, int* n_items);
+
+/*
  * hstu_launch_shape -- the grid the next launch for `plan` would use on the
  * current device: *grid persistent CTAs of *block threads with *smem_bytes
  * of dynamic shared memory.  Queries device attributes; launches nothing.

@@ -62,3 +62,21 @@ def items_targets(offsets, num_targets, heads: int, block_m: int = BLOCK_M):
     hs = np.array([hist for (*_, hist) in rows], dtype=np.int32)
     return it.reshape(-1, 4), hs
 
+
+
+def items_bwd(offsets, heads: int, block_m: int = BLOCK_M) -> np.ndarray:
+    """Backward work items: one per (sequence, head, key block kt), which the
+    query blocks kt .. nq - 1 see (causal), costing nq - kt; ordered by cost
+    descending, then b, h, kt ascending.  int32 (n, 4): (first token, length,
+    head, kt)."""
+    offsets = [int(x) for x in offsets]
+    rows = []
+    for b in range(len(offsets) - 1):
+        n = offsets[b + 1] - offsets[b]
+        nq = (n + block_m - 1) // block_m
+        for h in range(heads):
+            for kt in range(nq):
+                rows.append((-(nq - kt), b, h, kt, offsets[b], n))
+    rows.sort()
+    out = np.array([(s0, n, h, kt) for (_, b, h, kt, s0, n) in rows], dtype=np.int32)
+    return out.reshape(-1, 4)

@@ -211,3 +211,26 @@ def test_rab_draws_are_in_range():
     off = w.offsets
     for b in range(w.batch):
         assert np.all(np.diff(ts[off[b]:off[b + 1]].astype(np.int64)) >= 0)
+
+
+# ------------------------------------------------ backward work list
+@pytest.mark.parametrize("seed", range(8))
+def test_bwd_worklist_bit_exact_random(seed):
+    rng = np.random.default_rng(900 + seed)
+    nb = int(rng.integers(0, 30))
+    lengths = rng.integers(0, 900, size=nb)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    heads = int(rng.integers(1, 5))
+    got = binding.hstu_worklist_build_bwd(off, heads)
+    assert np.array_equal(got, oracle_worklist.items_bwd(off, heads).reshape(-1, 4))
+
+
+def test_bwd_validation_before_any_cuda_call():
+    off = np.array([0, 4], np.int32)
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_attn_bwd(16, 16, 16, 16, off, 1, 2, 48, 4, 1.0, 1.0, 16, 16, 16, stream=0)
+    assert e.value.code == binding.HSTU_ERR_UNSUPPORTED
+    with pytest.raises(binding.HstuError) as e:
+        binding.hstu_attn_bwd(16, 16, 16, 16, off, 1, 0, 64, 4, 1.0, 1.0, 16, 16, 16, stream=0)
+    assert e.value.code == binding.HSTU_ERR_INVALID_ARG
+    binding.hstu_attn_bwd(0, 0, 0, 0, np.zeros(1, np.int32), 0, 2, 64, 0, 1.0, 1.0, 0, 0, 0, stream=0)
