@@ -65,6 +65,40 @@ def causal_flops(w: workloads.Workload, num_targets=None) -> float:
     return float(4.0 * w.d * w.heads * pairs)
 
 
+BWD_METRIC = "HSTU jagged causal attn bwd (dQ, dK, dV): TFLOPS at 10 d FLOP per kept pair; ms/call"
+
+
+def bwd_flops(w: workloads.Workload) -> float:
+    """The backward's products per kept pair and head: S = Q K^T and dP = dO V^T
+    (recomputed), dV += P^T dO, dK += dS^T Q, dQ += dS K: 5 x 2 d FLOP."""
+    L = w.lengths.astype(np.float64)
+    return float(10.0 * w.d * w.heads * np.sum(L * (L + 1) / 2.0))
+
+
+def cpu_oracle_bwd_sample(w, q, k, v, do, target_s: float, threads: int | None = None):
+    """The oracle's backward on the first sequences of the workload, as many
+    as fit about target_s seconds (calibrated on the first one)."""
+    from oracle import reference
+    threads = threads or reference.default_threads()
+    off = w.offsets.astype(np.int64)
+
+    def run(nb):
+        e = int(off[nb])
+        t0 = time.perf_counter()
+        reference.hstu_bwd(q[:e], k[:e], v[:e], do[:e], off[:nb + 1], w.alpha, w.inv_n, threads=threads)
+        return time.perf_counter() - t0
+
+    nb = 1
+    dt = run(nb)
+    while nb < w.batch and dt * (nb + 1) / nb < target_s:
+        nb = min(w.batch, max(nb + 1, int(nb * target_s / max(dt, 1e-3))))
+        dt = run(nb)
+    sub = workloads.custom(w.lengths[:nb], w.heads, w.d, alpha=w.alpha, inv_n=w.inv_n)
+    desc = (f"the first {nb} of {w.batch} sequences of the {w.name} workload "
+            f"({bwd_flops(sub) / 1e9:.2f} backward GFLOP), fp64 C oracle, {threads} threads")
+    return bwd_flops(sub) / dt / 1e12, desc, threads, dt
+
+
 def workload_by_name(name: str):
     """(workload, num_targets or None)."""
     if name == "candidates":
@@ -236,6 +270,34 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
     return fl / dt / 1e12, desc, threads, dt
 
 
+def run_reference_bwd(args, w):
+    world, rank, _ = dist_init()
+    if rank != 0:
+        return 0
+    q, k, v = workloads.draw_qkv(w)
+    rng = np.random.default_rng(4000 + max(w.index, 0))
+    do = workloads.bf16_round(rng.standard_normal(q.shape).astype(np.float32))
+    arrs = [t.float().numpy() for t in (q, k, v, do)]
+    per_step_s = max(1.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
+    vals = []
+    desc, threads = "", 0
+    for s_ in range(args.warmup + args.steps):
+        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, per_step_s)
+        if s_ >= args.warmup:
+            vals.append(val)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **w.describe(), "pass": "backward"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def _norm_gate_desc(args) -> dict:
     if not args.norm_gate:
         return {}
@@ -296,6 +358,124 @@ def _targets_desc(nt) -> dict:
     return {"mask": "M-FALCON candidates (HSTU paper Appendix H)",
             "num_targets_per_sequence": int(np.asarray(nt)[0]) if len(set(np.asarray(nt).tolist())) == 1
             else "varies"}
+
+
+def run_ours_bwd(args, w):
+    """The backward on its own plan: kernel-only value, one-shot e2e with host buffers."""
+    import torch
+    from hstu_jagged_attention_gb300 import binding, build
+
+    world, rank, local = dist_init()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}), flush=True)
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    q_h, k_h, v_h = workloads.draw_qkv(w)
+    rng = np.random.default_rng(4000 + max(w.index, 0))
+    do_h = workloads.bf16_round(rng.standard_normal(q_h.shape).astype(np.float32))
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    grads = [torch.empty_like(q) for _ in range(3)]
+    plan = binding.hstu_plan_create_ex(w.offsets, None, w.batch, w.heads, w.d, w.max_seqlen,
+                                       binding.HSTU_PLAN_BACKWARD)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(local)
+    t_warm = time.perf_counter()
+    for _ in range(args.warmup):
+        binding.hstu_attn_bwd_plan(plan, q, k, v, do, w.alpha, w.inv_n, *grads, stream=stream)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        binding.hstu_attn_bwd_plan(plan, q, k, v, do, w.alpha, w.inv_n, *grads, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop(wall0, wall0 + wall, t_warm)
+    times_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    ms = statistics.mean(times_ms)
+    flops = bwd_flops(w)
+    value, ms_max = aggregate(flops, ms, world, dev)
+    st, site = binding.hstu_last_status()
+    if st != binding.HSTU_OK:
+        raise RuntimeError(f"device wait gave up during the timed region (site {site})")
+    # end to end: host inputs in, gradients out, through the one-shot call
+    pin = [t.pin_memory() for t in (q_h, k_h, v_h, do_h)]
+    outs_h = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+    ins = [torch.empty_like(q) for _ in range(4)]
+    g2 = [torch.empty_like(q) for _ in range(3)]
+    offsets_host = w.offsets.copy()
+
+    def e2e_step():
+        for dst, src in zip(ins, pin):
+            dst.copy_(src, non_blocking=True)
+        binding.hstu_attn_bwd(*ins, offsets_host, w.batch, w.heads, w.d, w.max_seqlen, w.alpha,
+                              w.inv_n, *g2, stream=stream)
+        for dst, src in zip(outs_h, g2):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        flush.zero_()
+        e2e_step()
+    e1.record(stream)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        flush.zero_()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max(e0.elapsed_time(e1) / args.steps - f0.elapsed_time(f1) / args.steps, 1e-6)
+    e2e_value, e2e_ms = aggregate(flops, e2e_ms, world, dev)
+    elem = w.total * w.heads * w.d * 2
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        arrs = [t.float().numpy() for t in (q_h, k_h, v_h, do_h)]
+        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+    binding.hstu_plan_destroy(plan)
+    peaks = load_peaks()
+    achieved = flops / (ms * 1e-3) / 1e12
+    if rank == 0:
+        line = {
+            "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**w.describe(), "pass": "backward", "l2": "flushed between steps (256 MiB write)",
+                       "work_items": len(binding.hstu_worklist_build_bwd(w.offsets, w.heads)),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": UNIT, "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16_tflops (burst)"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * elem + offsets_host.nbytes,
+                    "d2h_bytes_per_step": 3 * elem, "ms_per_step": e2e_ms},
+            "cpu_baseline": cpu,
+            # the backward kernel and the dQ conversion per step
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+            "timed_wall_s": wall,
+            "ms_per_step_min": min(times_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
 
 
 def run_ours(args, w, nt=None):
@@ -496,6 +676,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--norm-gate", action="store_true",
                     help="fuse the layer's output stage Norm(A V) * U into the timed call")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (dQ, dK, dV) instead of the forward")
     ap.add_argument("--rab", action="store_true",
                     help="add the relative attention bias rab_{p,t} (timestamps and bucketed tables)")
     args = ap.parse_args(argv)
@@ -505,7 +687,10 @@ def main(argv=None):
     rc = 0
     for name in names:
         w, nt = workload_by_name(name)
-        rc |= run_reference(args, w, nt) if args.impl == "reference" else run_ours(args, w, nt)
+        if args.backward:
+            rc |= run_reference_bwd(args, w) if args.impl == "reference" else run_ours_bwd(args, w)
+        else:
+            rc |= run_reference(args, w, nt) if args.impl == "reference" else run_ours(args, w, nt)
     return rc
 
 

@@ -86,6 +86,8 @@ _SIGNATURES = {
                                         ctypes.c_float, _VP, _VP]),
     "hstu_attn_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP, _VP, _VP, _VP]),
+    "hstu_attn_bwd_plan": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_float, ctypes.c_float, _VP,
+                                          _VP, _VP, _VP]),
     "hstu_worklist_build_bwd": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int,
                                                _IP]),
     "hstu_attn_fwd_norm_gate": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP,
@@ -95,6 +97,7 @@ _SIGNATURES = {
 }
 
 HSTU_PLAN_NORM_GATE = 1
+HSTU_PLAN_BACKWARD = 2
 
 _lib = None
 
@@ -277,6 +280,13 @@ def hstu_attn_bwd(q, k, v, dout, offsets, batch: int, heads: int, d: int, max_se
                                int(heads), int(d), int(max_seqlen), float(alpha), float(inv_n),
                                _addr(dq), _addr(dk), _addr(dv), _stream(stream)), "hstu_attn_bwd")
     del keep
+
+
+def hstu_attn_bwd_plan(plan: Plan, q, k, v, dout, alpha: float, inv_n: float, dq, dk, dv,
+                       stream=None) -> None:
+    _check(lib().hstu_attn_bwd_plan(plan.handle, _addr(q), _addr(k), _addr(v), _addr(dout),
+                                    float(alpha), float(inv_n), _addr(dq), _addr(dk), _addr(dv),
+                                    _stream(stream)), "hstu_attn_bwd_plan")
 
 
 def hstu_worklist_build_bwd(host_offsets, heads: int) -> np.ndarray:

@@ -308,6 +308,9 @@ struct hstu_plan {
   int32_t* d_hist = nullptr;
   // output-stage scratch (HSTU_PLAN_NORM_GATE): xs, then stats
   char* d_norm = nullptr;
+  // backward (HSTU_PLAN_BACKWARD): its work list, then the fp32 dQ accumulator
+  int n_bwd = 0;
+  char* d_bwd = nullptr;
   int device = -1;
 };
 
@@ -324,8 +327,10 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
               unsigned flags, hstu_plan** plan) {
   if (!plan) return HSTU_ERR_INVALID_ARG;
   *plan = nullptr;
-  if (heads < 1 || max_seqlen < 0 || (flags & ~(unsigned)HSTU_PLAN_NORM_GATE))
+  if (heads < 1 || max_seqlen < 0 ||
+      (flags & ~(unsigned)(HSTU_PLAN_NORM_GATE | HSTU_PLAN_BACKWARD)))
     return HSTU_ERR_INVALID_ARG;
+  if ((flags & HSTU_PLAN_BACKWARD) && nt) return HSTU_ERR_INVALID_ARG;  // causal only
   const bool norm = (flags & HSTU_PLAN_NORM_GATE) != 0;
   if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
   int rc = check_offsets(off, batch, max_seqlen);
@@ -350,6 +355,7 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
   auto fail = [&](int code) {
     if (p->d_items) cudaFree(p->d_items);
     if (p->d_norm) cudaFree(p->d_norm);
+    if (p->d_bwd) cudaFree(p->d_bwd);
     delete p;
     return code;
   };
@@ -371,6 +377,22 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
     if ((e = cudaMalloc(reinterpret_cast<void**>(&p->d_norm),
                         hstu::norm_scratch_bytes(p->total, heads, d))) != cudaSuccess)
       return fail(mem_code(e));
+  }
+  if (flags & HSTU_PLAN_BACKWARD) {
+    std::vector<hstu::Item> bw;
+    try {
+      bw.resize(p->items.size());
+    } catch (const std::bad_alloc&) {
+      return fail(HSTU_ERR_NO_MEMORY);
+    }
+    hstu::fill_items_bwd(off, batch, heads, bw.data());
+    p->n_bwd = (int)bw.size();
+    const size_t bbytes = bw.size() * sizeof(hstu::Item);
+    if ((e = cudaMalloc(reinterpret_cast<void**>(&p->d_bwd),
+                        bbytes + (size_t)p->total * heads * d * sizeof(float))) != cudaSuccess)
+      return fail(mem_code(e));
+    if (cudaMemcpy(p->d_bwd, bw.data(), bbytes, cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(HSTU_ERR_CUDA);
   }
   *plan = p;
   return HSTU_OK;
@@ -539,6 +561,7 @@ int hstu_plan_destroy(hstu_plan* plan) {
   int rc = HSTU_OK;
   if (plan->d_items && cudaFree(plan->d_items) != cudaSuccess) rc = HSTU_ERR_CUDA;
   if (plan->d_norm && cudaFree(plan->d_norm) != cudaSuccess) rc = HSTU_ERR_CUDA;
+  if (plan->d_bwd && cudaFree(plan->d_bwd) != cudaSuccess) rc = HSTU_ERR_CUDA;
   delete plan;
   return rc;
 }
@@ -766,6 +789,20 @@ int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
                        reinterpret_cast<float*>(block), dq, dk, dv, s);
   if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
   return rc;
+}
+
+int hstu_attn_bwd_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                       const void* dout, float alpha, float inv_n, void* dq, void* dk, void* dv,
+                       hstu_stream_t stream) {
+  if (!plan || !(plan->flags & HSTU_PLAN_BACKWARD)) return HSTU_ERR_INVALID_ARG;
+  if (plan->items.empty()) return HSTU_OK;
+  int rc = check_buffers(q, k, v, dout);
+  if (rc != HSTU_OK || (rc = check_buffers(dq, dk, dv, dv)) != HSTU_OK) return rc;
+  const size_t bbytes = (size_t)plan->n_bwd * sizeof(hstu::Item);
+  return launch_backward(reinterpret_cast<const hstu::Item*>(plan->d_bwd), plan->n_bwd, plan->total,
+                         plan->heads, plan->d, q, k, v, dout, alpha, inv_n,
+                         reinterpret_cast<float*>(plan->d_bwd + bbytes), dq, dk, dv,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_last_status(int* device_status, int* site) {

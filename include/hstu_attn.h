@@ -366,6 +366,14 @@ int hstu_attn_fwd_norm_gate(const void* q, const void* k, const void* v, const v
 int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
                   const int32_t* offsets, int batch, int heads, int d, int max_seqlen, float alpha,
                   float inv_n, void* dq, void* dk, void* dv, hstu_stream_t stream);
+/* The backward on a plan made by hstu_plan_create_ex with HSTU_PLAN_BACKWARD
+ * (no candidates): the plan owns the backward work list and the fp32 dQ
+ * accumulator; launches on one stream at a time per plan.  A plan without
+ * the flag: HSTU_ERR_INVALID_ARG. */
+#define HSTU_PLAN_BACKWARD 2u
+int hstu_attn_bwd_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                       const void* dout, float alpha, float inv_n, void* dq, void* dk, void* dv,
+                       hstu_stream_t stream);
 int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
                             int capacity, int* n_items);
 

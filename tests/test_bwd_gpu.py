@@ -73,3 +73,24 @@ def test_bwd_is_deterministic_in_dk_dv_and_close_in_dq():
     (b, _) = _run(w, seed=860)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
     assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2 * a[0].float().abs().max().item()
+
+
+def test_bwd_plan_equals_one_shot():
+    w = workloads.custom(LENGTHS, heads=2, d=64)
+    (a, _) = _run(w, seed=870)
+    q, k, v = workloads.draw_qkv(w, seed=870)
+    rng = np.random.default_rng(871)
+    do = workloads.bf16_round(rng.standard_normal(q.shape).astype(np.float32))
+    qd, kd, vd, dod = (t.to("cuda").contiguous() for t in (q, k, v, do))
+    g = [torch.empty_like(qd) for _ in range(3)]
+    plan = binding.hstu_plan_create_ex(w.offsets, None, w.batch, w.heads, w.d, w.max_seqlen,
+                                       binding.HSTU_PLAN_BACKWARD)
+    try:
+        binding.hstu_attn_bwd_plan(plan, qd, kd, vd, dod, w.alpha, w.inv_n, *g)
+        binding.hstu_attn_bwd_plan(plan, qd, kd, vd, dod, w.alpha, w.inv_n, *g)  # the accumulator restarts
+        torch.cuda.synchronize()
+    finally:
+        binding.hstu_plan_destroy(plan)
+    assert torch.equal(g[1], a[1]) and torch.equal(g[2], a[2])
+    assert (g[0].float() - a[0].float()).abs().max().item() <= 1e-2 * a[0].float().abs().max().item()
+    parity.assert_device_ok()
