@@ -11,9 +11,10 @@
 //
 // Work item: one 128-key block kt of one (sequence, head); the CTA walks the
 // query blocks qt = kt .. last that see it.  K and V load once per item,
-// Q and dO once per query block.  One thread issues the copies and the
-// products; the 128 threads (thread r owns TMEM lane r) turn S and dP into
-// P and dS.  Per query block:
+// Q and dO once per query block (double-buffered where shared memory has
+// room).  One thread issues the copies and the products; two warpgroups
+// (thread r and r + 128 share TMEM lane r, each taking half of the key
+// columns) turn S and dP into P and dS.  Per query block:
 //   1. S = Q K^T and dP = dO V^T into TMEM (fp32).
 //   2. P = inv_n silu(alpha S), split into bf16 hi + lo, written to two
 //      128B-swizzled shared tiles (rows = queries, 64-key chunks).
@@ -26,7 +27,9 @@
 //      (vector atomics): query block qt gets one part per key block.
 // At the item's end dV and alpha dK leave TMEM as bf16.  The P and dS
 // splits keep the products' error at the bf16 output rounding, as in the
-// forward.  Phases run one after another (synchronous waits).
+// forward.  Where shared memory has room (d <= 64) P and dS have tiles of
+// their own: one pass computes both, and steps 3 and 5 issue together.
+// Phases run one after another (synchronous waits).
 
 template <int D>
 struct BCfg {
@@ -40,14 +43,24 @@ struct BCfg {
   // P / dS tiles: 128 rows x 128 keys bf16 as two 64-key chunks, 128B swizzle
   static constexpr int PCHUNKB = kBM * 128;
   static constexpr int PTILEB = 2 * PCHUNKB;
+  // Q and dO blocks: double-buffered (the next query block loads during
+  // the current one) where shared memory has room
+  static constexpr int QB = 6 * TILEB + 2 * PTILEB + 4096 <= 232448 - 1024 ? 2 : 1;
+  // P and dS in tiles of their own (one pass computes both, and all the
+  // products of a block issue together) where shared memory has room; else
+  // dS reuses P's tiles after the dV products
+  static constexpr bool MERGED = 2 * TILEB + 2 * QB * TILEB + 4 * PTILEB + 2048 <= 232448 - 1024;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILEB;
-  static constexpr int Q_OFF = V_OFF + TILEB;
-  static constexpr int DO_OFF = Q_OFF + TILEB;
-  static constexpr int HI_OFF = DO_OFF + TILEB;
+  static constexpr int Q_OFF = V_OFF + TILEB;        // QB buffers
+  static constexpr int DO_OFF = Q_OFF + QB * TILEB;  // QB buffers
+  static constexpr int HI_OFF = DO_OFF + QB * TILEB;
   static constexpr int LO_OFF = HI_OFF + PTILEB;
-  static constexpr int BAR_OFF = LO_OFF + PTILEB;
-  static constexpr int B_KV = 0, B_QD = 1, B_MMA = 2, B_DRAIN = 3, NBARS = 4;
+  static constexpr int DHI_OFF = MERGED ? LO_OFF + PTILEB : HI_OFF;  // dS tiles
+  static constexpr int DLO_OFF = MERGED ? DHI_OFF + PTILEB : LO_OFF;
+  static constexpr int BAR_OFF = (MERGED ? DLO_OFF : LO_OFF) + PTILEB;
+  static constexpr int B_KV = 0, B_QD = 1 /* [QB] */, B_MMA = 1 + QB, B_DRAIN = 2 + QB,
+                       NBARS = 3 + QB;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int SMEM = ((USED + 1023) / 1024) * 1024 + 1024;  // + realignment slack
@@ -59,7 +72,9 @@ struct BCfg {
   static_assert(256 + 2 * D <= (int)kTmemCols, "TMEM budget");
 };
 
-constexpr int kBwdThreads = 128;
+// Two warpgroups: warps w and w + 4 share TMEM lanes 32 (w % 4) ..; each
+// takes half of a block's key columns (and half of the d columns).
+constexpr int kBwdThreads = 256;
 
 // Instruction descriptor with both operand majors: A MN-major at bit 15.
 __host__ __device__ constexpr uint32_t make_idesc_ab(int M, int N, int a_mn_major, int b_mn_major) {
@@ -91,6 +106,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127;  // TMEM lane: the query row (or key row at the item's end)
+  const int wg = tid >> 7;    // column half
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
@@ -115,26 +132,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_tm = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+  const uint32_t lane_tm = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's TMEM lanes
   const WaitCtx w{a.timeout_ns, abort_flag};
 
   constexpr uint32_t IDESC_S = make_idesc(kBM, kBN, 0);
   constexpr uint32_t IDESC_T = make_idesc_ab(kBM, D, 1, 1);   // dV, dK: A and B MN-major
   constexpr uint32_t IDESC_DQ = make_idesc_ab(kBM, D, 0, 1);  // dQ: A K-major, B MN-major
   constexpr int DSTEPS = D / 16, SPC = C::CHUNK / 16;
-  const uint64_t q_kmaj = smem_desc(base + C::Q_OFF, 16, C::ATOMB, C::LAYOUT);
+  const uint64_t q_kmaj0 = smem_desc(base + C::Q_OFF, 16, C::ATOMB, C::LAYOUT);
   const uint64_t k_kmaj = smem_desc(base + C::K_OFF, 16, C::ATOMB, C::LAYOUT);
   const uint64_t v_kmaj = smem_desc(base + C::V_OFF, 16, C::ATOMB, C::LAYOUT);
-  const uint64_t do_kmaj = smem_desc(base + C::DO_OFF, 16, C::ATOMB, C::LAYOUT);
-  const uint64_t q_mn = smem_desc(base + C::Q_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
+  const uint64_t do_kmaj0 = smem_desc(base + C::DO_OFF, 16, C::ATOMB, C::LAYOUT);
+  const uint64_t q_mn0 = smem_desc(base + C::Q_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
   const uint64_t k_mn = smem_desc(base + C::K_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
-  const uint64_t do_mn = smem_desc(base + C::DO_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
+  const uint64_t do_mn0 = smem_desc(base + C::DO_OFF, C::CHUNKB, C::ATOMB, C::LAYOUT);
+  auto buf_desc = [&](uint64_t d0, int qb) { return d0 + (uint64_t)((qb * C::TILEB) >> 4); };
   const uint64_t hi_mn = smem_desc(base + C::HI_OFF, C::PCHUNKB, 1024, 2);
   const uint64_t lo_mn = smem_desc(base + C::LO_OFF, C::PCHUNKB, 1024, 2);
-  const uint64_t hi_kmaj = smem_desc(base + C::HI_OFF, 16, 1024, 2);
-  const uint64_t lo_kmaj = smem_desc(base + C::LO_OFF, 16, 1024, 2);
+  const uint64_t dhi_mn = smem_desc(base + C::DHI_OFF, C::PCHUNKB, 1024, 2);
+  const uint64_t dlo_mn = smem_desc(base + C::DLO_OFF, C::PCHUNKB, 1024, 2);
+  const uint64_t dhi_kmaj = smem_desc(base + C::DHI_OFF, 16, 1024, 2);
+  const uint64_t dlo_kmaj = smem_desc(base + C::DLO_OFF, 16, 1024, 2);
 
-  uint32_t ph_kv = 0, ph_qd = 0, ph_mma = 0;
+  uint32_t ph_kv = 0, ph_qd[2] = {0, 0}, ph_mma = 0;
+  uint32_t qiter = 0;  // query blocks done by this CTA: buffer qiter % QB
   bool ok = true;
   // every thread waits (bounded); the CTA continues only if all succeeded
   auto wait_all = [&](int b, uint32_t& ph, int site) -> bool {
@@ -184,10 +205,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
   // Element (row r = tid, key c) of the current block pair is kept.
   const float alpha = a.alpha, inv_n = a.inv_n;
-  uint8_t* hi_tile = smem + C::HI_OFF;
-  uint8_t* lo_tile = smem + C::LO_OFF;
-  // write 8 keys (c8 .. c8 + 7) of row tid, split into hi and lo
-  auto put8 = [&](int c8, const float (&v)[8]) {
+  // write 8 keys (c8 .. c8 + 7) of this thread's row, split into hi and lo
+  auto put8 = [&](uint8_t* hi_tile, uint8_t* lo_tile, int c8, const float (&v)[8]) {
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -197,7 +216,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       hw[m] = ph;
       lw[m] = pack_bf16x2(r0, r1);
     }
-    const uint32_t o = ptile_off(tid, c8);
+    const uint32_t o = ptile_off(row, c8);
     *reinterpret_cast<uint4*>(hi_tile + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     *reinterpret_cast<uint4*>(lo_tile + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   };
@@ -212,15 +231,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       load_tile(&tm_k, C::K_OFF, C::B_KV, b.h, b.s0 + kBN * b.kt);
       load_tile(&tm_v, C::V_OFF, C::B_KV, b.h, b.s0 + kBN * b.kt);
     }
+    auto load_qd = [&](int qb, int qt) {
+      mbar_arrive_expect_tx(bar(C::B_QD + qb), 2 * C::TILEB);
+      load_tile(&tm_q, C::Q_OFF + qb * C::TILEB, C::B_QD + qb, b.h, b.s0 + kBM * qt);
+      load_tile(&tm_do, C::DO_OFF + qb * C::TILEB, C::B_QD + qb, b.h, b.s0 + kBM * qt);
+    };
+    if (tid == 0) load_qd((int)(qiter % C::QB), b.kt);
     if (!(ok = wait_all(C::B_KV, ph_kv, kSiteKFull))) break;
-    for (int qt = b.kt; qt < nq; ++qt) {
+    for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
       const bool first = qt == b.kt;
-      if (tid == 0) {
-        mbar_arrive_expect_tx(bar(C::B_QD), 2 * C::TILEB);
-        load_tile(&tm_q, C::Q_OFF, C::B_QD, b.h, b.s0 + kBM * qt);
-        load_tile(&tm_do, C::DO_OFF, C::B_QD, b.h, b.s0 + kBM * qt);
-      }
-      if (!(ok = wait_all(C::B_QD, ph_qd, kSiteQFull))) break;
+      const int qb = (int)(qiter % C::QB);
+      // the next query block's Q and dO into the other buffer: its last
+      // readers (the previous block's products) are done
+      if (C::QB == 2 && tid == 0 && qt + 1 < nq) load_qd(qb ^ 1, qt + 1);
+      if (!(ok = wait_all(C::B_QD + qb, ph_qd[qb], kSiteQFull))) break;
+      const uint64_t q_kmaj = buf_desc(q_kmaj0, qb), do_kmaj = buf_desc(do_kmaj0, qb);
+      const uint64_t q_mn = buf_desc(q_mn0, qb), do_mn = buf_desc(do_mn0, qb);
       if (tid == 0) {
         tc_fence_after();
         mma_xyt(C::S_COL, q_kmaj, k_kmaj);
@@ -231,13 +257,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       // row tid of query block qt sees key c of block kt iff both exist and
       // the key is not after the row
-      const int row_i = kBM * qt + tid;               // sequence-local query
+      const int row_i = kBM * qt + row;               // sequence-local query
       const int lim = row_i - kBN * b.kt;             // keys c <= lim are not after the row
       const int cmax = key_rows < lim + 1 ? key_rows : lim + 1;  // kept keys: c < cmax
       const bool row_ok = row_i < b.n;
-      // 2. P
+      if constexpr (C::MERGED) {
+        // 2-4. P and dS in one pass over this warpgroup's two 32-key chunks
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+          uint32_t sr[32], pr[32];
+          tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
+          tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            float vp[8], vs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int col = 32 * c + 8 * g + e;
+              const bool keep = row_ok && col < cmax;
+              const float x = alpha * __uint_as_float(sr[8 * g + e]);
+              const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+              const float isg = inv_n * sg;
+              vp[e] = keep ? isg * x : 0.0f;
+              vs[e] = keep ? isg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[8 * g + e]) : 0.0f;
+            }
+            put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, vp);
+            put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, vs);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        // 3 and 5. every product of the block at once
+        if (tid == 0) {
+          tc_fence_after();
+          mma_tt(C::DV_COL, hi_mn, do_mn, first);
+          mma_tt(C::DV_COL, lo_mn, do_mn, false);
+          mma_tt(C::DK_COL, dhi_mn, q_mn, first);
+          mma_tt(C::DK_COL, dlo_mn, q_mn, false);
+          mma_dq(dhi_kmaj, true);
+          mma_dq(dlo_kmaj, false);
+          mma_commit(bar(C::B_MMA));
+        }
+      } else {
+      // 2. P (this warpgroup's two 32-key chunks)
+#pragma unroll 1
+      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
         uint32_t sr[32];
         tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
 #pragma unroll
@@ -250,7 +315,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
             v[e] = (row_ok && col < cmax) ? inv_n * x * sg : 0.0f;
           }
-          put8(32 * c + 8 * g, v);
+          put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, v);
         }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -267,7 +332,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       // 4. dS
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
         uint32_t sr[32], pr[32];
         tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
         tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
@@ -282,7 +347,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float ds = inv_n * sg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[8 * g + e]);
             v[e] = (row_ok && col < cmax) ? ds : 0.0f;
           }
-          put8(32 * c + 8 * g, v);
+          put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, v);
         }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -291,17 +356,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // 5. dK += dS^T Q, dQ_part = dS K (over S: every thread has read it)
       if (tid == 0) {
         tc_fence_after();
-        mma_tt(C::DK_COL, hi_mn, q_mn, first);
-        mma_tt(C::DK_COL, lo_mn, q_mn, false);
-        mma_dq(hi_kmaj, true);
-        mma_dq(lo_kmaj, false);
+        mma_tt(C::DK_COL, dhi_mn, q_mn, first);
+        mma_tt(C::DK_COL, dlo_mn, q_mn, false);
+        mma_dq(dhi_kmaj, true);
+        mma_dq(dlo_kmaj, false);
         mma_commit(bar(C::B_MMA));
       }
+      }  // the two-pass path
       if (!(ok = wait_all(C::B_MMA, ph_mma, kSiteVFull))) break;
       tc_fence_after();
-      // 6. dQ += alpha dQ_part, for the rows that exist
+      // single buffer: Q and dO are free now; load the next block under the atomics
+      if (C::QB == 1 && tid == 0 && qt + 1 < nq) load_qd(0, qt + 1);
+      // 6. dQ += alpha dQ_part, for the rows that exist (32-column chunks
+      // alternate between the warpgroups)
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = wg; c < D / 32; c += 2) {
         uint32_t r[32];
         tmem_ld32(lane_tm + C::S_COL + 32u * c, r);
         if (row_ok) {
@@ -319,13 +388,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncthreads();  // S, dP, the tiles and Q / dO are free for the next block
     }
     if (!ok) break;
-    // dV and alpha dK of the item's keys (key row tid)
+    // dV and alpha dK of the item's keys (key row = TMEM lane)
     tc_fence_after();
     {
-      const bool key_ok = tid < key_rows;
-      const size_t trow = ((size_t)(b.s0 + kBN * b.kt + tid) * a.heads + b.h) * D;
+      const bool key_ok = row < key_rows;
+      const size_t trow = ((size_t)(b.s0 + kBN * b.kt + row) * a.heads + b.h) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = wg; c < D / 32; c += 2) {
         uint32_t rv[32], rk[32];
         tmem_ld32(lane_tm + C::DV_COL + 32u * c, rv);
         tmem_ld32(lane_tm + C::DK_COL + 32u * c, rk);
