@@ -120,6 +120,21 @@ int make_map(CUtensorMap* m, const void* ptr, long long total, int heads, int d)
   return r == CUDA_SUCCESS ? HSTU_OK : HSTU_ERR_CUDA;
 }
 
+// fp32 (d, heads, total) view with box (32, 1, 128) and the 128-byte
+// swizzle: the backward's dQ accumulator, target of bulk reductions.
+int make_map_f32(CUtensorMap* m, const void* ptr, long long total, int heads, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return HSTU_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)total};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 4u, (cuuint64_t)heads * (cuuint64_t)d * 4u};
+  const cuuint32_t box[3] = {32u, 1u, (cuuint32_t)HSTU_BLOCK_M};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
 int device_check(int* sm_count) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return HSTU_ERR_CUDA;
@@ -476,11 +491,12 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   int sms = 0;
   int rc = device_check(&sms);
   if (rc != HSTU_OK) return rc;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if ((rc = make_map(&tq, q, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map(&tk, k, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map(&tv, v, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map(&tdo, dout, total, heads, d)) != HSTU_OK) return rc;
+  if ((rc = make_map_f32(&tdq, dq_acc, total, heads, d)) != HSTU_OK) return rc;
   hstu::BwdArgs a;
   a.items = d_items;
   a.n_items = n_items;
@@ -496,7 +512,7 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   // the accumulator starts at zero on the stream, before the kernel
   if (cudaMemsetAsync(dq_acc, 0, (size_t)total * heads * d * sizeof(float), stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
-  const cudaError_t e = hstu::launch_bwd(d, tq, tk, tv, tdo, a, grid_for(n_items, sms), stream);
+  const cudaError_t e = hstu::launch_bwd(d, tq, tk, tv, tdo, tdq, a, grid_for(n_items, sms), stream);
   if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
     return HSTU_ERR_UNSUPPORTED;
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;

@@ -24,7 +24,8 @@
 //   5. dK += dS^T Q (as step 3) and dQ_part = dS K (the tile read as a
 //      K-major A operand, K as an MN-major B), dQ_part over S in TMEM.
 //   6. dQ_part * alpha is added into an fp32 accumulator in global memory
-//      (vector atomics): query block qt gets one part per key block.
+//      by bulk tensor reductions from a shared staging tile: query block qt
+//      gets one part per key block.
 // At the item's end dV and alpha dK leave TMEM as bf16.  The P and dS
 // splits keep the products' error at the bf16 output rounding, as in the
 // forward.  Where shared memory has room (d <= 64) P and dS have tiles of
@@ -59,17 +60,22 @@ struct BCfg {
   static constexpr int DHI_OFF = MERGED ? LO_OFF + PTILEB : HI_OFF;  // dS tiles
   static constexpr int DLO_OFF = MERGED ? DHI_OFF + PTILEB : LO_OFF;
   static constexpr int BAR_OFF = (MERGED ? DLO_OFF : LO_OFF) + PTILEB;
-  static constexpr int B_KV = 0, B_QD = 1 /* [QB] */, B_MMA = 1 + QB, B_DRAIN = 2 + QB,
-                       NBARS = 3 + QB;
+  // S / dP done; the other products done; drain
+  static constexpr int B_KV = 0, B_QD = 1 /* [QB] */, B_SDP = 1 + QB, B_PROD = 2 + QB,
+                       B_DRAIN = 3 + QB, NBARS = 4 + QB;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int SMEM = ((USED + 1023) / 1024) * 1024 + 1024;  // + realignment slack
   // more than half an SM's shared memory: one CTA (and one TMEM allocation) per SM
   static constexpr int SMEM_LAUNCH = SMEM < 120 * 1024 ? 120 * 1024 : SMEM;
   static_assert(SMEM <= 232448, "shared memory budget");
-  // TMEM columns: S (then dQ_part) at 0, dP at 128, dV at 256, dK at 256 + D
+  // TMEM columns: S at 0, dP at 128, dV at 256, dK at 256 + D, dQ_part at
+  // 256 + 2 D where TMEM has room (d <= 64; the next block's S and dP then
+  // run under the dQ staging), else over S
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+  static constexpr uint32_t DQ_COL = 256 + 3 * D <= (int)kTmemCols ? 256 + 2 * D : 0;
   static_assert(256 + 2 * D <= (int)kTmemCols, "TMEM budget");
+  static_assert(!MERGED || DQ_COL != 0, "the pipelined path keeps dQ_part apart from S");
 };
 
 // Two warpgroups: warps w and w + 4 share TMEM lanes 32 (w % 4) ..; each
@@ -97,7 +103,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     hstu_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -120,6 +126,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_do)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_dq)) : "memory");
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint64_t dhi_kmaj = smem_desc(base + C::DHI_OFF, 16, 1024, 2);
   const uint64_t dlo_kmaj = smem_desc(base + C::DLO_OFF, 16, 1024, 2);
 
-  uint32_t ph_kv = 0, ph_qd[2] = {0, 0}, ph_mma = 0;
+  uint32_t ph_kv = 0, ph_qd[2] = {0, 0}, ph_sdp = 0, ph_prod = 0;
   uint32_t qiter = 0;  // query blocks done by this CTA: buffer qiter % QB
   bool ok = true;
   // every thread waits (bounded); the CTA continues only if all succeeded
@@ -198,9 +205,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t ad = tile_k + (uint64_t)(((kk >> 2) * C::PCHUNKB + (kk & 3) * 32) >> 4);
       const uint64_t b2 = k_mn + (uint64_t)((kk * 2 * C::ATOMB) >> 4);
       if (first && kk == 0)
-        mma_ss_c<0>(tmem + C::S_COL, ad, b2, IDESC_DQ);
+        mma_ss_c<0>(tmem + C::DQ_COL, ad, b2, IDESC_DQ);
       else
-        mma_ss_c<1>(tmem + C::S_COL, ad, b2, IDESC_DQ);
+        mma_ss_c<1>(tmem + C::DQ_COL, ad, b2, IDESC_DQ);
     }
   };
   // Element (row r = tid, key c) of the current block pair is kept.
@@ -236,33 +243,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       load_tile(&tm_q, C::Q_OFF + qb * C::TILEB, C::B_QD + qb, b.h, b.s0 + kBM * qt);
       load_tile(&tm_do, C::DO_OFF + qb * C::TILEB, C::B_QD + qb, b.h, b.s0 + kBM * qt);
     };
-    if (tid == 0) load_qd((int)(qiter % C::QB), b.kt);
-    if (!(ok = wait_all(C::B_KV, ph_kv, kSiteKFull))) break;
-    for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
-      const bool first = qt == b.kt;
-      const int qb = (int)(qiter % C::QB);
-      // the next query block's Q and dO into the other buffer: its last
-      // readers (the previous block's products) are done
-      if (C::QB == 2 && tid == 0 && qt + 1 < nq) load_qd(qb ^ 1, qt + 1);
-      if (!(ok = wait_all(C::B_QD + qb, ph_qd[qb], kSiteQFull))) break;
-      const uint64_t q_kmaj = buf_desc(q_kmaj0, qb), do_kmaj = buf_desc(do_kmaj0, qb);
-      const uint64_t q_mn = buf_desc(q_mn0, qb), do_mn = buf_desc(do_mn0, qb);
-      if (tid == 0) {
-        tc_fence_after();
-        mma_xyt(C::S_COL, q_kmaj, k_kmaj);
-        mma_xyt(C::DP_COL, do_kmaj, v_kmaj);
-        mma_commit(bar(C::B_MMA));
+    // row tid of query block qt sees key c of block kt iff both exist and
+    // the key is not after the row
+    auto mask_of = [&](int qt, int& cmax, bool& row_ok) {
+      const int row_i = kBM * qt + row;    // sequence-local query
+      const int lim = row_i - kBN * b.kt;  // keys c <= lim are not after the row
+      cmax = key_rows < lim + 1 ? key_rows : lim + 1;  // kept keys: c < cmax
+      row_ok = row_i < b.n;
+    };
+    // alpha dQ_part of block qt (TMEM columns DQ_COL) staged over the P
+    // tiles as 128B-swizzled fp32 boxes of 32 columns, then added into the
+    // accumulator by bulk tensor reductions.  Rows past the sequence carry
+    // dS = 0, so their parts are exactly zero; rows past the tensor are
+    // clipped by the copy.
+    auto put_dq = [&](int qt) {
+#pragma unroll 1
+      for (int c = wg; c < D / 32; c += 2) {
+        uint32_t r[32];
+        tmem_ld32(lane_tm + C::DQ_COL + 32u * c, r);
+        uint8_t* box = smem + C::HI_OFF + c * (kBM * 128);
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<float4*>(box + row * 128 + ((g ^ (row & 7)) << 4)) =
+              make_float4(alpha * __uint_as_float(r[4 * g]), alpha * __uint_as_float(r[4 * g + 1]),
+                          alpha * __uint_as_float(r[4 * g + 2]), alpha * __uint_as_float(r[4 * g + 3]));
       }
-      if (!(ok = wait_all(C::B_MMA, ph_mma, kSiteSFull))) break;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          asm volatile(
+              "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+              " [%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(&tm_dq)),
+              "r"(32 * c), "r"(b.h), "r"(b.s0 + kBM * qt), "r"(base + C::HI_OFF + c * (kBM * 128))
+              : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    };
+    auto issue_sdp = [&](int qb) {
       tc_fence_after();
-      // row tid of query block qt sees key c of block kt iff both exist and
-      // the key is not after the row
-      const int row_i = kBM * qt + row;               // sequence-local query
-      const int lim = row_i - kBN * b.kt;             // keys c <= lim are not after the row
-      const int cmax = key_rows < lim + 1 ? key_rows : lim + 1;  // kept keys: c < cmax
-      const bool row_ok = row_i < b.n;
-      if constexpr (C::MERGED) {
-        // 2-4. P and dS in one pass over this warpgroup's two 32-key chunks
+      mma_xyt(C::S_COL, buf_desc(q_kmaj0, qb), k_kmaj);
+      mma_xyt(C::DP_COL, buf_desc(do_kmaj0, qb), v_kmaj);
+      mma_commit(bar(C::B_SDP));
+    };
+    if constexpr (C::MERGED) {
+      // Pipelined: while block qt's products run, block qt + 1's S and dP
+      // follow them on the tensor cores, and the threads stage qt's dQ.
+      const int qb0 = (int)(qiter % C::QB);
+      if (tid == 0) {
+        load_qd(qb0, b.kt);
+        if (b.kt + 1 < nq) load_qd(qb0 ^ 1, b.kt + 1);
+      }
+      if (!(ok = wait_all(C::B_KV, ph_kv, kSiteKFull))) break;
+      if (tid == 0 && (ok = wait_one(bar(C::B_QD + qb0), ph_qd[qb0], w, kSiteQFull))) {
+        ph_qd[qb0] ^= 1u;
+        issue_sdp(qb0);
+      }
+      for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
+        const bool first = qt == b.kt;
+        const int qb = (int)(qiter % C::QB);
+        // the previous block's dQ reductions have read their staging (the P
+        // tiles, rewritten below)
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        if (!(ok = wait_all(C::B_SDP, ph_sdp, kSiteSFull))) break;
+        tc_fence_after();
+        int cmax;
+        bool row_ok;
+        mask_of(qt, cmax, row_ok);
+        // P and dS in one pass over this warpgroup's two 32-key chunks
 #pragma unroll 1
         for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
           uint32_t sr[32], pr[32];
@@ -287,105 +337,112 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
-        __syncthreads();
-        // 3 and 5. every product of the block at once
+        __syncthreads();  // S and dP read, the tiles written
         if (tid == 0) {
           tc_fence_after();
+          const uint64_t q_mn = buf_desc(q_mn0, qb), do_mn = buf_desc(do_mn0, qb);
           mma_tt(C::DV_COL, hi_mn, do_mn, first);
           mma_tt(C::DV_COL, lo_mn, do_mn, false);
           mma_tt(C::DK_COL, dhi_mn, q_mn, first);
           mma_tt(C::DK_COL, dlo_mn, q_mn, false);
           mma_dq(dhi_kmaj, true);
           mma_dq(dlo_kmaj, false);
-          mma_commit(bar(C::B_MMA));
-        }
-      } else {
-      // 2. P (this warpgroup's two 32-key chunks)
-#pragma unroll 1
-      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = 32 * c + 8 * g + e;
-            const float x = alpha * __uint_as_float(sr[8 * g + e]);
-            const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-            v[e] = (row_ok && col < cmax) ? inv_n * x * sg : 0.0f;
+          mma_commit(bar(C::B_PROD));
+          // the next block's S and dP, once its Q and dO have landed
+          if (qt + 1 < nq && (ok = wait_one(bar(C::B_QD + (qb ^ 1)), ph_qd[qb ^ 1], w, kSiteQFull))) {
+            ph_qd[qb ^ 1] ^= 1u;
+            issue_sdp(qb ^ 1);
           }
-          put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, v);
         }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      __syncthreads();
-      // 3. dV += P^T dO
-      if (tid == 0) {
+        if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteVFull))) break;
         tc_fence_after();
-        mma_tt(C::DV_COL, hi_mn, do_mn, first);
-        mma_tt(C::DV_COL, lo_mn, do_mn, false);
-        mma_commit(bar(C::B_MMA));
+        // buffer qb is free (its last readers were these products): the
+        // block after next loads into it
+        if (tid == 0 && qt + 2 < nq) load_qd(qb, qt + 2);
+        put_dq(qt);
       }
-      if (!(ok = wait_all(C::B_MMA, ph_mma, kSiteOFull))) break;
-      tc_fence_after();
-      // 4. dS
+    } else {
+      if (tid == 0) load_qd(0, b.kt);
+      if (!(ok = wait_all(C::B_KV, ph_kv, kSiteKFull))) break;
+      for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
+        const bool first = qt == b.kt;
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        if (!(ok = wait_all(C::B_QD, ph_qd[0], kSiteQFull))) break;
+        const uint64_t q_mn = buf_desc(q_mn0, 0), do_mn = buf_desc(do_mn0, 0);
+        if (tid == 0) issue_sdp(0);
+        if (!(ok = wait_all(C::B_SDP, ph_sdp, kSiteSFull))) break;
+        tc_fence_after();
+        int cmax;
+        bool row_ok;
+        mask_of(qt, cmax, row_ok);
+        // 2. P (this warpgroup's two 32-key chunks)
 #pragma unroll 1
-      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-        uint32_t sr[32], pr[32];
-        tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
-        tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float v[8];
+          for (int g = 0; g < 4; ++g) {
+            float v[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = 32 * c + 8 * g + e;
-            const float x = alpha * __uint_as_float(sr[8 * g + e]);
-            const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-            const float ds = inv_n * sg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[8 * g + e]);
-            v[e] = (row_ok && col < cmax) ? ds : 0.0f;
+            for (int e = 0; e < 8; ++e) {
+              const int col = 32 * c + 8 * g + e;
+              const float x = alpha * __uint_as_float(sr[8 * g + e]);
+              const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+              v[e] = (row_ok && col < cmax) ? inv_n * x * sg : 0.0f;
+            }
+            put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, v);
           }
-          put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, v);
         }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      __syncthreads();
-      // 5. dK += dS^T Q, dQ_part = dS K (over S: every thread has read it)
-      if (tid == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        // 3. dV += P^T dO
+        if (tid == 0) {
+          tc_fence_after();
+          mma_tt(C::DV_COL, hi_mn, do_mn, first);
+          mma_tt(C::DV_COL, lo_mn, do_mn, false);
+          mma_commit(bar(C::B_PROD));
+        }
+        if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteOFull))) break;
         tc_fence_after();
-        mma_tt(C::DK_COL, dhi_mn, q_mn, first);
-        mma_tt(C::DK_COL, dlo_mn, q_mn, false);
-        mma_dq(dhi_kmaj, true);
-        mma_dq(dlo_kmaj, false);
-        mma_commit(bar(C::B_MMA));
-      }
-      }  // the two-pass path
-      if (!(ok = wait_all(C::B_MMA, ph_mma, kSiteVFull))) break;
-      tc_fence_after();
-      // single buffer: Q and dO are free now; load the next block under the atomics
-      if (C::QB == 1 && tid == 0 && qt + 1 < nq) load_qd(0, qt + 1);
-      // 6. dQ += alpha dQ_part, for the rows that exist (32-column chunks
-      // alternate between the warpgroups)
+        // 4. dS, into the same tiles (the dV products are done)
 #pragma unroll 1
-      for (int c = wg; c < D / 32; c += 2) {
-        uint32_t r[32];
-        tmem_ld32(lane_tm + C::S_COL + 32u * c, r);
-        if (row_ok) {
-          float4* dst = reinterpret_cast<float4*>(
-              a.dq_acc + ((size_t)(b.s0 + row_i) * a.heads + b.h) * D + 32 * c);
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+          uint32_t sr[32], pr[32];
+          tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
+          tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
 #pragma unroll
-          for (int m = 0; m < 8; ++m)
-            atomicAdd(dst + m, make_float4(alpha * __uint_as_float(r[4 * m]),
-                                           alpha * __uint_as_float(r[4 * m + 1]),
-                                           alpha * __uint_as_float(r[4 * m + 2]),
-                                           alpha * __uint_as_float(r[4 * m + 3])));
+          for (int g = 0; g < 4; ++g) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int col = 32 * c + 8 * g + e;
+              const float x = alpha * __uint_as_float(sr[8 * g + e]);
+              const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+              const float ds = inv_n * sg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[8 * g + e]);
+              v[e] = (row_ok && col < cmax) ? ds : 0.0f;
+            }
+            put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, v);
+          }
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncthreads();
+        // 5. dK += dS^T Q, dQ_part = dS K (over S: every thread has read it)
+        if (tid == 0) {
+          tc_fence_after();
+          mma_tt(C::DK_COL, dhi_mn, q_mn, first);
+          mma_tt(C::DK_COL, dlo_mn, q_mn, false);
+          mma_dq(dhi_kmaj, true);
+          mma_dq(dlo_kmaj, false);
+          mma_commit(bar(C::B_PROD));
+        }
+        if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteVFull))) break;
+        tc_fence_after();
+        // 6. the single Q / dO buffer is free: the next block loads under the staging
+        if (tid == 0 && qt + 1 < nq) load_qd(0, qt + 1);
+        put_dq(qt);
       }
-      tc_fence_before();
-      __syncthreads();  // S, dP, the tiles and Q / dO are free for the next block
     }
     if (!ok) break;
     // dV and alpha dK of the item's keys (key row = TMEM lane)
@@ -424,6 +481,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mma_commit(bar(C::B_DRAIN));
     wait_drain(bar(C::B_DRAIN), 0);
   }
+  // the last reductions have finished before the CTA (and its shared memory) goes
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -446,12 +505,14 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* acc, uint1
 
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                         cudaStream_t stream) {
   using C = BCfg<D>;
+  static_assert(D / 32 * kBM * 128 <= 2 * C::PTILEB, "dQ staging fits the P tiles");
   cudaError_t e = cudaFuncSetAttribute(hstu_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_LAUNCH);
   if (e != cudaSuccess) return e;
-  hstu_bwd_kernel<D><<<grid, kBwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, tdo, a);
+  hstu_bwd_kernel<D><<<grid, kBwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, tdo, tdq, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long n8 = a.total * a.heads * D / 8;
   const int cgrid = (int)std::min<long long>((n8 + 255) / 256, 4LL * 1024);

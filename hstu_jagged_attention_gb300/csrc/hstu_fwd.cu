@@ -1409,11 +1409,12 @@ int fwd_smem_bytes(int d) {
 int fwd_swizzle_bytes(int d) { return d >= 64 ? 128 : 64; }
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                       cudaStream_t stream) {
   switch (d) {
-    case 32: return launch_bwd_d<32>(tq, tk, tv, tdo, a, grid, stream);
-    case 64: return launch_bwd_d<64>(tq, tk, tv, tdo, a, grid, stream);
-    case 128: return launch_bwd_d<128>(tq, tk, tv, tdo, a, grid, stream);
+    case 32: return launch_bwd_d<32>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case 64: return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    case 128: return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, a, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

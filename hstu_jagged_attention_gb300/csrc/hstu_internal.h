@@ -94,9 +94,11 @@ struct BwdArgs {
 // head, kt ascending.
 void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst);
 // The backward kernel for head dimension d on `grid` CTAs, then the dQ
-// conversion; tdo describes dout like q.
+// conversion; tdo describes dout like q, tdq the fp32 accumulator as
+// (d, heads, total) with box (32, 1, 128) and the 128-byte swizzle.
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, int grid, cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                       cudaStream_t stream);
 
 // Test hook: the MMA warp first waits on a barrier nothing signals.
 constexpr unsigned kDebugUnsignalledWait = 1u;
