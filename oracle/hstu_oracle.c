@@ -340,6 +340,26 @@ typedef struct {
     double *dq, *dk, *dv;
 } bwd_job_t;
 
+/* The terms of pair (i, j) (sequence-local, kept): P_ij and ds_ij. */
+static void bwd_terms(const job_t* J, const float* dout, int64_t s0, int64_t hist, int h,
+                      int64_t i, int64_t j, double* p_out, double* ds_out) {
+    const int d = J->d, heads = J->heads;
+    const float* qi = J->q + ((s0 + i) * heads + h) * (int64_t)d;
+    const float* doi = dout + ((s0 + i) * heads + h) * (int64_t)d;
+    const float* kj = J->k + ((s0 + j) * heads + h) * (int64_t)d;
+    const float* vj = J->v + ((s0 + j) * heads + h) * (int64_t)d;
+    double dot = 0.0, dp = 0.0;
+    for (int c = 0; c < d; ++c) {
+        dot += (double)qi[c] * (double)kj[c];
+        dp += (double)doi[c] * (double)vj[c];
+    }
+    const double bias = J->rab ? rab_bias(J->rab, s0, i, j, hist) : 0.0;
+    const double x = J->alpha * dot + bias;
+    const double sg = sigmoid(x);
+    *p_out = J->inv_n * x * sg;
+    *ds_out = J->inv_n * sg * (1.0 + x * (1.0 - sg)) * dp;
+}
+
 static void bwd_seq_head(const bwd_job_t* B, int b, int h) {
     const job_t* J = &B->base;
     const int64_t s0 = J->offsets[b], n = J->offsets[b + 1] - s0;
@@ -354,19 +374,10 @@ static void bwd_seq_head(const bwd_job_t* B, int b, int h) {
             if (!kept(i, j, hist)) continue;
             const int64_t tj = s0 + j;
             const float* kj = J->k + (tj * heads + h) * (int64_t)d;
-            const float* vj = J->v + (tj * heads + h) * (int64_t)d;
             double* dkj = B->dk + (tj * heads + h) * (int64_t)d;
             double* dvj = B->dv + (tj * heads + h) * (int64_t)d;
-            double dot = 0.0, dp = 0.0;
-            for (int c = 0; c < d; ++c) {
-                dot += (double)qi[c] * (double)kj[c];
-                dp += (double)doi[c] * (double)vj[c];
-            }
-            const double bias = J->rab ? rab_bias(J->rab, s0, i, j, hist) : 0.0;
-            const double x = J->alpha * dot + bias;
-            const double sg = sigmoid(x);
-            const double p = J->inv_n * x * sg;
-            const double ds = J->inv_n * sg * (1.0 + x * (1.0 - sg)) * dp;
+            double p, ds;
+            bwd_terms(J, B->dout, s0, hist, h, i, j, &p, &ds);
             for (int c = 0; c < d; ++c) {
                 dvj[c] += p * (double)doi[c];
                 dqi[c] += J->alpha * ds * (double)kj[c];
@@ -388,6 +399,51 @@ static void* worker_bwd(void* arg) {
         bwd_seq_head(B, (int)(u / J->heads), (int)(u % J->heads));
     }
     return NULL;
+}
+
+/* Sampled gradient rows: for token t = rows_t[r], head h = rows_h[r],
+ *   dq[r] = alpha sum_{j: kept(i, j)} ds_ij k_j        (i = t's position)
+ *   dk[r] = alpha sum_{i: kept(i, j)} ds_ij q_i        (j = t's position)
+ *   dv[r] = sum_{i: kept(i, j)} P_ij do_i
+ * each (nrows, d): the same terms as the full backward, summed one row at a
+ * time.  Causal, no bias. */
+int hstu_oracle_bwd_rows_f64(const float* q, const float* k, const float* v, const float* dout,
+                             const int64_t* offsets, int batch, int heads, int d, double alpha,
+                             double inv_n, const int64_t* rows_t, const int32_t* rows_h,
+                             int64_t nrows, double* dq, double* dk, double* dv) {
+    if (check_offsets(offsets, batch) || heads < 1 || d < 1 || nrows < 0) return -1;
+    job_t J = {q, k, v, offsets, NULL, NULL, batch, heads, d, alpha, inv_n, NULL, NULL, NULL, 0,
+               NULL, NULL};
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t t = rows_t[r];
+        const int h = rows_h[r];
+        const int b = seq_of(offsets, batch, t);
+        if (b < 0 || h < 0 || h >= heads) return -1;
+        const int64_t s0 = offsets[b], n = offsets[b + 1] - s0, pos = t - s0;
+        double* dqr = dq + r * (int64_t)d;
+        double* dkr = dk + r * (int64_t)d;
+        double* dvr = dv + r * (int64_t)d;
+        for (int c = 0; c < d; ++c) dqr[c] = dkr[c] = dvr[c] = 0.0;
+        for (int64_t j = 0; j < n; ++j) {  /* keys of row pos */
+            if (!kept(pos, j, n)) continue;
+            double p, ds;
+            bwd_terms(&J, dout, s0, n, h, pos, j, &p, &ds);
+            const float* kj = k + ((s0 + j) * heads + h) * (int64_t)d;
+            for (int c = 0; c < d; ++c) dqr[c] += alpha * ds * (double)kj[c];
+        }
+        for (int64_t i = 0; i < n; ++i) {  /* rows that see key pos */
+            if (!kept(i, pos, n)) continue;
+            double p, ds;
+            bwd_terms(&J, dout, s0, n, h, i, pos, &p, &ds);
+            const float* qi = q + ((s0 + i) * heads + h) * (int64_t)d;
+            const float* doi = dout + ((s0 + i) * heads + h) * (int64_t)d;
+            for (int c = 0; c < d; ++c) {
+                dkr[c] += alpha * ds * (double)qi[c];
+                dvr[c] += p * (double)doi[c];
+            }
+        }
+    }
+    return 0;
 }
 
 /* dq, dk, dv: fp64 (total, heads, d), written (zeroed here first).

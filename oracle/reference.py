@@ -80,6 +80,10 @@ def _load():
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, ctypes.c_double, d, d, d, ctypes.c_int]
         lib.hstu_oracle_bwd_f64.restype = ctypes.c_int
+        lib.hstu_oracle_bwd_rows_f64.argtypes = [f, f, f, f, i64, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_double, ctypes.c_double, i64,
+                                                 i32, ctypes.c_int64, d, d, d]
+        lib.hstu_oracle_bwd_rows_f64.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -276,6 +280,28 @@ def hstu_bwd(q, k, v, dout, offsets, alpha: float, inv_n: float, threads: int | 
                                      batch, heads, d, float(alpha), float(inv_n),
                                      _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
                                      _ptr(dv, ctypes.c_double), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return dq, dk, dv
+
+
+def hstu_bwd_rows(q, k, v, dout, offsets, alpha: float, inv_n: float, rows_t, rows_h):
+    """Sampled gradient rows (causal, no bias): for row r = (token rows_t[r],
+    head rows_h[r]) the fp64 dq, dk, dv rows, each (nrows, d)."""
+    qf, kf, vf, df = _f32(q), _f32(k), _f32(v), _f32(dout)
+    total, heads, d = qf.shape
+    off = np.ascontiguousarray(np.asarray(offsets), dtype=np.int64)
+    rt = np.ascontiguousarray(rows_t, dtype=np.int64)
+    rh = np.ascontiguousarray(rows_h, dtype=np.int32)
+    if rt.shape != rh.shape:
+        raise ValueError("rows_t and rows_h differ in length")
+    dq, dk, dv = (np.zeros((len(rt), d), dtype=np.float64) for _ in range(3))
+    rc = _load().hstu_oracle_bwd_rows_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
+                                          _ptr(vf, ctypes.c_float), _ptr(df, ctypes.c_float),
+                                          _ptr(off, ctypes.c_int64), len(off) - 1, heads, d,
+                                          float(alpha), float(inv_n), _ptr(rt, ctypes.c_int64),
+                                          _ptr(rh, ctypes.c_int32), len(rt), _ptr(dq, ctypes.c_double),
+                                          _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return dq, dk, dv

@@ -94,3 +94,30 @@ def test_bwd_plan_equals_one_shot():
     assert torch.equal(g[1], a[1]) and torch.equal(g[2], a[2])
     assert (g[0].float() - a[0].float()).abs().max().item() <= 1e-2 * a[0].float().abs().max().item()
     parity.assert_device_ok()
+
+
+def test_bwd_dense_workload_sampled():
+    # full size, in the launch configuration the benchmark times (a plan)
+    w = workloads.workload("dense")
+    q, k, v = workloads.draw_qkv(w)
+    rng = np.random.default_rng(4000 + w.index)
+    do = workloads.bf16_round(rng.standard_normal(q.shape).astype(np.float32))
+    qd, kd, vd, dod = (t.to("cuda").contiguous() for t in (q, k, v, do))
+    g = [torch.empty_like(qd) for _ in range(3)]
+    plan = binding.hstu_plan_create_ex(w.offsets, None, w.batch, w.heads, w.d, w.max_seqlen,
+                                       binding.HSTU_PLAN_BACKWARD)
+    try:
+        binding.hstu_attn_bwd_plan(plan, qd, kd, vd, dod, w.alpha, w.inv_n, *g)
+        torch.cuda.synchronize()
+    finally:
+        binding.hstu_plan_destroy(plan)
+    parity.assert_device_ok()
+    rt, rh, nu = parity.sample_rows(w, 192, seed=7)
+    refs = reference.hstu_bwd_rows(q, k, v, do, w.offsets, w.alpha, w.inv_n, rt, rh)
+    idx_t, idx_h = torch.as_tensor(rt, device="cuda"), torch.as_tensor(rh, device="cuda")
+    for name, gt, rf in zip(("dq", "dk", "dv"), g, refs):
+        got = gt[idx_t, idx_h].float().cpu().numpy().astype(np.float64)
+        rms = float(np.sqrt(np.mean(rf[:nu] ** 2)))
+        assert np.all(np.isfinite(got)), name
+        worst = parity.ratio(got, rf, rms).max()
+        assert worst <= 1.0, f"{name}: worst err/tol {worst:.3f}"

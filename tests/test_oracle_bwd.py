@@ -127,3 +127,14 @@ def test_bias_gradients_by_finite_differences():
             lp = _loss(*(xp if n == name else args[n] for n in "qkv"), do, off, 0.6, 0.2, [3, 2], rab)
             lm = _loss(*(xm if n == name else args[n] for n in "qkv"), do, off, 0.6, 0.2, [3, 2], rab)
             assert abs((lp - lm) / h - g[idx]) <= 1e-5 * max(1.0, abs(g[idx])), (name, idx)
+
+
+def test_sampled_rows_match_the_full_backward():
+    rng = np.random.default_rng(12)
+    q, k, v, do, off = _case(rng, [50, 3, 90, 1], 2, 8)
+    full = reference.hstu_bwd(q, k, v, do, off, 0.5, 0.1)
+    rows_t = np.array([0, 29, 49, 50, 52, 53, 100, 142, 143])
+    rows_h = np.array([0, 1, 1, 0, 1, 0, 1, 0, 1])
+    got = reference.hstu_bwd_rows(q, k, v, do, off, 0.5, 0.1, rows_t, rows_h)
+    for g, f in zip(got, full):
+        np.testing.assert_allclose(g, f[rows_t, rows_h], rtol=1e-12, atol=1e-15)

@@ -273,7 +273,7 @@ def test_rab_mutant_is_caught(tmp_path, name):
 # ------------------------------------------------ the backward pass
 BWD_MUTANTS = {
     "silu_derivative_first_term_only": ("sg * (1.0 + x * (1.0 - sg)) * dp", "sg * dp"),
-    "dv_without_inv_n": ("const double p = J->inv_n * x * sg;", "const double p = x * sg;"),
+    "dv_without_inv_n": ("*p_out = J->inv_n * x * sg;", "*p_out = x * sg;"),
     "dk_from_k": ("dkj[c] += J->alpha * ds * (double)qi[c];", "dkj[c] += J->alpha * ds * (double)kj[c];"),
     "dq_without_alpha": ("dqi[c] += J->alpha * ds * (double)kj[c];", "dqi[c] += ds * (double)kj[c];"),
     "dp_from_q": ("dp += (double)doi[c] * (double)vj[c];", "dp += (double)doi[c] * (double)qi[c];"),
