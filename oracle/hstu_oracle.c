@@ -91,10 +91,17 @@ int hstu_oracle_rab_bucket(int64_t delta, int nbuckets) {
     return b < nbuckets - 1 ? b : nbuckets - 1;
 }
 
-static double rab_bias(const rab_t* R, int64_t seq_start, int64_t i, int64_t j, int64_t hist) {
+/* The position and time buckets of pair (i, j) (sequence-local). */
+static void rab_buckets(const rab_t* R, int64_t seq_start, int64_t i, int64_t j, int64_t hist,
+                        int* bp, int* bt) {
     const int64_t pi = i < hist ? i : hist, pj = j < hist ? j : hist;
-    const int bp = hstu_oracle_rab_bucket(pi - pj, R->npos);
-    const int bt = hstu_oracle_rab_bucket(R->ts[seq_start + i] - R->ts[seq_start + j], R->ntime);
+    *bp = hstu_oracle_rab_bucket(pi - pj, R->npos);
+    *bt = hstu_oracle_rab_bucket(R->ts[seq_start + i] - R->ts[seq_start + j], R->ntime);
+}
+
+static double rab_bias(const rab_t* R, int64_t seq_start, int64_t i, int64_t j, int64_t hist) {
+    int bp, bt;
+    rab_buckets(R, seq_start, i, j, hist, &bp, &bt);
     return (double)R->pos[bp] + (double)R->time[bt];
 }
 
@@ -338,6 +345,7 @@ typedef struct {
     job_t base;          /* q, k, v, offsets, num_targets, rab, batch, heads, d, alpha, inv_n */
     const float* dout;   /* (total, heads, d) */
     double *dq, *dk, *dv;
+    double *dpos, *dtime; /* the bias tables' gradients (npos, ntime), or NULL */
 } bwd_job_t;
 
 /* The terms of pair (i, j) (sequence-local, kept): P_ij and ds_ij. */
@@ -360,7 +368,11 @@ static void bwd_terms(const job_t* J, const float* dout, int64_t s0, int64_t his
     *ds_out = J->inv_n * sg * (1.0 + x * (1.0 - sg)) * dp;
 }
 
-static void bwd_seq_head(const bwd_job_t* B, int b, int h) {
+/* The bias tables' gradients: x_ij = alpha q_i.k_j + pos[bp] + time[bt], so
+ * d pos[b] = sum of ds_ij over the kept pairs (all heads) whose position
+ * bucket is b, and d time likewise by time bucket.  gp, gt: this worker's
+ * partial sums. */
+static void bwd_seq_head(const bwd_job_t* B, int b, int h, double* gp, double* gt) {
     const job_t* J = &B->base;
     const int64_t s0 = J->offsets[b], n = J->offsets[b + 1] - s0;
     const int64_t hist = hist_of(J, b);
@@ -378,6 +390,12 @@ static void bwd_seq_head(const bwd_job_t* B, int b, int h) {
             double* dvj = B->dv + (tj * heads + h) * (int64_t)d;
             double p, ds;
             bwd_terms(J, B->dout, s0, hist, h, i, j, &p, &ds);
+            if (gp) {
+                int bp, bt;
+                rab_buckets(J->rab, s0, i, j, hist, &bp, &bt);
+                gp[bp] += ds;
+                gt[bt] += ds;
+            }
             for (int c = 0; c < d; ++c) {
                 dvj[c] += p * (double)doi[c];
                 dqi[c] += J->alpha * ds * (double)kj[c];
@@ -393,10 +411,23 @@ static void* worker_bwd(void* arg) {
     bwd_job_t* B = (bwd_job_t*)arg;
     job_t* J = &B->base;
     const int64_t units = (int64_t)J->batch * J->heads;
+    double *gp = NULL, *gt = NULL;
+    if (B->dpos) {
+        gp = (double*)calloc((size_t)J->rab->npos, sizeof(double));
+        gt = (double*)calloc((size_t)J->rab->ntime, sizeof(double));
+    }
     for (;;) {
         const int64_t u = take(J, 1);
         if (u >= units) break;
-        bwd_seq_head(B, (int)(u / J->heads), (int)(u % J->heads));
+        bwd_seq_head(B, (int)(u / J->heads), (int)(u % J->heads), gp, gt);
+    }
+    if (gp) { /* this worker's table sums into the totals */
+        pthread_mutex_lock(J->mu);
+        for (int e = 0; e < J->rab->npos; ++e) B->dpos[e] += gp[e];
+        for (int e = 0; e < J->rab->ntime; ++e) B->dtime[e] += gt[e];
+        pthread_mutex_unlock(J->mu);
+        free(gp);
+        free(gt);
     }
     return NULL;
 }
@@ -448,12 +479,13 @@ int hstu_oracle_bwd_rows_f64(const float* q, const float* k, const float* v, con
 
 /* dq, dk, dv: fp64 (total, heads, d), written (zeroed here first).
  * num_targets and the rab arguments as hstu_oracle_fwd_rab_f64 (ts NULL:
- * no bias). */
+ * no bias); with the bias, dpos and dtime (npos, ntime; may be NULL)
+ * receive the tables' gradients. */
 int hstu_oracle_bwd_f64(const float* q, const float* k, const float* v, const float* dout,
                         const int64_t* offsets, const int64_t* num_targets, const int64_t* ts,
                         const float* pos, int npos, const float* time, int ntime, int batch,
                         int heads, int d, double alpha, double inv_n, double* dq, double* dk,
-                        double* dv, int nthreads) {
+                        double* dv, double* dpos, double* dtime, int nthreads) {
     if (check_offsets(offsets, batch) || (num_targets && check_targets(offsets, num_targets, batch)) ||
         heads < 1 || d < 1 || (ts && (npos < 1 || ntime < 1)))
         return -1;
@@ -468,6 +500,12 @@ int hstu_oracle_bwd_f64(const float* q, const float* k, const float* v, const fl
     B.dq = dq;
     B.dk = dk;
     B.dv = dv;
+    B.dpos = ts ? dpos : NULL;
+    B.dtime = ts ? dtime : NULL;
+    if (B.dpos) {
+        for (int e = 0; e < npos; ++e) dpos[e] = 0.0;
+        for (int e = 0; e < ntime; ++e) dtime[e] = 0.0;
+    }
     /* run() hands each worker the job pointer; the job is the first member */
     return run(&B.base, nthreads, worker_bwd);
 }

@@ -78,7 +78,8 @@ def _load():
         lib.hstu_oracle_rows_rab_f64.restype = ctypes.c_int
         lib.hstu_oracle_bwd_f64.argtypes = [f, f, f, f, i64, i64, i64, f, ctypes.c_int, f,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_double, ctypes.c_double, d, d, d, ctypes.c_int]
+                                            ctypes.c_double, ctypes.c_double, d, d, d, d, d,
+                                            ctypes.c_int]
         lib.hstu_oracle_bwd_f64.restype = ctypes.c_int
         lib.hstu_oracle_bwd_rows_f64.argtypes = [f, f, f, f, i64, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_double, ctypes.c_double, i64,
@@ -255,10 +256,12 @@ def hstu_rows_norm_gate(q, k, v, u, gamma, beta, eps: float, offsets, alpha: flo
 
 
 def hstu_bwd(q, k, v, dout, offsets, alpha: float, inv_n: float, threads: int | None = None,
-             num_targets=None, rab=None):
+             num_targets=None, rab=None, table_grads: bool = False):
     """Gradients of sum(out * dout) with respect to q, k, v: fp64 arrays
     (total, heads, d) each (HSTU paper Appendix G: the backward of the
-    forward definition; the chain rule is written out in hstu_oracle.c)."""
+    forward definition; the chain rule is written out in hstu_oracle.c).
+    With ``rab`` and ``table_grads``, also the bias tables' gradients:
+    returns (dq, dk, dv, dpos, dtime)."""
     qf, kf, vf, df = _f32(q), _f32(k), _f32(v), _f32(dout)
     total, heads, d = qf.shape
     off = np.ascontiguousarray(np.asarray(offsets), dtype=np.int64)
@@ -274,14 +277,18 @@ def hstu_bwd(q, k, v, dout, offsets, alpha: float, inv_n: float, threads: int | 
         tsp, posp, timep = _ptr(ts, ctypes.c_int64), _ptr(pos, ctypes.c_float), _ptr(time, ctypes.c_float)
         npos, ntime = pos.size, time.size
     dq, dk, dv = (np.zeros((total, heads, d), dtype=np.float64) for _ in range(3))
+    gpos = np.zeros(max(npos, 1)), np.zeros(max(ntime, 1))
     rc = _load().hstu_oracle_bwd_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
                                      _ptr(vf, ctypes.c_float), _ptr(df, ctypes.c_float),
                                      _ptr(off, ctypes.c_int64), ntp, tsp, posp, npos, timep, ntime,
                                      batch, heads, d, float(alpha), float(inv_n),
                                      _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
-                                     _ptr(dv, ctypes.c_double), threads or default_threads())
+                                     _ptr(dv, ctypes.c_double), _ptr(gpos[0], ctypes.c_double),
+                                     _ptr(gpos[1], ctypes.c_double), threads or default_threads())
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
+    if rab is not None and table_grads:
+        return dq, dk, dv, gpos[0][:npos], gpos[1][:ntime]
     return dq, dk, dv
 
 

@@ -138,3 +138,28 @@ def test_sampled_rows_match_the_full_backward():
     got = reference.hstu_bwd_rows(q, k, v, do, off, 0.5, 0.1, rows_t, rows_h)
     for g, f in zip(got, full):
         np.testing.assert_allclose(g, f[rows_t, rows_h], rtol=1e-12, atol=1e-15)
+
+
+def test_bias_table_gradients_by_finite_differences():
+    rng = np.random.default_rng(13)
+    q, k, v, do, off = _case(rng, [12, 9, 1], 2, 4)
+    ts = np.concatenate([np.cumsum(rng.integers(0, 3000, size=n)) for n in (12, 9, 1)]).astype(np.int64)
+    pos = (0.3 * rng.standard_normal(6)).astype(np.float32)
+    time = (0.3 * rng.standard_normal(12)).astype(np.float32)
+    nt = [3, 0, 0]
+    got = reference.hstu_bwd(q, k, v, do, off, 0.6, 0.2, num_targets=nt, rab=(ts, pos, time),
+                             table_grads=True)
+    dpos, dtime = got[3], got[4]
+    eps = 1e-3
+    for name, tab, g in (("pos", pos, dpos), ("time", time, dtime)):
+        for e in range(len(tab)):
+            tp, tm = tab.copy(), tab.copy()
+            tp[e] = np.float32(tab[e] + eps)
+            tm[e] = np.float32(tab[e] - eps)
+            h = float(tp[e]) - float(tm[e])
+            rp = (ts, tp, time) if name == "pos" else (ts, pos, tp)
+            rm = (ts, tm, time) if name == "pos" else (ts, pos, tm)
+            fd = (_loss(q, k, v, do, off, 0.6, 0.2, nt, rp) - _loss(q, k, v, do, off, 0.6, 0.2, nt, rm)) / h
+            assert abs(fd - g[e]) <= 1e-5 * max(1.0, abs(g[e])), (name, e, fd, g[e])
+    # buckets that no kept pair uses get exactly zero
+    assert np.count_nonzero(dpos) <= len(pos) and np.all(np.isfinite(dtime))

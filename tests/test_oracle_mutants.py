@@ -217,8 +217,8 @@ RAB_MUTANTS = {
     "candidates_keep_their_position": ("pi = i < hist ? i : hist", "pi = i"),
     "bias_scaled_by_alpha": ("hstu_oracle_silu(alpha * dot + bias)",
                              "hstu_oracle_silu(alpha * (dot + bias))"),
-    "time_table_by_position_bucket": ("(double)R->pos[bp] + (double)R->time[bt]",
-                                      "(double)R->pos[bp] + (double)R->time[bp < R->ntime ? bp : 0]"),
+    "time_table_by_position_bucket": ("return (double)R->pos[bp] + (double)R->time[bt];",
+                                      "return (double)R->pos[bp] + (double)R->time[bp < R->ntime ? bp : 0];"),
 }
 
 
@@ -287,7 +287,7 @@ def _bwd_pins_pass(L) -> bool:
                     ctypes.POINTER(ctypes.c_int64))
     L.hstu_oracle_bwd_f64.argtypes = [f, f, f, f, i64, i64, i64, f, ctypes.c_int, f, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                                      ctypes.c_double, dptr, dptr, dptr, ctypes.c_int]
+                                      ctypes.c_double, dptr, dptr, dptr, dptr, dptr, ctypes.c_int]
     P = lambda a, t: a.ctypes.data_as(ctypes.POINTER(t))
     rng = np.random.default_rng(31)
     q, k, v, do, off = _case(rng, [13, 20], 2, 8)
@@ -296,7 +296,7 @@ def _bwd_pins_pass(L) -> bool:
     L.hstu_oracle_bwd_f64(P(q, ctypes.c_float), P(k, ctypes.c_float), P(v, ctypes.c_float),
                           P(do, ctypes.c_float), P(off, ctypes.c_int64), None, None, None, 0, None, 0,
                           len(off) - 1, q.shape[1], q.shape[2], 0.4, 0.05,
-                          *(P(g, ctypes.c_double) for g in grads), 2)
+                          *(P(g, ctypes.c_double) for g in grads), None, None, 2)
     want = _dense_torch(q, k, v, do, off, 0.4, 0.05)
     return all(np.abs(g - w_).max() <= 1e-12 * max(1.0, np.abs(w_).max()) for g, w_ in zip(grads, want))
 
