@@ -437,14 +437,20 @@ static void* worker_bwd(void* arg) {
  *   dk[r] = alpha sum_{i: kept(i, j)} ds_ij q_i        (j = t's position)
  *   dv[r] = sum_{i: kept(i, j)} P_ij do_i
  * each (nrows, d): the same terms as the full backward, summed one row at a
- * time.  Causal, no bias. */
+ * time.  Causal; the rab arguments as hstu_oracle_fwd_rab_f64 (ts NULL: no
+ * bias). */
 int hstu_oracle_bwd_rows_f64(const float* q, const float* k, const float* v, const float* dout,
-                             const int64_t* offsets, int batch, int heads, int d, double alpha,
-                             double inv_n, const int64_t* rows_t, const int32_t* rows_h,
-                             int64_t nrows, double* dq, double* dk, double* dv) {
-    if (check_offsets(offsets, batch) || heads < 1 || d < 1 || nrows < 0) return -1;
-    job_t J = {q, k, v, offsets, NULL, NULL, batch, heads, d, alpha, inv_n, NULL, NULL, NULL, 0,
-               NULL, NULL};
+                             const int64_t* offsets, const int64_t* ts, const float* pos, int npos,
+                             const float* time, int ntime, int batch, int heads, int d,
+                             double alpha, double inv_n, const int64_t* rows_t,
+                             const int32_t* rows_h, int64_t nrows, double* dq, double* dk,
+                             double* dv) {
+    if (check_offsets(offsets, batch) || heads < 1 || d < 1 || nrows < 0 ||
+        (ts && (npos < 1 || ntime < 1)))
+        return -1;
+    const rab_t R = {ts, pos, npos, time, ntime};
+    job_t J = {q, k, v, offsets, NULL, ts ? &R : NULL, batch, heads, d, alpha, inv_n, NULL, NULL,
+               NULL, 0, NULL, NULL};
     for (int64_t r = 0; r < nrows; ++r) {
         const int64_t t = rows_t[r];
         const int h = rows_h[r];

@@ -140,6 +140,24 @@ def test_sampled_rows_match_the_full_backward():
         np.testing.assert_allclose(g, f[rows_t, rows_h], rtol=1e-12, atol=1e-15)
 
 
+def test_sampled_rows_with_the_bias_match_the_full_backward():
+    rng = np.random.default_rng(14)
+    q, k, v, do, off = _case(rng, [50, 3, 90, 1], 2, 8)
+    ts = np.concatenate([np.cumsum(rng.integers(-200, 3000, size=n)) for n in (50, 3, 90, 1)])
+    ts = (ts - ts.min()).astype(np.int64)
+    pos = (0.4 * rng.standard_normal(7)).astype(np.float32)
+    time = (0.4 * rng.standard_normal(20)).astype(np.float32)
+    full = reference.hstu_bwd(q, k, v, do, off, 0.5, 0.1, rab=(ts, pos, time))
+    plain = reference.hstu_bwd(q, k, v, do, off, 0.5, 0.1)
+    rows_t = np.array([0, 29, 49, 50, 52, 53, 100, 142, 143])
+    rows_h = np.array([0, 1, 1, 0, 1, 0, 1, 0, 1])
+    got = reference.hstu_bwd_rows(q, k, v, do, off, 0.5, 0.1, rows_t, rows_h, rab=(ts, pos, time))
+    for g, f, p in zip(got, full, plain):
+        np.testing.assert_allclose(g, f[rows_t, rows_h], rtol=1e-12, atol=1e-15)
+        # the bias changes the rows (it is not dropped)
+        assert np.abs(g - p[rows_t, rows_h]).max() > 1e-3 * np.abs(g).max()
+
+
 def test_bias_table_gradients_by_finite_differences():
     rng = np.random.default_rng(13)
     q, k, v, do, off = _case(rng, [12, 9, 1], 2, 4)
