@@ -75,17 +75,20 @@ def bwd_flops(w: workloads.Workload) -> float:
     return float(10.0 * w.d * w.heads * np.sum(L * (L + 1) / 2.0))
 
 
-def cpu_oracle_bwd_sample(w, q, k, v, do, target_s: float, threads: int | None = None):
+def cpu_oracle_bwd_sample(w, q, k, v, do, target_s: float, threads: int | None = None, rab=None):
     """The oracle's backward on the first sequences of the workload, as many
-    as fit about target_s seconds (calibrated on the first one)."""
+    as fit about target_s seconds (calibrated on the first one).  With the
+    bias ``rab`` = (timestamps, pos, time), the tables' gradients too."""
     from oracle import reference
     threads = threads or reference.default_threads()
     off = w.offsets.astype(np.int64)
 
     def run(nb):
         e = int(off[nb])
+        r = None if rab is None else (rab[0][:e], rab[1], rab[2])
         t0 = time.perf_counter()
-        reference.hstu_bwd(q[:e], k[:e], v[:e], do[:e], off[:nb + 1], w.alpha, w.inv_n, threads=threads)
+        reference.hstu_bwd(q[:e], k[:e], v[:e], do[:e], off[:nb + 1], w.alpha, w.inv_n, threads=threads,
+                           rab=r, table_grads=r is not None)
         return time.perf_counter() - t0
 
     nb = 1
@@ -282,7 +285,7 @@ def run_reference_bwd(args, w):
     vals = []
     desc, threads = "", 0
     for s_ in range(args.warmup + args.steps):
-        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, per_step_s)
+        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, per_step_s, rab=_cpu_rab(args, w))
         if s_ >= args.warmup:
             vals.append(val)
     value = statistics.mean(vals)
@@ -290,7 +293,7 @@ def run_reference_bwd(args, w):
         "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, **w.describe(), "pass": "backward"},
+        "config": {"workload": w.name, **w.describe(), "pass": "backward", **_rab_desc(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -380,14 +383,30 @@ def run_ours_bwd(args, w):
     do_h = workloads.bf16_round(rng.standard_normal(q_h.shape).astype(np.float32))
     q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     grads = [torch.empty_like(q) for _ in range(3)]
+    rab = tgrads = None
+    if args.rab:
+        # the timestamps are per-batch inputs (copied in every e2e step); the
+        # tables are parameters, resident on the device
+        rab_h = workloads.draw_rab(w)
+        ts_pin = torch.from_numpy(rab_h[0]).pin_memory()
+        rab = (ts_pin.to(dev), torch.from_numpy(rab_h[1]).to(dev), torch.from_numpy(rab_h[2]).to(dev))
+        tgrads = (torch.empty_like(rab[1]), torch.empty_like(rab[2]))
     plan = binding.hstu_plan_create_ex(w.offsets, None, w.batch, w.heads, w.d, w.max_seqlen,
                                        binding.HSTU_PLAN_BACKWARD)
+
+    def plan_call():
+        if rab is None:
+            binding.hstu_attn_bwd_plan(plan, q, k, v, do, w.alpha, w.inv_n, *grads, stream=stream)
+        else:
+            binding.hstu_attn_bwd_plan_ex(plan, q, k, v, do, w.alpha, w.inv_n, *grads, rab=rab,
+                                          dpos=tgrads[0], dtime=tgrads[1], stream=stream)
+
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
     t_warm = time.perf_counter()
     for _ in range(args.warmup):
-        binding.hstu_attn_bwd_plan(plan, q, k, v, do, w.alpha, w.inv_n, *grads, stream=stream)
+        plan_call()
     torch.cuda.synchronize(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -398,7 +417,7 @@ def run_ours_bwd(args, w):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        binding.hstu_attn_bwd_plan(plan, q, k, v, do, w.alpha, w.inv_n, *grads, stream=stream)
+        plan_call()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -416,12 +435,24 @@ def run_ours_bwd(args, w):
     ins = [torch.empty_like(q) for _ in range(4)]
     g2 = [torch.empty_like(q) for _ in range(3)]
     offsets_host = w.offsets.copy()
+    if rab is not None:
+        tse = torch.empty_like(rab[0])
+        tg_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in tgrads]
+        tg2 = [torch.empty_like(t) for t in tgrads]
 
     def e2e_step():
         for dst, src in zip(ins, pin):
             dst.copy_(src, non_blocking=True)
-        binding.hstu_attn_bwd(*ins, offsets_host, w.batch, w.heads, w.d, w.max_seqlen, w.alpha,
-                              w.inv_n, *g2, stream=stream)
+        if rab is None:
+            binding.hstu_attn_bwd(*ins, offsets_host, w.batch, w.heads, w.d, w.max_seqlen, w.alpha,
+                                  w.inv_n, *g2, stream=stream)
+        else:
+            tse.copy_(ts_pin, non_blocking=True)
+            binding.hstu_attn_bwd_ex(*ins, offsets_host, w.batch, w.heads, w.d, w.max_seqlen, w.alpha,
+                                     w.inv_n, *g2, rab=(tse, rab[1], rab[2]), dpos=tg2[0],
+                                     dtime=tg2[1], stream=stream)
+            for dst, src in zip(tg_h, tg2):
+                dst.copy_(src, non_blocking=True)
         for dst, src in zip(outs_h, g2):
             dst.copy_(src, non_blocking=True)
 
@@ -443,10 +474,12 @@ def run_ours_bwd(args, w):
     e2e_ms = max(e0.elapsed_time(e1) / args.steps - f0.elapsed_time(f1) / args.steps, 1e-6)
     e2e_value, e2e_ms = aggregate(flops, e2e_ms, world, dev)
     elem = w.total * w.heads * w.d * 2
+    h2d_extra = 0 if rab is None else int(ts_pin.numel() * ts_pin.element_size())
+    d2h_extra = 0 if rab is None else int(sum(t.numel() * t.element_size() for t in tgrads))
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         arrs = [t.float().numpy() for t in (q_h, k_h, v_h, do_h)]
-        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, args.cpu_seconds)
+        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, args.cpu_seconds, rab=_cpu_rab(args, w))
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
     binding.hstu_plan_destroy(plan)
     peaks = load_peaks()
@@ -456,15 +489,17 @@ def run_ours_bwd(args, w):
             "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {**w.describe(), "pass": "backward", "l2": "flushed between steps (256 MiB write)",
+            "config": {**w.describe(), "pass": "backward", **_rab_desc(args),
+                       "l2": "flushed between steps (256 MiB write)",
                        "work_items": len(binding.hstu_worklist_build_bwd(w.offsets, w.heads)),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                          "unit": UNIT, "frac": achieved / peaks["bf16_tflops"], "traffic": None,
                          "peak_source": f"{peaks['source']} bf16_tflops (burst)"},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * elem + offsets_host.nbytes,
-                    "d2h_bytes_per_step": 3 * elem, "ms_per_step": e2e_ms},
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": 4 * elem + offsets_host.nbytes + h2d_extra,
+                    "d2h_bytes_per_step": 3 * elem + d2h_extra, "ms_per_step": e2e_ms},
             "cpu_baseline": cpu,
             # the backward kernel and the dQ conversion per step
             "gpu_launches": 2 * args.steps,

@@ -90,6 +90,11 @@ _SIGNATURES = {
                                           _VP, _VP, _VP]),
     "hstu_worklist_build_bwd": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int,
                                                _IP]),
+    "hstu_attn_bwd_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, _RABP, ctypes.c_float,
+                                        ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "hstu_attn_bwd_plan_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _RABP, ctypes.c_float,
+                                             ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP]),
     "hstu_attn_fwd_norm_gate": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP,
                                                _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP,
@@ -287,6 +292,27 @@ def hstu_attn_bwd_plan(plan: Plan, q, k, v, dout, alpha: float, inv_n: float, dq
     _check(lib().hstu_attn_bwd_plan(plan.handle, _addr(q), _addr(k), _addr(v), _addr(dout),
                                     float(alpha), float(inv_n), _addr(dq), _addr(dk), _addr(dv),
                                     _stream(stream)), "hstu_attn_bwd_plan")
+
+
+def hstu_attn_bwd_ex(q, k, v, dout, offsets, batch: int, heads: int, d: int, max_seqlen: int,
+                     alpha: float, inv_n: float, dq, dk, dv, rab=None, dpos=None, dtime=None,
+                     stream=None) -> None:
+    """hstu_attn_bwd with the bias ``rab`` = (timestamps, pos, time): dpos and
+    dtime (fp32 device, one entry per table entry) receive the tables' gradients."""
+    off_ptr, keep = _offsets_arg(offsets)
+    _check(lib().hstu_attn_bwd_ex(_addr(q), _addr(k), _addr(v), _addr(dout), off_ptr, int(batch),
+                                  int(heads), int(d), int(max_seqlen), _rab_struct(rab),
+                                  float(alpha), float(inv_n), _addr(dq), _addr(dk), _addr(dv),
+                                  _addr(dpos), _addr(dtime), _stream(stream)), "hstu_attn_bwd_ex")
+    del keep
+
+
+def hstu_attn_bwd_plan_ex(plan: Plan, q, k, v, dout, alpha: float, inv_n: float, dq, dk, dv,
+                          rab=None, dpos=None, dtime=None, stream=None) -> None:
+    _check(lib().hstu_attn_bwd_plan_ex(plan.handle, _addr(q), _addr(k), _addr(v), _addr(dout),
+                                       _rab_struct(rab), float(alpha), float(inv_n), _addr(dq),
+                                       _addr(dk), _addr(dv), _addr(dpos), _addr(dtime),
+                                       _stream(stream)), "hstu_attn_bwd_plan_ex")
 
 
 def hstu_worklist_build_bwd(host_offsets, heads: int) -> np.ndarray:

@@ -33,7 +33,8 @@ def nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "hstu_internal.h"), os.path.join(INCLUDE, "hstu_attn.h"),
+    files += [os.path.join(CSRC, "hstu_internal.h"), os.path.join(CSRC, "hstu_bwd.cuh"),
+              os.path.join(INCLUDE, "hstu_attn.h"),
               os.path.abspath(__file__)]
     return files
 

@@ -161,7 +161,7 @@ int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long l
   if ((rc = make_map(&tq, q, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map(&tk, k, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map(&tv, v, total, heads, d)) != HSTU_OK) return rc;
-  hstu::FwdArgs a;
+  hstu::FwdArgs a{};
   a.items = d_items;
   a.item_hist = d_hist;
   a.n_items = n_items;
@@ -467,7 +467,7 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
   e = cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && hbytes)
     e = cudaMemcpyAsync(d_hist, hist.data(), hbytes, cudaMemcpyHostToDevice, s);
-  hstu::NormGate ngw;
+  hstu::NormGate ngw{};
   if (ng && e == cudaSuccess) {
     ngw = norm_views(block, total, heads, d);
     ngw.u = ng->u;
@@ -485,9 +485,27 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
   return rc;
 }
 
+// The bias's table gradients: non-null, 4-byte aligned.
+int check_rab_grads(const float* dpos, const float* dtime) {
+  if (!dpos || !dtime) return HSTU_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dpos) | reinterpret_cast<uintptr_t>(dtime)) & 3u)
+    return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
+
+// No token: the tables' gradients are zero.
+int zero_rab_grads(const hstu_rab* rab, float* dpos, float* dtime, cudaStream_t s) {
+  if (!rab) return HSTU_OK;
+  if (cudaMemsetAsync(dpos, 0, (size_t)rab->num_pos * sizeof(float), s) != cudaSuccess ||
+      cudaMemsetAsync(dtime, 0, (size_t)rab->num_time * sizeof(float), s) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  return HSTU_OK;
+}
+
 int launch_backward(const hstu::Item* d_items, int n_items, long long total, int heads, int d,
                     const void* q, const void* k, const void* v, const void* dout, float alpha,
-                    float inv_n, float* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream) {
+                    float inv_n, float* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
+                    const hstu_rab* rab = nullptr, float* dpos = nullptr, float* dtime = nullptr) {
   int sms = 0;
   int rc = device_check(&sms);
   if (rc != HSTU_OK) return rc;
@@ -497,7 +515,7 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   if ((rc = make_map(&tv, v, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map(&tdo, dout, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map_f32(&tdq, dq_acc, total, heads, d)) != HSTU_OK) return rc;
-  hstu::BwdArgs a;
+  hstu::BwdArgs a{};  // every field zero: no bias unless set below
   a.items = d_items;
   a.n_items = n_items;
   a.heads = heads;
@@ -509,8 +527,20 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   a.dv = dv;
   a.total = total;
   a.timeout_ns = wait_timeout_ns();
-  // the accumulator starts at zero on the stream, before the kernel
+  if (rab) {
+    a.rab_ts = rab->timestamps;
+    a.rab_pos = rab->pos;
+    a.rab_time = rab->time;
+    a.rab_npos = rab->num_pos;
+    a.rab_ntime = rab->num_time;
+    a.dpos = dpos;
+    a.dtime = dtime;
+  }
+  // the accumulators start at zero on the stream, before the kernel
   if (cudaMemsetAsync(dq_acc, 0, (size_t)total * heads * d * sizeof(float), stream) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  if (rab && (cudaMemsetAsync(dpos, 0, (size_t)rab->num_pos * sizeof(float), stream) != cudaSuccess ||
+              cudaMemsetAsync(dtime, 0, (size_t)rab->num_time * sizeof(float), stream) != cudaSuccess))
     return HSTU_ERR_CUDA;
   const cudaError_t e = hstu::launch_bwd(d, tq, tk, tv, tdo, tdq, a, grid_for(n_items, sms), stream);
   if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
@@ -754,11 +784,22 @@ int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, i
 int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
                   const int32_t* offsets, int batch, int heads, int d, int max_seqlen, float alpha,
                   float inv_n, void* dq, void* dk, void* dv, hstu_stream_t stream) {
+  return hstu_attn_bwd_ex(q, k, v, dout, offsets, batch, heads, d, max_seqlen, nullptr, alpha, inv_n,
+                          dq, dk, dv, nullptr, nullptr, stream);
+}
+
+int hstu_attn_bwd_ex(const void* q, const void* k, const void* v, const void* dout,
+                     const int32_t* offsets, int batch, int heads, int d, int max_seqlen,
+                     const hstu_rab* rab, float alpha, float inv_n, void* dq, void* dk, void* dv,
+                     float* dpos, float* dtime, hstu_stream_t stream) {
   if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
+  int rc;
+  if (rab && ((rc = check_rab(rab)) != HSTU_OK || (rc = check_rab_grads(dpos, dtime)) != HSTU_OK))
+    return rc;
   if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
-  if (batch == 0) return HSTU_OK;
-  if (!offsets) return HSTU_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (batch == 0) return zero_rab_grads(rab, dpos, dtime, s);
+  if (!offsets) return HSTU_ERR_INVALID_ARG;
   std::vector<int32_t> host_off;
   const int32_t* off = offsets;
   cudaPointerAttributes attr;
@@ -775,10 +816,10 @@ int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
       return HSTU_ERR_CUDA;
     off = host_off.data();
   }
-  int rc = check_offsets(off, batch, max_seqlen);
+  rc = check_offsets(off, batch, max_seqlen);
   if (rc != HSTU_OK) return rc;
   const long long total = off[batch];
-  if (total == 0) return HSTU_OK;
+  if (total == 0) return zero_rab_grads(rab, dpos, dtime, s);
   if ((rc = check_buffers(q, k, v, dout)) != HSTU_OK || (rc = check_buffers(dq, dk, dv, dv)) != HSTU_OK)
     return rc;
   std::vector<hstu::Item> items;
@@ -788,7 +829,7 @@ int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
   } catch (const std::bad_alloc&) {
     return HSTU_ERR_NO_MEMORY;
   }
-  if (items.empty()) return HSTU_OK;
+  if (items.empty()) return zero_rab_grads(rab, dpos, dtime, s);
   if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
   // one stream-ordered allocation: the fp32 dQ accumulator, then the items
   const size_t abytes = (size_t)total * heads * d * sizeof(float);
@@ -802,7 +843,7 @@ int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
     return HSTU_ERR_CUDA;
   }
   rc = launch_backward(d_items, (int)items.size(), total, heads, d, q, k, v, dout, alpha, inv_n,
-                       reinterpret_cast<float*>(block), dq, dk, dv, s);
+                       reinterpret_cast<float*>(block), dq, dk, dv, s, rab, dpos, dtime);
   if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
   return rc;
 }
@@ -810,15 +851,26 @@ int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
 int hstu_attn_bwd_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
                        const void* dout, float alpha, float inv_n, void* dq, void* dk, void* dv,
                        hstu_stream_t stream) {
+  return hstu_attn_bwd_plan_ex(plan, q, k, v, dout, nullptr, alpha, inv_n, dq, dk, dv, nullptr,
+                               nullptr, stream);
+}
+
+int hstu_attn_bwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                          const void* dout, const hstu_rab* rab, float alpha, float inv_n, void* dq,
+                          void* dk, void* dv, float* dpos, float* dtime, hstu_stream_t stream) {
   if (!plan || !(plan->flags & HSTU_PLAN_BACKWARD)) return HSTU_ERR_INVALID_ARG;
-  if (plan->items.empty()) return HSTU_OK;
-  int rc = check_buffers(q, k, v, dout);
+  int rc;
+  if (rab && ((rc = check_rab(rab)) != HSTU_OK || (rc = check_rab_grads(dpos, dtime)) != HSTU_OK))
+    return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (plan->items.empty()) return zero_rab_grads(rab, dpos, dtime, s);
+  rc = check_buffers(q, k, v, dout);
   if (rc != HSTU_OK || (rc = check_buffers(dq, dk, dv, dv)) != HSTU_OK) return rc;
   const size_t bbytes = (size_t)plan->n_bwd * sizeof(hstu::Item);
   return launch_backward(reinterpret_cast<const hstu::Item*>(plan->d_bwd), plan->n_bwd, plan->total,
                          plan->heads, plan->d, q, k, v, dout, alpha, inv_n,
-                         reinterpret_cast<float*>(plan->d_bwd + bbytes), dq, dk, dv,
-                         reinterpret_cast<cudaStream_t>(stream));
+                         reinterpret_cast<float*>(plan->d_bwd + bbytes), dq, dk, dv, s, rab, dpos,
+                         dtime);
 }
 
 int hstu_last_status(int* device_status, int* site) {

@@ -32,7 +32,7 @@
 // their own: one pass computes both, and steps 3 and 5 issue together.
 // Phases run one after another (synchronous waits).
 
-template <int D>
+template <int D, bool RAB = false>
 struct BCfg {
   static constexpr int CHUNK = D < 64 ? D : 64;  // elements per swizzled row of a d-wide tile
   static constexpr int NCHUNK = D / CHUNK;
@@ -59,7 +59,11 @@ struct BCfg {
   static constexpr int LO_OFF = HI_OFF + PTILEB;
   static constexpr int DHI_OFF = MERGED ? LO_OFF + PTILEB : HI_OFF;  // dS tiles
   static constexpr int DLO_OFF = MERGED ? DHI_OFF + PTILEB : LO_OFF;
-  static constexpr int BAR_OFF = (MERGED ? DLO_OFF : LO_OFF) + PTILEB;
+  // bias variant: the CTA's 32 position and 32 time gradient sums, by the
+  // lane that holds the bucket's table entry
+  static constexpr int HIST_OFF = (MERGED ? DLO_OFF : LO_OFF) + PTILEB;
+  static constexpr int HISTB = RAB ? 64 * 4 : 0;
+  static constexpr int BAR_OFF = HIST_OFF + HISTB;
   // S / dP done; the other products done; drain
   static constexpr int B_KV = 0, B_QD = 1 /* [QB] */, B_SDP = 1 + QB, B_PROD = 2 + QB,
                        B_DRAIN = 3 + QB, NBARS = 4 + QB;
@@ -99,12 +103,12 @@ struct BwdBlock {
   int s0, n, h, kt;
 };
 
-template <int D>
+template <int D, bool RAB>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     hstu_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
-  using C = BCfg<D>;
+  using C = BCfg<D, RAB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -117,6 +121,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
+  if constexpr (RAB) {
+    float* hist = reinterpret_cast<float*>(smem + C::HIST_OFF);
+    for (int i = tid; i < 64; i += kBwdThreads) hist[i] = 0.f;
+  }
   if (tid == 0) {
     for (int i = 0; i < C::NBARS; ++i) mbar_init(bar(i), 1);
     *abort_flag = 0;
@@ -228,6 +236,176 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *reinterpret_cast<uint4*>(lo_tile + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   };
 
+  // The bias (variant RAB): lane l holds the tables' entries of bucket
+  // 31 - l (clamped); the lookup and the chunk shortcut are the forward's.
+  RabRow rr{};
+  if constexpr (RAB) {
+    const int bl = 31 - lane;
+    rr.pos_l = __ldg(a.rab_pos + (bl < a.rab_npos - 1 ? bl : a.rab_npos - 1));
+    rr.time_l = __ldg(a.rab_time + (bl < a.rab_ntime - 1 ? bl : a.rab_ntime - 1));
+  }
+  float* hp = reinterpret_cast<float*>(smem + C::HIST_OFF);  // the CTA's sums
+  float* ht = hp + 32;
+  // each thread's running sums of dS and the buckets (as lanes) they belong
+  // to, carried over chunks and blocks: added into the CTA's sums when the
+  // bucket changes, and at the end
+  float run_p = 0.f, run_t = 0.f;
+  int cur_p = 0, cur_t = 0;
+  // a running sum leaves bucket cur for nxt: where the whole warp leaves one
+  // bucket together (a bucket edge between chunks, a jump in time), its 32
+  // sums add as one; else each lane that leaves adds its own.  The warp is
+  // converged here.
+  auto flush_warp = [&](float* h, int& cur, float& sum, int nxt) {
+    const bool mine = nxt != cur;
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    if (m) {
+      const int c0 = __shfl_sync(0xffffffffu, cur, 0);
+      if (m == 0xffffffffu && __all_sync(0xffffffffu, cur == c0)) {
+        float v = sum;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) atomicAdd(h + c0, v);
+      } else if (mine) {
+        atomicAdd(h + cur, sum);
+      }
+      if (mine) {
+        sum = 0.f;
+        cur = nxt;
+      }
+    }
+  };
+  // the bias's view of this warp's two key chunks of the current item:
+  // the timestamps (lane = key) and whether they are in order; and of the
+  // current query block: each chunk's constant parts
+  int ts_key0 = 0, ts_key1 = 0;
+  bool ord0 = true, ord1 = true;
+  RabChunk rc0{}, rc1{};
+  // One 32-key chunk c of this thread's row: MODE 0 writes P and dS, 1 P,
+  // 2 dS.  With the bias, FP says that its position part is constant over
+  // the chunk; TM that its time part is constant (0), monotone in the key
+  // (1: the chunk's timestamps are in order) or neither (2).  The dS goes
+  // into the running sums: a row's bucket never moves back along a chunk
+  // (positions always, times when in order) and rarely changes between
+  // chunks, so the sums seldom flush; out-of-order times add per key.
+  auto chunk = [&](auto fp_t, auto tm_t, auto mode_t, int c, const uint32_t (&sr)[32],
+                   const uint32_t (&pr)[32], const RabChunk& rc, int j0, int cmax, bool row_ok) {
+    constexpr bool FP = decltype(fp_t)::value;
+    constexpr int TM = decltype(tm_t)::value;
+    constexpr int MODE = decltype(mode_t)::value;
+    float& sp = run_p;
+    float& st = run_t;
+    int& cp = cur_p;
+    int& ct = cur_t;
+    if constexpr (RAB && MODE != 1) {
+      // a constant part's bucket for the whole chunk
+      if constexpr (FP) flush_warp(hp, cp, sp, rc.lp0);
+      if constexpr (TM == 0) flush_warp(ht, ct, st, rc.lt0);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float vp[8], vs[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = 8 * g + e;
+        const int col = 32 * c + k;
+        const bool keep = row_ok && col < cmax;
+        float x = alpha * __uint_as_float(sr[k]);
+        [[maybe_unused]] int lp = cp, lt = ct;
+        if constexpr (RAB) {
+          float bias;
+          if constexpr (FP) {
+            bias = rc.pos_c;
+          } else {
+            lp = rab_lane(rr.pe_i - (j0 + k));
+            bias = __shfl_sync(0xffffffffu, rr.pos_l, lp);
+          }
+          if constexpr (TM == 0) {
+            bias += rc.time_c;
+          } else {
+            lt = rab_lane(rr.ts_i - __shfl_sync(0xffffffffu, rc.ts_lane, k));
+            bias += __shfl_sync(0xffffffffu, rr.time_l, lt);
+          }
+          x += bias;
+        }
+        const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+        const float isg = inv_n * sg;
+        if constexpr (MODE != 2) vp[e] = keep ? isg * x : 0.0f;
+        if constexpr (MODE != 1) {
+          const float ds = keep ? isg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[k]) : 0.0f;
+          vs[e] = ds;
+          if constexpr (RAB) {
+            if constexpr (!FP) {
+              if (lp != cp) {
+                atomicAdd(hp + cp, sp);
+                sp = 0.f;
+                cp = lp;
+              }
+            }
+            sp += ds;
+            if constexpr (TM == 1) flush_warp(ht, ct, st, lt);
+            if constexpr (TM == 2)
+              atomicAdd(ht + lt, ds);
+            else
+              st += ds;
+          }
+        }
+      }
+      if constexpr (MODE != 2) put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, vp);
+      if constexpr (MODE != 1) put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, vs);
+    }
+  };
+  using T_ = std::true_type;
+  using F_ = std::false_type;
+  using TM0 = std::integral_constant<int, 0>;
+  using TM1 = std::integral_constant<int, 1>;
+  using TM2 = std::integral_constant<int, 2>;
+  // the timestamp of this thread's row of query block qt (a row past the
+  // sequence reads the last token; its results are never kept)
+  auto row_ts = [&](int qt) -> int {
+    if constexpr (RAB) {
+      const int i = kBM * qt + row;
+      return __ldg(rr.ts + (i < rr.last ? i : rr.last));
+    } else {
+      return 0;
+    }
+  };
+  // the bias's constant parts of the two chunks for query block qt, whose
+  // row timestamp ts_i was loaded ahead
+  auto prep = [&](int qt, int ts_i, int kbase) {
+    if constexpr (RAB) {
+      rr.pe_i = kBM * qt + row;
+      rr.ts_i = ts_i;
+      rc0 = rab_chunk<false>(rr, kbase + 64 * wg, ts_key0);
+      rc1 = rab_chunk<false>(rr, kbase + 64 * wg + 32, ts_key1);
+    }
+  };
+  // the pass of MODE over this warpgroup's two chunks of query block qt
+  auto pass = [&](auto mode_t, int qt, int kbase, int cmax, bool row_ok) {
+#pragma unroll 1
+    for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+      uint32_t sr[32], pr[32];
+      tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
+      if constexpr (decltype(mode_t)::value != 1) tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
+      const int j0 = kbase + 32 * c;
+      if constexpr (RAB) {
+        const RabChunk rc = (c & 1) ? rc1 : rc0;
+        if (!((c & 1) ? ord1 : ord0))
+          chunk(F_{}, TM2{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+        else if (rc.fix_p && rc.fix_t)
+          chunk(T_{}, TM0{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+        else if (rc.fix_p)
+          chunk(T_{}, TM1{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+        else if (rc.fix_t)
+          chunk(F_{}, TM0{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+        else
+          chunk(F_{}, TM1{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+      } else {
+        const RabChunk rc{};
+        chunk(T_{}, TM0{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+      }
+    }
+  };
+
   for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
     const Item it = __ldg(&a.items[idx]);
     const BwdBlock b{it.x, it.y, it.z, it.w};
@@ -288,7 +466,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_xyt(C::DP_COL, buf_desc(do_kmaj0, qb), v_kmaj);
       mma_commit(bar(C::B_SDP));
     };
-    if constexpr (C::MERGED) {
+    if constexpr (RAB) {
+      rr.ts = a.rab_ts + b.s0;
+      rr.last = b.n - 1;
+      const int j0 = kBN * b.kt + 64 * wg + lane;
+      ts_key0 = __ldg(rr.ts + (j0 < rr.last ? j0 : rr.last));
+      ts_key1 = __ldg(rr.ts + (j0 + 32 < rr.last ? j0 + 32 : rr.last));
+      ord0 = __all_sync(0xffffffffu, lane == 31 || ts_key0 <= __shfl_down_sync(0xffffffffu, ts_key0, 1));
+      ord1 = __all_sync(0xffffffffu, lane == 31 || ts_key1 <= __shfl_down_sync(0xffffffffu, ts_key1, 1));
+      prep(b.kt, row_ts(b.kt), kBN * b.kt);
+    }
+    if constexpr (C::MERGED && C::QB == 2) {
       // Pipelined: while block qt's products run, block qt + 1's S and dP
       // follow them on the tensor cores, and the threads stage qt's dQ.
       const int qb0 = (int)(qiter % C::QB);
@@ -313,31 +501,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool row_ok;
         mask_of(qt, cmax, row_ok);
         // P and dS in one pass over this warpgroup's two 32-key chunks
-#pragma unroll 1
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          uint32_t sr[32], pr[32];
-          tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
-          tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float vp[8], vs[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int col = 32 * c + 8 * g + e;
-              const bool keep = row_ok && col < cmax;
-              const float x = alpha * __uint_as_float(sr[8 * g + e]);
-              const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-              const float isg = inv_n * sg;
-              vp[e] = keep ? isg * x : 0.0f;
-              vs[e] = keep ? isg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[8 * g + e]) : 0.0f;
-            }
-            put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, vp);
-            put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, vs);
-          }
-        }
+        pass(std::integral_constant<int, 0>{}, qt, kBN * b.kt, cmax, row_ok);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncthreads();  // S and dP read, the tiles written
+        const int ts_next = row_ts(qt + 1);  // loads under the product issue
         if (tid == 0) {
           tc_fence_after();
           const uint64_t q_mn = buf_desc(q_mn0, qb), do_mn = buf_desc(do_mn0, qb);
@@ -354,6 +522,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             issue_sdp(qb ^ 1);
           }
         }
+        // the next block's bias parts while the products run
+        if (qt + 1 < nq) prep(qt + 1, ts_next, kBN * b.kt);
         if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteVFull))) break;
         tc_fence_after();
         // buffer qb is free (its last readers were these products): the
@@ -362,10 +532,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         put_dq(qt);
       }
     } else {
+      // One block at a time: P and dS in one pass where they have tiles of
+      // their own, else P, dV, then dS in P's tiles.
       if (tid == 0) load_qd(0, b.kt);
       if (!(ok = wait_all(C::B_KV, ph_kv, kSiteKFull))) break;
       for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
         const bool first = qt == b.kt;
+        if (!first) prep(qt, row_ts(qt), kBN * b.kt);  // under the waits below
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         if (!(ok = wait_all(C::B_QD, ph_qd[0], kSiteQFull))) break;
         const uint64_t q_mn = buf_desc(q_mn0, 0), do_mn = buf_desc(do_mn0, 0);
@@ -375,67 +548,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int cmax;
         bool row_ok;
         mask_of(qt, cmax, row_ok);
-        // 2. P (this warpgroup's two 32-key chunks)
-#pragma unroll 1
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          uint32_t sr[32];
-          tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int col = 32 * c + 8 * g + e;
-              const float x = alpha * __uint_as_float(sr[8 * g + e]);
-              const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-              v[e] = (row_ok && col < cmax) ? inv_n * x * sg : 0.0f;
-            }
-            put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, v);
+        if constexpr (C::MERGED) {
+          pass(std::integral_constant<int, 0>{}, qt, kBN * b.kt, cmax, row_ok);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          __syncthreads();
+          if (tid == 0) {
+            tc_fence_after();
+            mma_tt(C::DV_COL, hi_mn, do_mn, first);
+            mma_tt(C::DV_COL, lo_mn, do_mn, false);
+            mma_tt(C::DK_COL, dhi_mn, q_mn, first);
+            mma_tt(C::DK_COL, dlo_mn, q_mn, false);
+            mma_dq(dhi_kmaj, true);
+            mma_dq(dlo_kmaj, false);
+            mma_commit(bar(C::B_PROD));
           }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        // 3. dV += P^T dO
-        if (tid == 0) {
-          tc_fence_after();
-          mma_tt(C::DV_COL, hi_mn, do_mn, first);
-          mma_tt(C::DV_COL, lo_mn, do_mn, false);
-          mma_commit(bar(C::B_PROD));
-        }
-        if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteOFull))) break;
-        tc_fence_after();
-        // 4. dS, into the same tiles (the dV products are done)
-#pragma unroll 1
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          uint32_t sr[32], pr[32];
-          tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
-          tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int col = 32 * c + 8 * g + e;
-              const float x = alpha * __uint_as_float(sr[8 * g + e]);
-              const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-              const float ds = inv_n * sg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[8 * g + e]);
-              v[e] = (row_ok && col < cmax) ? ds : 0.0f;
-            }
-            put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, v);
+        } else {
+          // 2. P
+          pass(std::integral_constant<int, 1>{}, qt, kBN * b.kt, cmax, row_ok);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          __syncthreads();
+          // 3. dV += P^T dO
+          if (tid == 0) {
+            tc_fence_after();
+            mma_tt(C::DV_COL, hi_mn, do_mn, first);
+            mma_tt(C::DV_COL, lo_mn, do_mn, false);
+            mma_commit(bar(C::B_PROD));
           }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        __syncthreads();
-        // 5. dK += dS^T Q, dQ_part = dS K (over S: every thread has read it)
-        if (tid == 0) {
+          if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteOFull))) break;
           tc_fence_after();
-          mma_tt(C::DK_COL, dhi_mn, q_mn, first);
-          mma_tt(C::DK_COL, dlo_mn, q_mn, false);
-          mma_dq(dhi_kmaj, true);
-          mma_dq(dlo_kmaj, false);
-          mma_commit(bar(C::B_PROD));
+          // 4. dS, into the same tiles (the dV products are done)
+          pass(std::integral_constant<int, 2>{}, qt, kBN * b.kt, cmax, row_ok);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          __syncthreads();
+          // 5. dK += dS^T Q, dQ_part = dS K
+          if (tid == 0) {
+            tc_fence_after();
+            mma_tt(C::DK_COL, dhi_mn, q_mn, first);
+            mma_tt(C::DK_COL, dlo_mn, q_mn, false);
+            mma_dq(dhi_kmaj, true);
+            mma_dq(dlo_kmaj, false);
+            mma_commit(bar(C::B_PROD));
+          }
         }
         if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteVFull))) break;
         tc_fence_after();
@@ -483,6 +639,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   // the last reductions have finished before the CTA (and its shared memory) goes
   if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if constexpr (RAB) {
+    // the running sums into the CTA's, those into the tables' gradients:
+    // lane sum L holds bucket min(31 - L, entries - 1)
+    atomicAdd(hp + cur_p, run_p);
+    atomicAdd(ht + cur_t, run_t);
+    __syncthreads();
+    if (ok && tid < 64) {
+      const float sum = hp[tid];
+      const int L = tid & 31;
+      if (sum != 0.f) {
+        if (tid < 32)
+          atomicAdd(a.dpos + (31 - L < a.rab_npos - 1 ? 31 - L : a.rab_npos - 1), sum);
+        else
+          atomicAdd(a.dtime + (31 - L < a.rab_ntime - 1 ? 31 - L : a.rab_ntime - 1), sum);
+      }
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -503,16 +676,25 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* acc, uint1
   }
 }
 
+template <int D, bool RAB>
+cudaError_t launch_bwd_dr(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                          cudaStream_t stream) {
+  using C = BCfg<D, RAB>;
+  static_assert(D / 32 * kBM * 128 <= 2 * C::PTILEB, "dQ staging fits the P tiles");
+  cudaError_t e = cudaFuncSetAttribute(hstu_bwd_kernel<D, RAB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
+  if (e != cudaSuccess) return e;
+  hstu_bwd_kernel<D, RAB><<<grid, kBwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, tdo, tdq, a);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
                          cudaStream_t stream) {
-  using C = BCfg<D>;
-  static_assert(D / 32 * kBM * 128 <= 2 * C::PTILEB, "dQ staging fits the P tiles");
-  cudaError_t e = cudaFuncSetAttribute(hstu_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_LAUNCH);
-  if (e != cudaSuccess) return e;
-  hstu_bwd_kernel<D><<<grid, kBwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, tdo, tdq, a);
+  cudaError_t e = a.rab_ts ? launch_bwd_dr<D, true>(tq, tk, tv, tdo, tdq, a, grid, stream)
+                           : launch_bwd_dr<D, false>(tq, tk, tv, tdo, tdq, a, grid, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long n8 = a.total * a.heads * D / 8;
   const int cgrid = (int)std::min<long long>((n8 + 255) / 256, 4LL * 1024);

@@ -858,7 +858,8 @@ struct RabRow {
 // only the other parts are looked up per key.
 struct RabChunk {
   int ts_lane;       // timestamp of key j0 + lane
-  float pos_c, time_c;  // the row's halved entries at the chunk's first key
+  float pos_c, time_c;  // the row's table entries (as the lanes hold them) at the chunk's first key
+  int lp0, lt0;         // the lanes that hold them
   bool fix_p, fix_t;    // warp-uniform: the part is constant over the chunk
 };
 
@@ -889,6 +890,8 @@ __device__ __forceinline__ RabChunk rab_chunk(const RabRow& r, int j0, int ts_la
   c.fix_t = in_order && __all_sync(0xffffffffu, lt0 == lt1);
   c.pos_c = __shfl_sync(0xffffffffu, r.pos_l, lp0);
   c.time_c = __shfl_sync(0xffffffffu, r.time_l, lt0);
+  c.lp0 = lp0;
+  c.lt0 = lt0;
   return c;
 }
 

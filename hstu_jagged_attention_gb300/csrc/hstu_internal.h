@@ -88,6 +88,15 @@ struct BwdArgs {
   void* dv;
   long long total;
   unsigned long long timeout_ns;
+  // The relative attention bias (null rab_ts: none), as FwdArgs; dpos and
+  // dtime (rab_npos, rab_ntime fp32, zeroed before the launch) receive the
+  // tables' gradients.
+  const int32_t* rab_ts = nullptr;
+  const float* rab_pos = nullptr;
+  const float* rab_time = nullptr;
+  int rab_npos = 0, rab_ntime = 0;
+  float* dpos = nullptr;
+  float* dtime = nullptr;
 };
 // Work list of the backward: one item per (sequence, head, key block kt),
 // costing nq - kt query blocks; ordered by cost descending, then sequence,

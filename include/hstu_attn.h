@@ -378,6 +378,32 @@ int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, i
                             int capacity, int* n_items);
 
 /*
+ * hstu_attn_bwd_ex / hstu_attn_bwd_plan_ex -- the backward with the
+ * relative attention bias (rab NULL: as hstu_attn_bwd / _plan).  The score
+ * is that of hstu_rab, ds_ij = inv_n silu'(score_ij) <dout[i], v[j]>, dq, dk
+ * and dv as above, and the tables' gradients (HSTU paper Appendix G: the
+ * bias's construction and its backward fused into the attention):
+ *
+ *   dpos[b]  = sum of ds_ij over the kept pairs and heads whose position
+ *              bucket is b (the clamped bucket: b = num_pos - 1 collects
+ *              every larger one); dtime likewise over the time buckets.
+ *
+ *   dpos, dtime  device fp32 of num_pos and num_time entries, 4-byte
+ *                aligned, overwritten (zeroed on `stream`, then added into
+ *                by the kernel's float atomics, so their last bits may vary
+ *                from run to run).  Ignored when rab is NULL.
+ * Errors: as hstu_attn_bwd, and HSTU_ERR_INVALID_ARG for the rab checks of
+ * hstu_attn_fwd_ex or NULL / misaligned dpos or dtime (with rab).
+ */
+int hstu_attn_bwd_ex(const void* q, const void* k, const void* v, const void* dout,
+                     const int32_t* offsets, int batch, int heads, int d, int max_seqlen,
+                     const hstu_rab* rab, float alpha, float inv_n, void* dq, void* dk, void* dv,
+                     float* dpos, float* dtime, hstu_stream_t stream);
+int hstu_attn_bwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, const void* v,
+                          const void* dout, const hstu_rab* rab, float alpha, float inv_n, void* dq,
+                          void* dk, void* dv, float* dpos, float* dtime, hstu_stream_t stream);
+
+/*
  * hstu_launch_shape -- the grid the next launch for `plan` would use on the
  * current device: *grid persistent CTAs of *block threads with *smem_bytes
  * of dynamic shared memory.  Queries device attributes; launches nothing.

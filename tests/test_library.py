@@ -234,3 +234,23 @@ def test_bwd_validation_before_any_cuda_call():
         binding.hstu_attn_bwd(16, 16, 16, 16, off, 1, 0, 64, 4, 1.0, 1.0, 16, 16, 16, stream=0)
     assert e.value.code == binding.HSTU_ERR_INVALID_ARG
     binding.hstu_attn_bwd(0, 0, 0, 0, np.zeros(1, np.int32), 0, 2, 64, 0, 1.0, 1.0, 0, 0, 0, stream=0)
+
+
+def test_bwd_rab_validation_before_any_cuda_call():
+    off = np.array([0, 4], np.int32)
+    good = dict(ts=16, pos=16, npos=8, time=16, ntime=8, dpos=32, dtime=32)
+    bad = [dict(ts=0), dict(pos=0), dict(ts=18), dict(npos=0), dict(ntime=33), dict(dpos=0),
+           dict(dtime=0), dict(dpos=34), dict(dtime=2)]
+    for kw in bad:
+        a = dict(good)
+        a.update(kw)
+        rab = binding.ctypes.pointer(binding._Rab(a["ts"], a["pos"], a["npos"], a["time"], a["ntime"]))
+        code = binding.lib().hstu_attn_bwd_ex(16, 16, 16, 16, off.ctypes.data, 1, 2, 64, 4, rab, 1.0,
+                                              1.0, 16, 16, 16, a["dpos"], a["dtime"], None)
+        assert code == binding.HSTU_ERR_INVALID_ARG, kw
+        code = binding.lib().hstu_attn_bwd_plan_ex(None, 16, 16, 16, 16, rab, 1.0, 1.0, 16, 16, 16,
+                                                   a["dpos"], a["dtime"], None)
+        assert code == binding.HSTU_ERR_INVALID_ARG, kw
+    # without the bias the table gradients are not looked at
+    binding.hstu_attn_bwd_ex(0, 0, 0, 0, np.zeros(1, np.int32), 0, 2, 64, 0, 1.0, 1.0, 0, 0, 0,
+                             stream=0)
