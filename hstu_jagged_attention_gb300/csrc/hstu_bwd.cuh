@@ -258,9 +258,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto flush_warp = [&](float* h, int& cur, float& sum, int nxt) {
     const bool mine = nxt != cur;
     const unsigned m = __ballot_sync(0xffffffffu, mine);
-    if (m) {
+    if (m) {  // m is the same in every lane: the warp stays converged
       const int c0 = __shfl_sync(0xffffffffu, cur, 0);
-      if (m == 0xffffffffu && __all_sync(0xffffffffu, cur == c0)) {
+      const bool one = __all_sync(0xffffffffu, cur == c0);
+      if (m == 0xffffffffu && one) {
         float v = sum;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -472,8 +473,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int j0 = kBN * b.kt + 64 * wg + lane;
       ts_key0 = __ldg(rr.ts + (j0 < rr.last ? j0 : rr.last));
       ts_key1 = __ldg(rr.ts + (j0 + 32 < rr.last ? j0 + 32 : rr.last));
-      ord0 = __all_sync(0xffffffffu, lane == 31 || ts_key0 <= __shfl_down_sync(0xffffffffu, ts_key0, 1));
-      ord1 = __all_sync(0xffffffffu, lane == 31 || ts_key1 <= __shfl_down_sync(0xffffffffu, ts_key1, 1));
+      // every lane takes part in the shuffles (none inside a condition)
+      const int nx0 = __shfl_down_sync(0xffffffffu, ts_key0, 1);
+      const int nx1 = __shfl_down_sync(0xffffffffu, ts_key1, 1);
+      ord0 = __all_sync(0xffffffffu, lane == 31 || ts_key0 <= nx0);
+      ord1 = __all_sync(0xffffffffu, lane == 31 || ts_key1 <= nx1);
       prep(b.kt, row_ts(b.kt), kBN * b.kt);
     }
     if constexpr (C::MERGED && C::QB == 2) {
