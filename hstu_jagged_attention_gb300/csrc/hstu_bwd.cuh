@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
 
   // The bias (variant RAB): lane l holds the tables' entries of bucket
-  // 31 - l (clamped); the lookup and the chunk shortcut are the forward's.
+  // 31 - l (clamped), so a lookup is one shuffle from lane rab_lane(delta).
   RabRow rr{};
   if constexpr (RAB) {
     const int bl = 31 - lane;
@@ -275,91 +275,165 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   };
-  // the bias's view of this warp's two key chunks of the current item:
-  // the timestamps (lane = key) and whether they are in order; and of the
-  // current query block: each chunk's constant parts
-  int ts_key0 = 0, ts_key1 = 0;
-  bool ord0 = true, ord1 = true;
-  RabChunk rc0{}, rc1{};
+  // A 32-key chunk of this warp's 32 rows, for the bias.  Along the keys a
+  // row's position bucket never grows, nor does its time bucket when the
+  // chunk's timestamps are in order.  So a part is one of:
+  //   0  constant over the chunk for every row: one value per row;
+  //   1  at most two adjacent buckets per row: the row's first key of the
+  //      lower bucket (kbp, kbt; 32 if none) decides between two values;
+  //   2  anything else (a diagonal chunk, out-of-order times): a lookup per
+  //      key.
+  // Modes are warp-uniform; a chunk with a part in mode 2 takes mode 2 for
+  // both.
+  struct BRab {
+    float p0, p1, t0, t1;  // the row's entries of its first and second buckets
+    uint32_t pk;           // lp0 | lt0 << 5 | kbp << 10 | kbt << 16 | pm << 22 | tm << 24
+  };
+  // the chunk of keys j0 .. j0 + 31, key j0 + lane's timestamp ts_key,
+  // ord: those are in order; rr holds the row's position and timestamp
+  auto prep_chunk = [&](int j0, int ts_key, bool ord) -> BRab {
+    const int d0 = rr.pe_i - j0;
+    const int lp0 = rab_lane(d0), lp1 = rab_lane(d0 - 31);
+    const int ts_first = __shfl_sync(0xffffffffu, ts_key, 0);
+    const int ts_last = __shfl_sync(0xffffffffu, ts_key, 31);
+    const int lt0 = rab_lane(rr.ts_i - ts_first), lt1 = rab_lane(rr.ts_i - ts_last);
+    const int dp = lp1 - lp0, dt = lt1 - lt0;
+    const bool p_fix = __all_sync(0xffffffffu, dp == 0);
+    const bool p_two = __all_sync(0xffffffffu, dp <= 1);
+    const bool t_fix = __all_sync(0xffffffffu, dt == 0);
+    const bool t_two = __all_sync(0xffffffffu, dt >= 0 && dt <= 1);
+    int pm = p_fix ? 0 : (p_two ? 1 : 2);
+    int tm = !ord ? 2 : (t_fix ? 0 : (t_two ? 1 : 2));
+    if (pm == 2 || tm == 2) pm = tm = 2;
+    // position: bucket 31 - lp0 holds deltas >= 2^(31 - lp0) - 1, so the
+    // first key below it is d0 + 2 - 2^(31 - lp0)
+    const int kbp = pm == 1 && dp == 1 ? d0 + 2 - (1 << (31 - lp0)) : 32;
+    // time: keys in order; the first bucket (>= 1 when it changes) holds
+    // the keys with ts <= ts_i + 1 - 2^(31 - lt0): count them by bisection
+    int kbt = 32;
+    if (tm == 1) {  // warp-uniform
+      const long long thr = (long long)rr.ts_i + 1 - (1LL << (31 - lt0));
+      int cnt = 0;
+#pragma unroll
+      for (int st = 16; st > 0; st >>= 1) {
+        const int probe = __shfl_sync(0xffffffffu, ts_key, cnt + st - 1);
+        cnt += (long long)probe <= thr ? st : 0;
+      }
+      const int probe = __shfl_sync(0xffffffffu, ts_key, cnt);
+      cnt += (long long)probe <= thr ? 1 : 0;
+      if (dt == 1) kbt = cnt;
+    }
+    BRab q;
+    q.p0 = __shfl_sync(0xffffffffu, rr.pos_l, lp0);
+    q.p1 = __shfl_sync(0xffffffffu, rr.pos_l, lp0 < 31 ? lp0 + 1 : 31);
+    q.t0 = __shfl_sync(0xffffffffu, rr.time_l, lt0);
+    q.t1 = __shfl_sync(0xffffffffu, rr.time_l, lt0 < 31 ? lt0 + 1 : 31);
+    q.pk = (uint32_t)lp0 | ((uint32_t)lt0 << 5) | ((uint32_t)kbp << 10) | ((uint32_t)kbt << 16) |
+           ((uint32_t)pm << 22) | ((uint32_t)tm << 24);
+    return q;
+  };
   // One 32-key chunk c of this thread's row: MODE 0 writes P and dS, 1 P,
-  // 2 dS.  With the bias, FP says that its position part is constant over
-  // the chunk; TM that its time part is constant (0), monotone in the key
-  // (1: the chunk's timestamps are in order) or neither (2).  The dS goes
-  // into the running sums: a row's bucket never moves back along a chunk
-  // (positions always, times when in order) and rarely changes between
-  // chunks, so the sums seldom flush; out-of-order times add per key.
-  auto chunk = [&](auto fp_t, auto tm_t, auto mode_t, int c, const uint32_t (&sr)[32],
-                   const uint32_t (&pr)[32], const RabChunk& rc, int j0, int cmax, bool row_ok) {
-    constexpr bool FP = decltype(fp_t)::value;
+  // 2 dS; PM and TM are the bias parts' modes.  The dS goes into the running
+  // sums: in modes 0 and 1 as at most two sums per part at the chunk's end;
+  // in mode 2 a running sum moves on where the row's bucket changes.
+  auto chunk = [&](auto pm_t, auto tm_t, auto mode_t, int c, const uint32_t (&sr)[32],
+                   const uint32_t (&pr)[32], const BRab& q, int ts_key, int j0, int cmax,
+                   bool row_ok) {
+    constexpr int PM = decltype(pm_t)::value;
     constexpr int TM = decltype(tm_t)::value;
     constexpr int MODE = decltype(mode_t)::value;
+    constexpr bool GEN = PM == 2;
+    [[maybe_unused]] const int lp0 = q.pk & 31, lt0 = (q.pk >> 5) & 31;
+    [[maybe_unused]] const int kbp = (q.pk >> 10) & 63, kbt = (q.pk >> 16) & 63;
     float& sp = run_p;
     float& st = run_t;
     int& cp = cur_p;
     int& ct = cur_t;
-    if constexpr (RAB && MODE != 1) {
-      // a constant part's bucket for the whole chunk
-      if constexpr (FP) flush_warp(hp, cp, sp, rc.lp0);
-      if constexpr (TM == 0) flush_warp(ht, ct, st, rc.lt0);
+    if constexpr (RAB && MODE != 1 && !GEN) {
+      // the running sums move to the chunk's first buckets
+      flush_warp(hp, cp, sp, lp0);
+      flush_warp(ht, ct, st, lt0);
     }
+    [[maybe_unused]] float tot = 0.f, ap1 = 0.f, at1 = 0.f;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
+      // eight keys without a branch (their lookups and SiLUs overlap), then
+      // their dS into the sums
       float vp[8], vs[8];
+      [[maybe_unused]] int lpv[8], ltv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int k = 8 * g + e;
         const int col = 32 * c + k;
         const bool keep = row_ok && col < cmax;
         float x = alpha * __uint_as_float(sr[k]);
-        [[maybe_unused]] int lp = cp, lt = ct;
         if constexpr (RAB) {
-          float bias;
-          if constexpr (FP) {
-            bias = rc.pos_c;
+          if constexpr (GEN) {
+            lpv[e] = rab_lane(rr.pe_i - (j0 + k));
+            ltv[e] = rab_lane(rr.ts_i - __shfl_sync(0xffffffffu, ts_key, k));
+            x += __shfl_sync(0xffffffffu, rr.pos_l, lpv[e]) +
+                 __shfl_sync(0xffffffffu, rr.time_l, ltv[e]);
           } else {
-            lp = rab_lane(rr.pe_i - (j0 + k));
-            bias = __shfl_sync(0xffffffffu, rr.pos_l, lp);
+            const float bp = (PM == 1 && k >= kbp) ? q.p1 : q.p0;
+            const float bt = (TM == 1 && k >= kbt) ? q.t1 : q.t0;
+            x += bp + bt;
           }
-          if constexpr (TM == 0) {
-            bias += rc.time_c;
-          } else {
-            lt = rab_lane(rr.ts_i - __shfl_sync(0xffffffffu, rc.ts_lane, k));
-            bias += __shfl_sync(0xffffffffu, rr.time_l, lt);
-          }
-          x += bias;
         }
         const float sg = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
         const float isg = inv_n * sg;
         if constexpr (MODE != 2) vp[e] = keep ? isg * x : 0.0f;
-        if constexpr (MODE != 1) {
-          const float ds = keep ? isg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[k]) : 0.0f;
-          vs[e] = ds;
-          if constexpr (RAB) {
-            if constexpr (!FP) {
-              if (lp != cp) {
-                atomicAdd(hp + cp, sp);
-                sp = 0.f;
-                cp = lp;
-              }
-            }
-            sp += ds;
-            if constexpr (TM == 1) flush_warp(ht, ct, st, lt);
-            if constexpr (TM == 2)
-              atomicAdd(ht + lt, ds);
-            else
-              st += ds;
-          }
-        }
+        if constexpr (MODE != 1)
+          vs[e] = keep ? isg * fmaf(x, 1.0f - sg, 1.0f) * __uint_as_float(pr[k]) : 0.0f;
       }
       if constexpr (MODE != 2) put8(smem + C::HI_OFF, smem + C::LO_OFF, 32 * c + 8 * g, vp);
       if constexpr (MODE != 1) put8(smem + C::DHI_OFF, smem + C::DLO_OFF, 32 * c + 8 * g, vs);
+      if constexpr (RAB && MODE != 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int k = 8 * g + e;
+          if constexpr (GEN) {
+            if (lpv[e] != cp) {  // rows cross a position edge at different keys
+              atomicAdd(hp + cp, sp);
+              sp = 0.f;
+              cp = lpv[e];
+            }
+            sp += vs[e];
+            flush_warp(ht, ct, st, ltv[e]);
+            st += vs[e];
+          } else {
+            tot += vs[e];
+            if constexpr (PM == 1) ap1 += k >= kbp ? vs[e] : 0.0f;
+            if constexpr (TM == 1) at1 += k >= kbt ? vs[e] : 0.0f;
+          }
+        }
+      }
+    }
+    if constexpr (RAB && MODE != 1 && !GEN) {
+      if constexpr (PM == 0) {
+        sp += tot;
+      } else {
+        sp += tot - ap1;
+        flush_warp(hp, cp, sp, kbp < 32 ? lp0 + 1 : lp0);
+        sp += ap1;
+      }
+      if constexpr (TM == 0) {
+        st += tot;
+      } else {
+        st += tot - at1;
+        flush_warp(ht, ct, st, kbt < 32 ? lt0 + 1 : lt0);
+        st += at1;
+      }
     }
   };
-  using T_ = std::true_type;
-  using F_ = std::false_type;
-  using TM0 = std::integral_constant<int, 0>;
-  using TM1 = std::integral_constant<int, 1>;
-  using TM2 = std::integral_constant<int, 2>;
+  using I0 = std::integral_constant<int, 0>;
+  using I1 = std::integral_constant<int, 1>;
+  using I2 = std::integral_constant<int, 2>;
+  // the bias's view of this warp's two key chunks of the current item:
+  // the timestamps (lane = key) and whether they are in order; and of the
+  // current query block, each chunk's modes and values
+  int ts_key0 = 0, ts_key1 = 0;
+  bool ord0 = true, ord1 = true;
+  BRab q0{}, q1{};
   // the timestamp of this thread's row of query block qt (a row past the
   // sequence reads the last token; its results are never kept)
   auto row_ts = [&](int qt) -> int {
@@ -370,14 +444,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return 0;
     }
   };
-  // the bias's constant parts of the two chunks for query block qt, whose
-  // row timestamp ts_i was loaded ahead
+  // the two chunks' modes and values for query block qt, whose row
+  // timestamp ts_i was loaded ahead
   auto prep = [&](int qt, int ts_i, int kbase) {
     if constexpr (RAB) {
       rr.pe_i = kBM * qt + row;
       rr.ts_i = ts_i;
-      rc0 = rab_chunk<false>(rr, kbase + 64 * wg, ts_key0);
-      rc1 = rab_chunk<false>(rr, kbase + 64 * wg + 32, ts_key1);
+      q0 = prep_chunk(kbase + 64 * wg, ts_key0, ord0);
+      q1 = prep_chunk(kbase + 64 * wg + 32, ts_key1, ord1);
     }
   };
   // the pass of MODE over this warpgroup's two chunks of query block qt
@@ -389,20 +463,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if constexpr (decltype(mode_t)::value != 1) tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
       const int j0 = kbase + 32 * c;
       if constexpr (RAB) {
-        const RabChunk rc = (c & 1) ? rc1 : rc0;
-        if (!((c & 1) ? ord1 : ord0))
-          chunk(F_{}, TM2{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
-        else if (rc.fix_p && rc.fix_t)
-          chunk(T_{}, TM0{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
-        else if (rc.fix_p)
-          chunk(T_{}, TM1{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
-        else if (rc.fix_t)
-          chunk(F_{}, TM0{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+        const BRab q = (c & 1) ? q1 : q0;
+        const int tsk = (c & 1) ? ts_key1 : ts_key0;
+        const uint32_t modes = (q.pk >> 22) & 15u;  // pm | tm << 2, warp-uniform
+        if (modes == 0u)
+          chunk(I0{}, I0{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+        else if (modes == 1u)
+          chunk(I1{}, I0{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+        else if (modes == 4u)
+          chunk(I0{}, I1{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+        else if (modes == 5u)
+          chunk(I1{}, I1{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
         else
-          chunk(F_{}, TM1{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+          chunk(I2{}, I2{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
       } else {
-        const RabChunk rc{};
-        chunk(T_{}, TM0{}, mode_t, c, sr, pr, rc, j0, cmax, row_ok);
+        const BRab q{};
+        chunk(I0{}, I0{}, mode_t, c, sr, pr, q, 0, j0, cmax, row_ok);
       }
     }
   };
