@@ -65,6 +65,14 @@ def causal_flops(w: workloads.Workload, num_targets=None) -> float:
     return float(4.0 * w.d * w.heads * pairs)
 
 
+def candidate_row_flops(w: workloads.Workload, num_targets) -> float:
+    """4 d FLOPs per kept pair of the candidates' rows only: a candidate of
+    sequence b sees its hist_b history keys and itself."""
+    L = w.lengths.astype(np.float64)
+    bm = np.asarray(num_targets, dtype=np.float64)
+    return float(4.0 * w.d * w.heads * np.sum(bm * (L - bm + 1)))
+
+
 BWD_METRIC = "HSTU jagged causal attn bwd (dQ, dK, dV): TFLOPS at 10 d FLOP per kept pair; ms/call"
 
 
@@ -219,11 +227,12 @@ def aggregate(flops_per_rank: float, ms_local: float, world: int, device=None):
 
 
 def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int | None = None,
-                      num_targets=None, norm_gate=None, rab=None):
+                      num_targets=None, norm_gate=None, rab=None, candidates_only: bool = False):
     """Time the oracle on a bounded, uniformly random sample of rows.
 
     With ``norm_gate`` = (u, gamma, beta, eps) the sample is of tokens, each
-    with all its heads and the output stage.
+    with all its heads and the output stage.  With ``candidates_only`` the
+    rows are drawn from the candidates' rows.
     Returns (flops_of_sample / seconds, description, threads, seconds)."""
     from oracle import reference
     threads = threads or reference.default_threads()
@@ -235,9 +244,13 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
 
     per_row = w.heads if norm_gate is not None else 1
 
+    pool = None
+    if candidates_only:
+        pool = np.concatenate([np.arange(off[b] + hist_of[b], off[b + 1]) for b in range(w.batch)])
+
     def rows(nr):
         nr = max(1, nr // per_row)
-        t = rng.integers(0, w.total, size=nr)
+        t = rng.integers(0, w.total, size=nr) if pool is None else pool[rng.integers(0, len(pool), nr)]
         h = rng.integers(0, w.heads, size=nr)
         i = t - off[seq_of[t]]
         hist = hist_of[seq_of[t]]
@@ -268,7 +281,8 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
                 f"of the {w.name} workload ({fl / 1e9:.2f} causal GFLOP), fp64 C oracle, "
                 f"{threads} threads")
     else:
-        desc = (f"{n} uniformly sampled (token, head) output rows of the {w.name} workload "
+        desc = (f"{n} uniformly sampled (token, head) output rows "
+                f"{'(candidates only) ' if candidates_only else ''}of the {w.name} workload "
                 f"({fl / 1e9:.2f} causal GFLOP), fp64 C oracle, {threads} threads")
     return fl / dt / 1e12, desc, threads, dt
 
@@ -338,7 +352,8 @@ def run_reference(args, w, nt=None):
     desc, threads = "", 0
     for s in range(args.warmup + args.steps):
         val, desc, threads, dt = cpu_oracle_sample(w, qf, kf, vf, per_step_s, seed=s,
-                                                   num_targets=nt, norm_gate=ng, rab=_cpu_rab(args, w))
+                                                   num_targets=nt, norm_gate=ng, rab=_cpu_rab(args, w),
+                                                   candidates_only=args.candidates_only)
         if s >= args.warmup:
             vals.append(val)
     value = statistics.mean(vals)
@@ -347,12 +362,19 @@ def run_reference(args, w, nt=None):
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, **w.describe(), **_targets_desc(nt), **_norm_gate_desc(args),
-                   **_rab_desc(args)},
+                   **_rab_desc(args), **_co_desc(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _co_desc(args) -> dict:
+    if not args.candidates_only:
+        return {}
+    return {"rows": "the candidates' only (HSTU_PLAN_CANDIDATES_ONLY): the history's keys and "
+                    "values are a resident cache"}
 
 
 def _targets_desc(nt) -> dict:
@@ -545,8 +567,12 @@ def run_ours(args, w, nt=None):
         ts_h, pos_h, time_h = workloads.draw_rab(w)
         ts_pin = torch.from_numpy(ts_h).pin_memory()
         rab = (ts_pin.to(dev), torch.from_numpy(pos_h).to(dev), torch.from_numpy(time_h).to(dev))
+    co = args.candidates_only
+    if co and (nt is None or ng):
+        raise SystemExit("--candidates-only needs the candidates workload and no --norm-gate")
     plan = binding.hstu_plan_create_ex(w.offsets, nt, w.batch, w.heads, w.d, w.max_seqlen,
-                                       binding.HSTU_PLAN_NORM_GATE if ng else 0)
+                                       (binding.HSTU_PLAN_NORM_GATE if ng else 0) |
+                                       (binding.HSTU_PLAN_CANDIDATES_ONLY if co else 0))
 
     def launch():
         binding.hstu_attn_fwd_plan_ex(plan, q, k, v, w.alpha, w.inv_n, out, rab=rab,
@@ -585,7 +611,7 @@ def run_ours(args, w, nt=None):
     clocks = sampler.stop(wall0, wall0 + wall, t_warm)
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(times_ms)
-    flops = causal_flops(w, nt)
+    flops = candidate_row_flops(w, nt) if co else causal_flops(w, nt)
     value, ms_max = aggregate(flops, ms, world, dev)
     st, site = binding.hstu_last_status()
     if st != binding.HSTU_OK:
@@ -607,8 +633,33 @@ def run_ours(args, w, nt=None):
     offsets_host = w.offsets.copy()
 
     tse = torch.empty_like(rab[0]) if rab is not None else None
+    # candidates only: the history's keys and values (and queries) are the
+    # resident cache; each step brings the candidates' q, k, v rows and
+    # returns their outputs, one copy per sequence and tensor
+    cand_rows = []
+    if co:
+        for dst, src in zip((qe, ke, ve), pin[:3]):
+            dst.copy_(src)
+        off = w.offsets.astype(np.int64)
+        cand_rows = [(int(off[b + 1] - nt[b]), int(off[b + 1])) for b in range(w.batch) if nt[b] > 0]
+
+    def e2e_step_candidates():
+        for s0, s1 in cand_rows:
+            qe[s0:s1].copy_(pin[0][s0:s1], non_blocking=True)
+            ke[s0:s1].copy_(pin[1][s0:s1], non_blocking=True)
+            ve[s0:s1].copy_(pin[2][s0:s1], non_blocking=True)
+        binding.hstu_attn_fwd_plan_ex(plan, qe, ke, ve, w.alpha, w.inv_n, oe,
+                                      rab=(tse, rab[1], rab[2]) if rab is not None else None,
+                                      stream=stream)
+        for s0, s1 in cand_rows:
+            out_h[s0:s1].copy_(oe[s0:s1], non_blocking=True)
 
     def e2e_step():
+        if co:
+            if rab is not None:
+                tse.copy_(ts_pin, non_blocking=True)
+            e2e_step_candidates()
+            return
         qe.copy_(pin[0], non_blocking=True)
         ke.copy_(pin[1], non_blocking=True)
         ve.copy_(pin[2], non_blocking=True)
@@ -659,13 +710,17 @@ def run_ours(args, w, nt=None):
     if rab is not None:
         h2d += 4 * w.total
     d2h = w.total * w.heads * w.d * elem
+    if co:
+        n_cand = sum(s1 - s0 for s0, s1 in cand_rows)
+        h2d = 3 * n_cand * w.heads * w.d * elem + (4 * w.total if rab is not None else 0)
+        d2h = n_cand * w.heads * w.d * elem
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         qf, kf, vf = (t.float().numpy() for t in (q_h, k_h, v_h))
         val, desc, threads, _ = cpu_oracle_sample(w, qf, kf, vf, args.cpu_seconds, num_targets=nt,
                                                   norm_gate=_cpu_norm_gate(args, w),
-                                                  rab=_cpu_rab(args, w))
+                                                  rab=_cpu_rab(args, w), candidates_only=co)
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
 
     binding.hstu_plan_destroy(plan)
@@ -675,6 +730,7 @@ def run_ours(args, w, nt=None):
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {**w.describe(), **_targets_desc(nt), **_norm_gate_desc(args), **_rab_desc(args),
+                       **_co_desc(args),
                        "l2": "flushed between steps (256 MiB write)",
                        "work_items": n_items, "grid": grid, "block": block, "smem_bytes": smem,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -713,11 +769,17 @@ def main(argv=None):
                     help="fuse the layer's output stage Norm(A V) * U into the timed call")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (dQ, dK, dV) instead of the forward")
+    ap.add_argument("--candidates-only", action="store_true",
+                    help="with --workload candidates: compute the candidates' rows only "
+                         "(the history's keys and values cached)")
     ap.add_argument("--rab", action="store_true",
                     help="add the relative attention bias rab_{p,t} (timestamps and bucketed tables)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.candidates_only and (args.workload != "candidates" or args.backward or args.sweep
+                                 or args.norm_gate):
+        ap.error("--candidates-only goes with --workload candidates (forward, no --norm-gate)")
     names = list(workloads.WORKLOAD_NAMES) + ["candidates"] if args.sweep else [args.workload]
     rc = 0
     for name in names:

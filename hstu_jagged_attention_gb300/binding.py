@@ -75,6 +75,8 @@ _SIGNATURES = {
     "hstu_plan_item_hist": (ctypes.c_int, [_VP, _I32P, ctypes.c_int, _IP]),
     "hstu_worklist_build_targets": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int, _I32P,
                                                    _I32P, ctypes.c_int, _IP]),
+    "hstu_worklist_build_candidates": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int,
+                                                      _I32P, _I32P, ctypes.c_int, _IP]),
     "hstu_plan_create_ex": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_uint32, ctypes.POINTER(_VP)]),
     "hstu_attn_fwd_norm_gate_plan": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float,
@@ -103,6 +105,7 @@ _SIGNATURES = {
 
 HSTU_PLAN_NORM_GATE = 1
 HSTU_PLAN_BACKWARD = 2
+HSTU_PLAN_CANDIDATES_ONLY = 4
 
 _lib = None
 
@@ -446,22 +449,30 @@ def hstu_plan_item_hist(plan: Plan) -> np.ndarray:
     return buf[:got.value]
 
 
-def hstu_worklist_build_targets(host_offsets, num_targets, heads: int):
-    """Host-only candidate work list: (items int32 (n, 4), hist int32 (n,))."""
+def _worklist_with_hist(name: str, host_offsets, num_targets, heads: int):
     off = _host_offsets(host_offsets)
     batch = len(off) - 1
     nt = _host_targets(num_targets, batch)
+    fn = getattr(lib(), name)
     n = ctypes.c_int()
-    _check(lib().hstu_worklist_build_targets(off.ctypes.data_as(_I32P), nt.ctypes.data_as(_I32P),
-                                             batch, int(heads), None, None, 0, ctypes.byref(n)),
-           "hstu_worklist_build_targets")
+    _check(fn(off.ctypes.data_as(_I32P), nt.ctypes.data_as(_I32P), batch, int(heads), None, None, 0,
+              ctypes.byref(n)), name)
     items = np.zeros((max(n.value, 1), 4), dtype=np.int32)
     hist = np.zeros(max(n.value, 1), dtype=np.int32)
-    _check(lib().hstu_worklist_build_targets(off.ctypes.data_as(_I32P), nt.ctypes.data_as(_I32P),
-                                             batch, int(heads), items.ctypes.data_as(_I32P),
-                                             hist.ctypes.data_as(_I32P), n.value, ctypes.byref(n)),
-           "hstu_worklist_build_targets")
+    _check(fn(off.ctypes.data_as(_I32P), nt.ctypes.data_as(_I32P), batch, int(heads),
+              items.ctypes.data_as(_I32P), hist.ctypes.data_as(_I32P), n.value, ctypes.byref(n)), name)
     return items[:n.value], hist[:n.value]
+
+
+def hstu_worklist_build_targets(host_offsets, num_targets, heads: int):
+    """Host-only candidate work list: (items int32 (n, 4), hist int32 (n,))."""
+    return _worklist_with_hist("hstu_worklist_build_targets", host_offsets, num_targets, heads)
+
+
+def hstu_worklist_build_candidates(host_offsets, num_targets, heads: int):
+    """Host-only work list of a HSTU_PLAN_CANDIDATES_ONLY plan: the candidate
+    work list's items whose query block holds a candidate row."""
+    return _worklist_with_hist("hstu_worklist_build_candidates", host_offsets, num_targets, heads)
 
 
 def hstu_attn_fwd_plan(plan: Plan, q, k, v, alpha: float, inv_n: float, out, stream=None) -> None:

@@ -56,12 +56,28 @@ int check_targets(const int32_t* off, const int32_t* nt, int batch) {
 
 // Work list and (with candidates) the per-item history lengths.
 int build_worklist(const int32_t* off, const int32_t* nt, int batch, int heads,
-                   std::vector<hstu::Item>& items, std::vector<int32_t>& hist) {
+                   std::vector<hstu::Item>& items, std::vector<int32_t>& hist,
+                   bool candidates_only = false) {
   try {
     items.resize((size_t)hstu::count_items(off, batch, heads));
     if (nt) {
       hist.resize(items.size());
       hstu::fill_items_targets(off, nt, batch, heads, items.data(), hist.data());
+      if (candidates_only) {
+        // keep the query blocks that hold a candidate row (rows hist .. n-1):
+        // qt >= hist / 128, with at least one candidate; the order stays
+        size_t m = 0;
+        for (size_t i = 0; i < items.size(); ++i) {
+          const int n = items[i].y, qt = items[i].w, hs = hist[i];
+          if (hs < n && qt >= hs / HSTU_BLOCK_M) {
+            items[m] = items[i];
+            hist[m] = hist[i];
+            ++m;
+          }
+        }
+        items.resize(m);
+        hist.resize(m);
+      }
     } else {
       hstu::fill_items(off, batch, heads, items.data());
     }
@@ -343,9 +359,14 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
   if (!plan) return HSTU_ERR_INVALID_ARG;
   *plan = nullptr;
   if (heads < 1 || max_seqlen < 0 ||
-      (flags & ~(unsigned)(HSTU_PLAN_NORM_GATE | HSTU_PLAN_BACKWARD)))
+      (flags & ~(unsigned)(HSTU_PLAN_NORM_GATE | HSTU_PLAN_BACKWARD | HSTU_PLAN_CANDIDATES_ONLY)))
     return HSTU_ERR_INVALID_ARG;
   if ((flags & HSTU_PLAN_BACKWARD) && nt) return HSTU_ERR_INVALID_ARG;  // causal only
+  // the candidates' rows only: needs candidates; the output stage normalises
+  // every row and the backward every pair, so neither combines with it
+  const bool cand_only = (flags & HSTU_PLAN_CANDIDATES_ONLY) != 0;
+  if (cand_only && (!nt || (flags & (HSTU_PLAN_NORM_GATE | HSTU_PLAN_BACKWARD))))
+    return HSTU_ERR_INVALID_ARG;
   const bool norm = (flags & HSTU_PLAN_NORM_GATE) != 0;
   if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
   int rc = check_offsets(off, batch, max_seqlen);
@@ -359,7 +380,7 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
   p->max_seqlen = max_seqlen;
   p->flags = flags;
   p->total = batch ? off[batch] : 0;
-  if ((rc = build_worklist(off, nt, batch, heads, p->items, p->hist)) != HSTU_OK) {
+  if ((rc = build_worklist(off, nt, batch, heads, p->items, p->hist, cand_only)) != HSTU_OK) {
     delete p;
     return rc;
   }
@@ -648,6 +669,26 @@ int hstu_worklist_build_targets(const int32_t* host_offsets, const int32_t* host
   std::vector<hstu::Item> items;
   std::vector<int32_t> hist;
   if ((rc = build_worklist(host_offsets, host_num_targets, batch, heads, items, hist)) != HSTU_OK)
+    return rc;
+  *n_items = (int)items.size();
+  const size_t n = std::min(items.size(), (size_t)capacity);
+  if (host_items) std::memcpy(host_items, items.data(), n * sizeof(hstu::Item));
+  if (host_hist) std::memcpy(host_hist, hist.data(), n * sizeof(int32_t));
+  return HSTU_OK;
+}
+
+int hstu_worklist_build_candidates(const int32_t* host_offsets, const int32_t* host_num_targets,
+                                   int batch, int heads, int32_t* host_items, int32_t* host_hist,
+                                   int capacity, int* n_items) {
+  if (!n_items || heads < 1 || capacity < 0 || (!host_num_targets && batch > 0))
+    return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(host_offsets, batch, -1);
+  if (rc != HSTU_OK) return rc;
+  if ((rc = check_targets(host_offsets, host_num_targets, batch)) != HSTU_OK) return rc;
+  std::vector<hstu::Item> items;
+  std::vector<int32_t> hist;
+  if ((rc = build_worklist(host_offsets, host_num_targets, batch, heads, items, hist, true)) !=
+      HSTU_OK)
     return rc;
   *n_items = (int)items.size();
   const size_t n = std::min(items.size(), (size_t)capacity);

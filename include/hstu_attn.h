@@ -288,6 +288,31 @@ int hstu_plan_create_ex(const int32_t* host_offsets, const int32_t* host_num_tar
                         int heads, int d, int max_seqlen, uint32_t flags, hstu_plan** plan);
 
 /*
+ * The candidates' rows only -- HSTU paper section 3.4 (M-FALCON): the
+ * history's keys and values are computed once and serve every batch of
+ * candidates.  A plan made by hstu_plan_create_ex with host_num_targets
+ * and HSTU_PLAN_CANDIDATES_ONLY keeps only the work items of query blocks
+ * that hold a candidate row (qt >= hist / 128, num_targets[b] > 0).  So
+ * hstu_attn_fwd_plan and hstu_attn_fwd_plan_ex (rab allowed, ng not)
+ * compute:
+ *   - every candidate row, as with the full candidate mask;
+ *   - the history rows that share a 128-row block with the first
+ *     candidates, with the same values as the full pass;
+ *   - no other history row: those rows of out are left as they were.
+ * The keys and values of the history are read from k and v: these hold the
+ * cached history followed by the candidates.
+ *
+ * HSTU_PLAN_CANDIDATES_ONLY needs host_num_targets; with
+ * HSTU_PLAN_NORM_GATE or HSTU_PLAN_BACKWARD: HSTU_ERR_INVALID_ARG.
+ * hstu_worklist_build_candidates  the host-only work list of such a plan
+ * (items and their history lengths, as hstu_worklist_build_targets).
+ */
+#define HSTU_PLAN_CANDIDATES_ONLY 4u
+int hstu_worklist_build_candidates(const int32_t* host_offsets, const int32_t* host_num_targets,
+                                   int batch, int heads, int32_t* host_items, int32_t* host_hist,
+                                   int capacity, int* n_items);
+
+/*
  * Relative attention bias rab_{p,t}: HSTU paper section 3 (a bias that
  * merges relative position p and time t, added inside the attention's
  * nonlinearity), section 3.4 (M-FALCON modifies it for candidates) and

@@ -64,6 +64,17 @@ def items_targets(offsets, num_targets, heads: int, block_m: int = BLOCK_M):
 
 
 
+def items_candidates(offsets, num_targets, heads: int, block_m: int = BLOCK_M):
+    """The candidates-only work list: the items of items_targets whose query
+    block holds a candidate row (rows hist .. n-1 of a sequence with at least
+    one candidate), in the same order."""
+    it, hs = items_targets(offsets, num_targets, heads, block_m)
+    keep = [r for r in range(len(hs))
+            if hs[r] < it[r, 1] and any(hs[r] <= i < it[r, 1]
+                                        for i in range(it[r, 3] * block_m, (it[r, 3] + 1) * block_m))]
+    return it[keep].reshape(-1, 4), hs[keep]
+
+
 def items_bwd(offsets, heads: int, block_m: int = BLOCK_M) -> np.ndarray:
     """Backward work items: one per (sequence, head, key block kt), which the
     query blocks kt .. nq - 1 see (causal), costing nq - kt; ordered by cost

@@ -254,3 +254,44 @@ def test_bwd_rab_validation_before_any_cuda_call():
     # without the bias the table gradients are not looked at
     binding.hstu_attn_bwd_ex(0, 0, 0, 0, np.zeros(1, np.int32), 0, 2, 64, 0, 1.0, 1.0, 0, 0, 0,
                              stream=0)
+
+
+# ------------------------------------------------ candidates only (M-FALCON's cached history)
+@pytest.mark.parametrize("seed", range(8))
+def test_candidates_only_worklist_bit_exact_random(seed):
+    rng = np.random.default_rng(1300 + seed)
+    nb = int(rng.integers(0, 20))
+    lengths = rng.integers(0, 700, size=nb)
+    # edges: no candidates, all candidates, history a multiple of 128
+    nt = [int(rng.choice([0, n, n % 128, rng.integers(0, n + 1)])) if n else 0 for n in lengths]
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    heads = int(rng.integers(1, 4))
+    items, hist = binding.hstu_worklist_build_candidates(off, np.array(nt, np.int32), heads)
+    ref_items, ref_hist = oracle_worklist.items_candidates(off, nt, heads)
+    assert np.array_equal(items, ref_items.reshape(-1, 4))
+    assert np.array_equal(hist, ref_hist)
+
+
+def test_candidates_only_worklist_is_a_subsequence_of_the_candidate_one():
+    w, nt = workloads.candidate_workload()
+    full, fh = binding.hstu_worklist_build_targets(w.offsets, nt, w.heads)
+    part, ph = binding.hstu_worklist_build_candidates(w.offsets, nt, w.heads)
+    keys = {tuple(r) for r in full.tolist()}
+    assert all(tuple(r) in keys for r in part.tolist())
+    pos = [full.tolist().index(r) for r in part.tolist()[:50]]
+    assert pos == sorted(pos)
+    # each sequence keeps its candidates' blocks: 1024 candidates span 8 or 9 blocks
+    per_seq = len(part) // w.heads
+    assert 8 * w.batch <= per_seq <= 9 * w.batch
+
+
+def test_candidates_only_plan_flag_validation_before_any_cuda_call():
+    off = np.array([0, 300], np.int32)
+    nt = np.array([20], np.int32)
+    for flags, targets in ((binding.HSTU_PLAN_CANDIDATES_ONLY, None),
+                           (binding.HSTU_PLAN_CANDIDATES_ONLY | binding.HSTU_PLAN_NORM_GATE, nt),
+                           (binding.HSTU_PLAN_CANDIDATES_ONLY | binding.HSTU_PLAN_BACKWARD, nt),
+                           (8, nt)):
+        with pytest.raises(binding.HstuError) as e:
+            binding.hstu_plan_create_ex(off, targets, 1, 2, 64, 300, flags)
+        assert e.value.code == binding.HSTU_ERR_INVALID_ARG, flags
