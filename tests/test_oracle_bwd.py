@@ -7,7 +7,10 @@ chain rule out (hstu_oracle.c).  Pins, each independent of that code:
 * torch autograd of a dense fp64 formulation (the post's PyTorch
   definition: score matmul, scale, SiLU, tril mask, 1/n, matmul with V);
 * linearity: the gradients are linear in dout;
-* a one-token sequence's closed form.
+* a one-token sequence's closed form;
+* with the bias: torch autograd of the dense definition with the tables
+  as parameters and the bias matrix indexed by numpy's float-log2 buckets
+  (the tables' gradients included).
 """
 import numpy as np
 import pytest
@@ -181,3 +184,62 @@ def test_bias_table_gradients_by_finite_differences():
             assert abs(fd - g[e]) <= 1e-5 * max(1.0, abs(g[e])), (name, e, fd, g[e])
     # buckets that no kept pair uses get exactly zero
     assert np.count_nonzero(dpos) <= len(pos) and np.all(np.isfinite(dtime))
+
+
+def _bucket_np(delta, n):
+    delta = np.maximum(np.asarray(delta, dtype=np.float64), 0.0)
+    return np.minimum(np.floor(np.log2(delta + 1.0)), n - 1).astype(np.int64)
+
+
+def dense_torch_rab(q, k, v, do, off, ts, pos, time, alpha, inv_n, num_targets=None):
+    """torch autograd (fp64) of the dense definition with the bias: the
+    tables are leaf tensors, indexed by buckets that numpy computes from
+    float log2; candidates (if any) sit at position hist and see the history
+    and themselves.  Returns (dq, dk, dv, dpos, dtime)."""
+    Q, K, V = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    Pt = torch.tensor(np.asarray(pos, np.float64), requires_grad=True)
+    Tt = torch.tensor(np.asarray(time, np.float64), requires_grad=True)
+    loss = 0.0
+    for b in range(len(off) - 1):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        n = s1 - s0
+        if n == 0:
+            continue
+        hist = n - (int(num_targets[b]) if num_targets is not None else 0)
+        i = np.arange(n)[:, None]
+        j = np.arange(n)[None, :]
+        bp = _bucket_np(np.minimum(i, hist) - np.minimum(j, hist), len(pos))
+        t = np.asarray(ts[s0:s1], dtype=np.float64)
+        bt = _bucket_np(t[:, None] - t[None, :], len(time))
+        mask = torch.tensor(((j <= i) & ((j < hist) | (j == i))).astype(np.float64))
+        bias = Pt[torch.tensor(bp)] + Tt[torch.tensor(bt)]
+        qb, kb, vb = (x[s0:s1].transpose(0, 1) for x in (Q, K, V))
+        s = alpha * qb @ kb.transpose(1, 2) + bias
+        p = torch.nn.functional.silu(s) * mask * inv_n
+        out = (p @ vb).transpose(0, 1)
+        loss = loss + (out * torch.tensor(do[s0:s1], dtype=torch.float64)).sum()
+    loss.backward()
+    return Q.grad.numpy(), K.grad.numpy(), V.grad.numpy(), Pt.grad.numpy(), Tt.grad.numpy()
+
+
+def rab_case(rng, lengths, heads, d, npos, ntime):
+    q, k, v, do, off = _case(rng, lengths, heads, d)
+    ts = np.concatenate([np.cumsum(rng.integers(-300, 4000, size=int(n))) for n in lengths])
+    ts = (ts - (ts.min() if ts.size else 0)).astype(np.int64)
+    pos = (0.4 * rng.standard_normal(npos)).astype(np.float32)
+    time = (0.4 * rng.standard_normal(ntime)).astype(np.float32)
+    return q, k, v, do, off, ts, pos, time
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bias_backward_matches_torch_autograd(seed):
+    rng = np.random.default_rng(40 + seed)
+    lengths = rng.integers(0, 45, size=4)
+    nt = [int(rng.integers(0, n + 1)) for n in lengths] if seed % 2 else None
+    npos, ntime = int(rng.integers(1, 33)), int(rng.integers(1, 33))
+    q, k, v, do, off, ts, pos, time = rab_case(rng, lengths, 2, 8, npos, ntime)
+    got = reference.hstu_bwd(q, k, v, do, off, 0.5, 0.07, num_targets=nt, rab=(ts, pos, time),
+                             table_grads=True)
+    want = dense_torch_rab(q, k, v, do, off, ts, pos, time, 0.5, 0.07, nt)
+    for g, w_ in zip(got, want):
+        assert np.abs(g - w_).max() <= 1e-12 * max(1.0, np.abs(w_).max())

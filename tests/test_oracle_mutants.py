@@ -311,3 +311,48 @@ def test_bwd_mutant_is_caught(tmp_path, name):
     old, new = BWD_MUTANTS[name]
     assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     assert not _bwd_pins_pass(_build(tmp_path, name, src.replace(old, new)))
+
+
+# The bias tables' gradients: each mutant plants a plausible mistake in the
+# per-pair sums; the pin is torch autograd of the dense definition with the
+# tables as parameters (tests/test_oracle_bwd.py).  Both tables have 32
+# entries here, so a bucket of one table always indexes the other in bounds.
+TABLE_GRAD_MUTANTS = {
+    "table_grads_from_p": ("gp[bp] += ds;", "gp[bp] += p;"),
+    "time_grads_by_position_bucket": ("gt[bt] += ds;", "gt[bp] += ds;"),
+    "table_grads_scaled_by_alpha": ("gp[bp] += ds;", "gp[bp] += J->alpha * ds;"),
+}
+
+
+def _table_grad_pins_pass(L) -> bool:
+    from tests.test_oracle_bwd import dense_torch_rab, rab_case
+    f, dptr, i64 = (ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
+                    ctypes.POINTER(ctypes.c_int64))
+    L.hstu_oracle_bwd_f64.argtypes = [f, f, f, f, i64, i64, i64, f, ctypes.c_int, f, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                      ctypes.c_double, dptr, dptr, dptr, dptr, dptr, ctypes.c_int]
+    P = lambda a, t: a.ctypes.data_as(ctypes.POINTER(t))
+    rng = np.random.default_rng(33)
+    q, k, v, do, off, ts, pos, time = rab_case(rng, [30, 17, 41], 2, 8, 32, 32)
+    off = off.astype(np.int64)
+    grads = [np.zeros(q.shape) for _ in range(3)] + [np.zeros(32), np.zeros(32)]
+    rc = L.hstu_oracle_bwd_f64(P(q, ctypes.c_float), P(k, ctypes.c_float), P(v, ctypes.c_float),
+                               P(do, ctypes.c_float), P(off, ctypes.c_int64), None,
+                               P(ts, ctypes.c_int64), P(pos, ctypes.c_float), 32,
+                               P(time, ctypes.c_float), 32, len(off) - 1, q.shape[1], q.shape[2],
+                               0.4, 0.05, *(P(g, ctypes.c_double) for g in grads), 2)
+    assert rc == 0
+    want = dense_torch_rab(q, k, v, do, off, ts, pos, time, 0.4, 0.05)
+    return all(np.abs(g - w_).max() <= 1e-12 * max(1.0, np.abs(w_).max()) for g, w_ in zip(grads, want))
+
+
+def test_unmutated_copy_passes_the_table_grad_pins(tmp_path):
+    assert _table_grad_pins_pass(_build(tmp_path, "orig_g", open(oracle_build.SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(TABLE_GRAD_MUTANTS))
+def test_table_grad_mutant_is_caught(tmp_path, name):
+    src = open(oracle_build.SRC).read()
+    old, new = TABLE_GRAD_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    assert not _table_grad_pins_pass(_build(tmp_path, name, src.replace(old, new)))
