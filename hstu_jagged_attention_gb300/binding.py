@@ -92,9 +92,11 @@ _SIGNATURES = {
                                           _VP, _VP, _VP]),
     "hstu_worklist_build_bwd": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int,
                                                _IP]),
-    "hstu_attn_bwd_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
+    "hstu_attn_bwd_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _I32P, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, _RABP, ctypes.c_float,
                                         ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "hstu_worklist_build_bwd_targets": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int,
+                                                       _I32P, _I32P, ctypes.c_int, _IP]),
     "hstu_attn_bwd_plan_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _RABP, ctypes.c_float,
                                              ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP]),
     "hstu_attn_fwd_norm_gate": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP,
@@ -298,12 +300,15 @@ def hstu_attn_bwd_plan(plan: Plan, q, k, v, dout, alpha: float, inv_n: float, dq
 
 
 def hstu_attn_bwd_ex(q, k, v, dout, offsets, batch: int, heads: int, d: int, max_seqlen: int,
-                     alpha: float, inv_n: float, dq, dk, dv, rab=None, dpos=None, dtime=None,
-                     stream=None) -> None:
-    """hstu_attn_bwd with the bias ``rab`` = (timestamps, pos, time): dpos and
-    dtime (fp32 device, one entry per table entry) receive the tables' gradients."""
+                     alpha: float, inv_n: float, dq, dk, dv, num_targets=None, rab=None, dpos=None,
+                     dtime=None, stream=None) -> None:
+    """hstu_attn_bwd with candidates (``num_targets``, host memory) and the
+    bias ``rab`` = (timestamps, pos, time): dpos and dtime (fp32 device, one
+    entry per table entry) receive the tables' gradients."""
     off_ptr, keep = _offsets_arg(offsets)
-    _check(lib().hstu_attn_bwd_ex(_addr(q), _addr(k), _addr(v), _addr(dout), off_ptr, int(batch),
+    nt = None if num_targets is None else _host_targets(num_targets, int(batch))
+    _check(lib().hstu_attn_bwd_ex(_addr(q), _addr(k), _addr(v), _addr(dout), off_ptr,
+                                  None if nt is None else nt.ctypes.data_as(_I32P), int(batch),
                                   int(heads), int(d), int(max_seqlen), _rab_struct(rab),
                                   float(alpha), float(inv_n), _addr(dq), _addr(dk), _addr(dv),
                                   _addr(dpos), _addr(dtime), _stream(stream)), "hstu_attn_bwd_ex")
@@ -467,6 +472,11 @@ def _worklist_with_hist(name: str, host_offsets, num_targets, heads: int):
 def hstu_worklist_build_targets(host_offsets, num_targets, heads: int):
     """Host-only candidate work list: (items int32 (n, 4), hist int32 (n,))."""
     return _worklist_with_hist("hstu_worklist_build_targets", host_offsets, num_targets, heads)
+
+
+def hstu_worklist_build_bwd_targets(host_offsets, num_targets, heads: int):
+    """Host-only work list of the backward with candidates: (items, hist)."""
+    return _worklist_with_hist("hstu_worklist_build_bwd_targets", host_offsets, num_targets, heads)
 
 
 def hstu_worklist_build_candidates(host_offsets, num_targets, heads: int):

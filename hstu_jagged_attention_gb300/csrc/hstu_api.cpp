@@ -297,23 +297,31 @@ void fill_items_targets(const int32_t* off, const int32_t* num_targets, int batc
   }
 }
 
-void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst) {
+void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst, const int32_t* num_targets,
+                    int32_t* hist_dst) {
   // (cost, b, h, kt) generated in b, h, kt order; a stable sort by cost
-  // descending then gives cost descending, then b, h, kt ascending
+  // descending then gives cost descending, then b, h, kt ascending.  With
+  // candidates, a key block without history keys is seen by its own rows
+  // only: cost 1 (the diagonal query block).
   struct Entry {
-    int cost;
+    int cost, hist;
     Item item;
   };
   std::vector<Entry> e;
   e.reserve((size_t)count_items(off, batch, heads));
   for (int b = 0; b < batch; ++b) {
     const int n = off[b + 1] - off[b];
+    const int hist = num_targets ? n - num_targets[b] : n;
     const int nq = (n + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
     for (int h = 0; h < heads; ++h)
-      for (int kt = 0; kt < nq; ++kt) e.push_back(Entry{nq - kt, make_int4(off[b], n, h, kt)});
+      for (int kt = 0; kt < nq; ++kt)
+        e.push_back(Entry{HSTU_BLOCK_M * kt >= hist ? 1 : nq - kt, hist, make_int4(off[b], n, h, kt)});
   }
   std::stable_sort(e.begin(), e.end(), [](const Entry& x, const Entry& y) { return x.cost > y.cost; });
-  for (size_t i = 0; i < e.size(); ++i) dst[i] = e[i].item;
+  for (size_t i = 0; i < e.size(); ++i) {
+    dst[i] = e[i].item;
+    if (hist_dst) hist_dst[i] = e[i].hist;
+  }
 }
 
 int host_check_offsets(const int32_t* off, int batch, long long max_len) {
@@ -339,9 +347,12 @@ struct hstu_plan {
   int32_t* d_hist = nullptr;
   // output-stage scratch (HSTU_PLAN_NORM_GATE): xs, then stats
   char* d_norm = nullptr;
-  // backward (HSTU_PLAN_BACKWARD): its work list, then the fp32 dQ accumulator
+  // backward (HSTU_PLAN_BACKWARD): its work list, (with candidates) each
+  // item's history length, then the fp32 dQ accumulator; one allocation
   int n_bwd = 0;
   char* d_bwd = nullptr;
+  int32_t* d_bwd_hist = nullptr;
+  float* d_bwd_acc = nullptr;
   int device = -1;
 };
 
@@ -361,7 +372,6 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
   if (heads < 1 || max_seqlen < 0 ||
       (flags & ~(unsigned)(HSTU_PLAN_NORM_GATE | HSTU_PLAN_BACKWARD | HSTU_PLAN_CANDIDATES_ONLY)))
     return HSTU_ERR_INVALID_ARG;
-  if ((flags & HSTU_PLAN_BACKWARD) && nt) return HSTU_ERR_INVALID_ARG;  // causal only
   // the candidates' rows only: needs candidates; the output stage normalises
   // every row and the backward every pair, so neither combines with it
   const bool cand_only = (flags & HSTU_PLAN_CANDIDATES_ONLY) != 0;
@@ -421,13 +431,24 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
     } catch (const std::bad_alloc&) {
       return fail(HSTU_ERR_NO_MEMORY);
     }
-    hstu::fill_items_bwd(off, batch, heads, bw.data());
+    std::vector<int32_t> bh;
+    try {
+      if (nt) bh.resize(bw.size());
+    } catch (const std::bad_alloc&) {
+      return fail(HSTU_ERR_NO_MEMORY);
+    }
+    hstu::fill_items_bwd(off, batch, heads, bw.data(), nt, nt ? bh.data() : nullptr);
     p->n_bwd = (int)bw.size();
     const size_t bbytes = bw.size() * sizeof(hstu::Item);
+    const size_t hbytes = (bh.size() * sizeof(int32_t) + 15) / 16 * 16;  // keeps the acc 16-aligned
     if ((e = cudaMalloc(reinterpret_cast<void**>(&p->d_bwd),
-                        bbytes + (size_t)p->total * heads * d * sizeof(float))) != cudaSuccess)
+                        bbytes + hbytes + (size_t)p->total * heads * d * sizeof(float))) != cudaSuccess)
       return fail(mem_code(e));
-    if (cudaMemcpy(p->d_bwd, bw.data(), bbytes, cudaMemcpyHostToDevice) != cudaSuccess)
+    if (nt) p->d_bwd_hist = reinterpret_cast<int32_t*>(p->d_bwd + bbytes);
+    p->d_bwd_acc = reinterpret_cast<float*>(p->d_bwd + bbytes + hbytes);
+    if (cudaMemcpy(p->d_bwd, bw.data(), bbytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+        (nt && cudaMemcpy(p->d_bwd_hist, bh.data(), bh.size() * sizeof(int32_t),
+                          cudaMemcpyHostToDevice) != cudaSuccess))
       return fail(HSTU_ERR_CUDA);
   }
   *plan = p;
@@ -526,7 +547,8 @@ int zero_rab_grads(const hstu_rab* rab, float* dpos, float* dtime, cudaStream_t 
 int launch_backward(const hstu::Item* d_items, int n_items, long long total, int heads, int d,
                     const void* q, const void* k, const void* v, const void* dout, float alpha,
                     float inv_n, float* dq_acc, void* dq, void* dk, void* dv, cudaStream_t stream,
-                    const hstu_rab* rab = nullptr, float* dpos = nullptr, float* dtime = nullptr) {
+                    const hstu_rab* rab = nullptr, float* dpos = nullptr, float* dtime = nullptr,
+                    const int32_t* d_hist = nullptr) {
   int sms = 0;
   int rc = device_check(&sms);
   if (rc != HSTU_OK) return rc;
@@ -548,6 +570,7 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   a.dv = dv;
   a.total = total;
   a.timeout_ns = wait_timeout_ns();
+  a.item_hist = d_hist;
   if (rab) {
     a.rab_ts = rab->timestamps;
     a.rab_pos = rab->pos;
@@ -803,6 +826,31 @@ int hstu_attn_fwd_targets(const void* q, const void* k, const void* v, const int
                  nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int hstu_worklist_build_bwd_targets(const int32_t* host_offsets, const int32_t* host_num_targets,
+                                    int batch, int heads, int32_t* host_items, int32_t* host_hist,
+                                    int capacity, int* n_items) {
+  if (!n_items || heads < 1 || capacity < 0 || (!host_num_targets && batch > 0))
+    return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(host_offsets, batch, -1);
+  if (rc != HSTU_OK) return rc;
+  if ((rc = check_targets(host_offsets, host_num_targets, batch)) != HSTU_OK) return rc;
+  std::vector<hstu::Item> items;
+  std::vector<int32_t> hist;
+  try {
+    items.resize((size_t)hstu::count_items(host_offsets, batch, heads));
+    hist.resize(items.size());
+    hstu::fill_items_bwd(host_offsets, batch, heads, items.data(), host_num_targets, hist.data());
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  *n_items = (int)items.size();
+  const size_t n = std::min(items.size(), (size_t)capacity);
+  if (host_items) std::memcpy(host_items, items.data(), n * sizeof(hstu::Item));
+  if (host_hist) std::memcpy(host_hist, hist.data(), n * sizeof(int32_t));
+  return HSTU_OK;
+}
+
 int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
                             int capacity, int* n_items) {
   if (!n_items || heads < 1 || capacity < 0) return HSTU_ERR_INVALID_ARG;
@@ -825,14 +873,14 @@ int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, i
 int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
                   const int32_t* offsets, int batch, int heads, int d, int max_seqlen, float alpha,
                   float inv_n, void* dq, void* dk, void* dv, hstu_stream_t stream) {
-  return hstu_attn_bwd_ex(q, k, v, dout, offsets, batch, heads, d, max_seqlen, nullptr, alpha, inv_n,
-                          dq, dk, dv, nullptr, nullptr, stream);
+  return hstu_attn_bwd_ex(q, k, v, dout, offsets, nullptr, batch, heads, d, max_seqlen, nullptr,
+                          alpha, inv_n, dq, dk, dv, nullptr, nullptr, stream);
 }
 
 int hstu_attn_bwd_ex(const void* q, const void* k, const void* v, const void* dout,
-                     const int32_t* offsets, int batch, int heads, int d, int max_seqlen,
-                     const hstu_rab* rab, float alpha, float inv_n, void* dq, void* dk, void* dv,
-                     float* dpos, float* dtime, hstu_stream_t stream) {
+                     const int32_t* offsets, const int32_t* host_num_targets, int batch, int heads,
+                     int d, int max_seqlen, const hstu_rab* rab, float alpha, float inv_n, void* dq,
+                     void* dk, void* dv, float* dpos, float* dtime, hstu_stream_t stream) {
   if (heads < 1 || max_seqlen < 0 || batch < 0) return HSTU_ERR_INVALID_ARG;
   int rc;
   if (rab && ((rc = check_rab(rab)) != HSTU_OK || (rc = check_rab_grads(dpos, dtime)) != HSTU_OK))
@@ -859,32 +907,41 @@ int hstu_attn_bwd_ex(const void* q, const void* k, const void* v, const void* do
   }
   rc = check_offsets(off, batch, max_seqlen);
   if (rc != HSTU_OK) return rc;
+  if (host_num_targets && (rc = check_targets(off, host_num_targets, batch)) != HSTU_OK) return rc;
   const long long total = off[batch];
   if (total == 0) return zero_rab_grads(rab, dpos, dtime, s);
   if ((rc = check_buffers(q, k, v, dout)) != HSTU_OK || (rc = check_buffers(dq, dk, dv, dv)) != HSTU_OK)
     return rc;
   std::vector<hstu::Item> items;
+  std::vector<int32_t> hist;
   try {
     items.resize((size_t)hstu::count_items(off, batch, heads));
-    hstu::fill_items_bwd(off, batch, heads, items.data());
+    if (host_num_targets) hist.resize(items.size());
+    hstu::fill_items_bwd(off, batch, heads, items.data(), host_num_targets,
+                         host_num_targets ? hist.data() : nullptr);
   } catch (const std::bad_alloc&) {
     return HSTU_ERR_NO_MEMORY;
   }
   if (items.empty()) return zero_rab_grads(rab, dpos, dtime, s);
   if (items.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
-  // one stream-ordered allocation: the fp32 dQ accumulator, then the items
+  // one stream-ordered allocation: the fp32 dQ accumulator, the items, then
+  // (with candidates) each item's history length
   const size_t abytes = (size_t)total * heads * d * sizeof(float);
   const size_t ibytes = items.size() * sizeof(hstu::Item);
+  const size_t hbytes = hist.size() * sizeof(int32_t);
   char* block = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&block), abytes + ibytes, s);
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&block), abytes + ibytes + hbytes, s);
   if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
   hstu::Item* d_items = reinterpret_cast<hstu::Item*>(block + abytes);
-  if (cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+  int32_t* d_hist = hbytes ? reinterpret_cast<int32_t*>(block + abytes + ibytes) : nullptr;
+  // pageable sources: each copy returns once its bytes are staged
+  if (cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      (hbytes && cudaMemcpyAsync(d_hist, hist.data(), hbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)) {
     cudaFreeAsync(block, s);
     return HSTU_ERR_CUDA;
   }
   rc = launch_backward(d_items, (int)items.size(), total, heads, d, q, k, v, dout, alpha, inv_n,
-                       reinterpret_cast<float*>(block), dq, dk, dv, s, rab, dpos, dtime);
+                       reinterpret_cast<float*>(block), dq, dk, dv, s, rab, dpos, dtime, d_hist);
   if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
   return rc;
 }
@@ -907,11 +964,9 @@ int hstu_attn_bwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, c
   if (plan->items.empty()) return zero_rab_grads(rab, dpos, dtime, s);
   rc = check_buffers(q, k, v, dout);
   if (rc != HSTU_OK || (rc = check_buffers(dq, dk, dv, dv)) != HSTU_OK) return rc;
-  const size_t bbytes = (size_t)plan->n_bwd * sizeof(hstu::Item);
   return launch_backward(reinterpret_cast<const hstu::Item*>(plan->d_bwd), plan->n_bwd, plan->total,
-                         plan->heads, plan->d, q, k, v, dout, alpha, inv_n,
-                         reinterpret_cast<float*>(plan->d_bwd + bbytes), dq, dk, dv, s, rab, dpos,
-                         dtime);
+                         plan->heads, plan->d, q, k, v, dout, alpha, inv_n, plan->d_bwd_acc, dq, dk,
+                         dv, s, rab, dpos, dtime, plan->d_bwd_hist);
 }
 
 int hstu_last_status(int* device_status, int* site) {

@@ -238,6 +238,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // The bias (variant RAB): lane l holds the tables' entries of bucket
   // 31 - l (clamped), so a lookup is one shuffle from lane rab_lane(delta).
+  // The current item's history length (its length, without candidates)
+  // and length.  A row's kept keys in the item's block: c < cmax (causal);
+  // with candidates, c < cm or c == dg (dg = -1 for a history row).
+  int item_hist = 0, item_n = 0;
+  struct RowMask {
+    int cmax, cm, dg;
+    bool ok;
+  };
   RabRow rr{};
   if constexpr (RAB) {
     const int bl = 31 - lane;
@@ -336,12 +344,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // 2 dS; PM and TM are the bias parts' modes.  The dS goes into the running
   // sums: in modes 0 and 1 as at most two sums per part at the chunk's end;
   // in mode 2 a running sum moves on where the row's bucket changes.
-  auto chunk = [&](auto pm_t, auto tm_t, auto mode_t, int c, const uint32_t (&sr)[32],
-                   const uint32_t (&pr)[32], const BRab& q, int ts_key, int j0, int cmax,
-                   bool row_ok) {
+  auto chunk = [&](auto pm_t, auto tm_t, auto mode_t, auto cm_t, int c, const uint32_t (&sr)[32],
+                   const uint32_t (&pr)[32], const BRab& q, int ts_key, int j0,
+                   const RowMask& rm) {
     constexpr int PM = decltype(pm_t)::value;
     constexpr int TM = decltype(tm_t)::value;
     constexpr int MODE = decltype(mode_t)::value;
+    constexpr bool CM = decltype(cm_t)::value;  // the chunk holds candidate keys
     constexpr bool GEN = PM == 2;
     [[maybe_unused]] const int lp0 = q.pk & 31, lt0 = (q.pk >> 5) & 31;
     [[maybe_unused]] const int kbp = (q.pk >> 10) & 63, kbt = (q.pk >> 16) & 63;
@@ -365,11 +374,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int e = 0; e < 8; ++e) {
         const int k = 8 * g + e;
         const int col = 32 * c + k;
-        const bool keep = row_ok && col < cmax;
+        const bool keep = CM ? rm.ok && (col < rm.cm || col == rm.dg) : rm.ok && col < rm.cmax;
         float x = alpha * __uint_as_float(sr[k]);
         if constexpr (RAB) {
           if constexpr (GEN) {
-            lpv[e] = rab_lane(rr.pe_i - (j0 + k));
+            const int jk = j0 + k;  // every candidate sits at position hist
+            lpv[e] = rab_lane(rr.pe_i - (jk < item_hist ? jk : item_hist));
             ltv[e] = rab_lane(rr.ts_i - __shfl_sync(0xffffffffu, ts_key, k));
             x += __shfl_sync(0xffffffffu, rr.pos_l, lpv[e]) +
                  __shfl_sync(0xffffffffu, rr.time_l, ltv[e]);
@@ -428,6 +438,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using I0 = std::integral_constant<int, 0>;
   using I1 = std::integral_constant<int, 1>;
   using I2 = std::integral_constant<int, 2>;
+  using CM0 = std::false_type;
+  using CM1 = std::true_type;
   // the bias's view of this warp's two key chunks of the current item:
   // the timestamps (lane = key) and whether they are in order; and of the
   // current query block, each chunk's modes and values
@@ -448,37 +460,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // timestamp ts_i was loaded ahead
   auto prep = [&](int qt, int ts_i, int kbase) {
     if constexpr (RAB) {
-      rr.pe_i = kBM * qt + row;
+      const int i = kBM * qt + row;
+      rr.pe_i = i < item_hist ? i : item_hist;
       rr.ts_i = ts_i;
       q0 = prep_chunk(kbase + 64 * wg, ts_key0, ord0);
       q1 = prep_chunk(kbase + 64 * wg + 32, ts_key1, ord1);
     }
   };
   // the pass of MODE over this warpgroup's two chunks of query block qt
-  auto pass = [&](auto mode_t, int qt, int kbase, int cmax, bool row_ok) {
+  auto pass = [&](auto mode_t, int kbase, const RowMask& rm) {
 #pragma unroll 1
     for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
       uint32_t sr[32], pr[32];
       tmem_ld32(lane_tm + C::S_COL + 32u * c, sr);
       if constexpr (decltype(mode_t)::value != 1) tmem_ld32(lane_tm + C::DP_COL + 32u * c, pr);
       const int j0 = kbase + 32 * c;
+      // a chunk holding candidate keys (warp-uniform) takes the candidate
+      // mask and, with the bias, the per-key lookups
+      const bool cand = item_hist < item_n && j0 + 31 >= item_hist;
       if constexpr (RAB) {
         const BRab q = (c & 1) ? q1 : q0;
         const int tsk = (c & 1) ? ts_key1 : ts_key0;
         const uint32_t modes = (q.pk >> 22) & 15u;  // pm | tm << 2, warp-uniform
-        if (modes == 0u)
-          chunk(I0{}, I0{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+        if (cand)
+          chunk(I2{}, I2{}, mode_t, CM1{}, c, sr, pr, q, tsk, j0, rm);
+        else if (modes == 0u)
+          chunk(I0{}, I0{}, mode_t, CM0{}, c, sr, pr, q, tsk, j0, rm);
         else if (modes == 1u)
-          chunk(I1{}, I0{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+          chunk(I1{}, I0{}, mode_t, CM0{}, c, sr, pr, q, tsk, j0, rm);
         else if (modes == 4u)
-          chunk(I0{}, I1{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+          chunk(I0{}, I1{}, mode_t, CM0{}, c, sr, pr, q, tsk, j0, rm);
         else if (modes == 5u)
-          chunk(I1{}, I1{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+          chunk(I1{}, I1{}, mode_t, CM0{}, c, sr, pr, q, tsk, j0, rm);
         else
-          chunk(I2{}, I2{}, mode_t, c, sr, pr, q, tsk, j0, cmax, row_ok);
+          chunk(I2{}, I2{}, mode_t, CM0{}, c, sr, pr, q, tsk, j0, rm);
       } else {
         const BRab q{};
-        chunk(I0{}, I0{}, mode_t, c, sr, pr, q, 0, j0, cmax, row_ok);
+        if (cand)
+          chunk(I0{}, I0{}, mode_t, CM1{}, c, sr, pr, q, 0, j0, rm);
+        else
+          chunk(I0{}, I0{}, mode_t, CM0{}, c, sr, pr, q, 0, j0, rm);
       }
     }
   };
@@ -486,7 +507,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
     const Item it = __ldg(&a.items[idx]);
     const BwdBlock b{it.x, it.y, it.z, it.w};
-    const int nq = (b.n + kBM - 1) / kBM;
+    item_hist = a.item_hist ? __ldg(a.item_hist + idx) : b.n;
+    item_n = b.n;
+    // a key block of candidates only is seen by its own rows: the diagonal
+    // query block alone
+    const int nq = kBN * b.kt >= item_hist ? b.kt + 1 : (b.n + kBM - 1) / kBM;
     const int key_rows = b.n - kBN * b.kt;  // keys of the block that exist (>= 1)
     if (tid == 0) {
       mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILEB);
@@ -499,12 +524,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       load_tile(&tm_do, C::DO_OFF + qb * C::TILEB, C::B_QD + qb, b.h, b.s0 + kBM * qt);
     };
     // row tid of query block qt sees key c of block kt iff both exist and
-    // the key is not after the row
-    auto mask_of = [&](int qt, int& cmax, bool& row_ok) {
+    // the key is not after the row; with candidates, iff also the key is in
+    // the history or is the row's own
+    auto mask_of = [&](int qt) -> RowMask {
       const int row_i = kBM * qt + row;    // sequence-local query
       const int lim = row_i - kBN * b.kt;  // keys c <= lim are not after the row
-      cmax = key_rows < lim + 1 ? key_rows : lim + 1;  // kept keys: c < cmax
-      row_ok = row_i < b.n;
+      RowMask m;
+      m.cmax = key_rows < lim + 1 ? key_rows : lim + 1;  // causal: kept keys c < cmax
+      m.ok = row_i < b.n;
+      const int hl = item_hist - kBN * b.kt;  // keys c < hl are history
+      m.cm = m.cmax < hl ? m.cmax : hl;
+      m.dg = row_i >= item_hist ? lim : -1;
+      return m;
     };
     // alpha dQ_part of block qt (TMEM columns DQ_COL) staged over the P
     // tiles as 128B-swizzled fp32 boxes of 32 columns, then added into the
@@ -577,11 +608,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         if (!(ok = wait_all(C::B_SDP, ph_sdp, kSiteSFull))) break;
         tc_fence_after();
-        int cmax;
-        bool row_ok;
-        mask_of(qt, cmax, row_ok);
+        const RowMask rm = mask_of(qt);
         // P and dS in one pass over this warpgroup's two 32-key chunks
-        pass(std::integral_constant<int, 0>{}, qt, kBN * b.kt, cmax, row_ok);
+        pass(std::integral_constant<int, 0>{}, kBN * b.kt, rm);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncthreads();  // S and dP read, the tiles written
@@ -625,11 +654,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (tid == 0) issue_sdp(0);
         if (!(ok = wait_all(C::B_SDP, ph_sdp, kSiteSFull))) break;
         tc_fence_after();
-        int cmax;
-        bool row_ok;
-        mask_of(qt, cmax, row_ok);
+        const RowMask rm = mask_of(qt);
         if constexpr (C::MERGED) {
-          pass(std::integral_constant<int, 0>{}, qt, kBN * b.kt, cmax, row_ok);
+          pass(std::integral_constant<int, 0>{}, kBN * b.kt, rm);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
           __syncthreads();
@@ -645,7 +672,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         } else {
           // 2. P
-          pass(std::integral_constant<int, 1>{}, qt, kBN * b.kt, cmax, row_ok);
+          pass(std::integral_constant<int, 1>{}, kBN * b.kt, rm);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
           __syncthreads();
@@ -659,7 +686,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = wait_all(C::B_PROD, ph_prod, kSiteOFull))) break;
           tc_fence_after();
           // 4. dS, into the same tiles (the dV products are done)
-          pass(std::integral_constant<int, 2>{}, qt, kBN * b.kt, cmax, row_ok);
+          pass(std::integral_constant<int, 2>{}, kBN * b.kt, rm);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_before();
           __syncthreads();

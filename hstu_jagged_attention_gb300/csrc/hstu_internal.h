@@ -97,11 +97,16 @@ struct BwdArgs {
   int rab_npos = 0, rab_ntime = 0;
   float* dpos = nullptr;
   float* dtime = nullptr;
+  // candidates (null: none): each item's history length, parallel to items
+  const int32_t* item_hist = nullptr;
 };
 // Work list of the backward: one item per (sequence, head, key block kt),
 // costing nq - kt query blocks; ordered by cost descending, then sequence,
 // head, kt ascending.
-void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst);
+// With num_targets (else null), hist_dst receives each item's history
+// length, and a key block of candidates only costs 1.
+void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst,
+                    const int32_t* num_targets = nullptr, int32_t* hist_dst = nullptr);
 // The backward kernel for head dimension d on `grid` CTAs, then the dQ
 // conversion; tdo describes dout like q, tdq the fp32 accumulator as
 // (d, heads, total) with box (32, 1, 128) and the 128-byte swizzle.

@@ -392,19 +392,30 @@ int hstu_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
                   const int32_t* offsets, int batch, int heads, int d, int max_seqlen, float alpha,
                   float inv_n, void* dq, void* dk, void* dv, hstu_stream_t stream);
 /* The backward on a plan made by hstu_plan_create_ex with HSTU_PLAN_BACKWARD
- * (no candidates): the plan owns the backward work list and the fp32 dQ
- * accumulator; launches on one stream at a time per plan.  A plan without
- * the flag: HSTU_ERR_INVALID_ARG. */
+ * (host_num_targets given: with the candidate mask, as the forward's): the
+ * plan owns the backward work list and the fp32 dQ accumulator; launches on
+ * one stream at a time per plan.  A plan without the flag:
+ * HSTU_ERR_INVALID_ARG. */
 #define HSTU_PLAN_BACKWARD 2u
 int hstu_attn_bwd_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
                        const void* dout, float alpha, float inv_n, void* dq, void* dk, void* dv,
                        hstu_stream_t stream);
 int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
                             int capacity, int* n_items);
+/* The backward's work list with candidates: as hstu_worklist_build_bwd,
+ * except that a key block without history keys (128 kt >= hist) is seen by
+ * its own rows only and costs 1; host_hist receives each item's history
+ * length.  Arguments as hstu_worklist_build_targets. */
+int hstu_worklist_build_bwd_targets(const int32_t* host_offsets, const int32_t* host_num_targets,
+                                    int batch, int heads, int32_t* host_items, int32_t* host_hist,
+                                    int capacity, int* n_items);
 
 /*
- * hstu_attn_bwd_ex / hstu_attn_bwd_plan_ex -- the backward with the
- * relative attention bias (rab NULL: as hstu_attn_bwd / _plan).  The score
+ * hstu_attn_bwd_ex / hstu_attn_bwd_plan_ex -- the backward with candidates
+ * and the relative attention bias.  host_num_targets (NULL: none) as
+ * hstu_attn_fwd_targets: the gradients are those of the forward with the
+ * candidate mask, the kept pairs being the mask's.  rab NULL: no bias (as
+ * hstu_attn_bwd / _plan).  The score
  * is that of hstu_rab, ds_ij = inv_n silu'(score_ij) <dout[i], v[j]>, dq, dk
  * and dv as above, and the tables' gradients (HSTU paper Appendix G: the
  * bias's construction and its backward fused into the attention):
@@ -421,9 +432,9 @@ int hstu_worklist_build_bwd(const int32_t* host_offsets, int batch, int heads, i
  * hstu_attn_fwd_ex or NULL / misaligned dpos or dtime (with rab).
  */
 int hstu_attn_bwd_ex(const void* q, const void* k, const void* v, const void* dout,
-                     const int32_t* offsets, int batch, int heads, int d, int max_seqlen,
-                     const hstu_rab* rab, float alpha, float inv_n, void* dq, void* dk, void* dv,
-                     float* dpos, float* dtime, hstu_stream_t stream);
+                     const int32_t* offsets, const int32_t* host_num_targets, int batch, int heads,
+                     int d, int max_seqlen, const hstu_rab* rab, float alpha, float inv_n, void* dq,
+                     void* dk, void* dv, float* dpos, float* dtime, hstu_stream_t stream);
 int hstu_attn_bwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, const void* v,
                           const void* dout, const hstu_rab* rab, float alpha, float inv_n, void* dq,
                           void* dk, void* dv, float* dpos, float* dtime, hstu_stream_t stream);

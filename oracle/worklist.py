@@ -75,6 +75,29 @@ def items_candidates(offsets, num_targets, heads: int, block_m: int = BLOCK_M):
     return it[keep].reshape(-1, 4), hs[keep]
 
 
+def items_bwd_targets(offsets, num_targets, heads: int, block_m: int = BLOCK_M):
+    """The backward's work list with candidates: (items (n, 4), hist (n,)).
+    Key block kt is seen by the query blocks that hold a row seeing one of
+    its keys: a history key by every later row, a candidate key by its own
+    row only.  So the item walks query blocks kt .. last when the block has
+    a history key, else block kt alone; cost descending, then b, h, kt."""
+    offsets = [int(x) for x in offsets]
+    rows = []
+    for b in range(len(offsets) - 1):
+        n = offsets[b + 1] - offsets[b]
+        hist = n - int(num_targets[b])
+        nq = (n + block_m - 1) // block_m
+        for h in range(heads):
+            for kt in range(nq):
+                has_history_key = any(j < hist for j in range(kt * block_m, min(n, (kt + 1) * block_m)))
+                cost = nq - kt if has_history_key else 1
+                rows.append((-cost, b, h, kt, offsets[b], n, hist))
+    rows.sort()
+    it = np.array([(s0, n, h, kt) for (_, b, h, kt, s0, n, _hist) in rows], dtype=np.int32)
+    hs = np.array([hist for (*_, hist) in rows], dtype=np.int32)
+    return it.reshape(-1, 4), hs
+
+
 def items_bwd(offsets, heads: int, block_m: int = BLOCK_M) -> np.ndarray:
     """Backward work items: one per (sequence, head, key block kt), which the
     query blocks kt .. nq - 1 see (causal), costing nq - kt; ordered by cost

@@ -245,8 +245,8 @@ def test_bwd_rab_validation_before_any_cuda_call():
         a = dict(good)
         a.update(kw)
         rab = binding.ctypes.pointer(binding._Rab(a["ts"], a["pos"], a["npos"], a["time"], a["ntime"]))
-        code = binding.lib().hstu_attn_bwd_ex(16, 16, 16, 16, off.ctypes.data, 1, 2, 64, 4, rab, 1.0,
-                                              1.0, 16, 16, 16, a["dpos"], a["dtime"], None)
+        code = binding.lib().hstu_attn_bwd_ex(16, 16, 16, 16, off.ctypes.data, None, 1, 2, 64, 4, rab,
+                                              1.0, 1.0, 16, 16, 16, a["dpos"], a["dtime"], None)
         assert code == binding.HSTU_ERR_INVALID_ARG, kw
         code = binding.lib().hstu_attn_bwd_plan_ex(None, 16, 16, 16, 16, rab, 1.0, 1.0, 16, 16, 16,
                                                    a["dpos"], a["dtime"], None)
@@ -295,3 +295,35 @@ def test_candidates_only_plan_flag_validation_before_any_cuda_call():
         with pytest.raises(binding.HstuError) as e:
             binding.hstu_plan_create_ex(off, targets, 1, 2, 64, 300, flags)
         assert e.value.code == binding.HSTU_ERR_INVALID_ARG, flags
+
+
+
+# ------------------------------------------------ backward with candidates
+@pytest.mark.parametrize("seed", range(8))
+def test_bwd_candidate_worklist_bit_exact_random(seed):
+    rng = np.random.default_rng(1500 + seed)
+    nb = int(rng.integers(0, 20))
+    lengths = rng.integers(0, 700, size=nb)
+    nt = [int(rng.choice([0, n, n % 128, rng.integers(0, n + 1)])) if n else 0 for n in lengths]
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    heads = int(rng.integers(1, 4))
+    items, hist = binding.hstu_worklist_build_bwd_targets(off, np.array(nt, np.int32), heads)
+    ref_items, ref_hist = oracle_worklist.items_bwd_targets(off, nt, heads)
+    assert np.array_equal(items, ref_items.reshape(-1, 4))
+    assert np.array_equal(hist, ref_hist)
+
+
+def test_bwd_candidate_worklist_without_candidates_is_the_causal_one():
+    w = workloads.workload("serving")
+    items, hist = binding.hstu_worklist_build_bwd_targets(w.offsets, np.zeros(w.batch, np.int32),
+                                                          w.heads)
+    assert np.array_equal(items, binding.hstu_worklist_build_bwd(w.offsets, w.heads))
+    assert np.array_equal(hist, items[:, 1])
+
+
+def test_bwd_candidates_validation():
+    off = np.array([0, 300], np.int32)
+    for nt in ([-1], [301]):
+        with pytest.raises(binding.HstuError) as e:
+            binding.hstu_worklist_build_bwd_targets(off, np.array(nt, np.int32), 2)
+        assert e.value.code == binding.HSTU_ERR_INVALID_ARG, nt
