@@ -76,14 +76,15 @@ def candidate_row_flops(w: workloads.Workload, num_targets) -> float:
 BWD_METRIC = "HSTU jagged causal attn bwd (dQ, dK, dV): TFLOPS at 10 d FLOP per kept pair; ms/call"
 
 
-def bwd_flops(w: workloads.Workload) -> float:
+def bwd_flops(w: workloads.Workload, num_targets=None) -> float:
     """The backward's products per kept pair and head: S = Q K^T and dP = dO V^T
-    (recomputed), dV += P^T dO, dK += dS^T Q, dQ += dS K: 5 x 2 d FLOP."""
-    L = w.lengths.astype(np.float64)
-    return float(10.0 * w.d * w.heads * np.sum(L * (L + 1) / 2.0))
+    (recomputed), dV += P^T dO, dK += dS^T Q, dQ += dS K: 5 x 2 d FLOP (the
+    kept pairs of the candidate mask with ``num_targets``)."""
+    return 2.5 * causal_flops(w, num_targets)
 
 
-def cpu_oracle_bwd_sample(w, q, k, v, do, target_s: float, threads: int | None = None, rab=None):
+def cpu_oracle_bwd_sample(w, q, k, v, do, target_s: float, threads: int | None = None, rab=None,
+                          num_targets=None):
     """The oracle's backward on the first sequences of the workload, as many
     as fit about target_s seconds (calibrated on the first one).  With the
     bias ``rab`` = (timestamps, pos, time), the tables' gradients too."""
@@ -94,9 +95,10 @@ def cpu_oracle_bwd_sample(w, q, k, v, do, target_s: float, threads: int | None =
     def run(nb):
         e = int(off[nb])
         r = None if rab is None else (rab[0][:e], rab[1], rab[2])
+        nt = None if num_targets is None else np.asarray(num_targets)[:nb]
         t0 = time.perf_counter()
         reference.hstu_bwd(q[:e], k[:e], v[:e], do[:e], off[:nb + 1], w.alpha, w.inv_n, threads=threads,
-                           rab=r, table_grads=r is not None)
+                           rab=r, table_grads=r is not None, num_targets=nt)
         return time.perf_counter() - t0
 
     nb = 1
@@ -105,9 +107,11 @@ def cpu_oracle_bwd_sample(w, q, k, v, do, target_s: float, threads: int | None =
         nb = min(w.batch, max(nb + 1, int(nb * target_s / max(dt, 1e-3))))
         dt = run(nb)
     sub = workloads.custom(w.lengths[:nb], w.heads, w.d, alpha=w.alpha, inv_n=w.inv_n)
+    sub_nt = None if num_targets is None else np.asarray(num_targets)[:nb]
+    fl = bwd_flops(sub, sub_nt)
     desc = (f"the first {nb} of {w.batch} sequences of the {w.name} workload "
-            f"({bwd_flops(sub) / 1e9:.2f} backward GFLOP), fp64 C oracle, {threads} threads")
-    return bwd_flops(sub) / dt / 1e12, desc, threads, dt
+            f"({fl / 1e9:.2f} backward GFLOP), fp64 C oracle, {threads} threads")
+    return fl / dt / 1e12, desc, threads, dt
 
 
 def workload_by_name(name: str):
@@ -287,7 +291,7 @@ def cpu_oracle_sample(w, q, k, v, target_s: float, seed: int = 0, threads: int |
     return fl / dt / 1e12, desc, threads, dt
 
 
-def run_reference_bwd(args, w):
+def run_reference_bwd(args, w, nt=None):
     world, rank, _ = dist_init()
     if rank != 0:
         return 0
@@ -299,7 +303,8 @@ def run_reference_bwd(args, w):
     vals = []
     desc, threads = "", 0
     for s_ in range(args.warmup + args.steps):
-        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, per_step_s, rab=_cpu_rab(args, w))
+        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, per_step_s, rab=_cpu_rab(args, w),
+                                                      num_targets=nt)
         if s_ >= args.warmup:
             vals.append(val)
     value = statistics.mean(vals)
@@ -307,7 +312,8 @@ def run_reference_bwd(args, w):
         "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, **w.describe(), "pass": "backward", **_rab_desc(args)},
+        "config": {"workload": w.name, **w.describe(), "pass": "backward", **_targets_desc(nt),
+                   **_rab_desc(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -385,7 +391,7 @@ def _targets_desc(nt) -> dict:
             else "varies"}
 
 
-def run_ours_bwd(args, w):
+def run_ours_bwd(args, w, nt=None):
     """The backward on its own plan: kernel-only value, one-shot e2e with host buffers."""
     import torch
     from hstu_jagged_attention_gb300 import binding, build
@@ -413,7 +419,7 @@ def run_ours_bwd(args, w):
         ts_pin = torch.from_numpy(rab_h[0]).pin_memory()
         rab = (ts_pin.to(dev), torch.from_numpy(rab_h[1]).to(dev), torch.from_numpy(rab_h[2]).to(dev))
         tgrads = (torch.empty_like(rab[1]), torch.empty_like(rab[2]))
-    plan = binding.hstu_plan_create_ex(w.offsets, None, w.batch, w.heads, w.d, w.max_seqlen,
+    plan = binding.hstu_plan_create_ex(w.offsets, nt, w.batch, w.heads, w.d, w.max_seqlen,
                                        binding.HSTU_PLAN_BACKWARD)
 
     def plan_call():
@@ -446,7 +452,7 @@ def run_ours_bwd(args, w):
     clocks = sampler.stop(wall0, wall0 + wall, t_warm)
     times_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
     ms = statistics.mean(times_ms)
-    flops = bwd_flops(w)
+    flops = bwd_flops(w, nt)
     value, ms_max = aggregate(flops, ms, world, dev)
     st, site = binding.hstu_last_status()
     if st != binding.HSTU_OK:
@@ -465,14 +471,17 @@ def run_ours_bwd(args, w):
     def e2e_step():
         for dst, src in zip(ins, pin):
             dst.copy_(src, non_blocking=True)
-        if rab is None:
+        if rab is None and nt is None:
             binding.hstu_attn_bwd(*ins, offsets_host, w.batch, w.heads, w.d, w.max_seqlen, w.alpha,
                                   w.inv_n, *g2, stream=stream)
+        elif rab is None:
+            binding.hstu_attn_bwd_ex(*ins, offsets_host, w.batch, w.heads, w.d, w.max_seqlen, w.alpha,
+                                     w.inv_n, *g2, num_targets=nt, stream=stream)
         else:
             tse.copy_(ts_pin, non_blocking=True)
             binding.hstu_attn_bwd_ex(*ins, offsets_host, w.batch, w.heads, w.d, w.max_seqlen, w.alpha,
-                                     w.inv_n, *g2, rab=(tse, rab[1], rab[2]), dpos=tg2[0],
-                                     dtime=tg2[1], stream=stream)
+                                     w.inv_n, *g2, num_targets=nt, rab=(tse, rab[1], rab[2]),
+                                     dpos=tg2[0], dtime=tg2[1], stream=stream)
             for dst, src in zip(tg_h, tg2):
                 dst.copy_(src, non_blocking=True)
         for dst, src in zip(outs_h, g2):
@@ -501,7 +510,8 @@ def run_ours_bwd(args, w):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         arrs = [t.float().numpy() for t in (q_h, k_h, v_h, do_h)]
-        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, args.cpu_seconds, rab=_cpu_rab(args, w))
+        val, desc, threads, _ = cpu_oracle_bwd_sample(w, *arrs, args.cpu_seconds, rab=_cpu_rab(args, w),
+                                                      num_targets=nt)
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
     binding.hstu_plan_destroy(plan)
     peaks = load_peaks()
@@ -511,7 +521,7 @@ def run_ours_bwd(args, w):
             "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {**w.describe(), "pass": "backward", **_rab_desc(args),
+            "config": {**w.describe(), "pass": "backward", **_targets_desc(nt), **_rab_desc(args),
                        "l2": "flushed between steps (256 MiB write)",
                        "work_items": len(binding.hstu_worklist_build_bwd(w.offsets, w.heads)),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -785,7 +795,7 @@ def main(argv=None):
     for name in names:
         w, nt = workload_by_name(name)
         if args.backward:
-            rc |= run_reference_bwd(args, w) if args.impl == "reference" else run_ours_bwd(args, w)
+            rc |= run_reference_bwd(args, w, nt) if args.impl == "reference" else run_ours_bwd(args, w, nt)
         else:
             rc |= run_reference(args, w, nt) if args.impl == "reference" else run_ours(args, w, nt)
     return rc
