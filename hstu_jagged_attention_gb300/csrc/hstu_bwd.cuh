@@ -1,7 +1,8 @@
 // Backward pass of the HSTU jagged attention (HSTU paper Appendix G: the
 // backward recomputes the attention; its gradients follow the forward
 // definition).  With s_ij = alpha q_i.k_j, P_ij = inv_n silu(s_ij) on kept
-// pairs (causal, same sequence) and out_i = sum_j P_ij v_j:
+// pairs (causal, same sequence; with candidates, the candidate mask) and
+// out_i = sum_j P_ij v_j:
 //
 //   dV = P^T dO,   dP = dO V^T,   dS = inv_n silu'(s) (.) dP (kept pairs),
 //   dQ = alpha dS K,   dK = alpha dS^T Q,   silu'(x) = sig(x) (1 + x (1 - sig(x))).
@@ -29,8 +30,19 @@
 // At the item's end dV and alpha dK leave TMEM as bf16.  The P and dS
 // splits keep the products' error at the bf16 output rounding, as in the
 // forward.  Where shared memory has room (d <= 64) P and dS have tiles of
-// their own: one pass computes both, and steps 3 and 5 issue together.
-// Phases run one after another (synchronous waits).
+// their own: one pass computes both, and steps 3 and 5 issue together, and
+// the next block's S and dP are issued behind the current products.
+//
+// Candidates (HSTU paper section 3.4, Appendix H): each item carries its
+// history length hist.  A candidate sees the history and itself, so a key
+// block of candidates only is walked for its own query block alone, and a
+// chunk holding candidate keys selects with the candidate mask.
+//
+// The bias rab_{p,t} (variant RAB): s_ij gains pos[bucket] + time[bucket],
+// recomputed as in the forward.  The tables' gradients are the sums of dS
+// over each bucket's kept pairs.  Each thread keeps running sums, added into
+// a CTA-wide histogram where its bucket changes, and into dpos / dtime at
+// exit.
 
 template <int D, bool RAB = false>
 struct BCfg {
