@@ -437,41 +437,42 @@ static void* worker_bwd(void* arg) {
  *   dk[r] = alpha sum_{i: kept(i, j)} ds_ij q_i        (j = t's position)
  *   dv[r] = sum_{i: kept(i, j)} P_ij do_i
  * each (nrows, d): the same terms as the full backward, summed one row at a
- * time.  Causal; the rab arguments as hstu_oracle_fwd_rab_f64 (ts NULL: no
- * bias). */
+ * time.  num_targets and the rab arguments as hstu_oracle_fwd_rab_f64
+ * (NULL: causal, no bias). */
 int hstu_oracle_bwd_rows_f64(const float* q, const float* k, const float* v, const float* dout,
-                             const int64_t* offsets, const int64_t* ts, const float* pos, int npos,
-                             const float* time, int ntime, int batch, int heads, int d,
-                             double alpha, double inv_n, const int64_t* rows_t,
+                             const int64_t* offsets, const int64_t* num_targets, const int64_t* ts,
+                             const float* pos, int npos, const float* time, int ntime, int batch,
+                             int heads, int d, double alpha, double inv_n, const int64_t* rows_t,
                              const int32_t* rows_h, int64_t nrows, double* dq, double* dk,
                              double* dv) {
-    if (check_offsets(offsets, batch) || heads < 1 || d < 1 || nrows < 0 ||
-        (ts && (npos < 1 || ntime < 1)))
+    if (check_offsets(offsets, batch) || (num_targets && check_targets(offsets, num_targets, batch)) ||
+        heads < 1 || d < 1 || nrows < 0 || (ts && (npos < 1 || ntime < 1)))
         return -1;
     const rab_t R = {ts, pos, npos, time, ntime};
-    job_t J = {q, k, v, offsets, NULL, ts ? &R : NULL, batch, heads, d, alpha, inv_n, NULL, NULL,
-               NULL, 0, NULL, NULL};
+    job_t J = {q, k, v, offsets, num_targets, ts ? &R : NULL, batch, heads, d, alpha, inv_n, NULL,
+               NULL, NULL, 0, NULL, NULL};
     for (int64_t r = 0; r < nrows; ++r) {
         const int64_t t = rows_t[r];
         const int h = rows_h[r];
         const int b = seq_of(offsets, batch, t);
         if (b < 0 || h < 0 || h >= heads) return -1;
         const int64_t s0 = offsets[b], n = offsets[b + 1] - s0, pos = t - s0;
+        const int64_t hist = hist_of(&J, b);
         double* dqr = dq + r * (int64_t)d;
         double* dkr = dk + r * (int64_t)d;
         double* dvr = dv + r * (int64_t)d;
         for (int c = 0; c < d; ++c) dqr[c] = dkr[c] = dvr[c] = 0.0;
         for (int64_t j = 0; j < n; ++j) {  /* keys of row pos */
-            if (!kept(pos, j, n)) continue;
+            if (!kept(pos, j, hist)) continue;
             double p, ds;
-            bwd_terms(&J, dout, s0, n, h, pos, j, &p, &ds);
+            bwd_terms(&J, dout, s0, hist, h, pos, j, &p, &ds);
             const float* kj = k + ((s0 + j) * heads + h) * (int64_t)d;
             for (int c = 0; c < d; ++c) dqr[c] += alpha * ds * (double)kj[c];
         }
         for (int64_t i = 0; i < n; ++i) {  /* rows that see key pos */
-            if (!kept(i, pos, n)) continue;
+            if (!kept(i, pos, hist)) continue;
             double p, ds;
-            bwd_terms(&J, dout, s0, n, h, i, pos, &p, &ds);
+            bwd_terms(&J, dout, s0, hist, h, i, pos, &p, &ds);
             const float* qi = q + ((s0 + i) * heads + h) * (int64_t)d;
             const float* doi = dout + ((s0 + i) * heads + h) * (int64_t)d;
             for (int c = 0; c < d; ++c) {

@@ -81,7 +81,7 @@ def _load():
                                             ctypes.c_double, ctypes.c_double, d, d, d, d, d,
                                             ctypes.c_int]
         lib.hstu_oracle_bwd_f64.restype = ctypes.c_int
-        lib.hstu_oracle_bwd_rows_f64.argtypes = [f, f, f, f, i64, i64, f, ctypes.c_int, f,
+        lib.hstu_oracle_bwd_rows_f64.argtypes = [f, f, f, f, i64, i64, i64, f, ctypes.c_int, f,
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_double, ctypes.c_double, i64,
                                                  i32, ctypes.c_int64, d, d, d]
@@ -293,12 +293,15 @@ def hstu_bwd(q, k, v, dout, offsets, alpha: float, inv_n: float, threads: int | 
     return dq, dk, dv
 
 
-def hstu_bwd_rows(q, k, v, dout, offsets, alpha: float, inv_n: float, rows_t, rows_h, rab=None):
-    """Sampled gradient rows (causal, ``rab`` as hstu_bwd): for row r = (token
-    rows_t[r], head rows_h[r]) the fp64 dq, dk, dv rows, each (nrows, d)."""
+def hstu_bwd_rows(q, k, v, dout, offsets, alpha: float, inv_n: float, rows_t, rows_h, rab=None,
+                  num_targets=None):
+    """Sampled gradient rows (``num_targets`` and ``rab`` as hstu_bwd): for row
+    r = (token rows_t[r], head rows_h[r]) the fp64 dq, dk, dv rows, each
+    (nrows, d)."""
     qf, kf, vf, df = _f32(q), _f32(k), _f32(v), _f32(dout)
     total, heads, d = qf.shape
     off = np.ascontiguousarray(np.asarray(offsets), dtype=np.int64)
+    nt, ntp = _targets_ptr(num_targets, len(off) - 1)
     tsp = posp = timep = None
     npos = ntime = 0
     if rab is not None:
@@ -312,8 +315,8 @@ def hstu_bwd_rows(q, k, v, dout, offsets, alpha: float, inv_n: float, rows_t, ro
     dq, dk, dv = (np.zeros((len(rt), d), dtype=np.float64) for _ in range(3))
     rc = _load().hstu_oracle_bwd_rows_f64(_ptr(qf, ctypes.c_float), _ptr(kf, ctypes.c_float),
                                           _ptr(vf, ctypes.c_float), _ptr(df, ctypes.c_float),
-                                          _ptr(off, ctypes.c_int64), tsp, posp, npos, timep, ntime,
-                                          len(off) - 1, heads, d,
+                                          _ptr(off, ctypes.c_int64), ntp, tsp, posp, npos, timep,
+                                          ntime, len(off) - 1, heads, d,
                                           float(alpha), float(inv_n), _ptr(rt, ctypes.c_int64),
                                           _ptr(rh, ctypes.c_int32), len(rt), _ptr(dq, ctypes.c_double),
                                           _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double))

@@ -161,6 +161,28 @@ def test_sampled_rows_with_the_bias_match_the_full_backward():
         assert np.abs(g - p[rows_t, rows_h]).max() > 1e-3 * np.abs(g).max()
 
 
+def test_sampled_rows_with_candidates_match_the_full_backward():
+    rng = np.random.default_rng(15)
+    q, k, v, do, off = _case(rng, [50, 3, 90, 1, 130], 2, 8)
+    nt = [20, 3, 0, 1, 129]
+    ts = np.concatenate([np.cumsum(rng.integers(0, 3000, size=n)) for n in (50, 3, 90, 1, 130)])
+    pos = (0.4 * rng.standard_normal(9)).astype(np.float32)
+    time = (0.4 * rng.standard_normal(14)).astype(np.float32)
+    rows_t = np.array([0, 29, 30, 49, 50, 52, 53, 142, 143, 144, 200, 273])
+    rows_h = np.array([0, 1, 0, 1, 1, 0, 1, 0, 1, 0, 1, 1])
+    for rab in (None, (ts.astype(np.int64), pos, time)):
+        full = reference.hstu_bwd(q, k, v, do, off, 0.5, 0.1, num_targets=nt, rab=rab)
+        causal = reference.hstu_bwd(q, k, v, do, off, 0.5, 0.1, rab=rab)
+        got = reference.hstu_bwd_rows(q, k, v, do, off, 0.5, 0.1, rows_t, rows_h, rab=rab,
+                                      num_targets=nt)
+        for g, f, c in zip(got, full, causal):
+            np.testing.assert_allclose(g, f[rows_t, rows_h], rtol=1e-12, atol=1e-15)
+        # the mask matters on these rows (candidates see neither each other
+        # nor are seen by later candidates)
+        assert any(np.abs(g - c[rows_t, rows_h]).max() > 1e-3 * np.abs(g).max()
+                   for g, c in zip(got, causal))
+
+
 def test_bias_table_gradients_by_finite_differences():
     rng = np.random.default_rng(13)
     q, k, v, do, off = _case(rng, [12, 9, 1], 2, 4)
