@@ -119,3 +119,36 @@ def test_bwd_candidates_plan_equals_one_shot():
     parity.assert_device_ok()
     assert torch.equal(g[1], a[1]) and torch.equal(g[2], a[2])
     assert (g[0].float() - a[0].float()).abs().max().item() <= 1e-2 * a[0].float().abs().max().item()
+
+
+def test_bwd_candidate_workload_sampled():
+    # full size, in the launch configuration the benchmark times (a plan):
+    # 32 histories of 2048..8192 tokens with 1024 candidates each
+    w, nt = workloads.candidate_workload()
+    q, k, v = workloads.draw_qkv(w)
+    rng = np.random.default_rng(4000 + w.index)
+    do = workloads.bf16_round(rng.standard_normal(q.shape).astype(np.float32))
+    qd, kd, vd, dod = (t.to("cuda").contiguous() for t in (q, k, v, do))
+    g = [torch.empty_like(qd) for _ in range(3)]
+    plan = binding.hstu_plan_create_ex(w.offsets, nt, w.batch, w.heads, w.d, w.max_seqlen,
+                                       binding.HSTU_PLAN_BACKWARD)
+    try:
+        binding.hstu_attn_bwd_plan(plan, qd, kd, vd, dod, w.alpha, w.inv_n, *g)
+        torch.cuda.synchronize()
+    finally:
+        binding.hstu_plan_destroy(plan)
+    parity.assert_device_ok()
+    rt, rh, nu = parity.sample_rows(w, 192, seed=9)
+    # and each of the first 8 sequences' last history row, first and last candidate
+    off = w.offsets.astype(np.int64)
+    extra = [t for b in range(8) for t in (off[b + 1] - nt[b] - 1, off[b + 1] - nt[b], off[b + 1] - 1)]
+    rt = np.concatenate([rt, np.array(extra, dtype=rt.dtype)])
+    rh = np.concatenate([rh, np.arange(len(extra), dtype=rh.dtype) % w.heads])
+    refs = reference.hstu_bwd_rows(q, k, v, do, w.offsets, w.alpha, w.inv_n, rt, rh, num_targets=nt)
+    idx_t, idx_h = torch.as_tensor(rt, device="cuda"), torch.as_tensor(rh, device="cuda")
+    for name, gt, rf in zip(("dq", "dk", "dv"), g, refs):
+        got = gt[idx_t, idx_h].float().cpu().numpy().astype(np.float64)
+        rms = float(np.sqrt(np.mean(rf[:nu] ** 2)))
+        assert np.all(np.isfinite(got)), name
+        worst = parity.ratio(got, rf, rms).max()
+        assert worst <= 1.0, f"{name}: worst err/tol {worst:.3f}"
