@@ -56,3 +56,19 @@ def test_single_rank_aggregation_needs_no_process_group():
     import bench
     value, ms = bench.aggregate(2e12, 4.0, 1)
     assert ms == 4.0 and value == pytest.approx(500.0)
+
+
+@pytest.mark.parametrize("extra", [[], ["--backward"], ["--workload", "candidates", "--candidates-only"]])
+def test_reference_arm_runs_on_rank_zero_only(extra):
+    # under torchrun every rank but 0 exits at once, prints nothing and
+    # touches the oracle not at all
+    import subprocess
+    import sys
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1",
+               MASTER_PORT=str(_free_port()))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3", *extra],
+                       env=env, capture_output=True, text=True, timeout=120, cwd=root)
+    assert r.returncode == 0, r.stderr[-500:]
+    assert r.stdout.strip() == ""
