@@ -15,6 +15,14 @@ TFLOP/s = 4 d heads sum_b n_b (n_b + 1) / 2 / time.  Under torchrun each
 rank runs the same workload on its own GPU (weak scaling, no data-path
 collective); rank 0 prints one JSON line with the max time over ranks.
 
+The default run (the dense workload, plain forward, one GPU) also times
+the five workloads the same way, one after another outside the timed
+region, and reports each under ``per_config``: ms/call, causal TFLOP/s and
+% of the bf16 peak, algorithmic GB/s (Q, K, V read and O written once) and
+% of the copy bandwidth, and the bound its arithmetic intensity selects
+against the ridge of the measured peaks.  ``cpu_baseline_single_thread``
+times the oracle on one host thread (tiny whole, dense sampled).
+
 ``--impl reference`` times the fp64 CPU oracle (the only reference this
 method has) on the host cores, each step a bounded sample of rows of the
 same workload.
@@ -124,6 +132,91 @@ def workload_by_name(name: str):
 def algorithmic_bytes(w: workloads.Workload, norm_gate: bool = False) -> float:
     # read Q, K, V (and U with the output stage) once and write O once, bf16
     return float((10.0 if norm_gate else 8.0) * w.d * w.heads * w.total)
+
+
+def roofline_entry(flops: float, nbytes: float, ms: float, peaks: dict) -> dict:
+    """Both roofs for one launch: causal TFLOP/s against the bf16 peak and
+    algorithmic GB/s against the copy bandwidth.  The bound is the roof the
+    launch's arithmetic intensity (causal FLOP per algorithmic byte) puts
+    first: below the ridge peak_flops / peak_bytes it is HBM."""
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    intensity = flops / nbytes if nbytes else float("inf")
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return {"ms": ms, "causal_tflops": tflops, "pct_of_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
+            "algorithmic_bytes": nbytes, "hbm_gbs": gbs, "pct_of_hbm_peak": 100.0 * gbs / peaks["hbm_gbs"],
+            "flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+            "bound": "tensor" if intensity >= ridge else "hbm"}
+
+
+def time_forward_plan(w: workloads.Workload, dev, stream, flush, steps: int, warmup: int):
+    """Kernel-only times (ms, one per step) of the plain forward on workload
+    w, as the headline is timed: a prebuilt plan over device buffers, L2
+    flushed between steps outside the events.  Returns (times, work items)."""
+    import torch
+    from hstu_jagged_attention_gb300 import binding
+    q, k, v = (t.to(dev) for t in workloads.draw_qkv(w))
+    out = torch.empty_like(q)
+    plan = binding.hstu_plan_create(w.offsets, w.batch, w.heads, w.d, w.max_seqlen)
+    try:
+        for _ in range(warmup):
+            binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            binding.hstu_attn_fwd_plan(plan, q, k, v, w.alpha, w.inv_n, out, stream)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        n_items = binding.hstu_plan_num_items(plan)
+    finally:
+        binding.hstu_plan_destroy(plan)
+    st, site = binding.hstu_last_status()
+    if st != binding.HSTU_OK:
+        raise RuntimeError(f"device wait gave up on the {w.name} workload (site {site})")
+    return [a.elapsed_time(b) for a, b in ev], n_items
+
+
+def per_config_report(dev, stream, flush, steps: int, warmup: int, peaks: dict, clock_sampler=None):
+    """One entry per workload of the five configs: median ms/call, causal
+    TFLOP/s, % of the bf16 peak, algorithmic GB/s, % of the copy bandwidth,
+    and the bound its intensity selects."""
+    rep = {}
+    for name in workloads.WORKLOAD_NAMES:
+        w = workloads.workload(name)
+        times, n_items = time_forward_plan(w, dev, stream, flush, steps, warmup)
+        ms = statistics.median(times)
+        e = roofline_entry(causal_flops(w), algorithmic_bytes(w), ms, peaks)
+        e.update({"ms_mean": statistics.mean(times), "ms_min": min(times), "steps": steps,
+                  "work_items": n_items, "shape": w.describe()})
+        rep[name] = e
+    return rep
+
+
+def cpu_single_thread_report(seconds: float) -> dict:
+    """The oracle on one host thread (the CPU baseline plan's single-thread
+    leg): the whole tiny workload, and a bounded sample of rows of dense."""
+    from oracle import reference
+    rep = {}
+    w = workloads.workload("tiny")
+    q, k, v = (t.float().numpy() for t in workloads.draw_qkv(w))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        reference.hstu_fwd(q, k, v, w.offsets, w.alpha, w.inv_n, threads=1)
+        reps += 1
+        if time.perf_counter() - t0 > 0.5:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    rep["tiny"] = {"ms_per_call": dt * 1e3, "causal_tflops": causal_flops(w) / dt / 1e12, "cores": 1,
+                   "sample": f"the whole tiny workload, {reps} calls, fp64 C oracle, 1 thread"}
+    w = workloads.workload("dense")
+    q, k, v = (t.float().numpy() for t in workloads.draw_qkv(w))
+    val, desc, threads, dt = cpu_oracle_sample(w, q, k, v, seconds, seed=7, threads=1)
+    rep["dense"] = {"causal_tflops": val, "cores": threads, "sample": desc,
+                    "ms_per_call_extrapolated": causal_flops(w) / (val * 1e12) * 1e3}
+    return rep
 
 
 def kernel_sha() -> str:
@@ -734,6 +827,14 @@ def run_ours(args, w, nt=None):
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
 
     binding.hstu_plan_destroy(plan)
+    per_config = cpu_st = None
+    if (rank == 0 and world == 1 and not args.no_per_config and not (ng or args.rab or co)
+            and nt is None and not args.sweep):
+        per_config = per_config_report(dev, stream, flush, args.steps, args.warmup, peaks)
+        if not args.no_cpu_baseline:
+            cpu_st = cpu_single_thread_report(args.cpu_single_seconds)
+    roof = roofline_entry(flops, algorithmic_bytes(w, ng), ms, peaks)
+    bound = roof["bound"]
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -745,14 +846,25 @@ def run_ours(args, w, nt=None):
                        "work_items": n_items, "grid": grid, "block": block, "smem_bytes": smem,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * achieved / peak,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peaks['source']} bf16_tflops (burst)",
-                         "algorithmic_bytes": algorithmic_bytes(w, ng)},
+            "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                          "frac": achieved / peak, "traffic": traffic,
+                          "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+                          "algorithmic_bytes": algorithmic_bytes(w, ng),
+                          "flop_per_byte": roof["flop_per_byte"], "ridge_flop_per_byte": roof["ridge_flop_per_byte"]}
+                         if bound == "tensor" else
+                         {"bound": "hbm", "achieved": roof["hbm_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": roof["hbm_gbs"] / peaks["hbm_gbs"], "traffic": traffic,
+                          "peak_source": f"{peaks['source']} hbm_gbs",
+                          "algorithmic_bytes": algorithmic_bytes(w, ng),
+                          "flop_per_byte": roof["flop_per_byte"], "ridge_flop_per_byte": roof["ridge_flop_per_byte"]}),
+            "hbm_gbs": roof["hbm_gbs"], "pct_of_hbm_peak": roof["pct_of_hbm_peak"],
+            "per_config": per_config,
+            "cpu_baseline_single_thread": cpu_st,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "cpu_baseline": cpu,
             # the attention kernel per step, and the output-stage kernel after it
+            # (the per-config timings run outside the timed region)
             "gpu_launches": args.steps * (2 if ng else 1),
             "clocks": clocks,
             "timed_wall_s": wall,
@@ -775,6 +887,10 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="one line per workload (extra lines)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-single-seconds", type=float, default=6.0,
+                    help="seconds of single-thread oracle work on the dense workload")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config timings of the five workloads")
     ap.add_argument("--norm-gate", action="store_true",
                     help="fuse the layer's output stage Norm(A V) * U into the timed call")
     ap.add_argument("--backward", action="store_true",

@@ -21,9 +21,10 @@ constexpr int kMaxDevices = 64;
 // until the process exits.  Shared by every call on that device.
 static __device__ __align__(256) hstu::Item g_noalloc_items[kMaxItems];
 
-// Host staging for the list.  A pageable-to-device cudaMemcpyAsync returns
-// once the source has been staged, so the array is free again when the
-// call returns; the mutex keeps concurrent callers from interleaving.
+// Host staging for the list.  A pageable-to-device cudaMemcpyAsync first
+// waits for the work already on the stream, then returns once the source
+// has been staged, so the array is free again when the call returns; the
+// mutex keeps concurrent callers from interleaving.
 hstu::Item g_host_items[kMaxItems];
 std::mutex g_mu;
 hstu::Item* g_dev_ptr[kMaxDevices] = {};

@@ -33,7 +33,8 @@
  * asynchronous on the given stream (a cudaStream_t; NULL = legacy default
  * stream) and return once the work is enqueued.  Outputs are complete when
  * the stream reaches that point.  Nothing here synchronises the device
- * except where a function says so.
+ * except where a function says so (hstu_attn_fwd_noalloc waits for the
+ * stream's earlier work; see there).
  *
  * Errors.  Every function returns HSTU_OK (0) or a negative hstu_status.
  * Argument checks happen before anything is enqueued; on an argument error
@@ -125,6 +126,11 @@ int hstu_attn_fwd(const void* q, const void* k, const void* v, const int32_t* of
  *     the GPU (other streams, other threads) overwrite each other's work
  *     list and give wrong results.  Each call writes every entry it reads,
  *     so nothing needs clearing between calls.
+ *   - The list is built on the host in a fixed pageable array and copied
+ *     in with cudaMemcpyAsync.  A copy from pageable memory first waits
+ *     for the work already enqueued on `stream`, so unlike hstu_attn_fwd
+ *     this call blocks the calling thread until that earlier work has
+ *     finished (the attention kernel itself is still only enqueued).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, once per device, with that device current);
  *     make that first call before any stream capture.

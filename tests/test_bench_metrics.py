@@ -42,3 +42,27 @@ def test_dense_workload_counts():
     # 16 sequences of 4096 tokens, 4 heads, d = 64: 137.47 causal GFLOP
     assert bench.causal_flops(w) / 1e9 == pytest.approx(137.47, rel=1e-4)
     assert bench.algorithmic_bytes(w) == 8 * 64 * 4 * 65536
+
+
+def test_roofline_entry_picks_the_bound_by_intensity():
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}   # ridge 250 FLOP/B
+    hi = bench.roofline_entry(flops=1e12, nbytes=1e9, ms=1.0, peaks=peaks)   # 1000 FLOP/B
+    lo = bench.roofline_entry(flops=1e10, nbytes=1e9, ms=1.0, peaks=peaks)   # 10 FLOP/B
+    assert hi["bound"] == "tensor" and lo["bound"] == "hbm"
+    assert hi["ridge_flop_per_byte"] == pytest.approx(250.0)
+    assert hi["causal_tflops"] == pytest.approx(1000.0) and hi["pct_of_bf16_peak"] == pytest.approx(50.0)
+    assert lo["hbm_gbs"] == pytest.approx(1000.0) and lo["pct_of_hbm_peak"] == pytest.approx(12.5)
+
+
+def test_tiny_is_hbm_side_and_dense_tensor_side_of_the_measured_ridge():
+    peaks = {"bf16_tflops": 1923.8, "hbm_gbs": 6796.9}
+    for name, want in (("tiny", "hbm"), ("dense", "tensor"), ("long", "tensor")):
+        w = workloads.workload(name)
+        e = bench.roofline_entry(bench.causal_flops(w), bench.algorithmic_bytes(w), 1.0, peaks)
+        assert e["bound"] == want, name
+
+
+def test_single_thread_oracle_report_runs_bounded():
+    rep = bench.cpu_single_thread_report(0.3)
+    assert rep["tiny"]["cores"] == 1 and rep["dense"]["cores"] == 1
+    assert rep["tiny"]["causal_tflops"] > 0 and rep["dense"]["causal_tflops"] > 0

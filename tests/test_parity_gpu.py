@@ -1,10 +1,11 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
 Tolerance per element: |gpu - ref| <= 1e-2 |ref| + 1e-3 rms(ref) (see
-tests/parity.py).  Small cases are compared element by element over the
-whole output; the full-size workloads are compared on a uniform random
-sample of rows plus edge rows, in the launch configuration the benchmark
-times (a prebuilt plan over device buffers).
+tests/parity.py).  Small cases and the full-size workloads are compared
+element by element over the whole output; the full-size workloads are also
+compared on a uniform random sample of rows plus edge rows (the sampled
+oracle), in the launch configuration the benchmark times (a prebuilt plan
+over device buffers).
 """
 import numpy as np
 import pytest
@@ -59,6 +60,19 @@ def test_many_short_sequences_full(d):
     (q, k, v), (qd, kd, vd) = _draw(w, seed=70 + d)
     out = parity.run_plan(w, qd, kd, vd)
     parity.full_check(w, q, k, v, out)
+
+
+@pytest.mark.parametrize("name", ["dense", "skewed", "long", "serving"])
+def test_full_size_workloads_every_element(name):
+    # Every output element of the full-size workload against the threaded
+    # fp64 oracle (tens of seconds on the host cores), in the launch
+    # configuration the benchmark times.
+    w = workloads.workload(name)
+    (q, k, v), (qd, kd, vd) = _draw(w)
+    out = parity.run_plan(w, qd, kd, vd)
+    parity.assert_device_ok()
+    worst = parity.full_check(w, q, k, v, out)
+    print(f"\n{name}: worst err/tol over every element {worst:.3f}")
 
 
 @pytest.mark.parametrize("name", ["dense", "skewed", "long", "serving"])

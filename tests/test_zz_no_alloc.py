@@ -5,8 +5,9 @@ fixed memory budget, or a framework whose allocator must not be bypassed)
 and cannot let the library call cudaMalloc or cudaMallocAsync.  This entry
 point keeps the work list in a fixed array inside the library instead.
 Its output must match hstu_attn_fwd's, call after call, within the parity
-tolerance the other GPU tests use.  This file is collected last so that a
-failure here does not hide the results of the other tests.
+tolerance the other GPU tests use, and the fp64 oracle's element by
+element.  This file is collected last so that a failure here does not hide
+the results of the other tests.
 """
 import numpy as np
 import pytest
@@ -51,6 +52,7 @@ def test_noalloc_matches_existing_entry_on_two_calls_in_a_row():
         ref = _existing(w, q, k, v)
         torch.cuda.synchronize()
         _assert_close(got, ref)
+        parity.full_check(w, q, k, v, got)
     assert binding.hstu_last_status() == (binding.HSTU_OK, 0)
 
 
