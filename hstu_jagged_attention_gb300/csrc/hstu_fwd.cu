@@ -526,12 +526,18 @@ struct Cursor {
   uint32_t tc;
   BlockOf<TGT> b, nb;
   bool valid, nvalid;
+  // The item's first key block: 0, except for a candidate item that walks
+  // its diagonal block alone (no history keys before it).
+  __device__ __forceinline__ int first_kt() const {
+    if constexpr (TGT) return b.nk == 1 ? b.qt : 0;
+    return 0;
+  }
   __device__ __forceinline__ void start(const FwdArgs& a) {
     it = 0;
-    kt = 0;
     ki = 0;
     tc = 0;
     valid = load_block<VAR>(a, 0, b);
+    kt = valid ? first_kt() : 0;
     nvalid = valid && load_block<VAR>(a, 1, nb);
   }
   __device__ __forceinline__ void advance(const FwdArgs& a) {
@@ -546,10 +552,10 @@ struct Cursor {
     }
     if (next_item) {
       ki = 0;
-      kt = 0;
       ++it;
       valid = nvalid;
       b = nb;
+      kt = valid ? first_kt() : 0;
       nvalid = valid && load_block<VAR>(a, it + 1, nb);
     }
   }
@@ -681,7 +687,7 @@ __device__ void role_mma_qk(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
     constexpr int J = decltype(jc)::value;
     if (!ok || !qc.valid) return false;
     const int qs = C::QS == 1 ? 0 : (qc.it & 1);
-    if (qc.kt == 0 &&
+    if (qc.ki == 0 &&
         !(ok = wait_one(bar(C::B_QFULL + qs), (uint32_t)(qc.it / C::QS) & 1u, w, kSiteQFull)))
       return false;
     if (!(ok = wait_one(bar(C::B_QKREADY + J), ph, w, kSiteKFull))) return false;
@@ -751,7 +757,7 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
       pa[2 * i + 1] = pin32(tmem + (uint32_t)(J * 128 + 32 * (kk >> 1) + 8 * (kk & 1) + 16));
       vb[i] = pin64(v_desc0 + (uint64_t)((J * C::TILEB + kk * 2 * C::ATOMB) >> 4));
     }
-    if (pc.kt != pc.b.qt && (H == 1 || pc.kt != 0)) {
+    if (pc.kt != pc.b.qt && (H == 1 || pc.ki != 0)) {
       // full half continuing an accumulation
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -763,7 +769,7 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
       // (only the 16-key steps that hold keys < n)
       const int cols = pc.b.cols(pc.kt);
       const int n_steps = (cols - 64 * H) / 16;  // <= 0: none in this half
-      const bool first = H == 0 && pc.kt == 0;
+      const bool first = H == 0 && pc.ki == 0;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (i < n_steps) {
@@ -785,7 +791,7 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
     const int ob = C::OB == 1 ? 0 : (pc.it & 1);
     const bool last = pc.kt == pc.b.qt;
     if (!pa_ready && !(ok = wait_one(bar(C::B_PFULL + J), ph, w, kSitePFull))) return false;
-    if (pc.kt == 0 &&
+    if (pc.ki == 0 &&
         !(ok = wait_one(bar(C::B_OEMPTY + ob), ((uint32_t)(pc.it / C::OB) & 1u) ^ 1u, w, kSiteOEmpty)))
       return false;
     if (!v_ready && !(ok = wait_one(bar(C::B_VFULL + J), ph, w, kSiteVFull))) return false;

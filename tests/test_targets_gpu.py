@@ -26,9 +26,11 @@ def _built():
 
 # lengths with the candidate count of each: the history ends inside a key
 # block, on a block boundary, before the first block ends, not at all (all
-# candidates), candidates spanning several query blocks, no candidates
+# candidates, in one block and over several: each query block then walks
+# its diagonal block alone), candidates spanning several query blocks, no
+# candidates
 CASES = [(300, 100), (513, 128), (256, 1), (700, 333), (90, 90), (129, 0), (0, 0), (1, 1),
-         (640, 500), (385, 2)]
+         (640, 500), (385, 2), (300, 300), (384, 384)]
 
 
 def _draw(w, seed):
