@@ -27,6 +27,7 @@ HSTU_NOALLOC_MAX_ITEMS = 65536
 BLOCK_M = 128
 HSTU_DEBUG_UNSIGNALLED_WAIT = 1
 HSTU_DEBUG_TRACE = 2
+HSTU_DEBUG_NO_PAIRS = 4
 TRACE_EVENTS = {1: "qk_issue", 2: "pv_issue", 3: "silu_start", 4: "silu_end", 5: "epi_start",
                 6: "epi_end", 7: "load_k", 8: "load_v", 9: "load_q", 10: "mma_k_ready",
                 11: "mma_qk_done", 12: "mma_p_ready", 13: "mma_pv_done"}
@@ -59,6 +60,9 @@ _SIGNATURES = {
     "hstu_attn_fwd_plan": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_float, ctypes.c_float, _VP, _VP]),
     "hstu_plan_destroy": (ctypes.c_int, [_VP]),
     "hstu_plan_num_items": (ctypes.c_int, [_VP, _IP]),
+    "hstu_plan_num_pairs": (ctypes.c_int, [_VP, _IP]),
+    "hstu_worklist_build_pairs": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int,
+                                                 _IP]),
     "hstu_plan_worklist": (ctypes.c_int, [_VP, _I32P, ctypes.c_int, _IP]),
     "hstu_worklist_build": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int, _IP]),
     "hstu_launch_shape": (ctypes.c_int, [_VP, _IP, _IP, _IP]),
@@ -108,6 +112,7 @@ _SIGNATURES = {
 HSTU_PLAN_NORM_GATE = 1
 HSTU_PLAN_BACKWARD = 2
 HSTU_PLAN_CANDIDATES_ONLY = 4
+HSTU_PLAN_PAIRS = 8
 
 _lib = None
 
@@ -500,6 +505,28 @@ def hstu_plan_num_items(plan: Plan) -> int:
     n = ctypes.c_int()
     _check(lib().hstu_plan_num_items(plan.handle, ctypes.byref(n)), "hstu_plan_num_items")
     return n.value
+
+
+def hstu_plan_num_pairs(plan: Plan) -> int:
+    """Pair items of the plan (0: one CTA per work item)."""
+    n = ctypes.c_int()
+    _check(lib().hstu_plan_num_pairs(plan.handle, ctypes.byref(n)), "hstu_plan_num_pairs")
+    return n.value
+
+
+def hstu_worklist_build_pairs(host_offsets, heads: int) -> np.ndarray:
+    """Host-only work list of CTA pairs (no CUDA call): int32 (n_items, 4),
+    rows (first token, length, head, qp)."""
+    off = _host_offsets(host_offsets)
+    batch = len(off) - 1
+    n = ctypes.c_int()
+    _check(lib().hstu_worklist_build_pairs(off.ctypes.data_as(_I32P), batch, int(heads), None, 0,
+                                           ctypes.byref(n)), "hstu_worklist_build_pairs")
+    buf = np.zeros((max(n.value, 1), 4), dtype=np.int32)
+    _check(lib().hstu_worklist_build_pairs(off.ctypes.data_as(_I32P), batch, int(heads),
+                                           buf.ctypes.data_as(_I32P), n.value, ctypes.byref(n)),
+           "hstu_worklist_build_pairs")
+    return buf[:n.value]
 
 
 def hstu_plan_worklist(plan: Plan) -> np.ndarray:

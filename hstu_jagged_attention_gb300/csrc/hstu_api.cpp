@@ -211,6 +211,81 @@ int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long l
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 
+// Tensor maps of the pair kernel: k with box (64, 1, 64) (each CTA holds 64
+// keys of a block), v with box (d/2, 1, 128) (each CTA holds half the
+// columns) and the swizzle of a d-byte row.
+int make_map_pair(CUtensorMap* m, const void* ptr, long long total, int heads, int d, int box_x,
+                  int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return HSTU_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)total};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2u, (cuuint64_t)heads * (cuuint64_t)d * 2u};
+  const cuuint32_t box[3] = {(cuuint32_t)box_x, 1u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapSwizzle sw = box_x * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+// Clusters of a pair launch: one per two SMs at most, and no more than
+// there are pair items; two CTAs each.
+int pair_grid_for(int n_pairs, int sms) { return 2 * std::min(n_pairs, sms / 2); }
+
+int launch_pairs(const hstu::Item* d_pairs, int n_pairs, long long total, int heads, int d, const void* q,
+                 const void* k, const void* v, float alpha, float inv_n, void* out, cudaStream_t stream) {
+  if (n_pairs == 0) return HSTU_OK;
+  int sms = 0;
+  int rc = device_check(&sms);
+  if (rc != HSTU_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_map(&tq, q, total, heads, d)) != HSTU_OK) return rc;
+  if ((rc = make_map_pair(&tk, k, total, heads, d, 64, HSTU_BLOCK_M / 2)) != HSTU_OK) return rc;
+  if ((rc = make_map_pair(&tv, v, total, heads, d, d / 2, HSTU_BLOCK_M)) != HSTU_OK) return rc;
+  hstu::FwdArgs a{};
+  a.items = d_pairs;
+  a.n_items = n_pairs;
+  a.out = out;
+  a.total = total;
+  a.heads = heads;
+  a.half_alpha = 0.5f * alpha;
+  a.inv_n = inv_n;
+  a.timeout_ns = wait_timeout_ns();
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
+  }
+  const cudaError_t e = hstu::launch_fwd_pairs(d, tq, tk, tv, a, pair_grid_for(n_pairs, sms), stream);
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+    return HSTU_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+bool pairs_disabled() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return (g_debug_flags & hstu::kDebugNoPairs) != 0;
+}
+
+// Whether a plan or call picks CTA pairs by itself: not at present.  A
+// pair step still gives each SM one block of SiLU work, and its issuing
+// thread's serial chain per step (barrier tests, products, commits) is as
+// long as the one-CTA kernel's, so pairs measured no faster on any of the
+// five workloads (dense 0.268 against 0.245 ms on GB300).  Plans made with
+// HSTU_PLAN_PAIRS still use them.  The waste rule below (within 15% of the
+// one-CTA work list's SM-blocks) is kept for when they are.
+constexpr bool kPairsByDefault = false;
+bool use_pairs(const int32_t* off, int batch, int d) {
+  if (!kPairsByDefault || (d != 64 && d != 128)) return false;
+  long long single = 0, pair = 0;
+  for (int b = 0; b < batch; ++b) {
+    const long long nq = (off[b + 1] - off[b] + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    single += nq * (nq + 1) / 2;
+    for (long long qp = 0; 2 * qp < nq; ++qp) pair += 2 * std::min(2 * qp + 2, nq);
+  }
+  return single > 0 && pair * 100 <= single * 115;
+}
+
 // (The plan type is defined below; make_plan and oneshot are declared here
 // and defined after it.)
 int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d, int max_seqlen,
@@ -269,6 +344,36 @@ void fill_items(const int32_t* off, int batch, int heads, Item* dst) {
       if ((n + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M > qt)
         for (int h = 0; h < heads; ++h) dst[i++] = make_int4(off[b], n, h, qt);
     }
+}
+
+// Pair items: (first token, length, head, qp) for qp < ceil(nq / 2), each
+// walking min(2 qp + 2, nq) key blocks; (cost, b, h, qp) generated in b, h,
+// qp order, then a stable sort by cost descending.
+long long count_pairs(const int32_t* off, int batch, int heads) {
+  long long n = 0;
+  for (int b = 0; b < batch; ++b) {
+    const long long nq = (off[b + 1] - off[b] + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    n += (nq + 1) / 2 * heads;
+  }
+  return n;
+}
+
+void fill_pairs(const int32_t* off, int batch, int heads, Item* dst) {
+  struct Entry {
+    int cost;
+    Item item;
+  };
+  std::vector<Entry> e;
+  e.reserve((size_t)count_pairs(off, batch, heads));
+  for (int b = 0; b < batch; ++b) {
+    const int n = off[b + 1] - off[b];
+    const int nq = (n + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
+    for (int h = 0; h < heads; ++h)
+      for (int qp = 0; 2 * qp < nq; ++qp)
+        e.push_back(Entry{std::min(2 * qp + 2, nq), make_int4(off[b], n, h, qp)});
+  }
+  std::stable_sort(e.begin(), e.end(), [](const Entry& x, const Entry& y) { return x.cost > y.cost; });
+  for (size_t i = 0; i < e.size(); ++i) dst[i] = e[i].item;
 }
 
 void fill_items_targets(const int32_t* off, const int32_t* num_targets, int batch, int heads,
@@ -353,6 +458,9 @@ struct hstu_plan {
   char* d_bwd = nullptr;
   int32_t* d_bwd_hist = nullptr;
   float* d_bwd_acc = nullptr;
+  // the plain forward on CTA pairs (where use_pairs holds): its work list
+  int n_pairs = 0;
+  hstu::Item* d_pairs = nullptr;
   int device = -1;
 };
 
@@ -370,8 +478,10 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
   if (!plan) return HSTU_ERR_INVALID_ARG;
   *plan = nullptr;
   if (heads < 1 || max_seqlen < 0 ||
-      (flags & ~(unsigned)(HSTU_PLAN_NORM_GATE | HSTU_PLAN_BACKWARD | HSTU_PLAN_CANDIDATES_ONLY)))
+      (flags & ~(unsigned)(HSTU_PLAN_NORM_GATE | HSTU_PLAN_BACKWARD | HSTU_PLAN_CANDIDATES_ONLY |
+                           HSTU_PLAN_PAIRS)))
     return HSTU_ERR_INVALID_ARG;
+  if ((flags & HSTU_PLAN_PAIRS) && nt) return HSTU_ERR_INVALID_ARG;
   // the candidates' rows only: needs candidates; the output stage normalises
   // every row and the backward every pair, so neither combines with it
   const bool cand_only = (flags & HSTU_PLAN_CANDIDATES_ONLY) != 0;
@@ -402,6 +512,7 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
     if (p->d_items) cudaFree(p->d_items);
     if (p->d_norm) cudaFree(p->d_norm);
     if (p->d_bwd) cudaFree(p->d_bwd);
+    if (p->d_pairs) cudaFree(p->d_pairs);
     delete p;
     return code;
   };
@@ -419,6 +530,22 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
       (hbytes &&
        cudaMemcpy(p->d_hist, p->hist.data(), hbytes, cudaMemcpyHostToDevice) != cudaSuccess))
     return fail(HSTU_ERR_CUDA);
+  if (!nt && (d == 64 || d == 128) && ((flags & HSTU_PLAN_PAIRS) || use_pairs(off, batch, d))) {
+    std::vector<hstu::Item> pairs;
+    try {
+      pairs.resize((size_t)hstu::count_pairs(off, batch, heads));
+    } catch (const std::bad_alloc&) {
+      return fail(HSTU_ERR_NO_MEMORY);
+    }
+    hstu::fill_pairs(off, batch, heads, pairs.data());
+    p->n_pairs = (int)pairs.size();
+    if ((e = cudaMalloc(reinterpret_cast<void**>(&p->d_pairs), pairs.size() * sizeof(hstu::Item))) !=
+        cudaSuccess)
+      return fail(mem_code(e));
+    if (cudaMemcpy(p->d_pairs, pairs.data(), pairs.size() * sizeof(hstu::Item), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return fail(HSTU_ERR_CUDA);
+  }
   if (norm) {
     if ((e = cudaMalloc(reinterpret_cast<void**>(&p->d_norm),
                         hstu::norm_scratch_bytes(p->total, heads, d))) != cudaSuccess)
@@ -490,6 +617,28 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
   if (total == 0) return HSTU_OK;
   if ((rc = check_buffers(q, k, v, out)) != HSTU_OK) return rc;
 
+  if (!ng && !rab && !num_targets && !pairs_disabled() && use_pairs(off, batch, d)) {
+    std::vector<hstu::Item> pairs;
+    try {
+      pairs.resize((size_t)hstu::count_pairs(off, batch, heads));
+    } catch (const std::bad_alloc&) {
+      return HSTU_ERR_NO_MEMORY;
+    }
+    hstu::fill_pairs(off, batch, heads, pairs.data());
+    if (pairs.empty()) return HSTU_OK;
+    const size_t pbytes = pairs.size() * sizeof(hstu::Item);
+    hstu::Item* d_pairs = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_pairs), pbytes, s);
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+    // pageable source: the copy returns once the bytes are staged
+    if (cudaMemcpyAsync(d_pairs, pairs.data(), pbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+      cudaFreeAsync(d_pairs, s);
+      return HSTU_ERR_CUDA;
+    }
+    rc = launch_pairs(d_pairs, (int)pairs.size(), total, heads, d, q, k, v, alpha, inv_n, out, s);
+    if (cudaFreeAsync(d_pairs, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
+    return rc;
+  }
   std::vector<hstu::Item> items;
   std::vector<int32_t> hist;
   if ((rc = build_worklist(off, num_targets, batch, heads, items, hist)) != HSTU_OK) return rc;
@@ -652,6 +801,7 @@ int hstu_plan_destroy(hstu_plan* plan) {
   if (plan->d_items && cudaFree(plan->d_items) != cudaSuccess) rc = HSTU_ERR_CUDA;
   if (plan->d_norm && cudaFree(plan->d_norm) != cudaSuccess) rc = HSTU_ERR_CUDA;
   if (plan->d_bwd && cudaFree(plan->d_bwd) != cudaSuccess) rc = HSTU_ERR_CUDA;
+  if (plan->d_pairs && cudaFree(plan->d_pairs) != cudaSuccess) rc = HSTU_ERR_CUDA;
   delete plan;
   return rc;
 }
@@ -659,6 +809,33 @@ int hstu_plan_destroy(hstu_plan* plan) {
 int hstu_plan_num_items(const hstu_plan* plan, int* n_items) {
   if (!plan || !n_items) return HSTU_ERR_INVALID_ARG;
   *n_items = (int)plan->items.size();
+  return HSTU_OK;
+}
+
+int hstu_plan_num_pairs(const hstu_plan* plan, int* n_pairs) {
+  if (!plan || !n_pairs) return HSTU_ERR_INVALID_ARG;
+  *n_pairs = plan->n_pairs;
+  return HSTU_OK;
+}
+
+int hstu_worklist_build_pairs(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
+                              int capacity, int* n_items) {
+  if (!n_items || heads < 1 || capacity < 0) return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(host_offsets, batch, -1);
+  if (rc != HSTU_OK) return rc;
+  std::vector<hstu::Item> pairs;
+  try {
+    pairs.resize((size_t)hstu::count_pairs(host_offsets, batch, heads));
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+  if (pairs.size() > (size_t)INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  hstu::fill_pairs(host_offsets, batch, heads, pairs.data());
+  *n_items = (int)pairs.size();
+  if (host_dst) {
+    const size_t n = std::min(pairs.size(), (size_t)capacity);
+    std::memcpy(host_dst, pairs.data(), n * sizeof(hstu::Item));
+  }
   return HSTU_OK;
 }
 
@@ -725,6 +902,12 @@ int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_by
   int sms = 0;
   const int rc = device_check(&sms);
   if (rc != HSTU_OK) return rc;
+  if (plan->d_pairs && !pairs_disabled()) {
+    *grid = pair_grid_for(plan->n_pairs, sms);
+    *block = hstu::kFwdThreads;
+    *smem_bytes = hstu::fwd_pair_smem_bytes(plan->d);
+    return HSTU_OK;
+  }
   *grid = grid_for((int)plan->items.size(), sms);
   *block = hstu::kFwdThreads;
   *smem_bytes = hstu::fwd_smem_bytes(plan->d);
@@ -737,6 +920,9 @@ int hstu_attn_fwd_plan(const hstu_plan* plan, const void* q, const void* k, cons
   if (plan->items.empty()) return HSTU_OK;
   int rc = check_buffers(q, k, v, out);
   if (rc != HSTU_OK) return rc;
+  if (plan->d_pairs && !pairs_disabled())
+    return launch_pairs(plan->d_pairs, plan->n_pairs, plan->total, plan->heads, plan->d, q, k, v, alpha,
+                        inv_n, out, reinterpret_cast<cudaStream_t>(stream));
   return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
                 plan->d, q, k, v, alpha, inv_n, out, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -776,6 +962,9 @@ int hstu_attn_fwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, c
     ngw.beta = ng->beta;
     ngw.eps = ng->eps;
   }
+  if (!ng && !rab && plan->d_pairs && !pairs_disabled())
+    return launch_pairs(plan->d_pairs, plan->n_pairs, plan->total, plan->heads, plan->d, q, k, v, alpha,
+                        inv_n, out, reinterpret_cast<cudaStream_t>(stream));
   return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
                 plan->d, q, k, v, alpha, inv_n, out, ng ? &ngw : nullptr,
                 reinterpret_cast<cudaStream_t>(stream), rab);
@@ -990,7 +1179,8 @@ int hstu_set_wait_timeout_ns(uint64_t ns) {
 }
 
 int hstu_set_debug_flags(uint32_t flags) {
-  if (flags & ~(uint32_t)(HSTU_DEBUG_UNSIGNALLED_WAIT | HSTU_DEBUG_TRACE)) return HSTU_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)(HSTU_DEBUG_UNSIGNALLED_WAIT | HSTU_DEBUG_TRACE | HSTU_DEBUG_NO_PAIRS))
+    return HSTU_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_debug_flags = flags;
   return HSTU_OK;

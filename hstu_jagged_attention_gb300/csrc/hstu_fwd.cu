@@ -1201,24 +1201,27 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
     uint4* dst = reinterpret_cast<uint4*>(
         out + ((size_t)(b.s0 + kBM * b.qt + row) * (size_t)a.heads + (size_t)b.h) * D);
     const bool live = row < b.rows();
-    // Each 32-column chunk is scaled, packed and stored as it is read.
+    // The whole row is read, scaled and packed first, so that the O buffer
+    // is released before the stores (the PV issuer waits on it at the next
+    // item but one).
+    uint32_t packed[D / 2];
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
       tmem_ld32(o_t + 32u * c, o);
-      uint32_t packed[16];
 #pragma unroll
       for (int m = 0; m < 16; ++m)
-        packed[m] = pack_bf16x2(__uint_as_float(o[2 * m]) * inv_n, __uint_as_float(o[2 * m + 1]) * inv_n);
-      if (live) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          dst[4 * c + u] = make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
-      }
+        packed[16 * c + m] =
+            pack_bf16x2(__uint_as_float(o[2 * m]) * inv_n, __uint_as_float(o[2 * m + 1]) * inv_n);
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + ob));
+    if (live) {
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u)
+        dst[u] = make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+    }
     trace(a, kEvEpiEnd, (unsigned)it);
   }
 }
@@ -1403,8 +1406,26 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 }
 
 #include "hstu_bwd.cuh"
+#include "hstu_fwd_pair.cuh"
 
 }  // namespace
+
+int fwd_pair_smem_bytes(int d) {
+  switch (d) {
+    case 64: return PCfg<64>::SMEM_LAUNCH;
+    case 128: return PCfg<128>::SMEM_LAUNCH;
+    default: return -1;
+  }
+}
+
+cudaError_t launch_fwd_pairs(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdArgs& a, int grid, cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch_pair_d<64>(tq, tk, tv, a, grid, stream);
+    case 128: return launch_pair_d<128>(tq, tk, tv, a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 int fwd_smem_bytes(int d) {
   switch (d) {

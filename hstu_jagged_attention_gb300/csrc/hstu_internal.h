@@ -119,6 +119,8 @@ constexpr unsigned kDebugUnsignalledWait = 1u;
 // Tracing: CTA 0 records a clock64 stamp per pipeline event (see
 // read_and_clear_trace).
 constexpr unsigned kDebugTrace = 2u;
+// The plain forward on one CTA per work item even where CTA pairs apply.
+constexpr unsigned kDebugNoPairs = 4u;
 
 // Trace records: {clock64, (event << 48) | (warp << 40) | index}.
 cudaError_t read_and_clear_trace(unsigned long long* dst, int capacity, int* n);
@@ -136,6 +138,23 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
 
 // Swizzle span in bytes of one shared-memory row for head dimension d (128 or 64).
 int fwd_swizzle_bytes(int d);
+
+// The forward on CTA pairs (2-CTA clusters, d = 64 or 128, plain causal):
+// items are pair items (first token, length, head, qp), each covering query
+// blocks 2 qp and 2 qp + 1 of one (sequence, head); grid is even (two CTAs
+// per cluster).  tq describes q as for launch_fwd (box (64, 1, 128)); tk
+// describes k with box (64, 1, 64) and the 128-byte swizzle; tv describes v
+// with box (d/2, 1, 128) and the swizzle of a d-byte row (64 or 128 bytes).
+cudaError_t launch_fwd_pairs(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdArgs& a, int grid, cudaStream_t stream);
+int fwd_pair_smem_bytes(int d);
+
+// Pair work list (host): one item per two consecutive query blocks of a
+// (sequence, head), (first token, length, head, qp), costing
+// min(2 qp + 2, ceil(n / 128)) key blocks; ordered by cost descending, then
+// sequence, head, qp ascending.
+long long count_pairs(const int32_t* off, int batch, int heads);
+void fill_pairs(const int32_t* off, int batch, int heads, Item* dst);
 
 // Device status word (bit 0: a bounded wait gave up) and the code of the
 // first wait that gave up; read and cleared together.

@@ -168,6 +168,11 @@ int hstu_plan_create(const int32_t* host_offsets, int batch, int heads, int d, i
  * hstu_attn_fwd_plan -- the forward operation for a plan's offsets and shape.
  * Arguments as hstu_attn_fwd.  Enqueues exactly one kernel (none when the
  * plan has no work items) and allocates nothing.
+ *
+ * At d = 64 and 128 the plain operation can also run on CTA pairs (two-CTA
+ * clusters whose tensor products cover 256 query rows over both SMs; see
+ * hstu_worklist_build_pairs) in plans made with HSTU_PLAN_PAIRS; the
+ * result is the same operation within the stated precision.
  */
 int hstu_attn_fwd_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
                        float alpha, float inv_n, void* out, hstu_stream_t stream);
@@ -177,6 +182,9 @@ int hstu_plan_destroy(hstu_plan* plan);
 
 /* Number of work items in a plan. */
 int hstu_plan_num_items(const hstu_plan* plan, int* n_items);
+
+/* Number of pair items in a plan: 0 when the plan runs on one CTA per item. */
+int hstu_plan_num_pairs(const hstu_plan* plan, int* n_pairs);
 
 /*
  * hstu_plan_worklist -- copy a plan's host-side work list out.
@@ -197,6 +205,21 @@ int hstu_plan_worklist(const hstu_plan* plan, int32_t* host_dst, int capacity, i
  */
 int hstu_worklist_build(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
                         int capacity, int* n_items);
+
+/*
+ * hstu_worklist_build_pairs -- the work list of CTA pairs, on the host only.
+ *
+ * A pair item covers two consecutive query blocks, 2 qp and 2 qp + 1 (256
+ * rows), of one (sequence, head); the two CTAs of a cluster take one block
+ * each and walk the key blocks 0 .. min(2 qp + 1, nq - 1) together
+ * (nq = ceil(n / 128)), so an item costs min(2 qp + 2, nq) key blocks; a
+ * sequence with an odd number of blocks ends in a pair whose second block
+ * is empty.  Items (first token, length, head, qp), ordered by cost
+ * descending, then sequence, head, qp ascending.  Arguments and errors as
+ * hstu_worklist_build.
+ */
+int hstu_worklist_build_pairs(const int32_t* host_offsets, int batch, int heads, int32_t* host_dst,
+                              int capacity, int* n_items);
 
 /*
  * Candidates (M-FALCON): HSTU paper section 3.4 and Appendix H, Algorithm 1.
@@ -314,6 +337,14 @@ int hstu_plan_create_ex(const int32_t* host_offsets, const int32_t* host_num_tar
  * (items and their history lengths, as hstu_worklist_build_targets).
  */
 #define HSTU_PLAN_CANDIDATES_ONLY 4u
+/*
+ * HSTU_PLAN_PAIRS: build the CTA-pair work list whenever the plain forward
+ * can run on CTA pairs (d = 64 or 128, no host_num_targets), not only when
+ * the pairs waste little work on these offsets; hstu_attn_fwd_plan and
+ * hstu_attn_fwd_plan_ex without rab and ng then use it.  With
+ * host_num_targets: HSTU_ERR_INVALID_ARG.  At d = 32 it has no effect.
+ */
+#define HSTU_PLAN_PAIRS 8u
 int hstu_worklist_build_candidates(const int32_t* host_offsets, const int32_t* host_num_targets,
                                    int batch, int heads, int32_t* host_items, int32_t* host_hist,
                                    int capacity, int* n_items);
@@ -481,10 +512,14 @@ int hstu_set_wait_timeout_ns(uint64_t ns);
  *       frees TMEM, returns, and hstu_last_status reports HSTU_ERR_TIMEOUT.
  *       The output is not written.  Used to test the give-up path without
  *       hanging or faulting the GPU.
+ *   HSTU_DEBUG_TRACE  record the pipeline trace (see hstu_trace_read).
+ *   HSTU_DEBUG_NO_PAIRS  run the plain forward on one CTA per work item even
+ *       where a plan or call would use CTA pairs (for comparing the two).
  * Errors: HSTU_ERR_INVALID_ARG for unknown bits.
  */
 #define HSTU_DEBUG_UNSIGNALLED_WAIT 1u
 #define HSTU_DEBUG_TRACE 2u
+#define HSTU_DEBUG_NO_PAIRS 4u
 int hstu_set_debug_flags(uint32_t flags);
 
 /*

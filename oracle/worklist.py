@@ -21,6 +21,12 @@ needs key blocks 0 .. min(qt, KH) - 1 and its diagonal block qt: a block
 strictly between them holds only keys of other candidates, which no row of
 the query block sees.  Such an item costs min(qt, KH) + 1 key blocks, and
 items_targets also returns each item's hist.
+
+The forward on CTA pairs takes two consecutive query blocks, 2 qp and
+2 qp + 1, of a (sequence, head) together: the pair walks the key blocks
+0 .. min(2 qp + 1, nq - 1) (nq = ceil(n / 128)), so a pair item costs
+min(2 qp + 2, nq) key blocks; items_pairs lists (first token, length,
+head, qp) by cost descending, then b, h, qp ascending.
 """
 from __future__ import annotations
 
@@ -113,4 +119,21 @@ def items_bwd(offsets, heads: int, block_m: int = BLOCK_M) -> np.ndarray:
                 rows.append((-(nq - kt), b, h, kt, offsets[b], n))
     rows.sort()
     out = np.array([(s0, n, h, kt) for (_, b, h, kt, s0, n) in rows], dtype=np.int32)
+    return out.reshape(-1, 4)
+
+
+def items_pairs(offsets, heads: int, block_m: int = BLOCK_M) -> np.ndarray:
+    """Pair items: int32 (n, 4) rows (first token, length, head, qp), one per
+    two consecutive query blocks of each (sequence, head); cost
+    min(2 qp + 2, nq) descending, then b, h, qp ascending."""
+    offsets = [int(x) for x in offsets]
+    rows = []
+    for b in range(len(offsets) - 1):
+        n = offsets[b + 1] - offsets[b]
+        nq = (n + block_m - 1) // block_m
+        for h in range(heads):
+            for qp in range((nq + 1) // 2):
+                rows.append((-min(2 * qp + 2, nq), b, h, qp, offsets[b], n))
+    rows.sort()
+    out = np.array([(s0, n, h, qp) for (_, b, h, qp, s0, n) in rows], dtype=np.int32)
     return out.reshape(-1, 4)

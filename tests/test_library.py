@@ -327,3 +327,24 @@ def test_bwd_candidates_validation():
         with pytest.raises(binding.HstuError) as e:
             binding.hstu_worklist_build_bwd_targets(off, np.array(nt, np.int32), 2)
         assert e.value.code == binding.HSTU_ERR_INVALID_ARG, nt
+
+
+@pytest.mark.parametrize("name", workloads.WORKLOAD_NAMES)
+def test_pair_worklist_bit_exact_vs_oracle(name):
+    w = workloads.workload(name)
+    got = binding.hstu_worklist_build_pairs(w.offsets, w.heads)
+    ref = oracle_worklist.items_pairs(w.offsets, w.heads)
+    assert got.dtype == np.int32 and got.shape == ref.shape
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_pair_worklist_bit_exact_random(seed):
+    rng = np.random.default_rng(500 + seed)
+    nb = int(rng.integers(0, 40))
+    lengths = rng.integers(0, 1200, size=nb) * (rng.random(nb) > 0.2)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    heads = int(rng.integers(1, 6))
+    got = binding.hstu_worklist_build_pairs(off, heads)
+    ref = oracle_worklist.items_pairs(off, heads)
+    assert np.array_equal(got.reshape(-1, 4), ref.reshape(-1, 4))

@@ -1,8 +1,10 @@
-"""Pins for the oracle's work lists of the backward and of the candidate mask.
+"""Pins for the oracle's work lists of the backward, of the candidate mask
+and of the forward on CTA pairs.
 
 ``oracle/worklist.py`` enumerates the work items of the backward
-(``items_bwd``, ``items_bwd_targets``) and of the candidate mask
-(``items_targets``, ``items_candidates``).  The C-ABI builders are checked
+(``items_bwd``, ``items_bwd_targets``), of the candidate mask
+(``items_targets``, ``items_candidates``) and of CTA pairs
+(``items_pairs``).  The C-ABI builders are checked
 bit for bit against these lists, so the lists themselves are pinned here to
 things other than themselves:
 
@@ -12,8 +14,11 @@ things other than themselves:
   steps 4-5, ``oracle/dense.py`` ``candidate_mask``): each item's blocks
   are exactly the blocks that hold a kept pair, every kept pair is covered
   exactly once, and the order is cost descending with the stated tie-break;
+* brute force over the causal mask for pair items: the two blocks' walk
+  covers each causal pair exactly once;
 * planted mistakes (a tie-break flip, an off-by-one in "holds a history
-  key", an off-by-one in "holds a candidate row") that these pins catch.
+  key", an off-by-one in "holds a candidate row", a pair walk one block
+  short) that these pins catch.
 """
 import importlib.util
 import os
@@ -50,6 +55,8 @@ def _list_of(wl, case):
     kind = case["kind"]
     if kind == "bwd":
         return wl.items_bwd(off, heads).tolist()
+    if kind == "pairs":
+        return wl.items_pairs(off, heads).tolist()
     fn = {"bwd_targets": wl.items_bwd_targets, "targets": wl.items_targets,
           "candidates": wl.items_candidates}[kind]
     it, hs = fn(off, tg, heads)
@@ -58,11 +65,11 @@ def _list_of(wl, case):
 
 def test_hand_cases_cover_every_kind():
     kinds = [c["kind"] for c in _read_cases()]
-    assert {"bwd", "bwd_targets", "targets", "candidates"} <= set(kinds)
-    assert len(kinds) == 11
+    assert {"bwd", "bwd_targets", "targets", "candidates", "pairs"} <= set(kinds)
+    assert len(kinds) == 14
 
 
-@pytest.mark.parametrize("idx", range(11))
+@pytest.mark.parametrize("idx", range(14))
 def test_hand_case(idx):
     case = _read_cases()[idx]
     assert _list_of(worklist, case) == case["expect"], case
@@ -200,6 +207,9 @@ MUTANTS = {
     "history_key_off_by_one": ("any(j < hist for j in", "any(j <= hist for j in"),
     # row hist not counted as a candidate row
     "candidate_row_off_by_one": ("any(hs[r] <= i < it[r, 1]", "any(hs[r] < i < it[r, 1]"),
+    # a pair's walk counted one block short
+    "pair_cost_off_by_one": ("rows.append((-min(2 * qp + 2, nq), b, h, qp, offsets[b], n))",
+                             "rows.append((-min(2 * qp + 1, nq), b, h, qp, offsets[b], n))"),
 }
 
 
@@ -226,3 +236,39 @@ def test_committed_worklist_passes_the_hand_cases():
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(tmp_path, name):
     assert not _hand_cases_pass(_mutant_module(tmp_path, name)), name
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_pair_walks_cover_each_causal_pair_once(seed):
+    # Every kept (causal) pair of a sequence lies in exactly one walked
+    # (query block, key block) of exactly one pair item, every walked key
+    # block holds a kept pair of one of the pair's two blocks, and the cost
+    # is the number of key blocks walked.
+    rng = np.random.default_rng(300 + seed)
+    off, _, heads = _random_case(rng)
+    it = worklist.items_pairs(off, heads)
+    seqs = {off[b]: (b, off[b + 1] - off[b]) for b in range(len(off) - 1) if off[b + 1] > off[b]}
+    cover = {(s0, h): np.zeros((n, n), dtype=np.int32) for s0, (_, n) in seqs.items() for h in range(heads)}
+    costs, keys = [], []
+    for s0, n, h, qp in it.tolist():
+        b, n_ref = seqs[s0]
+        assert n == n_ref
+        tri = np.tril(np.ones((n, n), dtype=bool))
+        nq = (n + BM - 1) // BM
+        walk = list(range(min(2 * qp + 1, nq - 1) + 1))
+        rows = slice(2 * BM * qp, min(n, 2 * BM * qp + 2 * BM))
+        assert rows.start < n
+        for kb in walk:
+            cols = slice(BM * kb, min(n, BM * kb + BM))
+            assert tri[rows, cols].any(), "a walked key block holds no kept pair"
+            cover[(s0, h)][rows, cols] += tri[rows, cols]
+        need = [kb for kb in range(nq) if tri[rows, BM * kb:BM * kb + BM].any()]
+        assert walk == need
+        costs.append(len(walk))
+        keys.append((b, h, qp))
+    for (s0, h), c in cover.items():
+        n = c.shape[0]
+        assert np.array_equal(c, np.tril(np.ones((n, n), dtype=np.int32)))
+    assert len(set(keys)) == len(keys)
+    order = sorted(range(len(keys)), key=lambda r: (-costs[r], keys[r]))
+    assert order == list(range(len(keys)))
