@@ -516,7 +516,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   };
 
-  for (int idx = blockIdx.x; ok && idx < a.n_items; idx += gridDim.x) {
+  // the CTA's items: a host-built schedule's range, else every grid-th item
+  const int idx0 = a.cta_first ? __ldg(&a.cta_first[blockIdx.x]) : (int)blockIdx.x;
+  const int idx_end = a.cta_first ? __ldg(&a.cta_first[blockIdx.x + 1]) : a.n_items;
+  const int idx_step = a.cta_first ? 1 : (int)gridDim.x;
+  for (int idx = idx0; ok && idx < idx_end; idx += idx_step) {
     const Item it = __ldg(&a.items[idx]);
     const BwdBlock b{it.x, it.y, it.z, it.w};
     item_hist = a.item_hist ? __ldg(a.item_hist + idx) : b.n;
