@@ -64,8 +64,8 @@ _SIGNATURES = {
     "hstu_worklist_build_pairs": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int,
                                                  _IP]),
     "hstu_plan_worklist": (ctypes.c_int, [_VP, _I32P, ctypes.c_int, _IP]),
-    "hstu_worklist_schedule": (ctypes.c_int, [_I32P, _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                              _I32P, _I32P, ctypes.POINTER(ctypes.c_longlong)]),
+    "hstu_worklist_schedule": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, _I32P,
+                                              ctypes.POINTER(ctypes.c_longlong)]),
     "hstu_worklist_build": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int, _IP]),
     "hstu_launch_shape": (ctypes.c_int, [_VP, _IP, _IP, _IP]),
     "hstu_last_status": (ctypes.c_int, [_IP, _IP]),
@@ -531,21 +531,18 @@ def hstu_worklist_build_pairs(host_offsets, heads: int) -> np.ndarray:
     return buf[:n.value]
 
 
-def hstu_worklist_schedule(items, cost, d: int, grid: int):
-    """Host-only static schedule of a longest-first work list (no CUDA
-    call): (order int32 (n,), first int32 (grid + 1,), makespan)."""
-    it = np.ascontiguousarray(items, dtype=np.int32).reshape(-1, 4)
+def hstu_worklist_schedule(cost, grid: int):
+    """Host-only list schedule of a longest-first work list (no CUDA call):
+    (order int32 (n,), first int32 (grid + 1,), makespan)."""
     c = np.ascontiguousarray(cost, dtype=np.int32).reshape(-1)
-    if len(c) != len(it):
-        raise ValueError("one cost per item")
-    order = np.zeros(max(len(it), 1), dtype=np.int32)
+    order = np.zeros(max(len(c), 1), dtype=np.int32)
     first = np.zeros(max(int(grid), 0) + 1, dtype=np.int32)
     span = ctypes.c_longlong()
-    _check(lib().hstu_worklist_schedule(it.ctypes.data_as(_I32P), c.ctypes.data_as(_I32P), len(it),
-                                        int(d), int(grid), order.ctypes.data_as(_I32P),
-                                        first.ctypes.data_as(_I32P), ctypes.byref(span)),
+    _check(lib().hstu_worklist_schedule(c.ctypes.data_as(_I32P), len(c), int(grid),
+                                        order.ctypes.data_as(_I32P), first.ctypes.data_as(_I32P),
+                                        ctypes.byref(span)),
            "hstu_worklist_schedule")
-    return order[:len(it)], first, span.value
+    return order[:len(c)], first, span.value
 
 
 def hstu_plan_worklist(plan: Plan) -> np.ndarray:

@@ -167,9 +167,9 @@ int device_check(int* sm_count) {
 // CTAs of a launch: one per SM at most, and no more than there are items.
 int grid_for(int n_items, int sms) { return std::min(n_items, sms); }
 
-// A work list in its device form: the items (and, with candidates, each
-// item's history length) in schedule order, then first[grid + 1]; one
-// allocation, in that order.
+// The backward's work list in its device form: the items (and, with
+// candidates, each item's history length) in schedule order, then
+// first[grid + 1]; one allocation, in that order.
 struct ListLayout {
   std::vector<hstu::Item> items;
   std::vector<int32_t> hist, first;
@@ -179,13 +179,11 @@ struct ListLayout {
   size_t bytes() const { return ibytes() + hbytes() + first.size() * sizeof(int32_t); }
 };
 
-// Lays out a longest-first list (items, hist: empty or one per item) for
-// `sms` SMs.  An item's cost: the forward walks key blocks 0 .. qt (with
-// candidates, those holding history keys up to qt - 1, then qt); the
-// backward walks query blocks kt .. nq - 1 (a block of candidate keys: kt
-// alone).
-int layout_list(const std::vector<hstu::Item>& items, const std::vector<int32_t>& hist,
-                bool backward, int d, int sms, ListLayout* L) {
+// Lays out the backward's longest-first list (items, hist: empty or one
+// per item) for `sms` SMs.  Item (.., kt) walks query blocks kt .. nq - 1,
+// or kt alone for a block of candidate keys.
+int layout_list_bwd(const std::vector<hstu::Item>& items, const std::vector<int32_t>& hist, int sms,
+                    ListLayout* L) {
   const int n = (int)items.size();
   try {
     std::vector<int32_t> cost((size_t)n), order((size_t)n);
@@ -193,16 +191,11 @@ int layout_list(const std::vector<hstu::Item>& items, const std::vector<int32_t>
       const hstu::Item& x = items[(size_t)i];
       const int nq = (x.y + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
       const int h = hist.empty() ? x.y : hist[(size_t)i];
-      if (backward) {
-        cost[(size_t)i] = HSTU_BLOCK_M * x.w >= h ? 1 : nq - x.w;
-      } else {
-        const int kh = (h + HSTU_BLOCK_M - 1) / HSTU_BLOCK_M;
-        cost[(size_t)i] = (x.w < kh ? x.w : kh) + 1;
-      }
+      cost[(size_t)i] = HSTU_BLOCK_M * x.w >= h ? 1 : nq - x.w;
     }
     L->grid = std::max(1, std::min(n, sms));
     L->first.resize((size_t)L->grid + 1);
-    hstu::schedule_items(items.data(), cost.data(), n, d, L->grid, order.data(), L->first.data());
+    hstu::schedule_items(cost.data(), n, L->grid, order.data(), L->first.data());
     L->items.resize((size_t)n);
     L->hist.resize(hist.size());
     for (int r = 0; r < n; ++r) {
@@ -238,12 +231,9 @@ int sm_count_of_current_device(int* sms) {
   return HSTU_OK;
 }
 
-// d_first null: the items are longest first and the grid is one CTA per
-// SM (serpentine); else the list's schedule over sched_grid CTAs.
 int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long long total,
            int heads, int d, const void* q, const void* k, const void* v, float alpha, float inv_n,
-           void* out, const hstu::NormGate* ng, cudaStream_t stream, const hstu_rab* rab = nullptr,
-           const int32_t* d_first = nullptr, int sched_grid = 0) {
+           void* out, const hstu::NormGate* ng, cudaStream_t stream, const hstu_rab* rab = nullptr) {
   if (n_items == 0) return HSTU_OK;
   int sms = 0;
   int rc = device_check(&sms);
@@ -279,8 +269,7 @@ int launch(const hstu::Item* d_items, const int32_t* d_hist, int n_items, long l
     std::lock_guard<std::mutex> lk(g_mu);
     a.debug_flags = g_debug_flags;
   }
-  a.cta_first = d_first;
-  const int grid = d_first ? sched_grid : grid_for(n_items, sms);
+  const int grid = grid_for(n_items, sms);
   const cudaError_t e = hstu::launch_fwd(d, tq, tk, tv, a, grid, stream);
   if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
     return HSTU_ERR_UNSUPPORTED;
@@ -505,113 +494,32 @@ void fill_items_bwd(const int32_t* off, int batch, int heads, Item* dst, const i
   }
 }
 
-// Static schedule of a longest-first work list over `grid` CTAs.  An item
-// takes cost + 1 units (its key or query blocks, plus its Q load and
-// epilogue); each goes, in list order, to the CTA that is free first (ties:
+// Static schedule of a longest-first work list over `grid` CTAs (list
+// scheduling): an item takes cost + 1 units (its blocks, plus its loads and
+// epilogue) and goes, in list order, to the CTA that is free first (ties:
 // the lower CTA), so no CTA ends more than one item's units after the mean.
-// Where the streamed operands of all (sequence, head) groups (two tensors
-// of length x d bf16 each) exceed kSchedOneBatchBytes, the groups are taken
-// in batches instead, largest group cost first, each batch's operands within
-// a cap, and each batch is one longest-first list: the CTAs then work on a
-// few groups at a time, whose operands stay in L2 while every block that
-// reads them runs.  The cap giving the shortest schedule wins (ties: the
-// smaller cap).  Output: order[] (item indices, CTA 0's first) and
-// first[grid + 1] (CTA c runs order[first[c] .. first[c + 1] - 1]).
-constexpr long long kSchedOneBatchBytes = 48ll << 20;
-
-long long schedule_items(const Item* items, const int32_t* cost, int n, int d, int grid,
-                         int32_t* order, int32_t* first) {
-  std::vector<int> idx;
+// Output: order[] (item indices, CTA 0's first) and first[grid + 1] (CTA c
+// runs order[first[c] .. first[c + 1] - 1], in list order).
+long long schedule_items(const int32_t* cost, int n, int grid, int32_t* order, int32_t* first) {
   std::vector<std::pair<long long, int>> heap;  // (free at, CTA): a min-heap
-  std::vector<int> owner;
-  auto assign = [&](const std::vector<int>& ord, long long* makespan) {
-    heap.clear();
-    for (int c = 0; c < grid; ++c) heap.emplace_back(0ll, c);
-    owner.assign((size_t)n, 0);
-    long long span = 0;
-    for (int i : ord) {
-      std::pop_heap(heap.begin(), heap.end(), std::greater<>());
-      auto& top = heap.back();
-      owner[(size_t)i] = top.second;
-      top.first += (long long)cost[i] + 1;
-      span = std::max(span, top.first);
-      std::push_heap(heap.begin(), heap.end(), std::greater<>());
-    }
-    *makespan = span;
-  };
-  // groups: (first token, head) in list order of their first item
-  std::vector<std::pair<std::pair<int, int>, int>> key((size_t)n);
-  for (int i = 0; i < n; ++i) key[(size_t)i] = {{items[i].x, items[i].z}, i};
-  std::sort(key.begin(), key.end());
-  std::vector<int> group((size_t)n);
-  struct Group {
-    long long cost = 0, bytes = 0;
-    int first_item = 0;
-  };
-  std::vector<Group> groups;
-  for (size_t r = 0; r < key.size(); ++r) {
-    const int i = key[r].second;
-    if (r == 0 || key[r].first != key[r - 1].first) {
-      Group g;
-      g.bytes = (long long)items[i].y * d * 4;
-      g.first_item = i;
-      groups.push_back(g);
-    }
-    group[(size_t)i] = (int)groups.size() - 1;
-    groups.back().cost += (long long)cost[i] + 1;
+  heap.reserve((size_t)grid);
+  for (int c = 0; c < grid; ++c) heap.emplace_back(0ll, c);
+  std::vector<int> owner((size_t)n);
+  long long span = 0;
+  for (int i = 0; i < n; ++i) {
+    std::pop_heap(heap.begin(), heap.end(), std::greater<>());
+    auto& top = heap.back();
+    owner[(size_t)i] = top.second;
+    top.first += (long long)cost[i] + 1;
+    span = std::max(span, top.first);
+    std::push_heap(heap.begin(), heap.end(), std::greater<>());
   }
-  long long all_bytes = 0;
-  for (const Group& g : groups) all_bytes += g.bytes;
-  std::vector<int> best;
-  long long best_span = -1;
-  std::vector<int> ord;
-  ord.reserve((size_t)n);
-  if (all_bytes <= kSchedOneBatchBytes) {
-    for (int i = 0; i < n; ++i) ord.push_back(i);
-    assign(ord, &best_span);
-    best = ord;
-  } else {
-    std::vector<int> gorder(groups.size());
-    for (size_t g = 0; g < groups.size(); ++g) gorder[g] = (int)g;
-    std::stable_sort(gorder.begin(), gorder.end(), [&](int a, int b) {
-      return groups[(size_t)a].cost != groups[(size_t)b].cost
-                 ? groups[(size_t)a].cost > groups[(size_t)b].cost
-                 : groups[(size_t)a].first_item < groups[(size_t)b].first_item;
-    });
-    std::vector<int> batch_of(groups.size());
-    for (long long cap : {16ll << 20, 24ll << 20, 32ll << 20, 48ll << 20}) {
-      int nb = 0;
-      long long acc = 0;
-      for (int g : gorder) {
-        batch_of[(size_t)g] = nb;
-        acc += groups[(size_t)g].bytes;
-        if (acc >= cap) {
-          ++nb;
-          acc = 0;
-        }
-      }
-      // the list order within a batch: the items are longest first already
-      ord.clear();
-      for (int i = 0; i < n; ++i) ord.push_back(i);
-      std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) {
-        return batch_of[(size_t)group[(size_t)a]] < batch_of[(size_t)group[(size_t)b]];
-      });
-      long long span = 0;
-      assign(ord, &span);
-      if (best_span < 0 || span < best_span) {
-        best_span = span;
-        best = ord;
-      }
-    }
-    assign(best, &best_span);
-  }
-  // lay the CTAs' lists out one after the other, each in assignment order
   std::fill(first, first + grid + 1, 0);
   for (int i = 0; i < n; ++i) ++first[owner[(size_t)i] + 1];
   for (int c = 0; c < grid; ++c) first[c + 1] += first[c];
   std::vector<int32_t> fill(first, first + grid);
-  for (int i : best) order[fill[(size_t)owner[(size_t)i]]++] = i;
-  return best_span;
+  for (int i = 0; i < n; ++i) order[fill[(size_t)owner[(size_t)i]]++] = i;
+  return span;
 }
 
 int host_check_offsets(const int32_t* off, int batch, long long max_len) {
@@ -633,16 +541,13 @@ struct hstu_plan {
   std::vector<hstu::Item> items;
   std::vector<int32_t> hist;        // history length per item; empty: no candidates
   unsigned flags = 0;               // HSTU_PLAN_* bits
-  // device copy of items and hist in schedule order, then the schedule's
-  // first[grid + 1] (one allocation)
-  hstu::Item* d_items = nullptr;
+  hstu::Item* d_items = nullptr;    // device copy of items, then hist (one allocation)
   int32_t* d_hist = nullptr;
-  int32_t* d_first = nullptr;
-  int grid = 0;
   // output-stage scratch (HSTU_PLAN_NORM_GATE): xs, then stats
   char* d_norm = nullptr;
-  // backward (HSTU_PLAN_BACKWARD): its work list, (with candidates) each
-  // item's history length, then the fp32 dQ accumulator; one allocation
+  // backward (HSTU_PLAN_BACKWARD): its work list and (with candidates) each
+  // item's history length in schedule order, the schedule's first[grid + 1],
+  // then the fp32 dQ accumulator; one allocation
   int n_bwd = 0;
   char* d_bwd = nullptr;
   int32_t* d_bwd_hist = nullptr;
@@ -711,20 +616,16 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
     return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
   };
   if (cudaGetDevice(&p->device) != cudaSuccess) return fail(HSTU_ERR_CUDA);
-  int sms = 0;
-  if ((rc = sm_count_of_current_device(&sms)) != HSTU_OK) return fail(rc);
-  {
-    ListLayout L;
-    if ((rc = layout_list(p->items, p->hist, false, d, sms, &L)) != HSTU_OK) return fail(rc);
-    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p->d_items), L.bytes());
-    if (e != cudaSuccess) return fail(mem_code(e));
-    char* base = reinterpret_cast<char*>(p->d_items);
-    if (L.hbytes()) p->d_hist = reinterpret_cast<int32_t*>(base + L.ibytes());
-    p->d_first = reinterpret_cast<int32_t*>(base + L.ibytes() + L.hbytes());
-    p->grid = L.grid;
-    if (copy_list(L, base, nullptr, true) != cudaSuccess) return fail(HSTU_ERR_CUDA);
-  }
-  cudaError_t e = cudaSuccess;
+  // one allocation: the items, then (with candidates) the history lengths
+  const size_t ibytes = p->items.size() * sizeof(hstu::Item);
+  const size_t hbytes = p->hist.size() * sizeof(int32_t);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p->d_items), ibytes + hbytes);
+  if (e != cudaSuccess) return fail(mem_code(e));
+  if (hbytes) p->d_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(p->d_items) + ibytes);
+  if (cudaMemcpy(p->d_items, p->items.data(), ibytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+      (hbytes &&
+       cudaMemcpy(p->d_hist, p->hist.data(), hbytes, cudaMemcpyHostToDevice) != cudaSuccess))
+    return fail(HSTU_ERR_CUDA);
   if (!nt && (d == 64 || d == 128) && ((flags & HSTU_PLAN_PAIRS) || use_pairs(off, batch, d))) {
     std::vector<hstu::Item> pairs;
     try {
@@ -761,8 +662,10 @@ int make_plan(const int32_t* off, const int32_t* nt, int batch, int heads, int d
     }
     hstu::fill_items_bwd(off, batch, heads, bw.data(), nt, nt ? bh.data() : nullptr);
     p->n_bwd = (int)bw.size();
+    int sms = 0;
+    if ((rc = sm_count_of_current_device(&sms)) != HSTU_OK) return fail(rc);
     ListLayout L;
-    if ((rc = layout_list(bw, bh, true, d, sms, &L)) != HSTU_OK) return fail(rc);
+    if ((rc = layout_list_bwd(bw, bh, sms, &L)) != HSTU_OK) return fail(rc);
     const size_t lbytes = (L.bytes() + 15) / 16 * 16;  // keeps the accumulator 16-aligned
     if ((e = cudaMalloc(reinterpret_cast<void**>(&p->d_bwd),
                         lbytes + (size_t)p->total * heads * d * sizeof(float))) != cudaSuccess)
@@ -838,22 +741,21 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
   std::vector<int32_t> hist;
   if ((rc = build_worklist(off, num_targets, batch, heads, items, hist)) != HSTU_OK) return rc;
   if (items.empty()) return HSTU_OK;
-  int sms = 0;
-  if ((rc = sm_count_of_current_device(&sms)) != HSTU_OK) return rc;
-  ListLayout L;
-  if ((rc = layout_list(items, hist, false, d, sms, &L)) != HSTU_OK) return rc;
-  // one stream-ordered allocation: the output-stage scratch (if any), then
-  // the list's layout
+  // one stream-ordered allocation: the output-stage scratch (if any), the
+  // items, then (with candidates) the history lengths
   const size_t nbytes = ng ? hstu::norm_scratch_bytes(total, heads, d) : 0;
+  const size_t ibytes = items.size() * sizeof(hstu::Item);
+  const size_t hbytes = hist.size() * sizeof(int32_t);
   char* block = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&block), nbytes + L.bytes(), s);
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&block), nbytes + ibytes + hbytes, s);
   if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
   hstu::Item* d_items = reinterpret_cast<hstu::Item*>(block + nbytes);
-  int32_t* d_hist = L.hbytes() ? reinterpret_cast<int32_t*>(block + nbytes + L.ibytes()) : nullptr;
-  const int32_t* d_first = reinterpret_cast<int32_t*>(block + nbytes + L.ibytes() + L.hbytes());
+  int32_t* d_hist = hbytes ? reinterpret_cast<int32_t*>(block + nbytes + ibytes) : nullptr;
   // Pageable sources: each copy returns once the bytes are staged, so the
   // host vectors may go out of scope afterwards.
-  e = copy_list(L, block + nbytes, s);
+  e = cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && hbytes)
+    e = cudaMemcpyAsync(d_hist, hist.data(), hbytes, cudaMemcpyHostToDevice, s);
   hstu::NormGate ngw{};
   if (ng && e == cudaSuccess) {
     ngw = norm_views(block, total, heads, d);
@@ -867,7 +769,7 @@ int oneshot(const void* q, const void* k, const void* v, const int32_t* offsets,
     return HSTU_ERR_CUDA;
   }
   rc = launch(d_items, d_hist, (int)items.size(), total, heads, d, q, k, v, alpha, inv_n, out,
-              ng ? &ngw : nullptr, s, rab, d_first, L.grid);
+              ng ? &ngw : nullptr, s, rab);
   if (cudaFreeAsync(block, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
   return rc;
 }
@@ -1038,17 +940,15 @@ int hstu_worklist_build_pairs(const int32_t* host_offsets, int batch, int heads,
   return HSTU_OK;
 }
 
-int hstu_worklist_schedule(const int32_t* host_items, const int32_t* host_cost, int n_items, int d,
-                           int grid, int32_t* host_order, int32_t* host_first, long long* makespan) {
-  if (!host_items || !host_cost || !host_order || !host_first || n_items < 1 || d < 1 || grid < 1 ||
-      grid > n_items)
+int hstu_worklist_schedule(const int32_t* host_cost, int n_items, int grid, int32_t* host_order,
+                           int32_t* host_first, long long* makespan) {
+  if (!host_cost || !host_order || !host_first || n_items < 1 || grid < 1 || grid > n_items)
     return HSTU_ERR_INVALID_ARG;
   for (int i = 0; i < n_items; ++i)
     if (host_cost[i] < 1) return HSTU_ERR_INVALID_ARG;
   long long span = 0;
   try {
-    span = hstu::schedule_items(reinterpret_cast<const hstu::Item*>(host_items), host_cost, n_items, d,
-                                grid, host_order, host_first);
+    span = hstu::schedule_items(host_cost, n_items, grid, host_order, host_first);
   } catch (const std::bad_alloc&) {
     return HSTU_ERR_NO_MEMORY;
   }
@@ -1125,7 +1025,7 @@ int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_by
     *smem_bytes = hstu::fwd_pair_smem_bytes(plan->d);
     return HSTU_OK;
   }
-  *grid = plan->grid;
+  *grid = grid_for((int)plan->items.size(), sms);
   *block = hstu::kFwdThreads;
   *smem_bytes = hstu::fwd_smem_bytes(plan->d);
   return HSTU_OK;
@@ -1141,8 +1041,7 @@ int hstu_attn_fwd_plan(const hstu_plan* plan, const void* q, const void* k, cons
     return launch_pairs(plan->d_pairs, plan->n_pairs, plan->total, plan->heads, plan->d, q, k, v, alpha,
                         inv_n, out, reinterpret_cast<cudaStream_t>(stream));
   return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
-                plan->d, q, k, v, alpha, inv_n, out, nullptr, reinterpret_cast<cudaStream_t>(stream),
-                nullptr, plan->d_first, plan->grid);
+                plan->d, q, k, v, alpha, inv_n, out, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_attn_fwd_norm_gate_plan(const hstu_plan* plan, const void* q, const void* k, const void* v,
@@ -1160,7 +1059,7 @@ int hstu_attn_fwd_norm_gate_plan(const hstu_plan* plan, const void* q, const voi
   ng.beta = beta;
   ng.eps = eps;
   return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
-                plan->d, q, k, v, alpha, inv_n, y, &ng, s, nullptr, plan->d_first, plan->grid);
+                plan->d, q, k, v, alpha, inv_n, y, &ng, s);
 }
 
 int hstu_attn_fwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, const void* v,
@@ -1185,7 +1084,7 @@ int hstu_attn_fwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, c
                         inv_n, out, reinterpret_cast<cudaStream_t>(stream));
   return launch(plan->d_items, plan->d_hist, (int)plan->items.size(), plan->total, plan->heads,
                 plan->d, q, k, v, alpha, inv_n, out, ng ? &ngw : nullptr,
-                reinterpret_cast<cudaStream_t>(stream), rab, plan->d_first, plan->grid);
+                reinterpret_cast<cudaStream_t>(stream), rab);
 }
 
 int hstu_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* offsets,
@@ -1334,7 +1233,7 @@ int hstu_attn_bwd_ex(const void* q, const void* k, const void* v, const void* do
   int sms = 0;
   if ((rc = sm_count_of_current_device(&sms)) != HSTU_OK) return rc;
   ListLayout L;
-  if ((rc = layout_list(items, hist, true, d, sms, &L)) != HSTU_OK) return rc;
+  if ((rc = layout_list_bwd(items, hist, sms, &L)) != HSTU_OK) return rc;
   // one stream-ordered allocation: the fp32 dQ accumulator, then the list's
   // layout
   const size_t abytes = (size_t)total * heads * d * sizeof(float);

@@ -497,14 +497,8 @@ constexpr bool has_rab = (VAR & kVarRab) != 0;
 template <int VAR>
 __device__ __forceinline__ bool load_block(const FwdArgs& a, int it, BlockOf<has_targets<VAR>>& b) {
   constexpr bool TGT = has_targets<VAR>;
-  int idx;
-  if (a.cta_first) {
-    idx = __ldg(&a.cta_first[blockIdx.x]) + it;
-    if (idx >= __ldg(&a.cta_first[blockIdx.x + 1])) return false;
-  } else {
-    idx = item_index(it, blockIdx.x, gridDim.x);
-    if (idx >= a.n_items) return false;
-  }
+  const int idx = item_index(it, blockIdx.x, gridDim.x);
+  if (idx >= a.n_items) return false;
   const Item x = __ldg(&a.items[idx]);
   b.s0 = x.x;
   b.n = x.y;

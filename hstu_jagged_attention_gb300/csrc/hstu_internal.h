@@ -19,8 +19,7 @@ long long count_items(const int32_t* off, int batch, int heads);
 // Static schedule of a longest-first work list over `grid` CTAs, an item
 // costing cost[i] + 1 units: order[] (item indices, CTA 0's first) and
 // first[grid + 1].  Returns the longest CTA's units.
-long long schedule_items(const Item* items, const int32_t* cost, int n, int d, int grid,
-                         int32_t* order, int32_t* first);
+long long schedule_items(const int32_t* cost, int n, int grid, int32_t* order, int32_t* first);
 void fill_items(const int32_t* off, int batch, int heads, Item* dst);
 // With candidates (the last num_targets[b] tokens of sequence b see the
 // history and themselves only): the same items, each costing
@@ -50,13 +49,9 @@ inline size_t norm_scratch_bytes(long long total, int heads, int d) {
 }
 
 struct FwdArgs {
-  const Item* items;   // device, n_items entries
+  const Item* items;   // device, n_items entries, longest first
   const int32_t* item_hist;  // device, history length per item; null: no candidates
   int n_items;
-  // device, grid + 1 entries: CTA c runs items cta_first[c] .. cta_first[c + 1] - 1
-  // in order (a schedule built on the host); null: the items are longest
-  // first and CTAs take them serpentine
-  const int32_t* cta_first;
   void* out;           // bf16 (total, heads, d): the attention output, or y with the output stage
   // Output stage y = Norm(out) (.) u (null u: none).  u bf16 (total, heads, d);
   // gamma, beta fp32 (heads * d); xs fp32 (total, heads * d) and stats
@@ -89,7 +84,9 @@ struct FwdArgs {
 struct BwdArgs {
   const Item* items;
   int n_items;
-  const int32_t* cta_first;  // as FwdArgs::cta_first; null: CTA c takes items c, c + grid, ...
+  // device, grid + 1 entries: CTA c runs items cta_first[c] .. cta_first[c + 1] - 1
+  // in order (a schedule built on the host); null: CTA c takes items c, c + grid, ...
+  const int32_t* cta_first;
   int heads;
   float alpha, inv_n;
   float* dq_acc;

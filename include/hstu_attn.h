@@ -207,35 +207,28 @@ int hstu_worklist_build(const int32_t* host_offsets, int batch, int heads, int32
                         int capacity, int* n_items);
 
 /*
- * hstu_worklist_schedule -- the static per-CTA schedule that plans and
- * one-shot calls give a work list, on the host only (no CUDA call).
+ * hstu_worklist_schedule -- the static per-CTA schedule that the backward
+ * (hstu_attn_bwd*, and plans made with HSTU_PLAN_BACKWARD) gives its work
+ * list, on the host only (no CUDA call).  The forward keeps the
+ * longest-first list, which its CTAs take serpentine.
  *
- *   host_items  int32[4 * n_items]: a work list as the builders give it,
- *               longest first: (first token, length, head, block).
- *   host_cost   int32[n_items]: each item's blocks (>= 1): key blocks in
- *               the forward, query blocks in the backward.
- *   d           head dimension: a (sequence, head) group streams two
- *               operands of length x d bf16.
+ *   host_cost   int32[n_items]: each item's blocks (>= 1), in the order of
+ *               a longest-first list (the backward's: query blocks walked).
  *   grid        CTAs, 1 .. n_items (launches use min(items, SMs)).
  *   host_order  int32[n_items], out: item indices, CTA 0's items first,
- *               each CTA's in the order it runs them.
+ *               each CTA's in list order.
  *   host_first  int32[grid + 1], out: CTA c runs host_order[host_first[c]]
  *               .. host_order[host_first[c + 1] - 1].
  *   makespan    out (NULL: not wanted): the longest CTA's units.
- * An item takes cost + 1 units (its blocks, plus its Q load and epilogue).
- * Items go, in list order, to the CTA that is free first (ties: the lower
- * CTA), so no CTA runs more than one item's units past the mean.  Where
- * the operands of all groups exceed 48 MiB, the groups are taken in batches
- * instead (largest total cost first, 16, 24, 32 or 48 MiB of operands a
- * batch: whichever cap gives the shortest schedule, ties to the smaller),
- * with the list order kept within each batch.  The CTAs then work on a few
- * groups at a time, whose K and V stay in L2 while every block that reads
- * them runs.
+ * List scheduling: an item takes cost + 1 units (its blocks, plus its
+ * loads and stores) and goes, in list order, to the CTA that is free first
+ * (ties: the lower CTA), so no CTA runs more than one item's units past the
+ * mean.
  * Errors: HSTU_ERR_INVALID_ARG for a NULL array, n_items < 1, grid outside
- * 1 .. n_items, d < 1 or a cost < 1.
+ * 1 .. n_items or a cost < 1.
  */
-int hstu_worklist_schedule(const int32_t* host_items, const int32_t* host_cost, int n_items, int d,
-                           int grid, int32_t* host_order, int32_t* host_first, long long* makespan);
+int hstu_worklist_schedule(const int32_t* host_cost, int n_items, int grid, int32_t* host_order,
+                           int32_t* host_first, long long* makespan);
 
 /*
  * hstu_worklist_build_pairs -- the work list of CTA pairs, on the host only.
