@@ -28,6 +28,7 @@ BLOCK_M = 128
 HSTU_DEBUG_UNSIGNALLED_WAIT = 1
 HSTU_DEBUG_TRACE = 2
 HSTU_DEBUG_NO_PAIRS = 4
+HSTU_DEBUG_BWD_ROWS = 8
 TRACE_EVENTS = {1: "qk_issue", 2: "pv_issue", 3: "silu_start", 4: "silu_end", 5: "epi_start",
                 6: "epi_end", 7: "load_k", 8: "load_v", 9: "load_q", 10: "mma_k_ready",
                 11: "mma_qk_done", 12: "mma_p_ready", 13: "mma_pv_done"}

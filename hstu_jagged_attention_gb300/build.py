@@ -34,7 +34,7 @@ def nvcc() -> str:
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += [os.path.join(CSRC, "hstu_internal.h"), os.path.join(CSRC, "hstu_bwd.cuh"),
-              os.path.join(CSRC, "hstu_fwd_pair.cuh"),
+              os.path.join(CSRC, "hstu_fwd_pair.cuh"), os.path.join(CSRC, "hstu_bwd_t.cuh"),
               os.path.join(INCLUDE, "hstu_attn.h"),
               os.path.abspath(__file__)]
     return files

@@ -819,6 +819,10 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   a.total = total;
   a.timeout_ns = wait_timeout_ns();
   a.item_hist = d_hist;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
+  }
   if (rab) {
     a.rab_ts = rab->timestamps;
     a.rab_pos = rab->pos;
@@ -1299,7 +1303,8 @@ int hstu_set_wait_timeout_ns(uint64_t ns) {
 }
 
 int hstu_set_debug_flags(uint32_t flags) {
-  if (flags & ~(uint32_t)(HSTU_DEBUG_UNSIGNALLED_WAIT | HSTU_DEBUG_TRACE | HSTU_DEBUG_NO_PAIRS))
+  if (flags & ~(uint32_t)(HSTU_DEBUG_UNSIGNALLED_WAIT | HSTU_DEBUG_TRACE | HSTU_DEBUG_NO_PAIRS |
+                          HSTU_DEBUG_BWD_ROWS))
     return HSTU_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_debug_flags = flags;

@@ -812,12 +812,27 @@ cudaError_t launch_bwd_dr(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   return cudaGetLastError();
 }
 
+// The transposed form (hstu_bwd_t.cuh), for d <= 64 without the bias.
+template <int D>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
+                         cudaStream_t stream);
+
 template <int D>
 cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,
                          cudaStream_t stream) {
-  cudaError_t e = a.rab_ts ? launch_bwd_dr<D, true>(tq, tk, tv, tdo, tdq, a, grid, stream)
-                           : launch_bwd_dr<D, false>(tq, tk, tv, tdo, tdq, a, grid, stream);
+  cudaError_t e;
+  if constexpr (D <= 64) {
+    if (!a.rab_ts && !(a.debug_flags & kDebugBwdRows))
+      e = launch_bwd_t<D>(tq, tk, tv, tdo, tdq, a, grid, stream);
+    else
+      e = a.rab_ts ? launch_bwd_dr<D, true>(tq, tk, tv, tdo, tdq, a, grid, stream)
+                   : launch_bwd_dr<D, false>(tq, tk, tv, tdo, tdq, a, grid, stream);
+  } else {
+    e = a.rab_ts ? launch_bwd_dr<D, true>(tq, tk, tv, tdo, tdq, a, grid, stream)
+                 : launch_bwd_dr<D, false>(tq, tk, tv, tdo, tdq, a, grid, stream);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long n8 = a.total * a.heads * D / 8;
   const int cgrid = (int)std::min<long long>((n8 + 255) / 256, 4LL * 1024);

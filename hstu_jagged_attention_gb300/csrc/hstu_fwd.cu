@@ -1406,6 +1406,7 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 }
 
 #include "hstu_bwd.cuh"
+#include "hstu_bwd_t.cuh"
 #include "hstu_fwd_pair.cuh"
 
 }  // namespace

@@ -106,6 +106,7 @@ struct BwdArgs {
   float* dtime = nullptr;
   // candidates (null: none): each item's history length, parallel to items
   const int32_t* item_hist = nullptr;
+  unsigned debug_flags = 0;  // kDebug* bits; 0 in normal use
 };
 // Work list of the backward: one item per (sequence, head, key block kt),
 // costing nq - kt query blocks; ordered by cost descending, then sequence,
@@ -128,6 +129,9 @@ constexpr unsigned kDebugUnsignalledWait = 1u;
 constexpr unsigned kDebugTrace = 2u;
 // The plain forward on one CTA per work item even where CTA pairs apply.
 constexpr unsigned kDebugNoPairs = 4u;
+// The backward in its row form (hstu_bwd.cuh) where the transposed form
+// (hstu_bwd_t.cuh) would run: d <= 64 without the bias.
+constexpr unsigned kDebugBwdRows = 8u;
 
 // Trace records: {clock64, (event << 48) | (warp << 40) | index}.
 cudaError_t read_and_clear_trace(unsigned long long* dst, int capacity, int* n);

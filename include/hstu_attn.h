@@ -539,11 +539,17 @@ int hstu_set_wait_timeout_ns(uint64_t ns);
  *   HSTU_DEBUG_TRACE  record the pipeline trace (see hstu_trace_read).
  *   HSTU_DEBUG_NO_PAIRS  run the plain forward on one CTA per work item even
  *       where a plan or call would use CTA pairs (for comparing the two).
+ *   HSTU_DEBUG_BWD_ROWS  run the backward in its row form (query rows on
+ *       the TMEM lanes) where it would run in its transposed form (key rows
+ *       on the lanes: d <= 64 without the bias), for comparing the two.
+ * The unsignalled wait applies to the forward and to the backward's
+ * transposed form.
  * Errors: HSTU_ERR_INVALID_ARG for unknown bits.
  */
 #define HSTU_DEBUG_UNSIGNALLED_WAIT 1u
 #define HSTU_DEBUG_TRACE 2u
 #define HSTU_DEBUG_NO_PAIRS 4u
+#define HSTU_DEBUG_BWD_ROWS 8u
 int hstu_set_debug_flags(uint32_t flags);
 
 /*
