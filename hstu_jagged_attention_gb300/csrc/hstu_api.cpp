@@ -800,13 +800,30 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   int sms = 0;
   int rc = device_check(&sms);
   if (rc != HSTU_OK) return rc;
+  unsigned dbg;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    dbg = g_debug_flags;
+  }
+  // the transposed form (d <= 64 without the bias) loads Q and dO half a
+  // block at a time
+  const bool transposed = d <= 64 && !rab && !(dbg & HSTU_DEBUG_BWD_ROWS);
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if ((rc = make_map(&tq, q, total, heads, d)) != HSTU_OK) return rc;
+  if (transposed) {
+    if ((rc = make_map_pair(&tq, q, total, heads, d, std::min(d, 64), HSTU_BLOCK_M / 2)) != HSTU_OK)
+      return rc;
+    if ((rc = make_map_pair(&tdo, dout, total, heads, d, std::min(d, 64), HSTU_BLOCK_M / 2)) != HSTU_OK)
+      return rc;
+  } else {
+    if ((rc = make_map(&tq, q, total, heads, d)) != HSTU_OK) return rc;
+    if ((rc = make_map(&tdo, dout, total, heads, d)) != HSTU_OK) return rc;
+  }
   if ((rc = make_map(&tk, k, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map(&tv, v, total, heads, d)) != HSTU_OK) return rc;
-  if ((rc = make_map(&tdo, dout, total, heads, d)) != HSTU_OK) return rc;
   if ((rc = make_map_f32(&tdq, dq_acc, total, heads, d)) != HSTU_OK) return rc;
   hstu::BwdArgs a{};  // every field zero: no bias unless set below
+  a.transposed = transposed;
+  a.debug_flags = dbg;
   a.items = d_items;
   a.n_items = n_items;
   a.heads = heads;
@@ -819,10 +836,6 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   a.total = total;
   a.timeout_ns = wait_timeout_ns();
   a.item_hist = d_hist;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    a.debug_flags = g_debug_flags;
-  }
   if (rab) {
     a.rab_ts = rab->timestamps;
     a.rab_pos = rab->pos;

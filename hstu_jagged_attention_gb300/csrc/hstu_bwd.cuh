@@ -824,12 +824,13 @@ cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          cudaStream_t stream) {
   cudaError_t e;
   if constexpr (D <= 64) {
-    if (!a.rab_ts && !(a.debug_flags & kDebugBwdRows))
+    if (a.transposed)
       e = launch_bwd_t<D>(tq, tk, tv, tdo, tdq, a, grid, stream);
     else
       e = a.rab_ts ? launch_bwd_dr<D, true>(tq, tk, tv, tdo, tdq, a, grid, stream)
                    : launch_bwd_dr<D, false>(tq, tk, tv, tdo, tdq, a, grid, stream);
   } else {
+    if (a.transposed) return cudaErrorInvalidValue;
     e = a.rab_ts ? launch_bwd_dr<D, true>(tq, tk, tv, tdo, tdq, a, grid, stream)
                  : launch_bwd_dr<D, false>(tq, tk, tv, tdo, tdq, a, grid, stream);
   }

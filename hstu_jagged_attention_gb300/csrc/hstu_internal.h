@@ -107,6 +107,9 @@ struct BwdArgs {
   // candidates (null: none): each item's history length, parallel to items
   const int32_t* item_hist = nullptr;
   unsigned debug_flags = 0;  // kDebug* bits; 0 in normal use
+  // the transposed form (hstu_bwd_t.cuh): d <= 64 without the bias; its Q
+  // and dO tensor maps then have 64-row boxes (half a block)
+  bool transposed = false;
 };
 // Work list of the backward: one item per (sequence, head, key block kt),
 // costing nq - kt query blocks; ordered by cost descending, then sequence,
