@@ -151,6 +151,14 @@ __device__ __forceinline__ void bwd_t_st16(uint32_t taddr, const uint32_t (&r)[1
   tmem_st8(taddr + 8u, t8);
 }
 
+// Bounded wait for the issuing thread: a non-blocking test first (a
+// try_wait on a phase that is already complete still holds the thread for
+// a few hundred cycles, and with it the stream of products it feeds).
+__device__ __forceinline__ bool wait_issuer(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+  if (mbar_test(bar, parity)) return true;
+  return wait_one(bar, parity, w, site);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdTThreads, 1)
     hstu_bwd_t_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -305,7 +313,7 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
       bool ok = true, pending = false;
       int pend_h = 0, pend_row = 0;
       // test hook: a wait on a barrier that nothing signals runs out
-      if (a.debug_flags & kDebugUnsignalledWait) ok = wait_one(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
+      if (a.debug_flags & kDebugUnsignalledWait) ok = wait_issuer(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
       auto load_half = [&](int qb, int h, const BwdBlock& b, int qt) {
         const int i = 2 * qb + h;
         const int row0 = b.s0 + kBM * qt + 64 * h;
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
       };
       auto wait_half = [&](int qb, int h) -> bool {
         const int i = 2 * qb + h;
-        const bool r = wait_one(bar(C::B_QD + i), w_qd[i] & 1u, w, kSiteQFull);
+        const bool r = wait_issuer(bar(C::B_QD + i), w_qd[i] & 1u, w, kSiteQFull);
         ++w_qd[i];
         return r;
       };
@@ -332,7 +340,7 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
         mma_commit(bar(C::B_SDP + h));
       };
       auto wait_pass = [&](int h) -> bool {
-        const bool r = wait_one(bar(C::B_PASS + h), ph_pass[h], w, kSitePFull);
+        const bool r = wait_issuer(bar(C::B_PASS + h), ph_pass[h], w, kSitePFull);
         ph_pass[h] ^= 1u;
         return r;
       };
@@ -343,10 +351,10 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
         const int nq = nq_of(b, hist);
         // the previous item's products have finished reading K, V, Q, dO
         if (n_prod) {
-          if (!(ok = wait_one(bar(C::B_PROD), (n_prod - 1) & 1u, w, kSiteVFull))) break;
-          if (!(ok = wait_one(bar(C::B_PROD + 1), (n_prod - 1) & 1u, w, kSiteVFull))) break;
+          if (!(ok = wait_issuer(bar(C::B_PROD), (n_prod - 1) & 1u, w, kSiteVFull))) break;
+          if (!(ok = wait_issuer(bar(C::B_PROD + 1), (n_prod - 1) & 1u, w, kSiteVFull))) break;
         }
-        if (n_dq && !(ok = wait_one(bar(C::B_DQ), (n_dq - 1) & 1u, w, kSiteOFull))) break;
+        if (n_dq && !(ok = wait_issuer(bar(C::B_DQ), (n_dq - 1) & 1u, w, kSiteOFull))) break;
         mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILEB);
 #pragma unroll
         for (int ch = 0; ch < C::NCHUNK; ++ch) {
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
           load_half(qb0 ^ 1, 0, b, b.kt + 1);
           load_half(qb0 ^ 1, 1, b, b.kt + 1);
         }
-        if (!(ok = wait_one(bar(C::B_KV), (n_kv - 1) & 1u, w, kSiteKFull))) break;
+        if (!(ok = wait_issuer(bar(C::B_KV), (n_kv - 1) & 1u, w, kSiteKFull))) break;
         if (!(ok = wait_half(qb0, 0))) break;
         issue_sdp(qb0, 0);
         if (!(ok = wait_half(qb0, 1))) break;
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
             if (qt + 1 < nq) {
               // the next block's half-h S^T and dP^T overwrite what these
               // products read; half h of buffer qb is then free for block qt + 2
-              if (!(ok = wait_one(bar(C::B_PROD + h), n_prod & 1u, w, kSiteVFull))) break;
+              if (!(ok = wait_issuer(bar(C::B_PROD + h), n_prod & 1u, w, kSiteVFull))) break;
               if (qt + 2 < nq) load_half(qb, h, b, qt + 2);
               if (!(ok = wait_half(qb ^ 1, h))) break;
               issue_sdp(qb ^ 1, h);
