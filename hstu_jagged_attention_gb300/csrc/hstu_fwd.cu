@@ -162,8 +162,10 @@ __device__ __noinline__ void signal_timeout(const WaitCtx& w, int site) {
 }
 
 // Bounded wait by one thread; false if the CTA aborted or the limit ran out.
+// A non-blocking test comes first: a try_wait on a phase that is already
+// complete still holds the thread for a few hundred cycles.
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
