@@ -23,7 +23,9 @@
 // halves); alpha dQ_part goes into the fp32 accumulator by bulk tensor
 // reductions from a staging tile, as in hstu_bwd.cuh.
 //
-// Warp 8 (one thread) issues the copies and the products; warps 0-7 do the
+// Warp 8 (one thread) issues the copies and the S^T, dP^T, dV and dK
+// products; warp 9 (one thread) issues dQ and its reductions, so that
+// neither stream waits behind the other's barriers; warps 0-7 do the
 // elementwise work, the dQ staging and the item's dV / dK stores.  The
 // halves pipeline: while the threads work on half 1, half 0's dV and dK
 // products run and then the next block's half-0 S^T and dP^T (which
@@ -69,9 +71,10 @@ struct TCfg {
   // K and V landed; Q and dO landed [buffer][half]; S^T and dP^T done
   // [half]; dV and dK products done [half]; dQ product done; a half's
   // elementwise pass done [half] (256 arrivals); the staging tile read by
-  // its reduction; drain
+  // its reduction; the two issuing threads' drains
   static constexpr int B_KV = 0, B_QD = 1 /* [4] */, B_SDP = 5 /* [2] */, B_PROD = 7 /* [2] */,
-                       B_DQ = 9, B_PASS = 10 /* [2] */, B_STG = 12, B_DRAIN = 13, NBARS = 14;
+                       B_DQ = 9, B_PASS = 10 /* [2] */, B_STG = 12, B_DRAIN = 13 /* [2] */,
+                       NBARS = 15;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
   static constexpr int USED = MISC_OFF + 16;
   static constexpr int SMEM = ((USED + 1023) / 1024) * 1024 + 1024;  // + realignment slack
@@ -87,8 +90,11 @@ struct TCfg {
   }
 };
 
-constexpr int kBwdTThreads = 288;  // 8 elementwise warps + the issuing warp
+// 8 elementwise warps, the warp that issues the copies and the S^T, dP^T,
+// dV and dK products, and the warp that issues dQ and its reductions
+constexpr int kBwdTThreads = 320;
 constexpr int kBwdTIssueWarp = 8;
+constexpr int kBwdTDqWarp = 9;
 
 // One 32-query chunk of a key row: P and dS from the recomputed scores s
 // and dP (fp32 TMEM words), split into bf16 hi + lo words (word m holds
@@ -207,14 +213,17 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
     return kBN * b.kt >= hist ? b.kt + 1 : (b.n + kBM - 1) / kBM;
   };
 
-  if (warp == kBwdTIssueWarp) {
-    // ------------------------------------------------------------ issuer
+  if (warp == kBwdTIssueWarp || warp == kBwdTDqWarp) {
+    // ------------------------------------------------------- issuers
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_do)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_dq)) : "memory");
+      if (warp == kBwdTIssueWarp) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_do)) : "memory");
+      } else {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_dq)) : "memory");
+      }
       constexpr uint32_t IDESC_S = make_idesc(kBM, kBN / 2, 0);     // N = 64 queries
       constexpr uint32_t IDESC_TS = make_idesc(kBM, D, 1);          // A from TMEM, B MN-major
       constexpr uint32_t IDESC_DQ = make_idesc_ab(kBM, D, 1, 1);    // A and B MN-major
@@ -305,136 +314,154 @@ __global__ void __launch_bounds__(kBwdTThreads, 1)
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       };
 
-      // copies issued / waited per Q-dO barrier ([buffer][half]), products
-      // committed per barrier, B_PASS phases waited
-      uint32_t n_kv = 0, n_qd[4] = {0, 0, 0, 0}, w_qd[4] = {0, 0, 0, 0};
-      uint32_t n_prod = 0, n_dq = 0, ph_pass[2] = {0, 0};
-      uint32_t qiter = 0;
-      bool ok = true, pending = false;
-      int pend_h = 0, pend_row = 0;
-      // test hook: a wait on a barrier that nothing signals runs out
-      if (a.debug_flags & kDebugUnsignalledWait) ok = wait_issuer(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
-      auto load_half = [&](int qb, int h, const BwdBlock& b, int qt) {
-        const int i = 2 * qb + h;
-        const int row0 = b.s0 + kBM * qt + 64 * h;
-        mbar_arrive_expect_tx(bar(C::B_QD + i), 2 * C::HALFB);
-#pragma unroll
-        for (int ch = 0; ch < C::NCHUNK; ++ch) {
-          tma_load_3d(base + C::Q_OFF + qb * C::TILEB + ch * C::CHUNKB + h * 64 * C::ROWB, &tm_q,
-                      bar(C::B_QD + i), ch * C::CHUNK, b.h, row0);
-          tma_load_3d(base + C::DO_OFF + qb * C::TILEB + ch * C::CHUNKB + h * 64 * C::ROWB, &tm_do,
-                      bar(C::B_QD + i), ch * C::CHUNK, b.h, row0);
-        }
-        ++n_qd[i];
-      };
-      auto wait_half = [&](int qb, int h) -> bool {
-        const int i = 2 * qb + h;
-        const bool r = wait_issuer(bar(C::B_QD + i), w_qd[i] & 1u, w, kSiteQFull);
-        ++w_qd[i];
-        return r;
-      };
-      auto issue_sdp = [&](int qb, int h) {
-        tc_fence_after();
-        mma_xyt(C::S_COL + 64u * h, k_kmaj, half_desc(q_kmaj0, qb, h));
-        mma_xyt(C::DP_COL + 64u * h, v_kmaj, half_desc(do_kmaj0, qb, h));
-        mma_commit(bar(C::B_SDP + h));
-      };
+      bool ok = true;
+      uint32_t ph_pass[2] = {0, 0};
       auto wait_pass = [&](int h) -> bool {
         const bool r = wait_issuer(bar(C::B_PASS + h), ph_pass[h], w, kSitePFull);
         ph_pass[h] ^= 1u;
         return r;
       };
-      for (int idx = idx0; ok && idx < idx_end; idx += idx_step) {
-        const Item it = __ldg(&a.items[idx]);
-        const BwdBlock b{it.x, it.y, it.z, it.w};
-        const int hist = a.item_hist ? __ldg(a.item_hist + idx) : b.n;
-        const int nq = nq_of(b, hist);
-        // the previous item's products have finished reading K, V, Q, dO
-        if (n_prod) {
-          if (!(ok = wait_issuer(bar(C::B_PROD), (n_prod - 1) & 1u, w, kSiteVFull))) break;
-          if (!(ok = wait_issuer(bar(C::B_PROD + 1), (n_prod - 1) & 1u, w, kSiteVFull))) break;
-        }
-        if (n_dq && !(ok = wait_issuer(bar(C::B_DQ), (n_dq - 1) & 1u, w, kSiteOFull))) break;
-        mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILEB);
+      if (warp == kBwdTIssueWarp) {
+        // copies issued / waited per Q-dO barrier ([buffer][half]); blocks
+        // whose products were issued (one dV/dK commit per half and one dQ
+        // commit each)
+        uint32_t n_kv = 0, n_qd[4] = {0, 0, 0, 0}, w_qd[4] = {0, 0, 0, 0};
+        uint32_t n_prod = 0, qiter = 0;
+        // test hook: a wait on a barrier that nothing signals runs out
+        if (a.debug_flags & kDebugUnsignalledWait) ok = wait_issuer(bar(C::B_DRAIN), 0u, w, kSiteUnsignalled);
+        auto load_half = [&](int qb, int h, const BwdBlock& b, int qt) {
+          const int i = 2 * qb + h;
+          const int row0 = b.s0 + kBM * qt + 64 * h;
+          mbar_arrive_expect_tx(bar(C::B_QD + i), 2 * C::HALFB);
 #pragma unroll
-        for (int ch = 0; ch < C::NCHUNK; ++ch) {
-          tma_load_3d(base + C::K_OFF + ch * C::CHUNKB, &tm_k, bar(C::B_KV), ch * C::CHUNK, b.h,
-                      b.s0 + kBN * b.kt);
-          tma_load_3d(base + C::V_OFF + ch * C::CHUNKB, &tm_v, bar(C::B_KV), ch * C::CHUNK, b.h,
-                      b.s0 + kBN * b.kt);
-        }
-        ++n_kv;
-        const int qb0 = (int)(qiter & 1u);
-        load_half(qb0, 0, b, b.kt);
-        load_half(qb0, 1, b, b.kt);
-        if (b.kt + 1 < nq) {
-          load_half(qb0 ^ 1, 0, b, b.kt + 1);
-          load_half(qb0 ^ 1, 1, b, b.kt + 1);
-        }
-        if (!(ok = wait_issuer(bar(C::B_KV), (n_kv - 1) & 1u, w, kSiteKFull))) break;
-        if (!(ok = wait_half(qb0, 0))) break;
-        issue_sdp(qb0, 0);
-        if (!(ok = wait_half(qb0, 1))) break;
-        issue_sdp(qb0, 1);
-        if (pending) {
-          // the previous item's last dQ, staged at that item's end
-          if (!(ok = wait_pass(1))) break;
-          reduce_dq(pend_h, pend_row);
-          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          mbar_arrive(bar(C::B_STG));
-          pending = false;
-        }
-        for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
-          const int qb = (int)(qiter & 1u);
-          const bool first = qt == b.kt;
-          for (int h = 0; h < 2; ++h) {
-            if (!(ok = wait_pass(h))) break;
-            tc_fence_after();
-            // half 1's pass staged the previous block's dQ
-            if (h == 1 && !first) reduce_dq(b.h, b.s0 + kBM * (qt - 1));
-            mma_t(C::DV_COL, C::S_COL, half_desc(do_mn0, qb, 0), h, first && h == 0);
-            mma_t(C::DK_COL, C::DP_COL, half_desc(q_mn0, qb, 0), h, first && h == 0);
-            mma_commit(bar(C::B_PROD + h));
-            if (qt + 1 < nq) {
-              // the next block's half-h S^T and dP^T overwrite what these
-              // products read; half h of buffer qb is then free for block qt + 2
-              if (!(ok = wait_issuer(bar(C::B_PROD + h), n_prod & 1u, w, kSiteVFull))) break;
-              if (qt + 2 < nq) load_half(qb, h, b, qt + 2);
-              if (!(ok = wait_half(qb ^ 1, h))) break;
-              issue_sdp(qb ^ 1, h);
-            }
-            if (h == 1) {
-              mma_dq((int)(qiter & 1u));
-              mma_commit(bar(C::B_DQ));
-              ++n_dq;
-              if (!first) {
-                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                mbar_arrive(bar(C::B_STG));
+          for (int ch = 0; ch < C::NCHUNK; ++ch) {
+            tma_load_3d(base + C::Q_OFF + qb * C::TILEB + ch * C::CHUNKB + h * 64 * C::ROWB, &tm_q,
+                        bar(C::B_QD + i), ch * C::CHUNK, b.h, row0);
+            tma_load_3d(base + C::DO_OFF + qb * C::TILEB + ch * C::CHUNKB + h * 64 * C::ROWB, &tm_do,
+                        bar(C::B_QD + i), ch * C::CHUNK, b.h, row0);
+          }
+          ++n_qd[i];
+        };
+        auto wait_half = [&](int qb, int h) -> bool {
+          const int i = 2 * qb + h;
+          const bool r = wait_issuer(bar(C::B_QD + i), w_qd[i] & 1u, w, kSiteQFull);
+          ++w_qd[i];
+          return r;
+        };
+        auto issue_sdp = [&](int qb, int h) {
+          tc_fence_after();
+          mma_xyt(C::S_COL + 64u * h, k_kmaj, half_desc(q_kmaj0, qb, h));
+          mma_xyt(C::DP_COL + 64u * h, v_kmaj, half_desc(do_kmaj0, qb, h));
+          mma_commit(bar(C::B_SDP + h));
+        };
+        for (int idx = idx0; ok && idx < idx_end; idx += idx_step) {
+          const Item it = __ldg(&a.items[idx]);
+          const BwdBlock b{it.x, it.y, it.z, it.w};
+          const int hist = a.item_hist ? __ldg(a.item_hist + idx) : b.n;
+          const int nq = nq_of(b, hist);
+          // the previous item's products have finished reading K, V, Q, dO
+          // (its last dQ, issued by the other thread, reads K)
+          if (n_prod) {
+            if (!(ok = wait_issuer(bar(C::B_PROD), (n_prod - 1) & 1u, w, kSiteVFull))) break;
+            if (!(ok = wait_issuer(bar(C::B_PROD + 1), (n_prod - 1) & 1u, w, kSiteVFull))) break;
+            if (!(ok = wait_issuer(bar(C::B_DQ), (n_prod - 1) & 1u, w, kSiteOFull))) break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILEB);
+#pragma unroll
+          for (int ch = 0; ch < C::NCHUNK; ++ch) {
+            tma_load_3d(base + C::K_OFF + ch * C::CHUNKB, &tm_k, bar(C::B_KV), ch * C::CHUNK, b.h,
+                        b.s0 + kBN * b.kt);
+            tma_load_3d(base + C::V_OFF + ch * C::CHUNKB, &tm_v, bar(C::B_KV), ch * C::CHUNK, b.h,
+                        b.s0 + kBN * b.kt);
+          }
+          ++n_kv;
+          const int qb0 = (int)(qiter & 1u);
+          load_half(qb0, 0, b, b.kt);
+          load_half(qb0, 1, b, b.kt);
+          if (b.kt + 1 < nq) {
+            load_half(qb0 ^ 1, 0, b, b.kt + 1);
+            load_half(qb0 ^ 1, 1, b, b.kt + 1);
+          }
+          if (!(ok = wait_issuer(bar(C::B_KV), (n_kv - 1) & 1u, w, kSiteKFull))) break;
+          if (!(ok = wait_half(qb0, 0))) break;
+          issue_sdp(qb0, 0);
+          // The previous item's end phase of the half-1 pass barrier: its dV
+          // and dK have left TMEM before this item's first products
+          // overwrite them.  It is waited for before this item's first
+          // half-1 S^T and dP^T are issued: no elementwise warp can then
+          // arrive for this item's first half-1 pass while another has yet
+          // to arrive for the end phase (the barrier counts arrivals, not
+          // who makes them), and the phase cannot be overtaken.
+          if (n_prod && !(ok = wait_pass(1))) break;
+          if (!(ok = wait_half(qb0, 1))) break;
+          issue_sdp(qb0, 1);
+          for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
+            const int qb = (int)(qiter & 1u);
+            const bool first = qt == b.kt;
+            for (int h = 0; h < 2; ++h) {
+              if (!(ok = wait_pass(h))) break;
+              tc_fence_after();
+              mma_t(C::DV_COL, C::S_COL, half_desc(do_mn0, qb, 0), h, first && h == 0);
+              mma_t(C::DK_COL, C::DP_COL, half_desc(q_mn0, qb, 0), h, first && h == 0);
+              mma_commit(bar(C::B_PROD + h));
+              if (qt + 1 < nq) {
+                // the next block's half-h S^T and dP^T overwrite what these
+                // products read; half h of buffer qb is then free for block qt + 2
+                if (!(ok = wait_issuer(bar(C::B_PROD + h), n_prod & 1u, w, kSiteVFull))) break;
+                if (qt + 2 < nq) load_half(qb, h, b, qt + 2);
+                if (!(ok = wait_half(qb ^ 1, h))) break;
+                issue_sdp(qb ^ 1, h);
               }
             }
+            if (!ok) break;
+            ++n_prod;
+          }
+        }
+        if (!ok) {
+          // drain: every product issued, then every copy issued, has landed
+          mma_commit(bar(C::B_DRAIN));
+          wait_drain(bar(C::B_DRAIN), 0);
+          if (n_kv) wait_drain(bar(C::B_KV), (n_kv - 1) & 1u);
+          for (int i = 0; i < 4; ++i)
+            if (n_qd[i] > w_qd[i]) wait_drain(bar(C::B_QD + i), (n_qd[i] - 1) & 1u);
+        }
+      } else {
+        // dQ: per block, once the elementwise pass has written dS^T (and
+        // staged the previous block's dQ_part), the reduction of that part,
+        // then the block's dQ product; at an item's end, the reduction of
+        // its last part.  The staging tile goes back to the elementwise
+        // warps once a reduction has read it.
+        uint32_t qiter = 0;
+        auto release_stg = [&]() {
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          mbar_arrive(bar(C::B_STG));
+        };
+        for (int idx = idx0; ok && idx < idx_end; idx += idx_step) {
+          const Item it = __ldg(&a.items[idx]);
+          const BwdBlock b{it.x, it.y, it.z, it.w};
+          const int hist = a.item_hist ? __ldg(a.item_hist + idx) : b.n;
+          const int nq = nq_of(b, hist);
+          for (int qt = b.kt; qt < nq; ++qt, ++qiter) {
+            if (!(ok = wait_pass(1))) break;
+            tc_fence_after();
+            if (qt > b.kt) reduce_dq(b.h, b.s0 + kBM * (qt - 1));
+            mma_dq((int)(qiter & 1u));
+            mma_commit(bar(C::B_DQ));
+            if (qt > b.kt) release_stg();
           }
           if (!ok) break;
-          ++n_prod;
+          // the item's end phase: its last dQ_part is staged
+          if (!(ok = wait_pass(1))) break;
+          reduce_dq(b.h, b.s0 + kBM * (nq - 1));
+          release_stg();
         }
-        if (!ok) break;
-        pending = true;
-        pend_h = b.h;
-        pend_row = b.s0 + kBM * (nq - 1);
+        if (!ok) {
+          mma_commit(bar(C::B_DRAIN + 1));
+          wait_drain(bar(C::B_DRAIN + 1), 0);
+        }
+        // the reductions have finished before the CTA (and its shared memory) goes
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
       }
-      if (ok && pending) {
-        // the last item's end phase: its last dQ is staged
-        if ((ok = wait_pass(1))) reduce_dq(pend_h, pend_row);
-      }
-      if (!ok) {
-        // drain: every product issued, then every copy issued, has landed
-        mma_commit(bar(C::B_DRAIN));
-        wait_drain(bar(C::B_DRAIN), 0);
-        if (n_kv) wait_drain(bar(C::B_KV), (n_kv - 1) & 1u);
-        for (int i = 0; i < 4; ++i)
-          if (n_qd[i] > w_qd[i]) wait_drain(bar(C::B_QD + i), (n_qd[i] - 1) & 1u);
-      }
-      // the reductions have finished before the CTA (and its shared memory) goes
-      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     __syncwarp();
   } else {
