@@ -90,14 +90,13 @@ def test_bwd_rab_long_sequences():
 @pytest.mark.parametrize("d", [32, 64, 128])
 def test_zero_tables_give_the_plain_dk_dv_bit_for_bit(d):
     # a zero bias adds exactly zero to every score: dk and dv (one CTA's
-    # sums each, in the same order) equal the plain kernel's in its row form
-    # (the bias runs in that form; without the bias d <= 64 runs the
-    # transposed form, whose sums go in another order: equal within the
-    # tolerance); dq sums parts with atomics in an order that may differ
+    # sums each, in the same order) equal the plain kernel's in the row form,
+    # which the bias runs in (HSTU_DEBUG_BWD_ROWS makes the plain call run
+    # it too), and the default plain form (transposed for d <= 64) within
+    # the tolerance; dq sums parts with atomics in an order that may differ
     w = workloads.custom([700, 1, 129, 256], heads=2, d=d)
     q, k, v, do, rab = _inputs(w, 960 + d)
     rab = (rab[0], np.zeros_like(rab[1]), np.zeros_like(rab[2]))
-    got = _run(w, q, k, v, do, rab)
     qd, kd, vd, dod, _ = _dev(q, k, v, do, rab)
 
     def plain_bwd():
@@ -107,6 +106,7 @@ def test_zero_tables_give_the_plain_dk_dv_bit_for_bit(d):
         torch.cuda.synchronize()
         return g
 
+    got = _run(w, q, k, v, do, rab)
     try:
         binding.hstu_set_debug_flags(binding.HSTU_DEBUG_BWD_ROWS)
         rows = plain_bwd()
