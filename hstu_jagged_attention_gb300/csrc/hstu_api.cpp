@@ -1043,7 +1043,7 @@ int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_by
     return HSTU_OK;
   }
   *grid = grid_for((int)plan->items.size(), sms);
-  *block = hstu::kFwdThreads;
+  *block = hstu::fwd_block_threads(plan->d, false);
   *smem_bytes = hstu::fwd_smem_bytes(plan->d);
   return HSTU_OK;
 }

@@ -8,7 +8,8 @@
 // section 4.2 jagged values + offsets.  HSTU paper section 3.2: the
 // attention becomes grouped GEMMs of different sizes over ragged sequences.)
 //
-// Design (one persistent CTA per SM, 16 warps, warp-specialised).  A work
+// Design (one persistent CTA per SM, 24 warps -- 16 with the bias or at
+// d = 128 -- warp-specialised).  A work
 // item is one 128-row query block of one (sequence, head); it walks the key
 // blocks 0..qt.  Step t is the t-th key block the CTA processes.
 //   warp 4        K producer (one thread): each item's Q block, then its K
@@ -18,9 +19,12 @@
 //   warp 5        QK issuer (one thread, owns TMEM): S = Q K^T
 //                 (tcgen05.mma kind::f16, fp32 accumulate) of step t into
 //                 TMEM S buffer t mod 3, up to three steps ahead of PV.
-//   warps 8-15    two "SiLU" warpgroups taking alternate steps.  Thread r
-//                 owns score row r: tcgen05.ld S (the next 32 columns load
-//                 while the current ones are computed),
+//   warps 8-23    four "SiLU" warpgroups in two pairs taking alternate
+//                 steps, each warpgroup of a pair 64 of the block's 128 key
+//                 columns (with the bias or at d = 128: warps 8-15, two
+//                 warpgroups taking alternate steps, all columns).  Thread r
+//                 owns score row r: tcgen05.ld S (the next 16 or 32 columns
+//                 load while the current ones are computed),
 //                 p = h + h tanh(h) with h = alpha s / 2
 //                 (= alpha s sigmoid(alpha s)), tril select on the diagonal
 //                 block, split p = bf16(p) + bf16(p - bf16(p)), tcgen05.st
@@ -36,9 +40,10 @@
 //
 // TMEM columns (512 allocated): three S buffers of 128 columns, then the O
 // accumulator (d columns), double-buffered where TMEM has room (d <= 64).
-// P of a block overwrites its own S buffer: for the 32-key chunk c, P_hi
-// key pairs go to columns 32c+[0,16) and P_lo to 32c+[16,32) (two bf16 per
-// 32-bit column).
+// P of a block overwrites its own S buffer, two bf16 per 32-bit column:
+// with four SiLU warpgroups, 16-key step k's P_hi goes to columns
+// 16k+[0,8) and its P_lo to 16k+[8,16); with two, the 32-key chunk c's P_hi
+// goes to 32c+[0,16) and its P_lo to 32c+[16,32).
 //
 // The diagonal key block of a sequence's last query block, when the sequence
 // ends inside it, computes only keys < n rounded up to 16: its QK uses
@@ -313,6 +318,28 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// 16 consecutive fp32 TMEM columns of this thread's lane, without the wait
+// (tmem_wait_ld16 below ties the registers to it).
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -372,6 +399,7 @@ __device__ __forceinline__ uint32_t* trace_counters();
 __device__ __forceinline__ void trace(const FwdArgs& a, unsigned ev, unsigned idx) {
   if (!(a.debug_flags & kDebugTrace) || blockIdx.x != 0 || (threadIdx.x & 31) != 0) return;
   const unsigned warp = threadIdx.x >> 5;
+  if (warp >= (unsigned)kTraceWarps) return;
   uint32_t* cnt = trace_counters() + warp;
   const unsigned slot = *cnt;
   if (slot < (unsigned)kTracePerWarp) {
@@ -439,10 +467,11 @@ struct Cfg {
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(128 * P + OB * D <= (int)kTmemCols, "TMEM budget");
   // Arrivals that complete a phase of barrier i: every thread of the SiLU
-  // warpgroup (P-full), one per epilogue warp (O-empty), the K copy's and
-  // the PV commit's (QK-ready), else one.
-  __host__ __device__ static constexpr uint32_t arrivals(int i) {
-    return (i >= B_PFULL && i < B_PFULL + P)       ? 128u
+  // warpgroup (P-full; both warpgroups of a pair when `wide`), one per
+  // epilogue warp (O-empty), the K copy's and the PV commit's (QK-ready),
+  // else one.
+  __host__ __device__ static constexpr uint32_t arrivals(int i, bool wide) {
+    return (i >= B_PFULL && i < B_PFULL + P)       ? (wide ? 256u : 128u)
            : (i >= B_OEMPTY && i < B_OEMPTY + OB)   ? 4u
            : (i >= B_QKREADY && i < B_QKREADY + P) ? 2u
                                                    : 1u;
@@ -493,6 +522,17 @@ template <int VAR>
 constexpr bool has_norm = (VAR & kVarNorm) != 0;
 template <int VAR>
 constexpr bool has_rab = (VAR & kVarRab) != 0;
+// Without the bias and at d <= 64 the kernel runs four SiLU warpgroups in
+// two pairs: a pair takes alternate blocks and each of its warpgroups 64 of
+// the block's 128 key columns, so that four SiLU warps share each SMSP.
+// This P layout puts each 16-key step's P_hi and P_lo in that step's own 16
+// columns.  The others (d = 128: 768 threads leave 80 registers a thread,
+// and its epilogue spills; the bias: its chunk modes need 32-key chunks)
+// run two warpgroups, each taking whole alternate blocks.
+template <int D, int VAR>
+constexpr bool kWideSilu = !has_rab<VAR> && D <= 64;
+template <int D, int VAR>
+constexpr int kFwdThreadsOf = kWideSilu<D, VAR> ? 768 : kFwdThreads;
 
 // TGT: items carry a history length (the candidate mask); otherwise every
 // item walks key blocks 0 .. qt.
@@ -755,8 +795,11 @@ __device__ void role_mma_pv(const FwdArgs& a, uint32_t base, uint32_t tmem, cons
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int kk = 4 * H + i;
-      pa[2 * i] = pin32(tmem + (uint32_t)(J * 128 + 32 * (kk >> 1) + 8 * (kk & 1)));
-      pa[2 * i + 1] = pin32(tmem + (uint32_t)(J * 128 + 32 * (kk >> 1) + 8 * (kk & 1) + 16));
+      // P_hi and P_lo of 16-key step kk (the SiLU stage's layout)
+      const int hi_col = kWideSilu<D, VAR> ? 16 * kk : 32 * (kk >> 1) + 8 * (kk & 1);
+      constexpr int lo_off = kWideSilu<D, VAR> ? 8 : 16;
+      pa[2 * i] = pin32(tmem + (uint32_t)(J * 128 + hi_col));
+      pa[2 * i + 1] = pin32(tmem + (uint32_t)(J * 128 + hi_col + lo_off));
       vb[i] = pin64(v_desc0 + (uint64_t)((J * C::TILEB + kk * 2 * C::ATOMB) >> 4));
     }
     if (pc.kt != pc.b.qt && (H == 1 || pc.ki != 0)) {
@@ -921,6 +964,21 @@ __device__ __forceinline__ float rab_half(const RabRow& r, const RabChunk& c, in
   return bp + bt;
 }
 
+// p = x + x tanh(x) for two values x = alpha s / 2 (= alpha s sigmoid(alpha s)).
+__device__ __forceinline__ float2 silu_pair(float2 x) {
+  return __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
+}
+
+// p = hi + lo with hi = bf16(p) and lo = bf16(p - hi), each pair packed
+// two to a 32-bit word.
+__device__ __forceinline__ void split_bf16(float2 p, uint32_t& hi, uint32_t& lo) {
+  const uint32_t ph = pack_bf16x2(p.x, p.y);
+  const float2 r = __fadd2_rn(
+      p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
+  hi = ph;
+  lo = pack_bf16x2(r.x, r.y);
+}
+
 // MASK 0: none; 1: keep key k iff k <= lim; 2: the candidate mask.  RAB:
 // add the relative attention bias of keys j0 .. j0 + 31 (sequence-local),
 // FP / FT: its position / time part is constant over the chunk.
@@ -942,7 +1000,7 @@ __device__ __forceinline__ void silu_store32_body(const uint32_t (&s)[32], float
       } else {
         x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
       }
-      float2 p = __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
+      float2 p = silu_pair(x);
       if (MASK == 1) {  // keep key k iff k <= lim (causal)
         p.x = (k > lim) ? 0.0f : p.x;
         p.y = (k + 1 > lim) ? 0.0f : p.y;
@@ -952,15 +1010,35 @@ __device__ __forceinline__ void silu_store32_body(const uint32_t (&s)[32], float
         p.x = (k > lim || (k >= lim_hist && k != lim)) ? 0.0f : p.x;
         p.y = (k + 1 > lim || (k + 1 >= lim_hist && k + 1 != lim)) ? 0.0f : p.y;
       }
-      const uint32_t ph = pack_bf16x2(p.x, p.y);
-      const float2 r = __fadd2_rn(
-          p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
-      hi[m] = ph;
-      lo[m] = pack_bf16x2(r.x, r.y);
+      split_bf16(p, hi[m], lo[m]);
     }
     tmem_st8(t + 8u * h, hi);
     tmem_st8(t + 16u + 8u * h, lo);
   }
+}
+
+// silu of 16 scores s of one row (the wide layout): P_hi of the 16 keys to
+// columns t + [0, 8), P_lo to t + [8, 16), over the scores just read.
+// MASK 0: none; 1: keep key k iff k <= lim; 2: the candidate mask.
+template <int MASK>
+__device__ __forceinline__ void silu_store16(const uint32_t (&s)[16], float2 ha2, int lim, int lim_hist,
+                                             uint32_t t) {
+  uint32_t hi[8], lo[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int k = 2 * m;
+    float2 p = silu_pair(__fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2));
+    if (MASK == 1) {
+      p.x = (k > lim) ? 0.0f : p.x;
+      p.y = (k + 1 > lim) ? 0.0f : p.y;
+    } else if (MASK == 2) {
+      p.x = (k > lim || (k >= lim_hist && k != lim)) ? 0.0f : p.x;
+      p.y = (k + 1 > lim || (k + 1 >= lim_hist && k + 1 != lim)) ? 0.0f : p.y;
+    }
+    split_bf16(p, hi[m], lo[m]);
+  }
+  tmem_st8(t, hi);
+  tmem_st8(t + 8u, lo);
 }
 
 template <int MASK, bool RAB = false, bool TGT = false>
@@ -984,7 +1062,9 @@ __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2
 
 // SiLU warpgroups (warps 8-11 and 12-15): warpgroup e takes the steps with
 // tc % 2 == e, all 128 key columns of the block (whole blocks amortise the
-// per-step waits and arrivals twice as well as half blocks do).  Thread r
+// per-step waits and arrivals twice as well as half blocks do).  In the
+// wide variant (warps 8-23) pair e = warpgroups 2e and 2e + 1 takes those
+// steps, warpgroup 2e + h the key columns [64 h, 64 h + 64).  Thread r
 // owns score row r.  Every lane waits on S-full and arrives on P-full
 // itself (a vote keeps the warp's view uniform), so no lane-0 relay or warp
 // barrier sits on the path.
@@ -996,7 +1076,10 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
   constexpr int P = C::P;
   const uint32_t bars = base + C::BAR_OFF;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-  const int e = (warp - kEwWarp0) >> 2;
+  constexpr bool WIDE = kWideSilu<D, VAR>;
+  const int wg = (warp - kEwWarp0) >> 2;
+  const int e = WIDE ? wg >> 1 : wg;  // takes the steps with tc % 2 == e
+  const int half = WIDE ? wg & 1 : 0;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -1048,7 +1131,51 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
     const uint32_t t_s = lane_base + (uint32_t)(j * 128);
     bool plain = cur.kt != cur.b.qt;
     if constexpr (TGT) plain = cur.b.unmasked(cur.kt);
-    if (RAB && plain && quarter * 32 < cur.b.rows()) {
+    if constexpr (WIDE) {
+      // this warpgroup's four 16-key steps k = 4 half + u of the block
+      if (quarter * 32 < cur.b.rows()) {
+        uint32_t w0[16], w1[16];
+        if (plain) {
+          const uint32_t t_h = t_s + 64u * (uint32_t)half;
+          tmem_ld16_async(t_h, w0);
+          tmem_wait_ld16(w0);
+#pragma unroll 1
+          for (int u = 0; u < 4; u += 2) {
+            tmem_ld16_async(t_h + 16u * (u + 1), w1);
+            silu_store16<0>(w0, ha2, 0, 0, t_h + 16u * u);
+            tmem_wait_ld16(w1);
+            if (u + 2 < 4) tmem_ld16_async(t_h + 16u * (u + 2), w0);
+            silu_store16<0>(w1, ha2, 0, 0, t_h + 16u * (u + 1));
+            if (u + 2 < 4) tmem_wait_ld16(w0);
+          }
+        } else {
+          // a masked block, as in the two-warpgroup path below, in 16-key
+          // steps: steps wholly above the diagonal for this warp are zeros,
+          // steps at or past cols are not read by the PV products
+          const int cols = cur.b.cols(cur.kt);
+          const bool diag = cur.kt == cur.b.qt;
+          const int lim0 = kBM * cur.b.qt + row - kBN * cur.kt;
+          int hist0 = 0;
+          if constexpr (TGT) hist0 = cur.b.hist - kBN * cur.kt;
+#pragma unroll 1
+          for (int u = 0; u < 4; ++u) {
+            const int k = 4 * half + u;
+            if (16 * k >= cols) break;
+            const uint32_t t_k = t_s + 16u * (uint32_t)k;
+            if (diag && (k >> 1) > quarter) {
+#pragma unroll
+              for (int m = 0; m < 16; ++m) w0[m] = 0u;
+              tmem_st16(t_k, w0);
+            } else {
+              tmem_ld16_async(t_k, w0);
+              tmem_wait_ld16(w0);
+              silu_store16<TGT ? 2 : 1>(w0, ha2, lim0 - 16 * k, hist0 - 16 * k, t_k);
+            }
+          }
+        }
+        tmem_wait_st();
+      }
+    } else if (RAB && plain && quarter * 32 < cur.b.rows()) {
       // one score buffer: the bias computation needs the registers
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -1229,7 +1356,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint32_t base, uint32_t tmem, co
 }
 
 template <int D, int VAR>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __launch_bounds__(kFwdThreadsOf<D, VAR>, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using C = Cfg<D>;
@@ -1243,7 +1370,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t bars = base + C::BAR_OFF;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBARS; ++i) mbar_init(bars + 8u * i, C::arrivals(i));
+    for (int i = 0; i < C::NBARS; ++i) mbar_init(bars + 8u * i, C::arrivals(i, kWideSilu<D, VAR>));
     // QK-ready phase 0 has no PV before it: arrive for it now
     for (int j = 0; j < C::P; ++j) mbar_arrive(bars + 8u * (C::B_QKREADY + j));
     *abort_flag = 0;
@@ -1282,7 +1409,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == kMmaWarpPV) {
     if (lane == 0) role_mma_pv<D, VAR>(a, base, tmem, w);
     __syncwarp();
-  } else if (warp >= kEwWarp0 && warp < kEwWarp0 + 8) {
+  } else if (warp >= kEwWarp0 && warp < kEwWarp0 + (kWideSilu<D, VAR> ? 16 : 8)) {
     role_silu<D, VAR>(a, base, tmem, w, warp, lane);
   } else if (warp < kEpiWarp0 + 4) {
     role_epilogue<D, VAR>(a, base, tmem, w, warp, lane);
@@ -1384,7 +1511,7 @@ cudaError_t launch_dt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<D, VAR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_LAUNCH);
   if (e != cudaSuccess) return e;
-  hstu_fwd_kernel<D, VAR><<<grid, kFwdThreads, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, a);
+  hstu_fwd_kernel<D, VAR><<<grid, kFwdThreadsOf<D, VAR>, C::SMEM_LAUNCH, stream>>>(tq, tk, tv, a);
   if ((e = cudaGetLastError()) != cudaSuccess || !has_norm<VAR>) return e;
   norm_gate_kernel<<<a.norm_grid, kNormThreads, 0, stream>>>(a, D, a.total);
   return cudaGetLastError();
@@ -1440,6 +1567,15 @@ int fwd_smem_bytes(int d) {
 }
 
 int fwd_swizzle_bytes(int d) { return d >= 64 ? 128 : 64; }
+
+int fwd_block_threads(int d, bool rab) {
+  switch (d) {
+    case 32: return rab ? kFwdThreadsOf<32, kVarRab> : kFwdThreadsOf<32, 0>;
+    case 64: return rab ? kFwdThreadsOf<64, kVarRab> : kFwdThreadsOf<64, 0>;
+    case 128: return rab ? kFwdThreadsOf<128, kVarRab> : kFwdThreadsOf<128, 0>;
+    default: return -1;
+  }
+}
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a, int grid,

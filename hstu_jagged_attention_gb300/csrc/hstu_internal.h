@@ -142,6 +142,10 @@ cudaError_t read_and_clear_trace(unsigned long long* dst, int capacity, int* n);
 // Shared-memory bytes and grid the d-specialised kernel needs.
 int fwd_smem_bytes(int d);
 constexpr int kFwdThreads = 512;
+// Threads of the single-CTA forward kernel for head dimension d, with or
+// without the bias: 768 (four SiLU warpgroups) for d <= 64 without it,
+// else kFwdThreads.
+int fwd_block_threads(int d, bool rab);
 
 // Launch the persistent kernel for head dimension d on `grid` CTAs (and,
 // with the output stage, the output-stage kernel after it).
