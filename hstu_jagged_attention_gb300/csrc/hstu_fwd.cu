@@ -8,8 +8,8 @@
 // section 4.2 jagged values + offsets.  HSTU paper section 3.2: the
 // attention becomes grouped GEMMs of different sizes over ragged sequences.)
 //
-// Design (one persistent CTA per SM, 24 warps -- 16 with the bias or at
-// d = 128 -- warp-specialised).  A work
+// Design (one persistent CTA per SM, 24 warps -- 16 with the bias, the
+// output stage or d = 128 -- warp-specialised).  A work
 // item is one 128-row query block of one (sequence, head); it walks the key
 // blocks 0..qt.  Step t is the t-th key block the CTA processes.
 //   warp 4        K producer (one thread): each item's Q block, then its K
@@ -21,8 +21,9 @@
 //                 TMEM S buffer t mod 3, up to three steps ahead of PV.
 //   warps 8-23    four "SiLU" warpgroups in two pairs taking alternate
 //                 steps, each warpgroup of a pair 64 of the block's 128 key
-//                 columns (with the bias or at d = 128: warps 8-15, two
-//                 warpgroups taking alternate steps, all columns).  Thread r
+//                 columns (with the bias, the output stage or d = 128:
+//                 warps 8-15, two warpgroups taking alternate steps, all
+//                 columns).  Thread r
 //                 owns score row r: tcgen05.ld S (the next 16 or 32 columns
 //                 load while the current ones are computed),
 //                 p = h + h tanh(h) with h = alpha s / 2
@@ -67,9 +68,10 @@ namespace hstu {
 __device__ unsigned int g_dev_status;
 __device__ unsigned int g_dev_site;
 
-// Trace buffer for kDebugTrace: per warp of CTA 0, kTracePerWarp events of
-// two 64-bit words; g_trace_n[w] counts warp w's events.
-constexpr int kTraceWarps = 16;
+// Trace buffer for kDebugTrace: per warp of CTA 0 (up to 24 warps),
+// kTracePerWarp events of two 64-bit words; g_trace_n[w] counts warp w's
+// events.
+constexpr int kTraceWarps = 24;
 constexpr int kTracePerWarp = 2048;
 __device__ unsigned long long g_trace[kTraceWarps * kTracePerWarp * 2];
 __device__ unsigned int g_trace_n[kTraceWarps];
@@ -399,7 +401,6 @@ __device__ __forceinline__ uint32_t* trace_counters();
 __device__ __forceinline__ void trace(const FwdArgs& a, unsigned ev, unsigned idx) {
   if (!(a.debug_flags & kDebugTrace) || blockIdx.x != 0 || (threadIdx.x & 31) != 0) return;
   const unsigned warp = threadIdx.x >> 5;
-  if (warp >= (unsigned)kTraceWarps) return;
   uint32_t* cnt = trace_counters() + warp;
   const unsigned slot = *cnt;
   if (slot < (unsigned)kTracePerWarp) {
@@ -522,15 +523,17 @@ template <int VAR>
 constexpr bool has_norm = (VAR & kVarNorm) != 0;
 template <int VAR>
 constexpr bool has_rab = (VAR & kVarRab) != 0;
-// Without the bias and at d <= 64 the kernel runs four SiLU warpgroups in
-// two pairs: a pair takes alternate blocks and each of its warpgroups 64 of
-// the block's 128 key columns, so that four SiLU warps share each SMSP.
+// Without the bias or the output stage and at d <= 64 the kernel runs four
+// SiLU warpgroups in two pairs: a pair takes alternate blocks and each of
+// its warpgroups 64 of the block's 128 key columns, so that four SiLU warps
+// share each SMSP.
 // This P layout puts each 16-key step's P_hi and P_lo in that step's own 16
 // columns.  The others (d = 128: 768 threads leave 80 registers a thread,
-// and its epilogue spills; the bias: its chunk modes need 32-key chunks)
-// run two warpgroups, each taking whole alternate blocks.
+// and its epilogue spills; the bias: its chunk modes need 32-key chunks;
+// the output stage: measured 1.3% slower on dense with four) run two
+// warpgroups, each taking whole alternate blocks.
 template <int D, int VAR>
-constexpr bool kWideSilu = !has_rab<VAR> && D <= 64;
+constexpr bool kWideSilu = !has_rab<VAR> && !has_norm<VAR> && D <= 64;
 template <int D, int VAR>
 constexpr int kFwdThreadsOf = kWideSilu<D, VAR> ? 768 : kFwdThreads;
 
@@ -964,21 +967,6 @@ __device__ __forceinline__ float rab_half(const RabRow& r, const RabChunk& c, in
   return bp + bt;
 }
 
-// p = x + x tanh(x) for two values x = alpha s / 2 (= alpha s sigmoid(alpha s)).
-__device__ __forceinline__ float2 silu_pair(float2 x) {
-  return __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
-}
-
-// p = hi + lo with hi = bf16(p) and lo = bf16(p - hi), each pair packed
-// two to a 32-bit word.
-__device__ __forceinline__ void split_bf16(float2 p, uint32_t& hi, uint32_t& lo) {
-  const uint32_t ph = pack_bf16x2(p.x, p.y);
-  const float2 r = __fadd2_rn(
-      p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
-  hi = ph;
-  lo = pack_bf16x2(r.x, r.y);
-}
-
 // MASK 0: none; 1: keep key k iff k <= lim; 2: the candidate mask.  RAB:
 // add the relative attention bias of keys j0 .. j0 + 31 (sequence-local),
 // FP / FT: its position / time part is constant over the chunk.
@@ -1000,7 +988,7 @@ __device__ __forceinline__ void silu_store32_body(const uint32_t (&s)[32], float
       } else {
         x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
       }
-      float2 p = silu_pair(x);
+      float2 p = __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
       if (MASK == 1) {  // keep key k iff k <= lim (causal)
         p.x = (k > lim) ? 0.0f : p.x;
         p.y = (k + 1 > lim) ? 0.0f : p.y;
@@ -1010,7 +998,11 @@ __device__ __forceinline__ void silu_store32_body(const uint32_t (&s)[32], float
         p.x = (k > lim || (k >= lim_hist && k != lim)) ? 0.0f : p.x;
         p.y = (k + 1 > lim || (k + 1 >= lim_hist && k + 1 != lim)) ? 0.0f : p.y;
       }
-      split_bf16(p, hi[m], lo[m]);
+      const uint32_t ph = pack_bf16x2(p.x, p.y);
+      const float2 r = __fadd2_rn(
+          p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
+      hi[m] = ph;
+      lo[m] = pack_bf16x2(r.x, r.y);
     }
     tmem_st8(t + 8u * h, hi);
     tmem_st8(t + 16u + 8u * h, lo);
@@ -1027,7 +1019,8 @@ __device__ __forceinline__ void silu_store16(const uint32_t (&s)[16], float2 ha2
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     const int k = 2 * m;
-    float2 p = silu_pair(__fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2));
+    const float2 x = __fmul2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), ha2);
+    float2 p = __ffma2_rn(x, make_float2(tanh_approx(x.x), tanh_approx(x.y)), x);
     if (MASK == 1) {
       p.x = (k > lim) ? 0.0f : p.x;
       p.y = (k + 1 > lim) ? 0.0f : p.y;
@@ -1035,7 +1028,11 @@ __device__ __forceinline__ void silu_store16(const uint32_t (&s)[16], float2 ha2
       p.x = (k > lim || (k >= lim_hist && k != lim)) ? 0.0f : p.x;
       p.y = (k + 1 > lim || (k + 1 >= lim_hist && k + 1 != lim)) ? 0.0f : p.y;
     }
-    split_bf16(p, hi[m], lo[m]);
+    const uint32_t ph = pack_bf16x2(p.x, p.y);
+    const float2 r = __fadd2_rn(
+        p, make_float2(-__uint_as_float(ph << 16), -__uint_as_float(ph & 0xFFFF0000u)));
+    hi[m] = ph;
+    lo[m] = pack_bf16x2(r.x, r.y);
   }
   tmem_st8(t, hi);
   tmem_st8(t + 8u, lo);
