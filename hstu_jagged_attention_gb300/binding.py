@@ -53,6 +53,9 @@ _RABP, _NGP = ctypes.POINTER(_Rab), ctypes.POINTER(_NormGate)
 _SIGNATURES = {
     "hstu_attn_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_float, ctypes.c_float, _VP, _VP]),
+    "hstu_attn_fwd_host": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                          _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP]),
     "hstu_attn_fwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                              ctypes.c_float, _VP, _VP]),
@@ -206,6 +209,25 @@ def hstu_attn_fwd(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: 
     _check(lib().hstu_attn_fwd(_addr(q), _addr(k), _addr(v), off_ptr, int(batch), int(heads), int(d),
                                int(max_seqlen), float(alpha), float(inv_n), _addr(out),
                                _stream(stream)), "hstu_attn_fwd")
+
+
+def hstu_attn_fwd_host(q, k, v, offsets, batch: int, heads: int, d: int, max_seqlen: int,
+                       alpha: float, inv_n: float, out, q_dev, k_dev, v_dev, out_dev,
+                       n_chunks: int = 0, stream=None) -> None:
+    """The forward from host q, k, v to host out (CPU tensors, page-locked
+    for overlap), staged through the caller's device tensors q_dev, k_dev,
+    v_dev, out_dev, in n_chunks runs of whole sequences (0: automatic) whose
+    copies overlap the kernel.  ``offsets``: host int32.  Enqueued on
+    ``stream``; out is valid once the stream reaches the call's end."""
+    for t in (q, k, v, out):
+        if hasattr(t, "is_cuda") and t.is_cuda:
+            raise ValueError("q, k, v and out must be host tensors")
+    off = _host_offsets(offsets)
+    _check(lib().hstu_attn_fwd_host(_addr(q), _addr(k), _addr(v), off.ctypes.data, int(batch),
+                                    int(heads), int(d), int(max_seqlen), float(alpha),
+                                    float(inv_n), _addr(out), _addr(q_dev), _addr(k_dev),
+                                    _addr(v_dev), _addr(out_dev), int(n_chunks), _stream(stream)),
+           "hstu_attn_fwd_host")
 
 
 def _host_targets(num_targets, batch: int) -> np.ndarray:

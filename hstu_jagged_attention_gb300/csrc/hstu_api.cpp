@@ -859,6 +859,164 @@ int launch_backward(const hstu::Item* d_items, int n_items, long long total, int
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 
+// The host-buffer forward's copy streams of the current device: one for
+// q, k, v (copies on more streams at once measured no faster: they share
+// one host link), one for out.  Non-blocking, created on first use, kept
+// until exit.
+constexpr int kMaxDevices = 64;
+constexpr int kCopyStreams = 2;
+std::mutex g_copy_mu;
+cudaStream_t g_copy_streams[kMaxDevices][kCopyStreams] = {};
+
+int copy_streams(cudaStream_t (&st)[kCopyStreams]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HSTU_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_copy_mu);
+  for (int i = 0; i < kCopyStreams; ++i) {
+    cudaStream_t& c = g_copy_streams[dev][i];
+    if (!c && cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking) != cudaSuccess) {
+      c = nullptr;
+      return HSTU_ERR_CUDA;
+    }
+    st[i] = c;
+  }
+  return HSTU_OK;
+}
+
+// Splits sequences 0 .. batch-1 into nc runs of whole sequences with about
+// equal token counts: run c is sequences first[c] .. first[c+1]-1 (a run
+// may be empty when one sequence holds most tokens).
+std::vector<int> chunk_sequences(const int32_t* off, int batch, int nc) {
+  std::vector<int> first((size_t)nc + 1, batch);
+  first[0] = 0;
+  const long long total = off[batch];
+  int b = 0;
+  for (int c = 1; c < nc; ++c) {
+    const long long target = total * c / nc;
+    while (b < batch && off[b] < target) ++b;
+    first[(size_t)c] = std::max(b, first[(size_t)c - 1]);
+  }
+  return first;
+}
+
+// Events of one host-buffer call, destroyed on scope exit (a pending
+// event's resources are released once it completes).
+struct EventSet {
+  std::vector<cudaEvent_t> ev;
+  ~EventSet() {
+    for (cudaEvent_t e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+  cudaEvent_t make() {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    ev.push_back(e);
+    return e;
+  }
+};
+
+int fwd_host(const void* q_host, const void* k_host, const void* v_host, const int32_t* off,
+             int batch, int heads, int d, int max_seqlen, float alpha, float inv_n, void* out_host,
+             void* q_dev, void* k_dev, void* v_dev, void* out_dev, int n_chunks, cudaStream_t s) {
+  if (heads < 1 || max_seqlen < 0 || batch < 0 || n_chunks < 0) return HSTU_ERR_INVALID_ARG;
+  if (!supported_d(d)) return HSTU_ERR_UNSUPPORTED;
+  if (batch == 0) return HSTU_OK;
+  if (!off) return HSTU_ERR_INVALID_ARG;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, off) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (attr.type == cudaMemoryTypeDevice) return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(off, batch, max_seqlen);
+  if (rc != HSTU_OK) return rc;
+  const long long total = off[batch];
+  if (total == 0) return HSTU_OK;
+  if (!q_host || !k_host || !v_host || !out_host) return HSTU_ERR_INVALID_ARG;
+  if ((rc = check_buffers(q_dev, k_dev, v_dev, out_dev)) != HSTU_OK) return rc;
+  cudaStream_t cs[kCopyStreams] = {};
+  if ((rc = copy_streams(cs)) != HSTU_OK) return rc;
+  cudaStream_t s_in = cs[0], s_out = cs[1];
+
+  const int nc = std::min(batch, n_chunks > 0 ? n_chunks : 4);
+  std::vector<hstu::Item> all, items;
+  std::vector<int32_t> hist;
+  std::vector<int> seq_first, item_first;
+  try {
+    if ((rc = build_worklist(off, nullptr, batch, heads, all, hist)) != HSTU_OK) return rc;
+    seq_first = chunk_sequences(off, batch, nc);
+    // each run's items, in the longest-first order of the whole list: a
+    // counting sort by run, keyed on the item's first row
+    std::vector<int32_t> run_row((size_t)nc);
+    for (int c = 0; c < nc; ++c) run_row[(size_t)c] = off[seq_first[(size_t)c + 1]];
+    auto run_of = [&](const hstu::Item& it) {
+      return (int)(std::upper_bound(run_row.begin(), run_row.end(), it.x) - run_row.begin());
+    };
+    item_first.assign((size_t)nc + 1, 0);
+    for (const hstu::Item& it : all) ++item_first[(size_t)run_of(it) + 1];
+    for (int c = 0; c < nc; ++c) item_first[(size_t)c + 1] += item_first[(size_t)c];
+    items.resize(all.size());
+    std::vector<int> fill(item_first.begin(), item_first.end() - 1);
+    for (const hstu::Item& it : all) items[(size_t)fill[(size_t)run_of(it)]++] = it;
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
+
+  const size_t ibytes = items.size() * sizeof(hstu::Item);
+  hstu::Item* d_items = nullptr;
+  if (ibytes) {
+    const cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_items), ibytes, s);
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? HSTU_ERR_NO_MEMORY : HSTU_ERR_CUDA;
+    // pageable source: the copy returns once the bytes are staged
+    if (cudaMemcpyAsync(d_items, items.data(), ibytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+      cudaFreeAsync(d_items, s);
+      return HSTU_ERR_CUDA;
+    }
+  }
+  EventSet evs;
+  rc = [&]() -> int {
+    cudaEvent_t start = evs.make(), done_out = evs.make();
+    if (!start || !done_out) return HSTU_ERR_CUDA;
+    // the copies in start after the caller's earlier work on s
+    if (cudaEventRecord(start, s) != cudaSuccess || cudaStreamWaitEvent(s_in, start, 0) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+    const size_t row = (size_t)heads * d * 2;
+    const void* src[3] = {q_host, k_host, v_host};
+    void* dst[3] = {q_dev, k_dev, v_dev};
+    std::vector<cudaEvent_t> landed((size_t)nc);  // run c's q, k, v are on the device
+    for (int c = 0; c < nc; ++c) {
+      const size_t r0 = (size_t)off[seq_first[(size_t)c]], r1 = (size_t)off[seq_first[(size_t)c + 1]];
+      for (int t = 0; t < 3 && r1 > r0; ++t)
+        if (cudaMemcpyAsync(static_cast<char*>(dst[t]) + r0 * row,
+                            static_cast<const char*>(src[t]) + r0 * row, (r1 - r0) * row,
+                            cudaMemcpyHostToDevice, s_in) != cudaSuccess)
+          return HSTU_ERR_CUDA;
+      if (!(landed[(size_t)c] = evs.make()) || cudaEventRecord(landed[(size_t)c], s_in) != cudaSuccess)
+        return HSTU_ERR_CUDA;
+    }
+    for (int c = 0; c < nc; ++c) {
+      const size_t r0 = (size_t)off[seq_first[(size_t)c]], r1 = (size_t)off[seq_first[(size_t)c + 1]];
+      if (cudaStreamWaitEvent(s, landed[(size_t)c], 0) != cudaSuccess) return HSTU_ERR_CUDA;
+      const int n = item_first[(size_t)c + 1] - item_first[(size_t)c];
+      const int lrc = launch(d_items + item_first[(size_t)c], nullptr, n, total, heads, d, q_dev,
+                             k_dev, v_dev, alpha, inv_n, out_dev, nullptr, s);
+      if (lrc != HSTU_OK) return lrc;
+      cudaEvent_t computed = evs.make();
+      if (!computed || cudaEventRecord(computed, s) != cudaSuccess ||
+          cudaStreamWaitEvent(s_out, computed, 0) != cudaSuccess)
+        return HSTU_ERR_CUDA;
+      if (r1 > r0 && cudaMemcpyAsync(static_cast<char*>(out_host) + r0 * row,
+                                     static_cast<const char*>(out_dev) + r0 * row, (r1 - r0) * row,
+                                     cudaMemcpyDeviceToHost, s_out) != cudaSuccess)
+        return HSTU_ERR_CUDA;
+    }
+    // later work on s sees out_host written
+    if (cudaEventRecord(done_out, s_out) != cudaSuccess ||
+        cudaStreamWaitEvent(s, done_out, 0) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+    return HSTU_OK;
+  }();
+  if (d_items && cudaFreeAsync(d_items, s) != cudaSuccess && rc == HSTU_OK) rc = HSTU_ERR_CUDA;
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1138,6 +1296,15 @@ int hstu_attn_fwd(const void* q, const void* k, const void* v, const int32_t* of
                   hstu_stream_t stream) {
   return oneshot(q, k, v, offsets, nullptr, batch, heads, d, max_seqlen, alpha, inv_n, out,
                  nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int hstu_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                       const int32_t* offsets, int batch, int heads, int d, int max_seqlen,
+                       float alpha, float inv_n, void* out_host, void* q_dev, void* k_dev,
+                       void* v_dev, void* out_dev, int n_chunks, hstu_stream_t stream) {
+  return fwd_host(q_host, k_host, v_host, offsets, batch, heads, d, max_seqlen, alpha, inv_n,
+                  out_host, q_dev, k_dev, v_dev, out_dev, n_chunks,
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hstu_attn_fwd_targets(const void* q, const void* k, const void* v, const int32_t* offsets,

@@ -146,6 +146,48 @@ int hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v, const int
                           void* out, hstu_stream_t stream);
 
 /*
+ * hstu_attn_fwd_host -- hstu_attn_fwd from host buffers to host buffers,
+ * with the copies overlapped with the kernel.
+ *
+ * No page defines this call; it serves callers whose q, k, v come from
+ * and whose out goes to host memory (a serving process fed from the host).
+ * The sequences are split into n_chunks runs of whole sequences with about
+ * equal token counts (0: min(batch, 4)).  Chunk c's q, k, v rows are copied
+ * in on an internal stream, its forward runs on `stream` once they have
+ * landed, and its out rows are copied back on a second internal stream.
+ * So chunk c + 1's copy in and chunk c - 1's copy out run under chunk c's
+ * kernel.  Each output row is computed by the same kernel arithmetic as
+ * hstu_attn_fwd's, so the two agree bit for bit.
+ *
+ *   q_host, k_host, v_host  host, (total, heads, d) bf16 row-major.
+ *   out_host                host, (total, heads, d) bf16, written.
+ *   q_dev, k_dev, v_dev,    device staging of the same shape, owned by the
+ *   out_dev                 caller (16-byte aligned), overwritten; q_dev,
+ *                           k_dev, v_dev and out_dev must not overlap.
+ *   offsets                 host pointer only, int32[batch+1].
+ *   n_chunks                >= 0; more chunks than sequences are capped.
+ * The host buffers must stay valid, and out_host must not be read, until
+ * `stream` reaches the end of the call.  Page-locked host memory
+ * (cudaHostAlloc, cudaHostRegister) lets the copies run asynchronously and
+ * overlap.  With pageable memory each copy waits for earlier work on its
+ * stream and the call blocks the calling thread.
+ * The two internal streams (non-blocking, one pair per device, created on
+ * first use and kept until exit) are joined to `stream` by events: work
+ * enqueued on `stream` before the call is done before the first copy, and
+ * work enqueued after it sees out_host written.  The work list goes into a
+ * stream-ordered allocation on `stream`, as in hstu_attn_fwd.
+ * A chunk's kernel may read, through the last 128-row tile of its last
+ * sequence, staged rows of the next chunk while they are being copied in.
+ * Those rows only feed masked terms, so the results do not depend on them.
+ * Errors: as hstu_attn_fwd, and HSTU_ERR_INVALID_ARG for a device offsets
+ * pointer, a negative n_chunks or a null host buffer.
+ */
+int hstu_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                       const int32_t* offsets, int batch, int heads, int d, int max_seqlen,
+                       float alpha, float inv_n, void* out_host, void* q_dev, void* k_dev,
+                       void* v_dev, void* out_dev, int n_chunks, hstu_stream_t stream);
+
+/*
  * hstu_plan_create -- validate host offsets and build the device work list once.
  *
  * The work list holds one item per (sequence, head, 128-row query block);
