@@ -180,7 +180,11 @@ int hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v, const int
  * sequence, staged rows of the next chunk while they are being copied in.
  * Those rows only feed masked terms, so the results do not depend on them.
  * Errors: as hstu_attn_fwd, and HSTU_ERR_INVALID_ARG for a device offsets
- * pointer, a negative n_chunks or a null host buffer.
+ * pointer, a negative n_chunks or a null host buffer; those are found
+ * before anything is enqueued.  A CUDA error while enqueuing (after the
+ * first copy) returns HSTU_ERR_CUDA with part of the work enqueued and
+ * `stream` not joined to the internal streams: synchronise the device
+ * before reusing the buffers.
  */
 int hstu_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
                        const int32_t* offsets, int batch, int heads, int d, int max_seqlen,
