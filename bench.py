@@ -683,8 +683,8 @@ def run_ours(args, w, nt=None):
 
     n_items = binding.hstu_plan_num_items(plan)
     grid, block, smem = binding.hstu_launch_shape(plan)
-    if rab is not None or ng:
-        block = 512  # two SiLU warpgroups (the shape query assumes a plain call)
+    if ng:
+        block = 512  # two SiLU warpgroups (the shape query assumes no output stage)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
 

@@ -8,8 +8,8 @@
 // section 4.2 jagged values + offsets.  HSTU paper section 3.2: the
 // attention becomes grouped GEMMs of different sizes over ragged sequences.)
 //
-// Design (one persistent CTA per SM, 24 warps -- 16 with the bias, the
-// output stage or d = 128 -- warp-specialised).  A work
+// Design (one persistent CTA per SM, 24 warps -- 16 with the output stage
+// or at d = 128 -- warp-specialised).  A work
 // item is one 128-row query block of one (sequence, head); it walks the key
 // blocks 0..qt.  Step t is the t-th key block the CTA processes.
 //   warp 4        K producer (one thread): each item's Q block, then its K
@@ -21,8 +21,8 @@
 //                 TMEM S buffer t mod 3, up to three steps ahead of PV.
 //   warps 8-23    four "SiLU" warpgroups in two pairs taking alternate
 //                 steps, each warpgroup of a pair 64 of the block's 128 key
-//                 columns (with the bias, the output stage or d = 128:
-//                 warps 8-15, two warpgroups taking alternate steps, all
+//                 columns (with the output stage or at d = 128: warps
+//                 8-15, two warpgroups taking alternate steps, all
 //                 columns).  Thread r
 //                 owns score row r: tcgen05.ld S (the next 16 or 32 columns
 //                 load while the current ones are computed),
@@ -523,17 +523,16 @@ template <int VAR>
 constexpr bool has_norm = (VAR & kVarNorm) != 0;
 template <int VAR>
 constexpr bool has_rab = (VAR & kVarRab) != 0;
-// Without the bias or the output stage and at d <= 64 the kernel runs four
-// SiLU warpgroups in two pairs: a pair takes alternate blocks and each of
-// its warpgroups 64 of the block's 128 key columns, so that four SiLU warps
-// share each SMSP.
-// This P layout puts each 16-key step's P_hi and P_lo in that step's own 16
-// columns.  The others (d = 128: 768 threads leave 80 registers a thread,
-// and its epilogue spills; the bias: its chunk modes need 32-key chunks;
-// the output stage: measured 1.3% slower on dense with four) run two
-// warpgroups, each taking whole alternate blocks.
+// Without the output stage and at d <= 64 the kernel runs four SiLU
+// warpgroups in two pairs: a pair takes alternate blocks and each of its
+// warpgroups 64 of the block's 128 key columns (the bias: two of its four
+// 32-key chunks), so that four SiLU warps share each SMSP.  This P layout
+// puts each 16-key step's P_hi and P_lo in that step's own 16 columns.  The
+// others (d = 128: 768 threads leave 80 registers a thread, and its
+// epilogue spills; the output stage: measured 1.3% slower on dense with
+// four) run two warpgroups, each taking whole alternate blocks.
 template <int D, int VAR>
-constexpr bool kWideSilu = !has_rab<VAR> && !has_norm<VAR> && D <= 64;
+constexpr bool kWideSilu = !has_norm<VAR> && D <= 64;
 template <int D, int VAR>
 constexpr int kFwdThreadsOf = kWideSilu<D, VAR> ? 768 : kFwdThreads;
 
@@ -970,7 +969,11 @@ __device__ __forceinline__ float rab_half(const RabRow& r, const RabChunk& c, in
 // MASK 0: none; 1: keep key k iff k <= lim; 2: the candidate mask.  RAB:
 // add the relative attention bias of keys j0 .. j0 + 31 (sequence-local),
 // FP / FT: its position / time part is constant over the chunk.
-template <int MASK, bool RAB = false, bool TGT = false, bool FP = false, bool FT = false>
+// WL: the wide P layout (16-key step k's P_hi at 16 k + [0, 8), P_lo at
+// 16 k + [8, 16)), else P_hi of keys 16h.. at t + 8h + [0, 8) and P_lo at
+// t + 16 + 8h + [0, 8).
+template <int MASK, bool RAB = false, bool TGT = false, bool FP = false, bool FT = false,
+          bool WL = false>
 __device__ __forceinline__ void silu_store32_body(const uint32_t (&s)[32], float2 ha2, int lim,
                                                   int lim_hist, uint32_t t, const RabRow* rab,
                                                   const RabChunk* rc, int j0) {
@@ -1004,8 +1007,8 @@ __device__ __forceinline__ void silu_store32_body(const uint32_t (&s)[32], float
       hi[m] = ph;
       lo[m] = pack_bf16x2(r.x, r.y);
     }
-    tmem_st8(t + 8u * h, hi);
-    tmem_st8(t + 16u + 8u * h, lo);
+    tmem_st8(t + (WL ? 16u * h : 8u * h), hi);
+    tmem_st8(t + (WL ? 16u * h + 8u : 16u + 8u * h), lo);
   }
 }
 
@@ -1038,22 +1041,23 @@ __device__ __forceinline__ void silu_store16(const uint32_t (&s)[16], float2 ha2
   tmem_st8(t + 8u, lo);
 }
 
-template <int MASK, bool RAB = false, bool TGT = false>
+template <int MASK, bool RAB = false, bool TGT = false, bool WL = false>
 __device__ __forceinline__ void silu_store32(const uint32_t (&s)[32], float2 ha2, int lim, int lim_hist,
                                              uint32_t t, const RabRow* rab = nullptr, int j0 = 0,
                                              int ts_lane = 0) {
   if constexpr (!RAB) {
-    silu_store32_body<MASK>(s, ha2, lim, lim_hist, t, nullptr, nullptr, 0);
+    silu_store32_body<MASK, false, false, false, false, WL>(s, ha2, lim, lim_hist, t, nullptr,
+                                                            nullptr, 0);
   } else {
     const RabChunk rc = rab_chunk<TGT>(*rab, j0, ts_lane);
     if (rc.fix_p && rc.fix_t)
-      silu_store32_body<MASK, true, TGT, true, true>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
+      silu_store32_body<MASK, true, TGT, true, true, WL>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
     else if (rc.fix_p)
-      silu_store32_body<MASK, true, TGT, true, false>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
+      silu_store32_body<MASK, true, TGT, true, false, WL>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
     else if (rc.fix_t)
-      silu_store32_body<MASK, true, TGT, false, true>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
+      silu_store32_body<MASK, true, TGT, false, true, WL>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
     else
-      silu_store32_body<MASK, true, TGT, false, false>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
+      silu_store32_body<MASK, true, TGT, false, false, WL>(s, ha2, lim, lim_hist, t, rab, &rc, j0);
   }
 }
 
@@ -1128,7 +1132,9 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
     const uint32_t t_s = lane_base + (uint32_t)(j * 128);
     bool plain = cur.kt != cur.b.qt;
     if constexpr (TGT) plain = cur.b.unmasked(cur.kt);
-    if constexpr (WIDE) {
+    // the 32-key chunks this warp takes: its half of the block when wide
+    const int c0 = WIDE ? 2 * half : 0, c1 = WIDE ? 2 * half + 2 : 4;
+    if constexpr (WIDE && !RAB) {
       // this warpgroup's four 16-key steps k = 4 half + u of the block
       if (quarter * 32 < cur.b.rows()) {
         uint32_t w0[16], w1[16];
@@ -1175,10 +1181,10 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
     } else if (RAB && plain && quarter * 32 < cur.b.rows()) {
       // one score buffer: the bias computation needs the registers
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = c0; c < c1; ++c) {
         tmem_ld32(t_s + 32u * c, s1);
         const int tsl = c == 0 ? tsk[0] : c == 1 ? tsk[1] : c == 2 ? tsk[2] : tsk[3];
-        silu_store32<0, RAB, TGT>(s1, ha2, 0, 0, t_s + 32u * c, &rr, kbase + 32 * c, tsl);
+        silu_store32<0, RAB, TGT, WIDE>(s1, ha2, 0, 0, t_s + 32u * c, &rr, kbase + 32 * c, tsl);
       }
       tmem_wait_st();
     } else if (plain && quarter * 32 < cur.b.rows()) {  // (without the bias)
@@ -1207,7 +1213,7 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
       int hist0 = 0;
       if constexpr (TGT) hist0 = cur.b.hist - kBN * cur.kt;
 #pragma unroll 1
-      for (int c = 0; c < 4 && 32 * c < cols; ++c) {
+      for (int c = c0; c < c1 && 32 * c < cols; ++c) {
         if (diag && c > quarter) {
           uint32_t z[16];
 #pragma unroll
@@ -1217,8 +1223,8 @@ __device__ void role_silu(const FwdArgs& a, uint32_t base, uint32_t tmem, const 
         } else {
           tmem_ld32(t_s + 32u * c, s1);
           const int tsl = c == 0 ? tsk[0] : c == 1 ? tsk[1] : c == 2 ? tsk[2] : tsk[3];
-          silu_store32<TGT ? 2 : 1, RAB, TGT>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c, t_s + 32u * c,
-                                              &rr, kbase + 32 * c, tsl);
+          silu_store32<TGT ? 2 : 1, RAB, TGT, WIDE>(s1, ha2, lim0 - 32 * c, hist0 - 32 * c,
+                                                    t_s + 32u * c, &rr, kbase + 32 * c, tsl);
         }
       }
       tmem_wait_st();

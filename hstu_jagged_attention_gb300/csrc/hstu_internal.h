@@ -144,7 +144,7 @@ int fwd_smem_bytes(int d);
 constexpr int kFwdThreads = 512;
 // Threads of the single-CTA forward kernel for head dimension d, with or
 // without the bias, and without the output stage: 768 (four SiLU
-// warpgroups) for d <= 64 without the bias, else kFwdThreads.
+// warpgroups) for d <= 64, else kFwdThreads.
 int fwd_block_threads(int d, bool rab);
 
 // Launch the persistent kernel for head dimension d on `grid` CTAs (and,

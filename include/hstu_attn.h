@@ -550,9 +550,9 @@ int hstu_attn_bwd_plan_ex(const hstu_plan* plan, const void* q, const void* k, c
  * hstu_launch_shape -- the grid the next launch for `plan` would use on the
  * current device: *grid persistent CTAs of *block threads with *smem_bytes
  * of dynamic shared memory.  Queries device attributes; launches nothing.
- * *block is that of a call without the bias or the output stage: 768 for
- * d <= 64 (four SiLU warpgroups), 512 for d = 128 and for pair plans; a
- * call with either runs 512.
+ * *block is that of a call without the output stage: 768 for d <= 64
+ * (four SiLU warpgroups), 512 for d = 128 and for pair plans; a call with
+ * the output stage runs 512.
  */
 int hstu_launch_shape(const hstu_plan* plan, int* grid, int* block, int* smem_bytes);
 
