@@ -70,6 +70,7 @@ _SIGNATURES = {
     "hstu_plan_worklist": (ctypes.c_int, [_VP, _I32P, ctypes.c_int, _IP]),
     "hstu_worklist_schedule": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, _I32P,
                                               ctypes.POINTER(ctypes.c_longlong)]),
+    "hstu_host_runs": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int, _IP]),
     "hstu_worklist_build": (ctypes.c_int, [_I32P, ctypes.c_int, ctypes.c_int, _I32P, ctypes.c_int, _IP]),
     "hstu_launch_shape": (ctypes.c_int, [_VP, _IP, _IP, _IP]),
     "hstu_last_status": (ctypes.c_int, [_IP, _IP]),
@@ -566,6 +567,22 @@ def hstu_worklist_schedule(cost, grid: int):
                                         ctypes.byref(span)),
            "hstu_worklist_schedule")
     return order[:len(c)], first, span.value
+
+
+def hstu_host_runs(offsets, n_chunks: int = 0) -> np.ndarray:
+    """Host-only (no CUDA call): the runs of whole sequences
+    hstu_attn_fwd_host takes, as first (int32, n_runs + 1): run c is
+    sequences first[c] .. first[c + 1] - 1."""
+    off = _host_offsets(offsets)
+    batch = len(off) - 1
+    n = ctypes.c_int()
+    _check(lib().hstu_host_runs(off.ctypes.data_as(_I32P), batch, int(n_chunks), None, 0,
+                                ctypes.byref(n)), "hstu_host_runs")
+    first = np.zeros(n.value + 1, dtype=np.int32)
+    _check(lib().hstu_host_runs(off.ctypes.data_as(_I32P), batch, int(n_chunks),
+                                first.ctypes.data_as(_I32P), len(first), ctypes.byref(n)),
+           "hstu_host_runs")
+    return first
 
 
 def hstu_plan_worklist(plan: Plan) -> np.ndarray:

@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <functional>
+#include <limits>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -883,6 +884,12 @@ int copy_streams(cudaStream_t (&st)[kCopyStreams]) {
   return HSTU_OK;
 }
 
+// Runs of the host-buffer forward when the caller asks for none.
+constexpr int kHostRuns = 4;
+int host_run_count(int batch, int n_chunks) {
+  return std::min(batch, n_chunks > 0 ? n_chunks : kHostRuns);
+}
+
 // Splits sequences 0 .. batch-1 into nc runs of whole sequences with about
 // equal token counts: run c is sequences first[c] .. first[c+1]-1 (a run
 // may be empty when one sequence holds most tokens).
@@ -935,7 +942,7 @@ int fwd_host(const void* q_host, const void* k_host, const void* v_host, const i
   if ((rc = copy_streams(cs)) != HSTU_OK) return rc;
   cudaStream_t s_in = cs[0], s_out = cs[1];
 
-  const int nc = std::min(batch, n_chunks > 0 ? n_chunks : 4);
+  const int nc = host_run_count(batch, n_chunks);
   std::vector<hstu::Item> all, items;
   std::vector<int32_t> hist;
   std::vector<int> seq_first, item_first;
@@ -1128,6 +1135,24 @@ int hstu_worklist_schedule(const int32_t* host_cost, int n_items, int grid, int3
     return HSTU_ERR_NO_MEMORY;
   }
   if (makespan) *makespan = span;
+  return HSTU_OK;
+}
+
+int hstu_host_runs(const int32_t* host_offsets, int batch, int n_chunks, int32_t* host_first,
+                   int capacity, int* n_runs) {
+  if (!host_offsets || !n_runs || batch < 0 || n_chunks < 0) return HSTU_ERR_INVALID_ARG;
+  int rc = check_offsets(host_offsets, batch, std::numeric_limits<int32_t>::max());
+  if (rc != HSTU_OK) return rc;
+  const int nc = host_run_count(batch, n_chunks);
+  *n_runs = nc;
+  if (!host_first) return HSTU_OK;
+  if (capacity < nc + 1) return HSTU_ERR_INVALID_ARG;
+  try {
+    const std::vector<int> first = chunk_sequences(host_offsets, batch, nc);
+    for (int c = 0; c <= nc; ++c) host_first[c] = first[(size_t)c];
+  } catch (const std::bad_alloc&) {
+    return HSTU_ERR_NO_MEMORY;
+  }
   return HSTU_OK;
 }
 

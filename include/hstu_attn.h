@@ -192,6 +192,24 @@ int hstu_attn_fwd_host(const void* q_host, const void* k_host, const void* v_hos
                        void* v_dev, void* out_dev, int n_chunks, hstu_stream_t stream);
 
 /*
+ * hstu_host_runs -- the runs of whole sequences hstu_attn_fwd_host takes
+ * for these offsets and n_chunks, on the host only (no CUDA call).
+ *   host_offsets  int32[batch+1], validated as in hstu_attn_fwd.
+ *   n_runs        out: min(batch, n_chunks), or min(batch, 4) for 0.
+ *   host_first    int32[n_runs + 1], out (NULL: only *n_runs): run c is
+ *                 sequences host_first[c] .. host_first[c + 1] - 1.
+ *   capacity      entries host_first holds (>= n_runs + 1).
+ * Run c (c < n_runs - 1) ends before the first sequence that starts at
+ * or past token floor(total * (c + 1) / n_runs), and after run c - 1; the
+ * last run ends at batch.  So every run holds at most about total / n_runs
+ * tokens plus one sequence, and a run may be empty.
+ * Errors: HSTU_ERR_INVALID_ARG for a NULL offsets or n_runs pointer,
+ * negative batch or n_chunks, invalid offsets or a short capacity.
+ */
+int hstu_host_runs(const int32_t* host_offsets, int batch, int n_chunks, int32_t* host_first,
+                   int capacity, int* n_runs);
+
+/*
  * hstu_plan_create -- validate host offsets and build the device work list once.
  *
  * The work list holds one item per (sequence, head, 128-row query block);
